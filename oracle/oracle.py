@@ -1,0 +1,182 @@
+"""CPU oracle for speculative-decoding verify-and-accept (ctypes binding).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+benchmark's CPU-baseline / reference leg, never by the product path.  The
+arithmetic lives in ``spec_oracle.c`` (plain C, IEEE double, index order); this
+module only builds that file with gcc, marshals numpy arrays into it, and adds
+the host-side tree metadata of the vLLM EAGLE walkthrough ("tree drafting in
+detail" section) in plain Python.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB = os.path.join(_HERE, "libspecoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16 = 0
+FP32 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile spec_oracle.c into libspecoracle.so next to it (gcc, no fast-math,
+    no FMA contraction, so both host architectures evaluate the same expressions)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+               "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm", "-lpthread"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.oracle_verify_chain.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, P, P, P, I]
+    lib.oracle_verify_chain.restype = I
+    lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P]
+    lib.oracle_verify_tree.restype = I
+    lib.oracle_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64]
+    lib.oracle_fixup_slots.restype = I
+    return lib
+
+
+def load_library(path: str):
+    """Bind a separately compiled copy of spec_oracle.c (the tests use this to
+    check that planted mistakes are caught by the pins)."""
+    return _bind(ctypes.CDLL(path))
+
+
+def _load(lib=None):
+    global _lib
+    if lib is not None:
+        return lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dt):
+    return None if a is None else np.ascontiguousarray(a, dtype=dt)
+
+
+def verify_chain(logits: np.ndarray, dtype: int, draft_tokens: np.ndarray,
+                 temperature: np.ndarray, u_sample: np.ndarray,
+                 draft_probs: Optional[np.ndarray] = None, u_accept: Optional[np.ndarray] = None,
+                 nthreads: int = 1, lib=None) -> dict:
+    """Chain verify for every request.  Returns out_tokens [B, k+1] (-1 padded),
+    num_accepted [B], flag_accept [B, k], flag_sample [B], b_alg [B] and
+    accept_ratio [B, k] (p/q of each accept test that ran, NaN otherwise)."""
+    lib = _load(lib)
+    B, k1, V = logits.shape
+    k = k1 - 1
+    z = np.ascontiguousarray(logits, dtype=np.uint16 if dtype == BF16 else np.float32)
+    tok = _c(draft_tokens, np.int32)
+    T = _c(temperature, np.float32)
+    us = _c(u_sample, np.float32)
+    q = _c(draft_probs, np.float32)
+    ua = _c(u_accept, np.float32)
+    out = dict(
+        out_tokens=np.empty((B, k + 1), np.int32), num_accepted=np.empty(B, np.int32),
+        flag_accept=np.empty((B, k), np.int32), flag_sample=np.empty(B, np.int32),
+        b_alg=np.empty(B, np.float64), accept_ratio=np.empty((B, k), np.float64))
+    rc = lib.oracle_verify_chain(
+        _ptr(z), dtype, _ptr(q), _ptr(tok), _ptr(T), _ptr(ua), _ptr(us), B, k, V,
+        _ptr(out["out_tokens"]), _ptr(out["num_accepted"]), _ptr(out["flag_accept"]),
+        _ptr(out["flag_sample"]), _ptr(out["b_alg"]), _ptr(out["accept_ratio"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify_chain rejected its arguments")
+    return out
+
+
+def verify_tree(logits: np.ndarray, dtype: int, node_tokens: np.ndarray, parent: np.ndarray,
+                max_depth: Optional[int] = None, lib=None) -> dict:
+    """Greedy tree verify.  Returns path [B, D+1], tokens [B, D+1], length [B], b_alg [B]."""
+    lib = _load(lib)
+    B, n1, V = logits.shape
+    N = n1 - 1
+    par = _c(parent, np.int32)
+    if max_depth is None:
+        max_depth = int(tree_depths(par).max()) if N > 0 else 0
+    z = np.ascontiguousarray(logits, dtype=np.uint16 if dtype == BF16 else np.float32)
+    toks = _c(node_tokens if N > 0 else np.zeros((B, 0), np.int32), np.int32)
+    out = dict(path=np.empty((B, max_depth + 1), np.int32),
+               tokens=np.empty((B, max_depth + 1), np.int32),
+               length=np.empty(B, np.int32), b_alg=np.empty(B, np.float64))
+    rc = lib.oracle_verify_tree(_ptr(z), dtype, _ptr(toks), _ptr(par), B, N, V, int(max_depth),
+                                _ptr(out["path"]), _ptr(out["tokens"]), _ptr(out["length"]),
+                                _ptr(out["b_alg"]))
+    if rc != 0:
+        raise ValueError("oracle_verify_tree rejected its arguments")
+    return out
+
+
+def fixup_slots(slot_mapping: np.ndarray, num_accepted: Optional[np.ndarray] = None,
+                path: Optional[np.ndarray] = None, pad: int = -1) -> np.ndarray:
+    """Returns a fixed-up copy of slot_mapping [B, P]."""
+    lib = _load()
+    s = np.array(slot_mapping, dtype=np.int64, copy=True, order="C")
+    B, P = s.shape
+    na = _c(num_accepted, np.int32)
+    pa = _c(path, np.int32)
+    stride = 0 if pa is None else pa.shape[1]
+    rc = lib.oracle_fixup_slots(_ptr(s), B, P, _ptr(na), _ptr(pa), stride, int(pad))
+    if rc != 0:
+        raise ValueError("oracle_fixup_slots rejected its arguments")
+    return s
+
+
+# ---------------------------------------------------------------------------
+# tree metadata (vLLM EAGLE walkthrough, "tree drafting in detail")
+# ---------------------------------------------------------------------------
+def tree_level_metadata(tree_choices: Sequence[Sequence[int]]):
+    """Depth is the length of the last tuple; level l holds the tuples of length
+    l+1; cu_drafts_per_level is the running total of the per-level counts and
+    child_drafts_per_level[l] = count[l] // count[l-1] (count[0] at level 0)."""
+    depth = len(tree_choices[-1])
+    counts = [0] * depth
+    for node in tree_choices:
+        counts[len(node) - 1] += 1
+    cu = [counts[0]]
+    child = [counts[0]]
+    for lvl in range(1, depth):
+        cu.append(cu[-1] + counts[lvl])
+        child.append(counts[lvl] // counts[lvl - 1])
+    return dict(depth=depth, num_drafts_per_level=counts, cu_drafts_per_level=cu,
+                child_drafts_per_level=child)
+
+
+def parent_from_choices(tree_choices: Sequence[Sequence[int]]) -> np.ndarray:
+    """Node n (1-based, in tree_choices order) is the tuple tree_choices[n-1]; its
+    parent is the node whose tuple is that tuple minus its last entry (the empty
+    tuple is the root, node 0)."""
+    index = {(): 0}
+    parent = [-1]
+    for n, t in enumerate(tree_choices, start=1):
+        t = tuple(int(v) for v in t)
+        parent.append(index[t[:-1]])
+        index[t] = n
+    return np.asarray(parent, dtype=np.int32)
+
+
+def tree_depths(parent: np.ndarray) -> np.ndarray:
+    d = np.zeros(len(parent), dtype=np.int32)
+    for n in range(1, len(parent)):
+        d[n] = d[parent[n]] + 1
+    return d

@@ -1,0 +1,429 @@
+/*
+ * spec_oracle.c -- CPU oracle for speculative-decoding verify-and-accept.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, fp64 statement of
+ * what the verification step computes.  Only the test suite, the smoke check
+ * and the benchmark's CPU-baseline leg may build or call it; the product path
+ * (the CUDA library and its binding) never does.  It shares no code, header,
+ * table or constant with the CUDA path.
+ *
+ * Sources (the speculative-decoding pages):
+ *  - EAGLE-3 review, "Speculative Decoding" (draft / verification / accept or
+ *    reject): target distributions at k+1 positions from one forward; check
+ *    drafts front to back; stop at the first rejection; resample the rejected
+ *    position; a bonus token when every draft is accepted.
+ *  - EAGLE-3 review, "small model answers" section: greedy rule (accept iff
+ *    the draft equals the target argmax, else emit the target argmax);
+ *    A(x) = min(1, p(x)/q(x)); residual norm(max(0, p - q)); identity
+ *    min(p,q) + max(0,p-q) = p.
+ *  - EAGLE-3 review, "EAGLE-3 inference" steps 4-5: greedy trees keep the
+ *    longest prefix that matches the target's choices; only the accepted
+ *    path's KV is kept.
+ *  - vLLM EAGLE walkthrough, "rejected tokens" / "slot mapping" sections:
+ *    rejected positions' slot_mapping entries become PADDING_SLOT_ID.
+ *  - serving-book chapter, "acceptance rule preserving the output
+ *    distribution": temperature 0 means greedy.
+ *
+ * Readings where the pages are silent (the same list is kept in the design
+ * notes): ties in argmax go to the lowest vocabulary index; q is used as given
+ * (no temperature applied to it); accept iff q(x) == 0 or u < p(x)/q(x); the
+ * resample of a request rejected at position a consumes u_sample[b][a], the
+ * bonus consumes u_sample[b][k]; the inverse CDF picks the smallest j whose
+ * prefix sum exceeds t = u * (total mass); a residual of zero total mass falls
+ * back to sampling from p; a draft token outside [0, V) is a rejection with
+ * p(x) = 0; tree ties at equal depth go to the smallest node index.
+ *
+ * All arithmetic on probabilities is IEEE double, evaluated in index order.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_BF16 0
+#define OR_FP32 1
+
+/* Flag windows for positions whose GPU result may legitimately differ. */
+#define OR_ACCEPT_WINDOW 1e-6   /* |u - p/q| below this flags the accept test   */
+#define OR_EDGE_WINDOW 1e-5     /* t within this fraction of a CDF edge flags it */
+
+/* ---------------------------------------------------------------- values -- */
+
+/* The real number a stored logit denotes.  bf16 is the upper half of an IEEE
+ * binary32, so widening is a 16-bit shift of the bit pattern. */
+static double logit_at(const void *z, int dtype, size_t idx)
+{
+    if (dtype == OR_BF16) {
+        uint32_t w = (uint32_t)((const uint16_t *)z)[idx] << 16;
+        float f;
+        memcpy(&f, &w, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)z)[idx];
+}
+
+/* argmax over one row, first occurrence of the maximum wins. */
+static int row_argmax(const void *z, int dtype, size_t off, int V)
+{
+    int best = 0;
+    double bv = logit_at(z, dtype, off);
+    for (int j = 1; j < V; ++j) {
+        double v = logit_at(z, dtype, off + (size_t)j);
+        if (v > bv) {
+            bv = v;
+            best = j;
+        }
+    }
+    return best;
+}
+
+/* p_j = exp(s_j - max s) / sum_i exp(s_i - max s), s_j = z_j / T. */
+static void row_softmax(const void *z, int dtype, size_t off, int V, double T, double *p)
+{
+    double m = -INFINITY;
+    for (int j = 0; j < V; ++j) {
+        p[j] = logit_at(z, dtype, off + (size_t)j) / T;
+        if (p[j] > m)
+            m = p[j];
+    }
+    double sum = 0.0;
+    for (int j = 0; j < V; ++j) {
+        p[j] = exp(p[j] - m);
+        sum += p[j];
+    }
+    for (int j = 0; j < V; ++j)
+        p[j] /= sum;
+}
+
+/* Inverse CDF over non-negative weights w: t = u * sum(w); the result is the
+ * smallest j with C_j = w_0 + ... + w_j > t.  If rounding leaves t >= C_{V-1},
+ * the last j with w_j > 0 is taken.  *near_edge reports whether t lies within
+ * OR_EDGE_WINDOW (relative) of the bucket's lower or upper edge. */
+static int inverse_cdf(const double *w, int V, double u, int *near_edge)
+{
+    double total = 0.0;
+    for (int j = 0; j < V; ++j)
+        total += w[j];
+    double t = u * total;
+    double c = 0.0;
+    int last_pos = -1;
+    for (int j = 0; j < V; ++j) {
+        double lo = c;
+        c += w[j];
+        if (w[j] > 0.0)
+            last_pos = j;
+        if (c > t) {
+            int flag = 0;
+            if (lo > 0.0 && t - lo <= OR_EDGE_WINDOW * lo)
+                flag = 1;
+            if (c - t <= OR_EDGE_WINDOW * c)
+                flag = 1;
+            *near_edge = flag;
+            return j;
+        }
+    }
+    *near_edge = 1;
+    return last_pos < 0 ? V - 1 : last_pos;
+}
+
+/* ------------------------------------------------------------- the chain -- */
+
+typedef struct {
+    const void *logits;
+    int dtype;
+    const float *q;
+    const int32_t *tokens;
+    const float *temperature;
+    const float *u_accept;
+    const float *u_sample;
+    int B, k, V;
+    int32_t *out_tokens;
+    int32_t *out_num_accepted;
+    int32_t *flag_accept; /* [B, k] or NULL: 1 where |u - p/q| < window */
+    int32_t *flag_sample; /* [B] or NULL: 1 where the sampled token sits near an edge */
+    double *b_alg;        /* [B] or NULL: bytes the method must read */
+    double *accept_ratio; /* [B, k] or NULL: p(x)/q(x) per accept test (NaN if not run) */
+    int nthreads;
+    int next;             /* shared request counter */
+    pthread_mutex_t lock;
+} chain_job;
+
+static void chain_one(chain_job *J, int b, double *p, double *r)
+{
+    const int k = J->k, V = J->V;
+    const size_t zs = (J->dtype == OR_BF16) ? 2 : 4;
+    const size_t row = (size_t)V;
+    const size_t zbase = (size_t)b * (size_t)(k + 1) * row;
+    const double T = (double)J->temperature[b];
+    int32_t *out = J->out_tokens + (size_t)b * (size_t)(k + 1);
+    for (int i = 0; i <= k; ++i)
+        out[i] = -1;
+    if (J->flag_accept)
+        for (int i = 0; i < k; ++i)
+            J->flag_accept[(size_t)b * k + i] = 0;
+    if (J->accept_ratio)
+        for (int i = 0; i < k; ++i)
+            J->accept_ratio[(size_t)b * k + i] = NAN;
+    if (J->flag_sample)
+        J->flag_sample[b] = 0;
+
+    int a = k;
+    double bytes = 0.0;
+    if (T == 0.0) {
+        /* greedy: accept while the draft equals the target argmax */
+        for (int i = 0; i <= k; ++i) {
+            int g = row_argmax(J->logits, J->dtype, zbase + (size_t)i * row, V);
+            bytes += (double)row * (double)zs;
+            if (i == k) {
+                out[k] = g;
+                a = k;
+                break;
+            }
+            int x = J->tokens[(size_t)b * k + i];
+            if (x != g) {
+                out[i] = g;
+                a = i;
+                break;
+            }
+            out[i] = x;
+        }
+    } else {
+        int sampled_row = -1; /* row whose distribution supplies the last token */
+        int residual = 0;
+        for (int i = 0; i < k; ++i) {
+            row_softmax(J->logits, J->dtype, zbase + (size_t)i * row, V, T, p);
+            bytes += (double)row * (double)zs;
+            int x = J->tokens[(size_t)b * k + i];
+            const float *qi = J->q + ((size_t)b * (size_t)k + (size_t)i) * row;
+            int accept;
+            if (x < 0 || x >= V) {
+                accept = 0; /* out-of-range draft: p(x) = 0 */
+            } else {
+                double ph = p[x];
+                double qh = (double)qi[x];
+                bytes += 4.0;
+                if (qh == 0.0) {
+                    accept = 1;
+                } else {
+                    double ratio = ph / qh;
+                    double u = (double)J->u_accept[(size_t)b * k + i];
+                    accept = u < ratio;
+                    if (J->accept_ratio)
+                        J->accept_ratio[(size_t)b * k + i] = ratio;
+                    if (J->flag_accept && fabs(u - ratio) < OR_ACCEPT_WINDOW)
+                        J->flag_accept[(size_t)b * k + i] = 1;
+                }
+            }
+            if (!accept) {
+                a = i;
+                sampled_row = i;
+                residual = 1;
+                /* residual r_j = max(0, p_j - q_j) */
+                for (int j = 0; j < V; ++j) {
+                    double d = p[j] - (double)qi[j];
+                    r[j] = d > 0.0 ? d : 0.0;
+                }
+                bytes += (double)row * 4.0;
+                break;
+            }
+            out[i] = x;
+        }
+        if (sampled_row < 0) {
+            a = k;
+            sampled_row = k;
+            row_softmax(J->logits, J->dtype, zbase + (size_t)k * row, V, T, p);
+            bytes += (double)row * (double)zs;
+        }
+        const double u = (double)J->u_sample[(size_t)b * (k + 1) + sampled_row];
+        const double *w = p;
+        if (residual) {
+            double Z = 0.0;
+            for (int j = 0; j < V; ++j)
+                Z += r[j];
+            if (Z > 0.0)
+                w = r; /* zero residual mass: sample from p instead */
+        }
+        int edge = 0;
+        out[sampled_row] = inverse_cdf(w, V, u, &edge);
+        if (J->flag_sample)
+            J->flag_sample[b] = edge;
+    }
+    J->out_num_accepted[b] = a;
+    if (J->b_alg)
+        J->b_alg[b] = bytes;
+}
+
+static void *chain_worker(void *arg)
+{
+    chain_job *J = (chain_job *)arg;
+    double *p = (double *)malloc(sizeof(double) * (size_t)J->V);
+    double *r = (double *)malloc(sizeof(double) * (size_t)J->V);
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int b = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (b >= J->B)
+            break;
+        chain_one(J, b, p, r);
+    }
+    free(p);
+    free(r);
+    return NULL;
+}
+
+/* Returns 0 on success, nonzero on bad arguments. */
+int oracle_verify_chain(const void *logits, int dtype, const float *draft_probs,
+                        const int32_t *draft_tokens, const float *temperature,
+                        const float *u_accept, const float *u_sample, int B, int k, int V,
+                        int32_t *out_tokens, int32_t *out_num_accepted, int32_t *flag_accept,
+                        int32_t *flag_sample, double *b_alg, double *accept_ratio, int nthreads)
+{
+    if (B < 0 || k < 1 || V < 1 || !logits || !draft_tokens || !temperature || !u_sample ||
+        !out_tokens || !out_num_accepted)
+        return 1;
+    for (int b = 0; b < B; ++b)
+        if (temperature[b] != 0.0f && (!draft_probs || !u_accept))
+            return 1;
+    chain_job J;
+    memset(&J, 0, sizeof J);
+    J.logits = logits;
+    J.dtype = dtype;
+    J.q = draft_probs;
+    J.tokens = draft_tokens;
+    J.temperature = temperature;
+    J.u_accept = u_accept;
+    J.u_sample = u_sample;
+    J.B = B;
+    J.k = k;
+    J.V = V;
+    J.out_tokens = out_tokens;
+    J.out_num_accepted = out_num_accepted;
+    J.flag_accept = flag_accept;
+    J.flag_sample = flag_sample;
+    J.b_alg = b_alg;
+    J.accept_ratio = accept_ratio;
+    J.next = 0;
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > B)
+        nthreads = B > 0 ? B : 1;
+    if (nthreads == 1) {
+        chain_worker(&J);
+    } else {
+        pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        for (int t = 0; t < nthreads; ++t)
+            pthread_create(&th[t], NULL, chain_worker, &J);
+        for (int t = 0; t < nthreads; ++t)
+            pthread_join(th[t], NULL);
+        free(th);
+    }
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
+/* -------------------------------------------------------------- the tree -- */
+
+/* Greedy tree: g_n = argmax of row n; node n is accepted iff its parent is
+ * accepted and token_n == g_{parent(n)}; the root (node 0) is accepted.  The
+ * chosen node n* is the deepest accepted node (smallest index on ties); the
+ * output is the path root..n*, the path's tokens, then g_{n*}. */
+int oracle_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
+                       const int32_t *parent, int B, int N, int V, int max_depth,
+                       int32_t *out_path, int32_t *out_tokens, int32_t *out_len, double *b_alg)
+{
+    if (B < 0 || N < 0 || V < 1 || max_depth < 0 || !logits || !parent || !out_path ||
+        !out_tokens || !out_len)
+        return 1;
+    if (N > 0 && !node_tokens)
+        return 1;
+    if (parent[0] != -1)
+        return 1;
+    int *depth = (int *)malloc(sizeof(int) * (size_t)(N + 1));
+    int *g = (int *)malloc(sizeof(int) * (size_t)(N + 1));
+    int *acc = (int *)malloc(sizeof(int) * (size_t)(N + 1));
+    int *has_child = (int *)calloc((size_t)(N + 1), sizeof(int));
+    depth[0] = 0;
+    int bad = 0;
+    for (int n = 1; n <= N; ++n) {
+        if (parent[n] < 0 || parent[n] >= n) {
+            bad = 1;
+            break;
+        }
+        depth[n] = depth[parent[n]] + 1;
+        if (depth[n] > max_depth)
+            bad = 1;
+        has_child[parent[n]] = 1;
+    }
+    if (!bad) {
+        const size_t zs = (dtype == OR_BF16) ? 2 : 4;
+        const size_t row = (size_t)V;
+        for (int b = 0; b < B; ++b) {
+            const size_t zbase = (size_t)b * (size_t)(N + 1) * row;
+            for (int n = 0; n <= N; ++n)
+                g[n] = row_argmax(logits, dtype, zbase + (size_t)n * row, V);
+            acc[0] = 1;
+            int best = 0;
+            for (int n = 1; n <= N; ++n) {
+                int x = node_tokens[(size_t)b * N + (n - 1)];
+                acc[n] = acc[parent[n]] && x == g[parent[n]];
+                if (acc[n] && depth[n] > depth[best])
+                    best = n;
+            }
+            int d = depth[best];
+            int32_t *path = out_path + (size_t)b * (size_t)(max_depth + 1);
+            int32_t *tok = out_tokens + (size_t)b * (size_t)(max_depth + 1);
+            for (int i = 0; i <= max_depth; ++i) {
+                path[i] = -1;
+                tok[i] = -1;
+            }
+            for (int n = best, i = d; i >= 0; n = parent[n], --i)
+                path[i] = n;
+            for (int i = 1; i <= d; ++i)
+                tok[i - 1] = node_tokens[(size_t)b * N + (path[i] - 1)];
+            tok[d] = g[best];
+            out_len[b] = d + 1;
+            if (b_alg) {
+                double rows = 0.0;
+                for (int n = 0; n <= N; ++n)
+                    if (n == 0 || n == best || (acc[n] && has_child[n]))
+                        rows += 1.0;
+                b_alg[b] = rows * (double)row * (double)zs;
+            }
+        }
+    }
+    free(depth);
+    free(g);
+    free(acc);
+    free(has_child);
+    return bad ? 1 : 0;
+}
+
+/* ------------------------------------------------------------ slot fix-up -- */
+
+/* Chain mode (path == NULL): entries j > num_accepted[b] become pad.
+ * Tree mode: entry j survives iff j == 0 or j appears in path[b, :]. */
+int oracle_fixup_slots(int64_t *slot_mapping, int B, int P, const int32_t *num_accepted,
+                       const int32_t *path, int path_stride, int64_t pad)
+{
+    if (B < 0 || P < 0 || !slot_mapping)
+        return 1;
+    if (!num_accepted && !path)
+        return 1;
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < P; ++j) {
+            int keep;
+            if (!path) {
+                keep = j <= num_accepted[b];
+            } else {
+                keep = (j == 0);
+                for (int i = 0; i < path_stride && !keep; ++i)
+                    keep = path[(size_t)b * path_stride + i] == j;
+            }
+            if (!keep)
+                slot_mapping[(size_t)b * P + j] = pad;
+        }
+    }
+    return 0;
+}

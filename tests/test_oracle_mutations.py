@@ -1,0 +1,145 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case copies spec_oracle.c, plants one mistake (a flipped sign, a dropped
+clip, a wrong row or index, a reversed comparison, a dropped ancestor term),
+compiles the copy on the CPU and checks that the corresponding pin fails on it
+while passing on the real oracle.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_chain_gb300 import workloads as W
+
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "spec_oracle.c")
+
+
+def _mutant(tmp_path, old, new, tag):
+    src = open(SRC).read()
+    assert src.count(old) == 1, old
+    path = tmp_path / ("mut_%s.c" % tag)
+    path.write_text(src.replace(old, new))
+    so = tmp_path / ("libmut_%s.so" % tag)
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-o", str(so), str(path), "-lm", "-lpthread"])
+    from oracle import oracle as O
+    return O.load_library(str(so))
+
+
+def _lossless(O, lib):
+    zp, q = pins._lossless_case(31)
+    x = W.chain_fixed_rows(32, 300_000, zp, q, temperature=1.0)
+    r = O.verify_chain(x.logits, x.dtype, x.draft_tokens, x.temperature, x.u_sample,
+                       x.draft_probs, x.u_accept, nthreads=os.cpu_count() or 1, lib=lib)
+    return min(pins._chi2_pvalues(r["out_tokens"], r["num_accepted"], zp, 1.0))
+
+
+def _residual_mismatches(O, lib):
+    g = np.random.default_rng(24)
+    B, k, V, T = 120, 3, 257, 0.8
+    z = (g.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    q = pins._softmax64(z[:, :k] + g.standard_normal((B, k, V)), 1.0).astype(np.float32)
+    tok = g.integers(0, V, size=(B, k)).astype(np.int32)
+    ua = W.method_uniforms(g, (B, k))
+    us = W.method_uniforms(g, (B, k + 1))
+    r = O.verify_chain(z, W.FP32, tok, np.full(B, T, np.float32), us, q, ua, lib=lib)
+    bad = 0
+    for b in range(B):
+        a = r["num_accepted"][b]
+        if a < k:
+            j, _, _ = pins._residual_token_numpy(z[b, a], T, q[b, a], float(us[b, a]))
+            bad += int(r["out_tokens"][b, a] != j)
+    return bad
+
+
+def _bonus_mismatches(O, lib):
+    g = np.random.default_rng(25)
+    B, k, V, T = 100, 2, 300, 1.3
+    z = (g.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    q = pins._softmax64(z[:, :k], 1.0).astype(np.float32)
+    tok = g.integers(0, V, size=(B, k)).astype(np.int32)
+    us = W.method_uniforms(g, (B, k + 1))
+    r = O.verify_chain(z, W.FP32, tok, np.full(B, T, np.float32), us, q,
+                       np.zeros((B, k), np.float32), lib=lib)
+    bad = 0
+    for b in range(B):
+        c = np.cumsum(pins._softmax64(z[b, k], T))
+        bad += int(r["out_tokens"][b, k] != np.searchsorted(c, float(us[b, k]) * c[-1], side="right"))
+    return bad
+
+
+def _accept_rate_z(O, lib):
+    g = np.random.default_rng(22)
+    V, n = 6, 100000
+    zp = g.standard_normal(V) * 1.5
+    q = pins._softmax64(zp + g.standard_normal(V), 1.0).astype(np.float32)
+    x = W.chain_fixed_rows(23, n, np.stack([zp, zp]).astype(np.float32), q[None, :])
+    r = O.verify_chain(x.logits, x.dtype, x.draft_tokens, x.temperature, x.u_sample,
+                       x.draft_probs, x.u_accept, lib=lib)
+    alpha = np.minimum(pins._softmax64(zp, 1.0), q.astype(np.float64)).sum()
+    acc = (r["num_accepted"] >= 1).mean()
+    return abs(acc - alpha) / np.sqrt(alpha * (1 - alpha) / n)
+
+
+def _tie_ok(O, lib):
+    z = np.zeros((1, 2, 16), np.float32)
+    z[0, :, 3] = 5.0
+    z[0, :, 9] = 5.0
+    r = O.verify_chain(z, W.FP32, np.array([[9]], np.int32), np.zeros(1, np.float32),
+                       np.zeros((1, 2), np.float32), lib=lib)
+    return r["num_accepted"][0] == 0 and r["out_tokens"][0, 0] == 3
+
+
+def _tree_mismatches(O, lib):
+    t = W.tree_greedy(seed=55, B=12, V=97, children_per_level=(4, 2, 2, 1, 1), p_match=0.75)
+    r = O.verify_tree(t.logits, t.dtype, t.node_tokens, t.parent, lib=lib)
+    zf = W.logits_as_f32(t.logits, t.dtype)
+    bad = 0
+    for b in range(t.B):
+        path, out = pins._tree_bruteforce(zf[b], t.node_tokens[b], t.parent)
+        bad += int(list(r["tokens"][b, :len(path)]) != out or r["length"][b] != len(path))
+    return bad
+
+
+CASES = [
+    ("residual_sign", "double d = p[j] - (double)qi[j];", "double d = (double)qi[j] - p[j];",
+     lambda O, lib: _lossless(O, lib) < 1e-6),
+    ("residual_noclip", "r[j] = d > 0.0 ? d : 0.0;", "r[j] = d > 0.0 ? d : -d;",
+     lambda O, lib: _lossless(O, lib) < 1e-6),
+    ("bonus_row", "row_softmax(J->logits, J->dtype, zbase + (size_t)k * row, V, T, p);",
+     "row_softmax(J->logits, J->dtype, zbase + (size_t)(k - 1) * row, V, T, p);",
+     lambda O, lib: _bonus_mismatches(O, lib) > 10),
+    ("accept_reversed", "accept = u < ratio;", "accept = u > ratio;",
+     lambda O, lib: _accept_rate_z(O, lib) > 10),
+    ("sample_uniform_index", "J->u_sample[(size_t)b * (k + 1) + sampled_row]",
+     "J->u_sample[(size_t)b * (k + 1)]", lambda O, lib: _residual_mismatches(O, lib) > 10),
+    ("no_temperature", "p[j] = logit_at(z, dtype, off + (size_t)j) / T;",
+     "p[j] = logit_at(z, dtype, off + (size_t)j);", lambda O, lib: _bonus_mismatches(O, lib) > 10),
+    ("tie_last", "if (v > bv) {", "if (v >= bv) {", lambda O, lib: not _tie_ok(O, lib)),
+    ("tree_no_ancestor", "acc[n] = acc[parent[n]] && x == g[parent[n]];",
+     "acc[n] = x == g[parent[n]];", lambda O, lib: _tree_mismatches(O, lib) > 0),
+    ("tree_parent_row", "acc[n] = acc[parent[n]] && x == g[parent[n]];",
+     "acc[n] = acc[parent[n]] && x == g[n];", lambda O, lib: _tree_mismatches(O, lib) > 0),
+]
+
+
+def test_real_oracle_passes_the_mutation_checks(oracle_mod):
+    O = oracle_mod
+    lib = O._load()
+    assert _lossless(O, lib) > 0.01
+    assert _residual_mismatches(O, lib) == 0
+    assert _bonus_mismatches(O, lib) == 0
+    assert _accept_rate_z(O, lib) < 4
+    assert _tie_ok(O, lib)
+    assert _tree_mismatches(O, lib) == 0
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_planted_mistake_is_caught(oracle_mod, tmp_path, case):
+    tag, old, new, caught = case
+    lib = _mutant(tmp_path, old, new, tag)
+    assert caught(oracle_mod, lib)
