@@ -1,0 +1,180 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify, the GB300 (sm_103a) verify-and-accept
+ * step of speculative decoding.
+ *
+ * What the step computes (the speculative-decoding pages):
+ *  - EAGLE-3 review, "Speculative Decoding" (draft, verification, accept or
+ *    reject): the target model scores k draft tokens in one forward pass and
+ *    returns next-token distributions at k+1 positions; drafts are checked
+ *    front to back; the first rejection ends the step and its position is
+ *    resampled; when all k drafts pass, the distribution at position k+1 gives
+ *    one more (bonus) token, so every step emits at least one token.
+ *  - EAGLE-3 review, section on whether a small draft model hurts quality:
+ *    greedy decoding accepts a draft iff it equals the target argmax and
+ *    otherwise emits that argmax; sampling accepts x with probability
+ *    min(1, p(x)/q(x)) and resamples a rejection from norm(max(0, p - q)).
+ *  - Serving-book chapter, "acceptance rule that preserves the output
+ *    distribution": temperature 0 is the greedy case.
+ *  - EAGLE-3 review, "EAGLE-3 inference" steps 3-5 and the vLLM EAGLE
+ *    walkthrough, "tree drafting in detail": a token tree is verified in one
+ *    forward; greedy verification keeps the longest root-to-node path whose
+ *    tokens all match the target's choices; tree_choices gives
+ *    num/cu/child drafts per level.
+ *  - vLLM EAGLE walkthrough, "handling rejected tokens" and "slot mapping and
+ *    KV-cache management": the slot_mapping entries of rejected tokens are
+ *    replaced by PADDING_SLOT_ID so their KV never lands in the cache.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer.  The library never allocates or
+ *    frees device memory and keeps no pointer after a call returns.
+ *  - Execution: device work is enqueued on `stream` (a cudaStream_t passed as
+ *    void*, NULL = the legacy default stream) on the calling thread's current
+ *    device; there is no host synchronisation inside a call.
+ *  - "device" pointers must be device-accessible memory of the current device;
+ *    "host" pointers are read during the call only.
+ *  - Layouts are dense row-major (C order) with the shapes given below.
+ *  - Host-side checks run before any launch; a failed check returns
+ *    SPEC_ERR_INVALID_ARG and enqueues nothing.  A device that is not
+ *    compute capability 10.3 returns SPEC_ERR_UNSUPPORTED.  A CUDA launch
+ *    failure returns SPEC_ERR_CUDA (spec_last_error() gives the text).
+ *  - Data problems found on the device never trap: they OR bits into the
+ *    caller's int32 status word (SPEC_STATUS_*), which the library never
+ *    clears.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,
+    SPEC_ERR_UNSUPPORTED = 2,
+    SPEC_ERR_CUDA = 3
+} spec_status_t;
+
+typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype_t;
+
+/* Bits OR-ed into the device status word. */
+#define SPEC_STATUS_TOKEN_RANGE 1  /* a draft token outside [0, V): treated as a rejection */
+#define SPEC_STATUS_NONFINITE 2    /* a NaN or infinite logit was read (results undefined) */
+#define SPEC_STATUS_WAIT_TIMEOUT 4 /* an inter-block wait gave up (results of that request undefined) */
+
+/* Largest rows per request (k+1 for chains, N+1 for trees). */
+#define SPEC_MAX_ROWS 256
+
+/* Workspace bytes needed by spec_verify_chain / spec_verify_tree for B requests
+ * of `rows` logits rows (k+1 or N+1) over vocabulary V.  The workspace is
+ * device memory owned by the caller; it must be zero-filled before its first
+ * use (spec_workspace_init) and every completed call leaves it zero-filled
+ * again, except the 64-byte counter block at offset 0 (see below).  One
+ * workspace must not be used by two calls that can run at the same time.
+ * Returns 0 for invalid sizes. */
+size_t spec_workspace_bytes(int B, int rows, int V, spec_dtype_t dtype);
+
+/* Zero-fills `bytes` of device workspace on `stream` (cudaMemsetAsync). */
+spec_status_t spec_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/*
+ * Chain verification (draft, verify, accept/reject as summarised above).
+ *
+ *  target_logits [B, k+1, V] device, dtype bf16 or fp32, 16-byte aligned.
+ *      Row i (0-based) is the target's next-token distribution after the
+ *      prefix plus drafts 1..i; row k scores the bonus token.
+ *  draft_probs   [B, k, V] fp32 device, 16-byte aligned, or NULL when every
+ *      request is greedy.  Row i is the draft distribution q that draft
+ *      token i+1 was drawn from; it is used as given (no temperature).
+ *  draft_tokens  [B, k] int32 device.
+ *  temperature   [B] fp32 device, or NULL (every request greedy).  T == 0 is
+ *      greedy; T > 0 samples from p = softmax(z / T).  Negative T is invalid.
+ *  u_accept      [B, k] fp32 device in [0, 1), or NULL when every request is
+ *      greedy.  Draft i+1 is accepted iff q(x) == 0 or u_accept[b,i] < p(x)/q(x).
+ *  u_sample      [B, k+1] fp32 device in [0, 1), or NULL when every request is
+ *      greedy.  A request rejected at row a draws its token with u_sample[b,a]
+ *      (the bonus row k uses u_sample[b,k]) by inverse CDF: the smallest j
+ *      whose prefix mass exceeds u * (total mass).
+ *  out_tokens    [B, k+1] int32 device: drafts 1..a, then the corrected or
+ *      bonus token, then -1 padding.
+ *  out_num_accepted [B] int32 device: a in [0, k].
+ *  d_status      one int32 device word (may be NULL): SPEC_STATUS_* bits.
+ *  workspace / workspace_bytes: see spec_workspace_bytes(B, k+1, V, dtype).
+ *  Sizes: 1 <= B, 1 <= k <= SPEC_MAX_ROWS-1, 1 <= V < 2^30.
+ */
+spec_status_t spec_verify_chain(const void *target_logits, spec_dtype_t dtype,
+                                const float *draft_probs, const int32_t *draft_tokens,
+                                const float *temperature, const float *u_accept,
+                                const float *u_sample, int B, int k, int V,
+                                int32_t *out_tokens, int32_t *out_num_accepted,
+                                int32_t *d_status, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
+ * Greedy token-tree verification (EAGLE-style tree, one verification forward).
+ *
+ *  target_logits [B, N+1, V] device, bf16 or fp32, 16-byte aligned.  Row n is
+ *      the target distribution after the prefix plus the path root..n; row 0
+ *      belongs to the root (the last accepted token).
+ *  node_tokens   [B, N] int32 device; column n-1 holds node n's token.
+ *  parent        [N+1] int32 HOST array, parent[0] = -1, 0 <= parent[n] < n
+ *      (level order, as spec_tree_from_choices returns).  Shared by all requests.
+ *  max_depth     row stride minus one of out_path / out_tokens; must be at
+ *      least the tree's depth.
+ *  Node n is accepted iff its parent is accepted and node_tokens[n] equals the
+ *  argmax of row parent[n] (lowest index on ties); the root is accepted.  The
+ *  chosen node n* is the deepest accepted node, smallest index on ties.
+ *  out_path   [B, max_depth+1] int32 device: root, ..., n*, then -1.
+ *  out_tokens [B, max_depth+1] int32 device: the path's tokens (excluding the
+ *      root), then argmax of row n*, then -1.
+ *  out_len    [B] int32 device: tokens emitted = depth(n*) + 1.
+ *  Sizes: 1 <= B, 0 <= N <= SPEC_MAX_ROWS-1, 1 <= V < 2^30.
+ */
+spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_t dtype,
+                               const int32_t *node_tokens, const int32_t *parent, int B, int N,
+                               int V, int max_depth, int32_t *out_path, int32_t *out_tokens,
+                               int32_t *out_len, int32_t *d_status, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * KV slot_mapping fix-up, in place on [B, P] int64 device memory.
+ *  Chain mode (num_accepted != NULL, path == NULL): entry j of request b keeps
+ *    its value iff j <= num_accepted[b] (row 0 is the last accepted token,
+ *    whose KV is written this step); other entries become padding_slot_id.
+ *  Tree mode (path != NULL): entry j keeps its value iff j == 0 or j occurs in
+ *    path[b, 0..path_stride).  Entries of accepted nodes off the chosen path
+ *    are padded too.
+ *  Kept entries are not written.  num_accepted / path are device arrays.
+ */
+spec_status_t spec_fixup_slots(int64_t *slot_mapping, int B, int P, const int32_t *num_accepted,
+                               const int32_t *path, int path_stride, int64_t padding_slot_id,
+                               void *stream);
+
+/*
+ * Host helper (no device work): tree_choices -> parent[] and level metadata,
+ * following the vLLM EAGLE walkthrough ("tree drafting in detail").
+ *  flat / lens / n: the n tuples of tree_choices, concatenated in `flat`,
+ *      lens[i] = length of tuple i.  Tuples must be in level order and each
+ *      tuple's prefix must appear before it.
+ *  parent [n+1] (out): parent[0] = -1; node i+1 is tuple i; its parent is the
+ *      node of the tuple without its last entry (the root for length 1).
+ *  cu_per_level, child_per_level [depth] (out, may be NULL; capacity
+ *      SPEC_MAX_ROWS): cumulative node count per level and count[l] /
+ *      count[l-1] (count[0] at level 0).
+ *  depth (out): length of the last tuple.
+ */
+spec_status_t spec_tree_from_choices(const int32_t *flat, const int32_t *lens, int n,
+                                     int32_t *parent, int32_t *cu_per_level,
+                                     int32_t *child_per_level, int *depth);
+
+/* Text of the last error recorded on the calling thread ("" if none). */
+const char *spec_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,5 +1,293 @@
 """GB300-native speculative-decoding verify-and-accept.
 
-The CUDA library (``libspecverify.so``, C ABI declared in ``include/spec_verify.h``)
-does every step of the path; this package only marshals arguments to it.
+Every step of the path runs in the CUDA library ``libspecverify.so`` (C ABI in
+``include/spec_verify.h``).  This module only marshals torch tensors into that
+ABI: it checks dtypes, devices and contiguity, passes ``data_ptr()`` values and
+the current CUDA stream, and keeps a zero-initialised workspace per
+(device, stream).  There is no CPU fallback: if the library is missing or the
+device is not sm_103, every call raises.
+
+Entry points (names as in the C ABI):
+
+* :func:`verify_chain`  -- chain verification, greedy (T = 0) or sampled.
+* :func:`verify_tree`   -- greedy EAGLE-style token-tree verification.
+* :func:`fixup_slots`   -- rewrite rejected KV slots to PADDING_SLOT_ID.
+* :func:`tree_from_choices` -- tree_choices -> parent[] and level metadata.
 """
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+__all__ = ["verify_chain", "verify_tree", "fixup_slots", "tree_from_choices", "workspace_bytes",
+           "SpecError", "PADDING_SLOT_ID", "STATUS_TOKEN_RANGE", "STATUS_NONFINITE",
+           "STATUS_WAIT_TIMEOUT", "library_path", "load_library"]
+
+PADDING_SLOT_ID = -1
+SPEC_BF16, SPEC_FP32 = 0, 1
+STATUS_TOKEN_RANGE, STATUS_NONFINITE, STATUS_WAIT_TIMEOUT = 1, 2, 4
+MAX_ROWS = 256
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+_lock = threading.Lock()
+_lib = None
+_workspaces = {}
+
+_STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_UNSUPPORTED", 3: "SPEC_ERR_CUDA"}
+
+
+class SpecError(RuntimeError):
+    """A non-zero spec_status_t from the library."""
+
+    def __init__(self, fn: str, code: int, detail: str):
+        super().__init__("%s -> %s: %s" % (fn, _STATUS_NAMES.get(code, code), detail))
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libspecverify.so (built by ``__graft_entry__.build()`` or
+    ``python -m speculative_decoding_verification_chain_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        import torch  # noqa: F401  (load torch's CUDA runtime first so both share it)
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError("libspecverify.so is not built (%s); run the build step first" % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.spec_workspace_bytes.argtypes = [I, I, I, I]
+        lib.spec_workspace_bytes.restype = Z
+        lib.spec_workspace_init.argtypes = [P, Z, P]
+        lib.spec_workspace_init.restype = I
+        lib.spec_verify_chain.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, P, Z, P]
+        lib.spec_verify_chain.restype = I
+        lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
+        lib.spec_verify_tree.restype = I
+        lib.spec_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64, P]
+        lib.spec_fixup_slots.restype = I
+        lib.spec_tree_from_choices.argtypes = [P, P, I, P, P, P, P]
+        lib.spec_tree_from_choices.restype = I
+        lib.spec_last_error.argtypes = []
+        lib.spec_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise SpecError(fn, rc, load_library().spec_last_error().decode(errors="replace"))
+
+
+# ------------------------------------------------------------------ torch --
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_FP32
+    raise TypeError("target_logits must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _need(t, name, dtype, shape, device):
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if t.device != device:
+        raise ValueError("%s must be on %s, got %s" % (name, device, t.device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _stream_handle(device, stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def workspace_bytes(B: int, rows: int, V: int, dtype_code: int = SPEC_BF16) -> int:
+    n = load_library().spec_workspace_bytes(int(B), int(rows), int(V), int(dtype_code))
+    if n == 0:
+        raise SpecError("spec_workspace_bytes", 1, "invalid sizes B=%d rows=%d V=%d" % (B, rows, V))
+    return int(n)
+
+
+def _workspace(device, stream_handle: int, nbytes: int):
+    """Zero-filled device workspace kept per (device, stream); grows on demand."""
+    torch = _torch()
+    key = (device.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def workspace_for(device=None, stream=None):
+    """The cached workspace tensor used for calls on (device, stream), or None."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return _workspaces.get((device.index, _stream_handle(device, stream)))
+
+
+def workspace_counters(ws) -> dict:
+    """Diagnostic counters the kernel accumulates at workspace offset 0:
+    A units loaded / skipped, B units loaded / skipped, bytes streamed."""
+    v = ws[:64].view(_torch().int64).cpu().tolist()
+    return dict(a_loaded=v[0], a_skipped=v[1], b_loaded=v[2], b_skipped=v[3], bytes_loaded=v[4])
+
+
+def reset_counters(ws):
+    ws[:64].zero_()
+
+
+# ---------------------------------------------------------------- entries --
+def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u_sample=None,
+                 draft_probs=None, *, out_tokens=None, out_num_accepted=None, status=None,
+                 workspace=None, stream=None) -> Tuple[object, object]:
+    """Chain verify-and-accept on the GPU.
+
+    target_logits [B, k+1, V] bf16/fp32 CUDA; draft_tokens [B, k] int32.
+    Sampled requests (temperature > 0) also need draft_probs [B, k, V] fp32,
+    u_accept [B, k] and u_sample [B, k+1] fp32.  With temperature None every
+    request is greedy.  Returns (out_tokens [B, k+1] int32, num_accepted [B] int32).
+    """
+    torch = _torch()
+    lib = load_library()
+    z = target_logits
+    if z.dim() != 3:
+        raise ValueError("target_logits must be [B, k+1, V]")
+    B, k1, V = z.shape
+    k = k1 - 1
+    dev = z.device
+    if dev.type != "cuda":
+        raise ValueError("target_logits must be a CUDA tensor")
+    if not z.is_contiguous():
+        raise ValueError("target_logits must be contiguous")
+    code = _dtype_code(z)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(u_accept, "u_accept", torch.float32, (B, k), dev)
+    _need(u_sample, "u_sample", torch.float32, (B, k + 1), dev)
+    _need(draft_probs, "draft_probs", torch.float32, (B, k, V), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    sh = _stream_handle(dev, stream)
+    nbytes = workspace_bytes(B, k + 1, V, code)
+    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes)
+    rc = lib.spec_verify_chain(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperature),
+                               _ptr(u_accept), _ptr(u_sample), B, k, V, _ptr(out_tokens),
+                               _ptr(out_num_accepted), _ptr(status), _ptr(ws), ws.numel(), sh)
+    _check("spec_verify_chain", rc)
+    return out_tokens, out_num_accepted
+
+
+def verify_tree(target_logits, node_tokens, parent: Sequence[int], max_depth: Optional[int] = None, *,
+                out_path=None, out_tokens=None, out_len=None, status=None, workspace=None,
+                stream=None):
+    """Greedy token-tree verify on the GPU.
+
+    target_logits [B, N+1, V] bf16/fp32 CUDA; node_tokens [B, N] int32 CUDA;
+    parent: N+1 host integers (parent[0] = -1, level order).  Returns
+    (out_path [B, D+1], out_tokens [B, D+1], out_len [B]) int32 CUDA tensors.
+    """
+    torch = _torch()
+    import numpy as np
+    lib = load_library()
+    z = target_logits
+    if z.dim() != 3:
+        raise ValueError("target_logits must be [B, N+1, V]")
+    B, n1, V = z.shape
+    N = n1 - 1
+    dev = z.device
+    if dev.type != "cuda" or not z.is_contiguous():
+        raise ValueError("target_logits must be a contiguous CUDA tensor")
+    code = _dtype_code(z)
+    par = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    if par.shape != (N + 1,):
+        raise ValueError("parent must hold N+1 = %d entries" % (N + 1))
+    if max_depth is None:
+        d = np.zeros(N + 1, np.int64)
+        for n in range(1, N + 1):
+            d[n] = d[par[n]] + 1 if 0 <= par[n] < n else 0
+        max_depth = int(d.max())
+    _need(node_tokens, "node_tokens", torch.int32, (B, N), dev)
+    D1 = max_depth + 1
+    if out_path is None:
+        out_path = torch.empty((B, D1), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, D1), dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    sh = _stream_handle(dev, stream)
+    nbytes = workspace_bytes(B, N + 1, V, code)
+    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes)
+    rc = lib.spec_verify_tree(_ptr(z), code, _ptr(node_tokens), par.ctypes.data, B, N, V, int(max_depth),
+                              _ptr(out_path), _ptr(out_tokens), _ptr(out_len), _ptr(status), _ptr(ws),
+                              ws.numel(), sh)
+    _check("spec_verify_tree", rc)
+    return out_path, out_tokens, out_len
+
+
+def fixup_slots(slot_mapping, num_accepted=None, path=None, padding_slot_id: int = PADDING_SLOT_ID,
+                stream=None):
+    """In-place slot_mapping fix-up ([B, P] int64 CUDA).  Chain mode with
+    num_accepted [B] int32, or tree mode with path [B, D+1] int32."""
+    torch = _torch()
+    lib = load_library()
+    if slot_mapping.dtype != torch.int64 or slot_mapping.dim() != 2 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous [B, P] int64 tensor")
+    B, P = slot_mapping.shape
+    dev = slot_mapping.device
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    if path is not None:
+        if path.dtype != torch.int32 or path.dim() != 2 or path.shape[0] != B or not path.is_contiguous():
+            raise ValueError("path must be a contiguous [B, D+1] int32 tensor")
+    stride = 0 if path is None else path.shape[1]
+    rc = lib.spec_fixup_slots(_ptr(slot_mapping), B, P, _ptr(num_accepted), _ptr(path), stride,
+                              int(padding_slot_id), _stream_handle(dev, stream))
+    _check("spec_fixup_slots", rc)
+    return slot_mapping
+
+
+def tree_from_choices(tree_choices: Sequence[Sequence[int]]) -> dict:
+    """tree_choices (level-ordered tuples) -> parent[], cu/child drafts per level, depth."""
+    import numpy as np
+    lib = load_library()
+    n = len(tree_choices)
+    lens = np.asarray([len(t) for t in tree_choices], dtype=np.int32)
+    flat = np.asarray([v for t in tree_choices for v in t] or [0], dtype=np.int32)
+    parent = np.zeros(n + 1, dtype=np.int32)
+    cu = np.zeros(MAX_ROWS, dtype=np.int32)
+    child = np.zeros(MAX_ROWS, dtype=np.int32)
+    depth = ctypes.c_int(0)
+    rc = lib.spec_tree_from_choices(flat.ctypes.data, lens.ctypes.data, n, parent.ctypes.data,
+                                    cu.ctypes.data, child.ctypes.data, ctypes.byref(depth))
+    _check("spec_tree_from_choices", rc)
+    d = depth.value
+    return dict(parent=parent, cu_drafts_per_level=cu[:d].tolist(),
+                child_drafts_per_level=child[:d].tolist(), depth=d)
