@@ -70,10 +70,16 @@ typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype_t;
 
 /* Workspace bytes needed by spec_verify_chain / spec_verify_tree for B requests
  * of `rows` logits rows (k+1 or N+1) over vocabulary V.  The workspace is
- * device memory owned by the caller; it must be zero-filled before its first
- * use (spec_workspace_init) and every completed call leaves it zero-filled
- * again, except the 64-byte counter block at offset 0 (see below).  One
- * workspace must not be used by two calls that can run at the same time.
+ * device memory owned by the caller, 16-byte aligned.  It must be zero-filled
+ * (spec_workspace_init) before its first use and before any call whose
+ * (B, rows, V, dtype) differs from the previous call on it: its counter
+ * region sits at offsets that depend on those sizes.  Every completed call
+ * leaves the counter region of its own layout zero again, so repeated calls
+ * (or CUDA-graph replays) with the same sizes need no re-initialisation.
+ * Bytes [0, 64) hold eight uint64 diagnostic counters the kernel only adds to
+ * (A-row chunks loaded, A chunks skipped, residual chunks loaded, residual
+ * chunks skipped, bytes streamed, 3 reserved).  One workspace must not be
+ * used by two calls that can run at the same time.
  * Returns 0 for invalid sizes. */
 size_t spec_workspace_bytes(int B, int rows, int V, spec_dtype_t dtype);
 

@@ -132,22 +132,30 @@ def workspace_bytes(B: int, rows: int, V: int, dtype_code: int = SPEC_BF16) -> i
     return int(n)
 
 
-def _workspace(device, stream_handle: int, nbytes: int):
-    """Zero-filled device workspace kept per (device, stream); grows on demand."""
+def _workspace(device, stream_handle: int, nbytes: int, layout: tuple):
+    """Device workspace kept per (device, stream).  The library leaves its
+    counters zero after every call for the same layout; a workspace that is
+    new, grown, or last used with a different (B, rows, V, dtype) is
+    zero-filled first, on the call's stream."""
     torch = _torch()
     key = (device.index, stream_handle)
-    ws = _workspaces.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
-        _workspaces[key] = ws
-    return ws
+    ent = _workspaces.get(key)
+    if ent is None or ent[0].numel() < nbytes:
+        ent = [torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device), layout]
+        _workspaces[key] = ent
+    elif ent[1] != layout:
+        _check("spec_workspace_init", load_library().spec_workspace_init(ent[0].data_ptr(), ent[0].numel(),
+                                                                       stream_handle))
+        ent[1] = layout
+    return ent[0]
 
 
 def workspace_for(device=None, stream=None):
     """The cached workspace tensor used for calls on (device, stream), or None."""
     torch = _torch()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    return _workspaces.get((device.index, _stream_handle(device, stream)))
+    ent = _workspaces.get((device.index, _stream_handle(device, stream)))
+    return None if ent is None else ent[0]
 
 
 def workspace_counters(ws) -> dict:
@@ -166,6 +174,10 @@ def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u
                  draft_probs=None, *, out_tokens=None, out_num_accepted=None, status=None,
                  workspace=None, stream=None) -> Tuple[object, object]:
     """Chain verify-and-accept on the GPU.
+
+    A caller-supplied ``workspace`` (uint8 CUDA tensor of at least
+    workspace_bytes(B, k+1, V) bytes) must be zero-filled before its first use
+    and again whenever it is reused for a different (B, k, V, dtype).
 
     target_logits [B, k+1, V] bf16/fp32 CUDA; draft_tokens [B, k] int32.
     Sampled requests (temperature > 0) also need draft_probs [B, k, V] fp32,
@@ -198,7 +210,7 @@ def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u
     _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
     sh = _stream_handle(dev, stream)
     nbytes = workspace_bytes(B, k + 1, V, code)
-    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes)
+    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes, ("chain", B, k + 1, V, code))
     rc = lib.spec_verify_chain(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperature),
                                _ptr(u_accept), _ptr(u_sample), B, k, V, _ptr(out_tokens),
                                _ptr(out_num_accepted), _ptr(status), _ptr(ws), ws.numel(), sh)
@@ -245,7 +257,7 @@ def verify_tree(target_logits, node_tokens, parent: Sequence[int], max_depth: Op
         out_len = torch.empty((B,), dtype=torch.int32, device=dev)
     sh = _stream_handle(dev, stream)
     nbytes = workspace_bytes(B, N + 1, V, code)
-    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes)
+    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes, ("tree", B, N + 1, V, code))
     rc = lib.spec_verify_tree(_ptr(z), code, _ptr(node_tokens), par.ctypes.data, B, N, V, int(max_depth),
                               _ptr(out_path), _ptr(out_tokens), _ptr(out_len), _ptr(status), _ptr(ws),
                               ws.numel(), sh)

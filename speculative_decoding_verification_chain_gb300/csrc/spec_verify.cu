@@ -488,7 +488,7 @@ __device__ int sample_row(const Params &P, int b, int row, bool residual, double
 // Warp 0: decode unit u and decide whether it must be loaded.
 __device__ void decode_unit(const Params &P, int u, Unit &U, int lane) {
     U.kind = kEnd;
-    if (u >= P.units_total) return;
+    if (u < 0 || u >= P.units_total) return;
     if (u < P.units_a) {
         const int per_node = P.B * P.nca;
         int n = u / per_node;
@@ -538,9 +538,10 @@ __device__ void decode_unit(const Params &P, int u, Unit &U, int lane) {
     uint32_t st = ld_acquire(P.req_state + b);
     U.kind = kBWait;
     if (st & kDecided) {
-        if (st & kNeedsResidual) {
+        const int a = static_cast<int>(st & kIdxMask);
+        if ((st & kNeedsResidual) && a < P.R - 1) {
             U.kind = kBLoad;
-            U.n = static_cast<int>(st & kIdxMask);
+            U.n = a;
         } else {
             U.kind = kBSkip;
         }
@@ -642,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_consta
                 if (!(st & kDecided)) {
                     set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
                     U.kind = kBSkip;
-                } else if (st & kNeedsResidual) {
+                } else if ((st & kNeedsResidual) && static_cast<int>(st & kIdxMask) < P.R - 1) {
                     U.kind = kBLoad;
                     U.n = static_cast<int>(st & kIdxMask);
                 } else {
