@@ -176,6 +176,42 @@ spec_status_t spec_tree_from_choices(const int32_t *flat, const int32_t *lens, i
                                      int32_t *parent, int32_t *cu_per_level,
                                      int32_t *child_per_level, int *depth);
 
+/*
+ * spec_verify_chain_noalloc -- spec_verify_chain for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this is a
+ * deployment convenience, not part of the method.)
+ *
+ * Who needs it: code that owns no device allocator and so cannot create the
+ * workspace spec_verify_chain asks for -- for example a plugin inside a serving
+ * runtime whose device memory is entirely owned and budgeted by the runtime's
+ * own allocator, or a C caller that is handed only device pointers to its
+ * inputs and outputs.  Such callers pass inputs and outputs exactly as for
+ * spec_verify_chain (same meaning, layout and checks), and the library uses a
+ * fixed scratch array of spec_noalloc_scratch_bytes() (16 MiB) that it
+ * reserves in its device module: every GPU on which the library is loaded
+ * holds that array until the process exits.  The entry point itself calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - Sizes whose workspace would exceed the scratch (see spec_workspace_bytes)
+ *    are rejected with SPEC_ERR_INVALID_ARG before any device work.
+ *  - The first call on a device does one-time set-up with that device current
+ *    (it looks up the scratch's device address and configures the kernels);
+ *    make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents:
+ *    each call clears the counters it needs (an async memset on `stream`), and
+ *    calls that can overlap on the GPU (other streams, other threads) race on
+ *    the scratch and must be serialised by the caller.
+ */
+spec_status_t spec_verify_chain_noalloc(const void *target_logits, spec_dtype_t dtype,
+                                        const float *draft_probs, const int32_t *draft_tokens,
+                                        const float *temperature, const float *u_accept,
+                                        const float *u_sample, int B, int k, int V,
+                                        int32_t *out_tokens, int32_t *out_num_accepted,
+                                        int32_t *d_status, void *stream);
+
+/* Bytes of the fixed scratch used by spec_verify_chain_noalloc. */
+size_t spec_noalloc_scratch_bytes(void);
+
 /* Text of the last error recorded on the calling thread ("" if none). */
 const char *spec_last_error(void);
 

@@ -23,7 +23,7 @@ from typing import Optional, Sequence, Tuple
 
 __all__ = ["verify_chain", "verify_tree", "fixup_slots", "tree_from_choices", "workspace_bytes",
            "SpecError", "PADDING_SLOT_ID", "STATUS_TOKEN_RANGE", "STATUS_NONFINITE",
-           "STATUS_WAIT_TIMEOUT", "library_path", "load_library"]
+           "STATUS_WAIT_TIMEOUT", "library_path", "load_library", "verify_chain_noalloc"]
 
 PADDING_SLOT_ID = -1
 SPEC_BF16, SPEC_FP32 = 0, 1
@@ -75,6 +75,10 @@ def load_library():
         lib.spec_fixup_slots.restype = I
         lib.spec_tree_from_choices.argtypes = [P, P, I, P, P, P, P]
         lib.spec_tree_from_choices.restype = I
+        lib.spec_verify_chain_noalloc.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, P]
+        lib.spec_verify_chain_noalloc.restype = I
+        lib.spec_noalloc_scratch_bytes.argtypes = []
+        lib.spec_noalloc_scratch_bytes.restype = Z
         lib.spec_last_error.argtypes = []
         lib.spec_last_error.restype = ctypes.c_char_p
         _lib = lib
@@ -303,3 +307,36 @@ def tree_from_choices(tree_choices: Sequence[Sequence[int]]) -> dict:
     d = depth.value
     return dict(parent=parent, cu_drafts_per_level=cu[:d].tolist(),
                 child_drafts_per_level=child[:d].tolist(), depth=d)
+
+
+def verify_chain_noalloc(target_logits, draft_tokens, temperature=None, u_accept=None, u_sample=None,
+                         draft_probs=None, *, out_tokens=None, out_num_accepted=None, status=None, stream=None):
+    """verify_chain without a workspace, for callers that cannot allocate device
+    memory: the library uses its own fixed 16 MiB device scratch, shared by all
+    calls (serialise calls that could overlap on the GPU).  Same arguments and
+    results as verify_chain; larger sizes raise SpecError."""
+    torch = _torch()
+    lib = load_library()
+    z = target_logits
+    if z.dim() != 3 or z.device.type != "cuda" or not z.is_contiguous():
+        raise ValueError("target_logits must be a contiguous [B, k+1, V] CUDA tensor")
+    B, k1, V = z.shape
+    k = k1 - 1
+    dev = z.device
+    code = _dtype_code(z)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(u_accept, "u_accept", torch.float32, (B, k), dev)
+    _need(u_sample, "u_sample", torch.float32, (B, k + 1), dev)
+    _need(draft_probs, "draft_probs", torch.float32, (B, k, V), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    rc = lib.spec_verify_chain_noalloc(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperature),
+                                       _ptr(u_accept), _ptr(u_sample), B, k, V, _ptr(out_tokens),
+                                       _ptr(out_num_accepted), _ptr(status), _stream_handle(dev, stream))
+    _check("spec_verify_chain_noalloc", rc)
+    return out_tokens, out_num_accepted

@@ -1040,6 +1040,7 @@ struct DeviceInfo {
     int sms = 0;
     int ok = 0;
     int blocks_per_sm[2] = {0, 0};
+    uint8_t *noalloc_scratch = nullptr;   // device address of g_noalloc_scratch on this device
 };
 
 std::mutex g_mu;
@@ -1124,6 +1125,33 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
         verify_kernel<4><<<static_cast<unsigned>(grid), kThreads, kStageBytes, st>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+// ------------------------------------------------------ no-alloc scratch --
+// Scratch of spec_verify_chain_noalloc: a fixed device array that exists on
+// every GPU on which the library's module is loaded, until the process exits.
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;   // 16 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Host code may not use g_noalloc_scratch's name as a pointer (it is a host-side
+// stand-in); the device address is looked up once per device, with that
+// device current, and cached.
+spec_status_t noalloc_scratch_ptr(uint8_t *&out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(SPEC_ERR_UNSUPPORTED, "device index out of range%s");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &D = g_dev[dev];
+    if (!D.noalloc_scratch) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(SPEC_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch): %s", cudaGetErrorString(e));
+        D.noalloc_scratch = static_cast<uint8_t *>(p);
+    }
+    out = D.noalloc_scratch;
     return SPEC_OK;
 }
 
@@ -1291,3 +1319,58 @@ extern "C" spec_status_t spec_tree_from_choices(const int32_t *flat, const int32
 }
 
 extern "C" const char *spec_last_error(void) { return g_err; }
+
+extern "C" size_t spec_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" spec_status_t spec_verify_chain_noalloc(const void *target_logits, spec_dtype_t dtype,
+                                                   const float *draft_probs, const int32_t *draft_tokens,
+                                                   const float *temperature, const float *u_accept,
+                                                   const float *u_sample, int B, int k, int V,
+                                                   int32_t *out_tokens, int32_t *out_num_accepted,
+                                                   int32_t *d_status, void *stream) {
+    g_err[0] = 0;
+    if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype%s");
+    if (B < 1 || k < 1 || k > kMaxRows - 1 || V < 1 || V >= (1 << 30))
+        return fail(SPEC_ERR_INVALID_ARG, "sizes out of range (1<=B, 1<=k<=255, 1<=V<2^30)%s");
+    if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted)
+        return fail(SPEC_ERR_INVALID_ARG, "a required pointer is NULL%s");
+    const bool sampled = draft_probs || u_accept || u_sample || temperature;
+    if (sampled && (!draft_probs || !u_accept || !u_sample || !temperature))
+        return fail(SPEC_ERR_INVALID_ARG,
+                    "draft_probs, temperature, u_accept and u_sample must be all given or all NULL%s");
+    if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
+        return fail(SPEC_ERR_INVALID_ARG, "target_logits and draft_probs must be 16-byte aligned%s");
+    Layout L;
+    if (!make_layout(B, k + 1, V, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
+    if (L.total > kNoAllocScratchBytes) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "these sizes need %zu bytes of scratch; the static scratch holds %zu bytes",
+                 L.total, kNoAllocScratchBytes);
+        return fail(SPEC_ERR_INVALID_ARG, "%s (use spec_verify_chain with a workspace)", buf);
+    }
+    uint8_t *scratch = nullptr;
+    spec_status_t s = noalloc_scratch_ptr(scratch);
+    if (s != SPEC_OK) return s;
+    // The scratch keeps whatever the previous call left; only this layout's
+    // counter region has to start at zero.
+    cudaError_t e = cudaMemsetAsync(scratch + L.reset, 0, L.reset_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "clearing the no-alloc scratch: %s", cudaGetErrorString(e));
+    Params P;
+    memset(&P, 0, sizeof P);
+    P.logits = static_cast<const uint8_t *>(target_logits);
+    P.q = draft_probs;
+    P.tokens = draft_tokens;
+    P.temperature = temperature;
+    P.u_accept = u_accept;
+    P.u_sample = u_sample;
+    P.out_tokens = out_tokens;
+    P.out_count = out_num_accepted;
+    P.out_path = nullptr;
+    P.status = d_status;
+    P.B = B;
+    P.R = k + 1;
+    P.V = V;
+    P.D = k;
+    P.tree = 0;
+    return launch_verify(P, dtype, scratch, kNoAllocScratchBytes, stream);
+}
