@@ -1,43 +1,46 @@
 // spec_verify.cu -- GB300 (sm_103a) verify-and-accept for speculative decoding.
 //
-// One persistent kernel verifies chains (greedy or sampled, per request) and
-// greedy token trees.  A chain is handled as a tree whose node n has parent
-// n-1, so both share one scheduler:
+// One persistent kernel (one block per SM) verifies chains (greedy or sampled,
+// per request) and greedy token trees.  A chain is handled as a tree whose
+// node n has parent n-1, so both share one scheduler.
 //
-//   * Work is cut into units.  An "A unit" is one chunk of one logits row of
-//     one request; a "B unit" is one chunk of the rejected row of a sampled
-//     request (residual pass).  Units are numbered row-major over
-//     (node, request, chunk) so that every row's chunks are claimed together
-//     and a parent row is claimed long before its children.
-//   * Each block claims units with one global atomic, checks whether the row
-//     is still needed (a row is needed only if its node can still be
-//     accepted: every ancestor edge either unresolved or matching), streams
-//     the chunk into shared memory with one bulk-async copy (cp.async.bulk
-//     completing on an mbarrier) and reduces it: argmax (greedy) or max and
-//     sum of exp2 (sampled) plus 256-element block sums for the inverse CDF.
-//   * The last unit of a row (arrival counter) combines the chunk partials
-//     and resolves the row: its argmax, or its softmax statistics and the
-//     accept test min(1, p/q) of the one child.  The last unit of a request
-//     walks the tree, picks the deepest accepted node and writes the outputs;
-//     a sampled request rejected at row a then releases its B units, whose
-//     last one locates u * (residual mass) in the block sums and scans one
-//     256-element block for the token.  No row of the residual max(0, p - q)
-//     is ever written to memory.
-//   * Rows of a node that is already known to be rejected are skipped without
-//     being read, so the logits actually streamed approach the bytes the
-//     method needs (rows up to the first rejection).
+// Work.  An "A unit" is one split of one logits row of one request (a whole
+// row, or a few adjacent 16 KiB sub-chunks of it when the batch is too small
+// to fill the GPU with whole rows); a "B unit" is a 16384-element chunk of the
+// rejected row of a sampled request (residual pass).  Units are numbered
+// (node, request, split)-major, so a parent row is claimed long before its
+// children; B units come after every A unit.
 //
-// Every inter-block wait is bounded by a wall-clock limit and reports
+// Roles inside a block:
+//   * warp 0, producer: claims units with one global atomic (one claim ahead),
+//     drops a row whose node is already known to be rejected (some ancestor
+//     edge resolved and failed) without reading it, and streams the rest into
+//     a ring of shared-memory stages with cp.async.bulk copies that complete
+//     on per-stage mbarriers;
+//   * warps 2..9, consumers: reduce each 16 KiB stage -- running argmax
+//     (greedy) or, per 256-element block, the block max M and
+//     sum 2^((z - M) log2(e)/T) (sampled), or the residual block sums of
+//     max(0, p - q) (B units) -- and hand each finished unit to the epilogue;
+//   * warp 1, epilogue: combines a unit's partials; the last split of a row
+//     resolves it (its argmax, or its softmax statistics and the accept test
+//     min(1, p/q) of its one child); the last row of a request walks the
+//     tree, picks the deepest accepted node and writes the outputs; a sampled
+//     request rejected at row a then releases its B units, whose last one
+//     locates u * (residual mass) in the block sums and scans one
+//     256-element block for the token.  The residual is never written out.
+//
+// Every wait is bounded by a wall-clock limit and reports
 // SPEC_STATUS_WAIT_TIMEOUT instead of hanging.  The last block to exit clears
 // the workspace counters, so the next call (or graph replay) starts clean.
 //
-// Arithmetic: logits are widened to fp32 exactly; exponentials use the
-// hardware ex2 approximation on (z - max) * log2(e)/T; chunk combinations
-// and the inverse-CDF prefix across blocks are in fp64.
+// Arithmetic: logits are widened to fp32 exactly; exponentials use the SFU
+// ex2 approximation on (z - M) * log2(e)/T with M a block max; row statistics
+// and the inverse-CDF prefix across blocks are combined in fp64.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -47,32 +50,37 @@
 namespace sv {
 
 // ---------------------------------------------------------------- config --
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kBlk = 256;                 // canonical block: 32 lanes x 8 elements
-constexpr int kChunkA = 8192;             // elements per A unit (row chunk)
-constexpr int kChunkB = 4096;             // elements per B unit (residual chunk)
-constexpr int kQOff = 16384 + 64;         // q area offset inside a stage (B units)
-constexpr int kStageBytes = 32768 + 128;  // z chunk (<= 32 KiB) or z + q of a B unit
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (2 + kConsumerWarps);   // producer, epilogue, consumers
+constexpr int kStages = 12;
+constexpr int kSubBytes = 16384;                       // logits bytes per A stage
+constexpr int kStageBytes = kSubBytes + 128;
+constexpr int kQOff = 8192 + 64;                        // q area of a B stage
+constexpr int kSubB = 2048;                             // elements per B stage
+constexpr int kSubPerB = 8;                             // B stages per B unit
+constexpr int kChunkB = kSubB * kSubPerB;               // elements per B unit
+constexpr int kResSlots = 4;
+constexpr int kBlk = 256;                               // canonical block: 32 lanes x 8 elements
 constexpr int kMaxRows = SPEC_MAX_ROWS;
 constexpr uint32_t kResolved = 0x80000000u;
 constexpr uint32_t kIdxMask = 0x3fffffffu;
 constexpr uint32_t kDecided = 0x80000000u;
 constexpr uint32_t kNeedsResidual = 0x40000000u;
+constexpr uint32_t kSkipInc = 0x10000u;                 // split counter: skipped splits count here
 constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s
+constexpr float kLog2e = 1.4426950408889634f;
 
-enum UnitKind : int { kEnd = 0, kALoad = 1, kASkip = 2, kBLoad = 3, kBSkip = 4, kBWait = 5 };
+enum Kind : int { kEnd = 0, kA = 1, kB = 2 };
 
 struct RowStat {
     float m;      // row max of raw logits
     float pad;
-    double S;     // sum_j exp2((z_j - m) * c2)
+    double S;     // sum_j 2^((z_j - m) * c2)
 };
 
-struct Partial {
-    float v;      // chunk max
-    int32_t idx;  // argmax (row index), greedy only
-    double s;     // sum of exp2((z - v) * c2) over the chunk, sampled only
+struct Partial {  // greedy split result
+    float v;
+    int32_t idx;
 };
 
 struct Params {
@@ -89,40 +97,67 @@ struct Params {
     // workspace
     unsigned long long *stats;   // [8], never cleared by the kernel
     uint32_t *ctrl;              // [32]: 0 claim counter, 1 exit counter
-    uint32_t *row_done;          // [B*R]
+    uint32_t *row_ctr;           // [B*R] split arrival counters
     uint32_t *rowstate;          // [B*R]
-    uint32_t *req_done;          // [B]
-    uint32_t *req_state;         // [B]
-    uint32_t *res_done;          // [B]
+    uint32_t *req_ctr;           // [B] settled rows
+    uint32_t *req_state;         // [B] decision
+    uint32_t *res_ctr;           // [B] residual units done
     uint32_t *reset_base;
     uint32_t reset_words;
     RowStat *rowstat;            // [B*R]
-    Partial *partial;            // [B*R*nca]
-    float *bsumA;                // [B*R*nblk]
-    float *bsumB;                // [B*nblk]
-    unsigned long long logits_end;  // one past the last logits byte (address)
+    Partial *partial;            // [B*R*nsub]
+    float *bmaxA;                // [B*R*nblk] block maxima (sampled rows)
+    float *bsumA;                // [B*R*nblk] block sums of 2^((z - M) c2)
+    float *bsumB;                // [B*nblk]   residual block sums
+    unsigned long long logits_end;
     unsigned long long q_end;
     int B, R, V, D;
     int esize;
-    int nca, ncb, nblk;
+    int esub;                    // elements per A stage (16 KiB of logits)
+    int nsub;                    // A stages per row
+    int ns;                      // splits per row
+    int sps;                     // A stages per split
+    int ncb, nblk;
     int units_a, units_total;
     int tree;
     int16_t parent[kMaxRows];
     uint8_t depth[kMaxRows];
 };
 
-struct Unit {
+struct StageInfo {
     int kind;
-    int b, n, c;
-    int cnt;            // elements in this chunk
-    int sh, tail;       // z: byte shift of element 0 in the stage, elements [tail,cnt) from global
-    int shq, tailq;     // q (B units)
-    uint32_t bytes;     // bulk bytes expected on the stage barrier
-    float c2;           // log2(e) / T, or 0 for greedy
-    float m;            // row max (B units)
-    float invS;         // 1 / S (B units)
-    const uint8_t *gz;  // global address of element 0 of the z chunk
-    const uint8_t *gq;  // global address of element 0 of the q chunk
+    int last;            // last stage of its unit
+    int b, n, j;         // request, row, split (A) / chunk (B)
+    int e0, cnt;         // element offset within the row, element count
+    int sh, tail;        // z: byte shift of element 0; elements [tail, cnt) come from global
+    int shq, tailq;      // q (B)
+    float c2;            // log2(e)/T, 0 for greedy
+    float m, invS;       // row statistics (B)
+    const uint8_t *gz;
+    const uint8_t *gq;
+};
+
+struct ResSlot {
+    int kind, b, n, j;
+    float c2;
+    float v[kConsumerWarps];
+    int idx[kConsumerWarps];
+};
+
+struct Smem {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t res_full[kResSlots];
+    uint64_t res_empty[kResSlots];
+    StageInfo info[kStages];
+    ResSlot res[kResSlots];
+    uint32_t fin_rs[2][kMaxRows];   // request finalisation scratch, per finalising warp
+    int fin_tok[2][kMaxRows];
+    uint8_t fin_acc[2][kMaxRows];
+    int abort_flag;
+    int issued;                     // stages issued by the producer
+    int consumed;                   // stages released by the consumers
+    int last_flag;
 };
 
 // ------------------------------------------------------- ptx wrappers --
@@ -134,19 +169,23 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(phase)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -169,6 +208,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -185,7 +230,7 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
-// 2^x by the SFU approximation (flushes results below 2^-126 to zero).
+// 2^x by the SFU approximation (results below 2^-126 flush to zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -196,9 +241,25 @@ __device__ __forceinline__ void set_status(const Params &P, int bits) {
     if (P.status) atomicOr(P.status, bits);
 }
 
+// Bounded wait on an mbarrier phase; gives up (and raises the block's abort
+// flag) after kWaitLimitNs or as soon as another role has aborted.
+__device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*reinterpret_cast<volatile int *>(&S.abort_flag)) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *reinterpret_cast<volatile int *>(&S.abort_flag) = 1;
+            set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------------ weights --
-// The two per-element weights of the inverse CDF.  Written with explicit
-// rounding intrinsics so every call site evaluates them bit-identically.
+// Per-element weights of the inverse CDF, written with explicit rounding
+// intrinsics so every call site evaluates them bit-identically.
 __device__ __forceinline__ float w_exp(float z, float M, float c2) {
     return ex2(__fmul_rn(__fsub_rn(z, M), c2));
 }
@@ -219,7 +280,7 @@ __device__ __forceinline__ uint32_t nonfinite_f32(uint32_t w) {
     return (w & 0x7f800000u) == 0x7f800000u;
 }
 
-// Element view of one chunk: elements [0, tail) live in shared memory at s,
+// Element view of one stage: elements [0, tail) live in shared memory at s,
 // elements [tail, cnt) are read from global memory at g.
 struct View {
     const uint8_t *s;
@@ -243,7 +304,7 @@ __device__ __forceinline__ float ld_one(const View &v, int e, uint32_t &bad) {
     }
 }
 
-// Loads the 8 elements [e0, e0+8) of a view; returns how many are valid.
+// Loads elements [e0, e0+8) of a view; returns how many are valid.
 template <int ES>
 __device__ __forceinline__ int load8(const View &v, int e0, float x[8], uint32_t &bad) {
     int nv = v.cnt - e0;
@@ -301,6 +362,12 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
     }
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
 // Canonical block sum: lane partials combined by an xor butterfly; lane 0's
 // value is the block's sum.
 __device__ __forceinline__ float warp_butterfly_sum(float s) {
@@ -326,6 +393,7 @@ __device__ __forceinline__ double warp_incl_scan_d(double s, int lane) {
 
 // ------------------------------------------------------------ topology --
 __device__ __forceinline__ int parent_of(const Params &P, int n) { return P.tree ? P.parent[n] : n - 1; }
+__device__ __forceinline__ int depth_of(const Params &P, int n) { return P.tree ? P.depth[n] : n; }
 
 __device__ __forceinline__ int node_token(const Params &P, int b, int n) {
     return __ldg(P.tokens + static_cast<size_t>(b) * (P.R - 1) + (n - 1));
@@ -337,25 +405,26 @@ __device__ __forceinline__ bool edge_ok(uint32_t rs, bool greedy, int child_toke
     return greedy ? (static_cast<int>(rs & kIdxMask) == child_token) : ((rs & 1u) != 0u);
 }
 
+__device__ __forceinline__ bool is_greedy(const Params &P, int b) {
+    return !P.temperature || !(__ldg(P.temperature + b) > 0.0f);
+}
+
 // ---------------------------------------------------- inverse-CDF search --
-// Block weights for the search: residual blocks (bsumB) or exp blocks of one
-// row scaled by their chunk's factor 2^((M_c - m) c2).
+// Block weights of one row: residual block sums (bmax == null), or exp block
+// sums scaled by 2^((M_beta - m) c2), M_beta the block's own max.
 struct BlockSource {
-    const float *bsum;       // nblk block sums of this row
-    const Partial *part;     // chunk partials of the row (exp mode), or null
-    float m, c2;             // row max and scale (exp mode)
+    const float *bsum;
+    const float *bmax;
+    float m, c2;
 };
 
-__device__ __forceinline__ double chunk_factor(const BlockSource &S, int c) {
-    if (!S.part) return 1.0;
-    float Mc = __ldcg(&S.part[c].v);
-    return static_cast<double>(ex2(__fmul_rn(__fsub_rn(Mc, S.m), S.c2)));
+__device__ __forceinline__ double block_factor(const BlockSource &S, int beta) {
+    if (!S.bmax) return 1.0;
+    return static_cast<double>(ex2(__fmul_rn(__fsub_rn(__ldcg(S.bmax + beta), S.m), S.c2)));
 }
 
 __device__ __forceinline__ double block_weight(const BlockSource &S, int beta) {
-    double w = static_cast<double>(__ldcg(S.bsum + beta));
-    if (S.part) w *= chunk_factor(S, beta / (kChunkA / kBlk));
-    return w;
+    return static_cast<double>(__ldcg(S.bsum + beta)) * block_factor(S, beta);
 }
 
 // Warp-wide: total weight and the block holding t = u * total.  Returns the
@@ -405,29 +474,25 @@ __device__ double locate_block(const BlockSource &S, int nblk, double u, int lan
 }
 
 // Warp-wide scan inside block beta of row (b, row): the first element whose
-// running weight exceeds t.  mode 0: exp weights relative to the chunk max,
-// scaled by the chunk factor; mode 1: residual weights.
-__device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, double base,
-                          double t, int mode, float m, float invS, int lane) {
+// running weight exceeds t.  residual == false: exp weights relative to the
+// block max, scaled by the block factor; residual == true: max(0, p - q).
+__device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, double base, double t,
+                          bool residual, float invS, int lane) {
     const size_t rowz = (static_cast<size_t>(b) * P.R + row) * static_cast<size_t>(P.V);
     const int e0 = beta * kBlk + lane * 8;
     float w[8];
     float s = 0.0f;
-    float Mc = 0.0f;
-    double fac = 1.0;
-    if (mode == 0) {
-        int c = beta / (kChunkA / kBlk);
-        Mc = __ldcg(&S.part[c].v);
-        fac = chunk_factor(S, c);
-    }
-    const float *qrow = (mode == 1) ? P.q + (static_cast<size_t>(b) * (P.R - 1) + row) * static_cast<size_t>(P.V) : nullptr;
+    float Mb = residual ? 0.0f : __ldcg(S.bmax + beta);
+    double fac = residual ? 1.0 : block_factor(S, beta);
+    const float *qrow =
+        residual ? P.q + (static_cast<size_t>(b) * (P.R - 1) + row) * static_cast<size_t>(P.V) : nullptr;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         int e = e0 + i;
         float wi = 0.0f;
         if (e < P.V) {
             float z = logit_global(P, rowz + e);
-            wi = (mode == 0) ? w_exp(z, Mc, S.c2) : w_res(z, __ldg(qrow + e), m, S.c2, invS);
+            wi = residual ? w_res(z, __ldg(qrow + e), S.m, S.c2, invS) : w_exp(z, Mb, S.c2);
         }
         w[i] = wi;
         s = __fadd_rn(s, wi);
@@ -459,505 +524,609 @@ __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row,
     return j;
 }
 
-// Sample one token from row `row` of request b: residual weights (bsumB) if
-// `residual`, else p itself (exp block sums of that row).  Warp-wide.
+// Sample one token from row `row` of request b (warp-wide): residual weights
+// if `residual` (falling back to p when the residual has no mass), else p.
 __device__ int sample_row(const Params &P, int b, int row, bool residual, double u, int lane) {
-    RowStat rs;
-    rs.m = __ldcg(&P.rowstat[static_cast<size_t>(b) * P.R + row].m);
-    rs.S = __ldcg(&P.rowstat[static_cast<size_t>(b) * P.R + row].S);
-    const float T = P.temperature[b];
-    const float c2 = 1.4426950408889634f / T;
+    const size_t ri = static_cast<size_t>(b) * P.R + row;
+    const float m = __ldcg(&P.rowstat[ri].m);
+    const double Srow = __ldcg(&P.rowstat[ri].S);
+    const float c2 = kLog2e / __ldg(P.temperature + b);
     int beta;
     double base;
     if (residual) {
-        BlockSource S{P.bsumB + static_cast<size_t>(b) * P.nblk, nullptr, rs.m, c2};
+        BlockSource S{P.bsumB + static_cast<size_t>(b) * P.nblk, nullptr, m, c2};
         double Z = locate_block(S, P.nblk, u, lane, beta, base);
         if (Z > 0.0) {
-            float invS = static_cast<float>(1.0 / rs.S);
-            return scan_block(P, S, b, row, beta, base, u * Z, 1, rs.m, invS, lane);
+            float invS = static_cast<float>(1.0 / Srow);
+            return scan_block(P, S, b, row, beta, base, u * Z, true, invS, lane);
         }
-        // zero residual mass: sample from p of the same row
     }
-    const size_t rowi = static_cast<size_t>(b) * P.R + row;
-    BlockSource S{P.bsumA + rowi * P.nblk, P.partial + rowi * P.nca, rs.m, c2};
+    BlockSource S{P.bsumA + ri * P.nblk, P.bmaxA + ri * P.nblk, m, c2};
     double tot = locate_block(S, P.nblk, u, lane, beta, base);
-    return scan_block(P, S, b, row, beta, base, u * tot, 0, rs.m, 0.0f, lane);
+    return scan_block(P, S, b, row, beta, base, u * tot, false, 0.0f, lane);
 }
 
-// ------------------------------------------------------- unit decoding --
-// Warp 0: decode unit u and decide whether it must be loaded.
-__device__ void decode_unit(const Params &P, int u, Unit &U, int lane) {
-    U.kind = kEnd;
-    if (u < 0 || u >= P.units_total) return;
-    if (u < P.units_a) {
-        const int per_node = P.B * P.nca;
-        int n = u / per_node;
-        int rem = u - n * per_node;
-        int b = rem / P.nca;
-        int c = rem - b * P.nca;
-        float T = P.temperature ? __ldg(P.temperature + b) : 0.0f;
-        bool greedy = !(T > 0.0f);
-        // Is node n already known to be rejected?  Lane i checks the i-th
-        // edge on the path from n up to the root.
-        bool dead = false;
-        if (n > 0) {
-            int d = P.tree ? P.depth[n] : n;
-            for (int base = 0; base < d && !dead; base += 32) {
-                int i = base + lane;
-                bool bad = false;
-                if (i < d) {
-                    int child = n;
-                    if (P.tree) {
-                        for (int s = 0; s < i; ++s) child = P.parent[child];
+// --------------------------------------------------- request finalisation --
+// Warp-wide.  Every row of request b is settled: walk the tree, write the
+// outputs, publish the decision (and draw the bonus token of a sampled
+// request that accepted every draft).
+__device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int lane) {
+    uint32_t *rs = S.fin_rs[slot];
+    int *tok = S.fin_tok[slot];
+    uint8_t *acc = S.fin_acc[slot];
+    __threadfence();
+    int range_bad = 0;
+    for (int i = lane; i < P.R; i += 32) {
+        rs[i] = ld_relaxed(P.rowstate + static_cast<size_t>(b) * P.R + i);
+        tok[i] = i > 0 ? node_token(P, b, i) : -1;
+        if (i > 0 && (tok[i] < 0 || tok[i] >= P.V)) range_bad = 1;
+    }
+    if (__any_sync(0xffffffffu, range_bad) && lane == 0) set_status(P, SPEC_STATUS_TOKEN_RANGE);
+    __syncwarp();
+    const bool greedy = is_greedy(P, b);
+    int bonus = 0;
+    uint32_t decision = kDecided;
+    if (lane == 0) {
+        acc[0] = 1;
+        int best = 0;
+        for (int i = 1; i < P.R; ++i) {
+            int p = parent_of(P, i);
+            bool ok = acc[p] && edge_ok(rs[p], greedy, tok[i]);
+            acc[i] = ok;
+            if (ok && depth_of(P, i) > depth_of(P, best)) best = i;
+        }
+        const int d = depth_of(P, best);
+        int32_t *ot = P.out_tokens + static_cast<size_t>(b) * (P.D + 1);
+        int32_t *op = P.out_path ? P.out_path + static_cast<size_t>(b) * (P.D + 1) : nullptr;
+        int node = best;
+        for (int i = d; i >= 1; --i) {
+            ot[i - 1] = tok[node];
+            if (op) op[i] = node;
+            node = parent_of(P, node);
+        }
+        if (op) {
+            op[0] = 0;
+            for (int i = d + 1; i <= P.D; ++i) op[i] = -1;
+        }
+        for (int i = d + 1; i <= P.D; ++i) ot[i] = -1;
+        if (greedy) {
+            uint32_t r = rs[best];
+            ot[d] = (r & kResolved) ? static_cast<int>(r & kIdxMask) : 0;
+        } else if (d < P.R - 1) {
+            decision |= kNeedsResidual | static_cast<uint32_t>(d);
+            ot[d] = -1;   // written by the residual pass
+        } else {
+            bonus = 1;
+        }
+        P.out_count[b] = P.tree ? d + 1 : d;
+    }
+    bonus = __shfl_sync(0xffffffffu, bonus, 0);
+    if (bonus) {
+        const int a = P.R - 1;
+        double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + a));
+        int t = sample_row(P, b, a, false, u, lane);
+        if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = t;
+    }
+    if (lane == 0) {
+        __threadfence();
+        st_release(P.req_state + b, decision);
+    }
+    __syncwarp();
+}
+
+// One more row of request b is settled (resolved or known dead).
+__device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) {
+    uint32_t old = 0;
+    if (lane == 0) old = atom_add_acqrel(P.req_ctr + b, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == static_cast<uint32_t>(P.R - 1)) finalize_request(P, S, slot, b, lane);
+}
+
+// Warp-wide: resolve row n of request b from its finished splits.  Greedy:
+// (v, idx) is the whole row's argmax.  Sampled: m and S from the block data,
+// then the accept test of child n+1.
+__device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, int lane) {
+    const size_t ri = static_cast<size_t>(b) * P.R + n;
+    uint32_t rsv;
+    if (greedy) {
+        int g = (gidx < 0 || gidx >= P.V) ? 0 : gidx;
+        rsv = kResolved | static_cast<uint32_t>(g);
+    } else {
+        const float *bm = P.bmaxA + ri * P.nblk;
+        const float *bs = P.bsumA + ri * P.nblk;
+        float m = -INFINITY;
+        for (int i = lane; i < P.nblk; i += 32) m = fmaxf(m, __ldcg(bm + i));
+        m = warp_max(m);
+        double Ssum = 0.0;
+        for (int i = lane; i < P.nblk; i += 32)
+            Ssum += static_cast<double>(__ldcg(bs + i)) *
+                    static_cast<double>(ex2(__fmul_rn(__fsub_rn(__ldcg(bm + i), m), c2)));
+        Ssum = warp_sum_d(Ssum);
+        uint32_t acc = 0;
+        if (lane == 0) {
+            RowStat st;
+            st.m = m;
+            st.pad = 0.0f;
+            st.S = Ssum;
+            P.rowstat[ri] = st;
+            if (n < P.R - 1) {
+                int x = node_token(P, b, n + 1);
+                if (x < 0 || x >= P.V) {
+                    set_status(P, SPEC_STATUS_TOKEN_RANGE);
+                } else {
+                    float zx = logit_global(P, ri * P.V + x);
+                    double ph = static_cast<double>(ex2(__fmul_rn(__fsub_rn(zx, m), c2))) / Ssum;
+                    float qh = __ldg(P.q + (static_cast<size_t>(b) * (P.R - 1) + n) * P.V + x);
+                    if (qh == 0.0f) {
+                        acc = 1;
                     } else {
-                        child = n - i;
+                        double ua = static_cast<double>(__ldg(P.u_accept + static_cast<size_t>(b) * (P.R - 1) + n));
+                        acc = ua < ph / static_cast<double>(qh);
                     }
-                    int par = parent_of(P, child);
-                    uint32_t rs = *reinterpret_cast<volatile const uint32_t *>(P.rowstate + static_cast<size_t>(b) * P.R + par);
-                    if (rs & kResolved) bad = !edge_ok(rs, greedy, node_token(P, b, child));
                 }
-                dead = __any_sync(0xffffffffu, bad);
             }
         }
-        U.b = b;
-        U.n = n;
-        U.c = c;
-        U.c2 = greedy ? 0.0f : 1.4426950408889634f / T;
-        U.kind = dead ? kASkip : kALoad;
-        U.cnt = min(kChunkA, P.V - c * kChunkA);
-        size_t elem = (static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V) + static_cast<size_t>(c) * kChunkA;
-        U.gz = P.logits + elem * P.esize;
-        return;
+        rsv = kResolved | __shfl_sync(0xffffffffu, acc, 0);
     }
-    const int v = u - P.units_a;
-    const int b = v / P.ncb;
-    const int c = v - b * P.ncb;
-    U.b = b;
-    U.c = c;
-    U.cnt = min(kChunkB, P.V - c * kChunkB);
-    uint32_t st = ld_acquire(P.req_state + b);
-    U.kind = kBWait;
-    if (st & kDecided) {
-        const int a = static_cast<int>(st & kIdxMask);
-        if ((st & kNeedsResidual) && a < P.R - 1) {
-            U.kind = kBLoad;
-            U.n = a;
-        } else {
-            U.kind = kBSkip;
+    if (lane == 0) {
+        __threadfence();
+        st_release(P.rowstate + ri, rsv);
+    }
+    __syncwarp();
+}
+
+// --------------------------------------------------------------- roles --
+// Producer (warp 0): is node n of request b already known to be rejected?
+__device__ bool node_dead(const Params &P, int b, int n, bool greedy, int lane) {
+    if (n == 0) return false;
+    const int d = depth_of(P, n);
+    bool dead = false;
+    for (int base = 0; base < d && !dead; base += 32) {
+        int i = base + lane;
+        bool bad = false;
+        if (i < d) {
+            int child = n;
+            if (P.tree) {
+                for (int s = 0; s < i; ++s) child = P.parent[child];
+            } else {
+                child = n - i;
+            }
+            int par = parent_of(P, child);
+            uint32_t rs = ld_relaxed(P.rowstate + static_cast<size_t>(b) * P.R + par);
+            if (rs & kResolved) bad = !edge_ok(rs, greedy, node_token(P, b, child));
         }
+        dead = __any_sync(0xffffffffu, bad);
+    }
+    return dead;
+}
+
+// Copy geometry: 16-byte aligned bulk range covering [g, g + cnt*es), clipped
+// to the tensor's last full 16 bytes; elements past the clip come from global.
+__device__ __forceinline__ void copy_geom(const uint8_t *g, int cnt, int es, unsigned long long end, int &sh,
+                                          int &tail, const uint8_t *&src, uint32_t &nbytes) {
+    unsigned long long a0 = reinterpret_cast<unsigned long long>(g);
+    unsigned long long a1 = a0 + static_cast<unsigned long long>(cnt) * es;
+    unsigned long long lo = a0 & ~15ull;
+    unsigned long long hi = (a1 + 15ull) & ~15ull;
+    unsigned long long lim = end & ~15ull;
+    if (hi > lim) hi = lim;
+    sh = static_cast<int>(a0 - lo);
+    if (hi <= lo) {
+        nbytes = 0;
+        tail = 0;
+    } else {
+        nbytes = static_cast<uint32_t>(hi - lo);
+        long long covered = static_cast<long long>(hi) - static_cast<long long>(a0);
+        tail = covered >= static_cast<long long>(cnt) * es ? cnt : static_cast<int>(covered / es);
+        if (tail < 0) tail = 0;
+    }
+    src = reinterpret_cast<const uint8_t *>(lo);
+}
+
+template <int ES>
+__device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
+    int it = 0;   // stages issued
+    int u_next = 0;
+    if (lane == 0) u_next = static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+    bool aborted = false;
+    unsigned long long loaded_bytes = 0;
+    int a_loaded = 0, a_skipped = 0, b_loaded = 0, b_skipped = 0;
+
+    // Reserve the next stage (wait until the consumers released its previous use).
+    auto acquire_stage = [&](int &st) -> bool {
+        st = it % kStages;
+        if (it >= kStages) {
+            if (!wait_bar(P, S, &S.empty[st], static_cast<uint32_t>((it / kStages - 1) & 1))) return false;
+        }
+        return true;
+    };
+
+    while (!aborted) {
+        int u = __shfl_sync(0xffffffffu, u_next, 0);
+        if (u < 0 || u >= P.units_total) break;
+        if (lane == 0) u_next = static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+        if (u < P.units_a) {
+            // ---------------- A unit: split j of row n of request b
+            const int per_node = P.B * P.ns;
+            const int n = u / per_node;
+            const int rem = u - n * per_node;
+            const int b = rem / P.ns;
+            const int j = rem - b * P.ns;
+            const bool greedy = is_greedy(P, b);
+            const float c2 = greedy ? 0.0f : kLog2e / __ldg(P.temperature + b);
+            const int s0 = j * P.sps;
+            const int s1 = min(P.nsub, s0 + P.sps);
+            if (node_dead(P, b, n, greedy, lane)) {
+                ++a_skipped;
+                if (P.ns == 1) {
+                    settle_row(P, S, 0, b, lane);
+                } else {
+                    uint32_t old = 0;
+                    if (lane == 0) old = atom_add_acqrel(P.row_ctr + static_cast<size_t>(b) * P.R + n, kSkipInc);
+                    old = __shfl_sync(0xffffffffu, old, 0) + kSkipInc;
+                    if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) settle_row(P, S, 0, b, lane);
+                }
+                continue;
+            }
+            ++a_loaded;
+            const size_t rowe = (static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V);
+            for (int s = s0; s < s1; ++s) {
+                int st;
+                if (!acquire_stage(st)) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0) {
+                    StageInfo &I = S.info[st];
+                    I.kind = kA;
+                    I.last = (s == s1 - 1);
+                    I.b = b;
+                    I.n = n;
+                    I.j = j;
+                    I.e0 = s * P.esub;
+                    I.cnt = min(P.esub, P.V - I.e0);
+                    I.c2 = c2;
+                    I.gz = P.logits + (rowe + I.e0) * ES;
+                    const uint8_t *src;
+                    uint32_t nb;
+                    copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
+                    loaded_bytes += nb;
+                    fence_proxy_async();
+                    if (nb) {
+                        mbar_expect_tx(&S.full[st], nb);
+                        bulk_g2s(ring + static_cast<size_t>(st) * kStageBytes, src, nb, &S.full[st]);
+                    } else {
+                        mbar_arrive(&S.full[st]);
+                    }
+                }
+                ++it;
+            }
+        } else {
+            // ---------------- B unit: chunk c of the rejected row of request b
+            const int v = u - P.units_a;
+            const int b = v / P.ncb;
+            const int c = v - b * P.ncb;
+            uint32_t stv = 0;
+            if (lane == 0) {
+                stv = ld_acquire(P.req_state + b);
+                if (!(stv & kDecided)) {
+                    unsigned long long t0 = globaltimer();
+                    while (!(stv & kDecided)) {
+                        if (globaltimer() - t0 > kWaitLimitNs) break;
+                        __nanosleep(200);
+                        stv = ld_acquire(P.req_state + b);
+                    }
+                    if (!(stv & kDecided)) set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
+                }
+            }
+            stv = __shfl_sync(0xffffffffu, stv, 0);
+            const int a = static_cast<int>(stv & kIdxMask);
+            if (!(stv & kDecided) || !(stv & kNeedsResidual) || a >= P.R - 1) {
+                ++b_skipped;
+                continue;
+            }
+            ++b_loaded;
+            const size_t ri = static_cast<size_t>(b) * P.R + a;
+            const float m = __ldcg(&P.rowstat[ri].m);
+            const double Srow = __ldcg(&P.rowstat[ri].S);
+            const float c2 = kLog2e / __ldg(P.temperature + b);
+            const size_t rowe = ri * static_cast<size_t>(P.V);
+            const size_t qrowe = (static_cast<size_t>(b) * (P.R - 1) + a) * static_cast<size_t>(P.V);
+            const int e_begin = c * kChunkB;
+            const int e_end = min(P.V, e_begin + kChunkB);
+            for (int e = e_begin; e < e_end; e += kSubB) {
+                int st;
+                if (!acquire_stage(st)) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0) {
+                    StageInfo &I = S.info[st];
+                    I.kind = kB;
+                    I.last = (e + kSubB >= e_end);
+                    I.b = b;
+                    I.n = a;
+                    I.j = c;
+                    I.e0 = e;
+                    I.cnt = min(kSubB, P.V - e);
+                    I.c2 = c2;
+                    I.m = m;
+                    I.invS = static_cast<float>(1.0 / Srow);
+                    I.gz = P.logits + (rowe + e) * ES;
+                    I.gq = reinterpret_cast<const uint8_t *>(P.q + qrowe + e);
+                    const uint8_t *sz, *sq;
+                    uint32_t nz, nq;
+                    copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, sz, nz);
+                    copy_geom(I.gq, I.cnt, 4, P.q_end, I.shq, I.tailq, sq, nq);
+                    loaded_bytes += nz + nq;
+                    fence_proxy_async();
+                    uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
+                    if (nz + nq) {
+                        mbar_expect_tx(&S.full[st], nz + nq);
+                        if (nz) bulk_g2s(dst, sz, nz, &S.full[st]);
+                        if (nq) bulk_g2s(dst + kQOff, sq, nq, &S.full[st]);
+                    } else {
+                        mbar_arrive(&S.full[st]);
+                    }
+                }
+                ++it;
+            }
+        }
+    }
+    // End marker (not after an abort: the consumers are leaving already).
+    if (!aborted) {
+        int st;
+        if (acquire_stage(st)) {
+            if (lane == 0) {
+                S.info[st].kind = kEnd;
+                mbar_arrive(&S.full[st]);
+            }
+            ++it;
+        }
+    }
+    if (lane == 0) {
+        S.issued = it;
+        if (a_loaded) atomicAdd(P.stats + 0, static_cast<unsigned long long>(a_loaded));
+        if (a_skipped) atomicAdd(P.stats + 1, static_cast<unsigned long long>(a_skipped));
+        if (b_loaded) atomicAdd(P.stats + 2, static_cast<unsigned long long>(b_loaded));
+        if (b_skipped) atomicAdd(P.stats + 3, static_cast<unsigned long long>(b_skipped));
+        if (loaded_bytes) atomicAdd(P.stats + 4, loaded_bytes);
     }
 }
 
-// Thread 0: compute copy geometry for a load unit and issue its bulk copies.
-__device__ void issue_unit(const Params &P, Unit &U, uint8_t *stage, uint64_t *bar) {
-    auto geom = [](const uint8_t *g, int cnt, int es, unsigned long long end, int &sh, int &tail,
-                   const uint8_t *&src, uint32_t &nbytes) {
-        unsigned long long a0 = reinterpret_cast<unsigned long long>(g);
-        unsigned long long a1 = a0 + static_cast<unsigned long long>(cnt) * es;
-        unsigned long long lo = a0 & ~15ull;
-        unsigned long long hi = (a1 + 15ull) & ~15ull;
-        unsigned long long lim = end & ~15ull;
-        if (hi > lim) hi = lim;
-        sh = static_cast<int>(a0 - lo);
-        if (hi <= lo) {
-            nbytes = 0;
-            tail = 0;
-        } else {
-            nbytes = static_cast<uint32_t>(hi - lo);
-            long long covered = static_cast<long long>(hi) - static_cast<long long>(a0);
-            tail = covered >= static_cast<long long>(cnt) * es ? cnt : static_cast<int>(covered / es);
-            if (tail < 0) tail = 0;
+template <int ES>
+__device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, int lane, uint32_t &bad) {
+    int it = 0;      // stages consumed
+    int uc = 0;      // units handed to the epilogue
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    while (true) {
+        const int st = it % kStages;
+        if (!wait_bar(P, S, &S.full[st], static_cast<uint32_t>((it / kStages) & 1))) break;
+        const StageInfo &I = S.info[st];
+        const int kind = I.kind;
+        if (kind == kEnd) {
+            // forward the end marker to the epilogue
+            const int slot = uc % kResSlots;
+            if (uc >= kResSlots && !wait_bar(P, S, &S.res_empty[slot], static_cast<uint32_t>((uc / kResSlots - 1) & 1)))
+                break;
+            if (lane == 0) {
+                if (cw == 0) S.res[slot].kind = kEnd;
+                mbar_arrive(&S.res_full[slot]);
+            }
+            ++it;
+            break;
         }
-        src = reinterpret_cast<const uint8_t *>(lo);
-    };
-    const uint8_t *srcz;
-    uint32_t nz;
-    geom(U.gz, U.cnt, P.esize, P.logits_end, U.sh, U.tail, srcz, nz);
-    uint32_t nq = 0;
-    const uint8_t *srcq = nullptr;
-    if (U.kind == kBLoad) {
-        geom(U.gq, U.cnt, 4, P.q_end, U.shq, U.tailq, srcq, nq);
+        const uint8_t *stage = ring + static_cast<size_t>(st) * kStageBytes;
+        const View vz{stage + I.sh, I.gz, I.cnt, I.tail, I.sh == 0};
+        const int nb = (I.cnt + kBlk - 1) / kBlk;
+        const int beta0 = I.e0 / kBlk;
+        const int b = I.b, n = I.n, j = I.j, last = I.last;
+        const float c2 = I.c2;
+        if (kind == kA) {
+            if (c2 == 0.0f) {
+                for (int blk = cw; blk < nb; blk += kConsumerWarps) {
+                    float x[8];
+                    const int e = blk * kBlk + lane * 8;
+                    const int nv = load8<ES>(vz, e, x, bad);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i < nv && x[i] > bv) {
+                            bv = x[i];
+                            bi = I.e0 + e + i;
+                        }
+                }
+            } else {
+                const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + beta0;
+                for (int blk = cw; blk < nb; blk += kConsumerWarps) {
+                    float x[8];
+                    const int e = blk * kBlk + lane * 8;
+                    const int nv = load8<ES>(vz, e, x, bad);
+                    float lm = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i < nv) lm = fmaxf(lm, x[i]);
+                    const float M = warp_max(lm);
+                    float s = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i < nv) s = __fadd_rn(s, w_exp(x[i], M, c2));
+                    s = warp_butterfly_sum(s);
+                    if (lane == 0) {
+                        P.bmaxA[rb + blk] = M;
+                        P.bsumA[rb + blk] = s;
+                    }
+                }
+            }
+        } else {
+            const View vq{stage + kQOff + I.shq, I.gq, I.cnt, I.tailq, I.shq == 0};
+            const float m = I.m, invS = I.invS;
+            uint32_t qbad = 0;
+            for (int blk = cw; blk < nb; blk += kConsumerWarps) {
+                float x[8], y[8];
+                const int e = blk * kBlk + lane * 8;
+                const int nv = load8<ES>(vz, e, x, bad);
+                load8<4>(vq, e, y, qbad);
+                float s = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < nv) s = __fadd_rn(s, w_res(x[i], y[i], m, c2, invS));
+                s = warp_butterfly_sum(s);
+                if (lane == 0) P.bsumB[static_cast<size_t>(b) * P.nblk + beta0 + blk] = s;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[st]);
+        ++it;
+        if (last) {
+            // hand the unit to the epilogue
+            const int slot = uc % kResSlots;
+            if (uc >= kResSlots && !wait_bar(P, S, &S.res_empty[slot], static_cast<uint32_t>((uc / kResSlots - 1) & 1)))
+                break;
+            float v = bv;
+            int i = bi;
+            if (kind == kA && c2 == 0.0f) warp_argmax(v, i);
+            if (lane == 0) {
+                ResSlot &R = S.res[slot];
+                R.v[cw] = v;
+                R.idx[cw] = i;
+                if (cw == 0) {
+                    R.kind = kind;
+                    R.b = b;
+                    R.n = n;
+                    R.j = j;
+                    R.c2 = c2;
+                }
+                mbar_arrive(&S.res_full[slot]);
+            }
+            ++uc;
+            bv = -INFINITY;
+            bi = 0x7fffffff;
+        }
     }
-    U.bytes = nz + nq;
-    if (U.bytes) {
-        fence_proxy_async();
-        mbar_expect_tx(bar, U.bytes);
-        if (nz) bulk_g2s(stage, srcz, nz, bar);
-        if (nq) bulk_g2s(stage + kQOff, srcq, nq, bar);
+    if (lane == 0 && cw == 0) S.consumed = it;
+}
+
+__device__ void epilogue(const Params &P, Smem &S, int lane) {
+    int uc = 0;
+    while (true) {
+        const int slot = uc % kResSlots;
+        if (!wait_bar(P, S, &S.res_full[slot], static_cast<uint32_t>((uc / kResSlots) & 1))) break;
+        const ResSlot &R = S.res[slot];
+        const int kind = R.kind;
+        if (kind == kEnd) break;
+        const int b = R.b, n = R.n, j = R.j;
+        const float c2 = R.c2;
+        float v = lane < kConsumerWarps ? R.v[lane] : -INFINITY;
+        int idx = lane < kConsumerWarps ? R.idx[lane] : 0x7fffffff;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.res_empty[slot]);
+        ++uc;
+        if (kind == kA) {
+            const bool greedy = (c2 == 0.0f);
+            if (greedy) warp_argmax(v, idx);
+            const size_t ri = static_cast<size_t>(b) * P.R + n;
+            if (P.ns == 1) {
+                resolve_row(P, b, n, greedy, c2, idx, lane);
+                settle_row(P, S, 1, b, lane);
+            } else {
+                uint32_t old = 0;
+                if (lane == 0) {
+                    if (greedy) {
+                        Partial pr;
+                        pr.v = v;
+                        pr.idx = idx;
+                        P.partial[ri * P.ns + j] = pr;
+                    }
+                    __threadfence();
+                    old = atom_add_acqrel(P.row_ctr + ri, 1u);
+                }
+                old = __shfl_sync(0xffffffffu, old, 0) + 1u;
+                if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) {
+                    if ((old >> 16) == 0u) {
+                        // every split loaded: resolve the row
+                        int gi = 0x7fffffff;
+                        if (greedy) {
+                            float gv = -INFINITY;
+                            for (int q = lane; q < P.ns; q += 32) {
+                                const Partial *pp = P.partial + ri * P.ns + q;
+                                argmax_merge(gv, gi, __ldcg(&pp->v), __ldcg(&pp->idx));
+                            }
+                            warp_argmax(gv, gi);
+                        }
+                        resolve_row(P, b, n, greedy, c2, gi, lane);
+                    }
+                    settle_row(P, S, 1, b, lane);
+                }
+            }
+        } else {
+            // B unit: the last chunk of a request's residual draws the token
+            uint32_t old = 0;
+            if (lane == 0) {
+                __threadfence();
+                old = atom_add_acqrel(P.res_ctr + b, 1u);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == static_cast<uint32_t>(P.ncb - 1)) {
+                __threadfence();
+                double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + n));
+                int t = sample_row(P, b, n, true, u, lane);
+                if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + n] = t;
+            }
+        }
     }
 }
 
 // --------------------------------------------------------------- kernel --
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_constant__ Params P) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ Unit s_unit[2];
-    __shared__ float s_rv[kWarps];
-    __shared__ int s_ri[kWarps];
-    __shared__ double s_rd[kWarps];
-    __shared__ int s_flag[4];
-    __shared__ uint32_t s_rs[kMaxRows];
-    __shared__ int s_tok[kMaxRows];
-    __shared__ uint8_t s_acc[kMaxRows];
-
+__global__ void __launch_bounds__(kThreads, 1) verify_kernel(const __grid_constant__ Params P) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    uint8_t *ring = smem_raw + ((sizeof(Smem) + 127) & ~static_cast<size_t>(127));
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    uint8_t *stage = smem;
-    uint32_t phase = 0;
     uint32_t bad = 0;
 
     if (tid == 0) {
-        mbar_init(&bar, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], kConsumerWarps);
+        }
+        for (int i = 0; i < kResSlots; ++i) {
+            mbar_init(&S.res_full[i], kConsumerWarps);
+            mbar_init(&S.res_empty[i], 1);
+        }
+        S.abort_flag = 0;
+        S.issued = 0;
+        S.consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // first claim
-    if (warp == 0) {
-        int u = 0;
-        if (lane == 0) u = static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
-        u = __shfl_sync(0xffffffffu, u, 0);
-        Unit U;
-        decode_unit(P, u, U, lane);
-        if (lane == 0) s_unit[0] = U;
-    }
     __syncthreads();
-    int cur = 0;
 
-    while (true) {
-        Unit &U = s_unit[cur];
-        const int kind0 = U.kind;
-        if (kind0 == kEnd) break;
-        __syncthreads();   // every thread has read kind0 before thread 0 may rewrite U
-        // ---- wait for a B unit's decision (only after all earlier units are done)
-        if (kind0 == kBWait) {
-            if (tid == 0) {
-                unsigned long long t0 = globaltimer();
-                uint32_t st = 0;
-                while (true) {
-                    st = ld_acquire(P.req_state + U.b);
-                    if (st & kDecided) break;
-                    if (globaltimer() - t0 > kWaitLimitNs) break;
-                    __nanosleep(256);
-                }
-                if (!(st & kDecided)) {
-                    set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
-                    U.kind = kBSkip;
-                } else if ((st & kNeedsResidual) && static_cast<int>(st & kIdxMask) < P.R - 1) {
-                    U.kind = kBLoad;
-                    U.n = static_cast<int>(st & kIdxMask);
-                } else {
-                    U.kind = kBSkip;
-                }
-            }
-        }
-        // ---- issue the bulk copy
-        if (tid == 0 && (U.kind == kALoad || U.kind == kBLoad)) {
-            if (U.kind == kBLoad) {
-                const size_t ri = static_cast<size_t>(U.b) * P.R + U.n;
-                RowStat rs;
-                rs.m = __ldcg(&P.rowstat[ri].m);
-                rs.S = __ldcg(&P.rowstat[ri].S);
-                float T = P.temperature[U.b];
-                U.c2 = 1.4426950408889634f / T;
-                U.m = rs.m;
-                U.invS = static_cast<float>(1.0 / rs.S);
-                size_t elem = (static_cast<size_t>(U.b) * P.R + U.n) * static_cast<size_t>(P.V) +
-                              static_cast<size_t>(U.c) * kChunkB;
-                U.gz = P.logits + elem * P.esize;
-                size_t qe = (static_cast<size_t>(U.b) * (P.R - 1) + U.n) * static_cast<size_t>(P.V) +
-                            static_cast<size_t>(U.c) * kChunkB;
-                U.gq = reinterpret_cast<const uint8_t *>(P.q + qe);
-            }
-            issue_unit(P, U, stage, &bar);
-        }
-        __syncthreads();
-        // ---- claim and decode the next unit while the copy is in flight
-        const int nxt = cur ^ 1;
-        if (warp == 0) {
-            int u = 0;
-            if (lane == 0) u = static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
-            u = __shfl_sync(0xffffffffu, u, 0);
-            Unit N;
-            decode_unit(P, u, N, lane);
-            if (lane == 0) s_unit[nxt] = N;
-        }
-        const int kind = U.kind;
-        const int b = U.b, n = U.n, c = U.c;
-        // ---- wait for the data
-        if ((kind == kALoad || kind == kBLoad) && U.bytes) {
-            unsigned long long t0 = 0;
-            int spins = 0;
-            while (!mbar_try_wait(&bar, phase)) {
-                if (++spins == 64) t0 = globaltimer();
-                if (spins > 64 && globaltimer() - t0 > kWaitLimitNs) {
-                    // The copy never completed: report and stop using this block.
-                    set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
-                    break;
-                }
-            }
-            phase ^= 1u;
-        }
-        View vz{stage + U.sh, U.gz, U.cnt, U.tail, U.sh == 0};
+    if (warp == 0) producer<ES>(P, S, ring, lane);
+    else if (warp == 1) epilogue(P, S, lane);
+    else consumer<ES>(P, S, ring, warp - 2, lane, bad);
 
-        if (kind == kALoad) {
-            // ---------------- A unit: argmax (+ softmax statistics) of one chunk
-            const int nb = (U.cnt + kBlk - 1) / kBlk;
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int blk = warp; blk < nb; blk += kWarps) {
-                float x[8];
-                int e0 = blk * kBlk + lane * 8;
-                int nv = load8<ES>(vz, e0, x, bad);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (i < nv && x[i] > bv) {
-                        bv = x[i];
-                        bi = e0 + i;
-                    }
-            }
-            warp_argmax(bv, bi);
-            if (lane == 0) {
-                s_rv[warp] = bv;
-                s_ri[warp] = bi;
-            }
-            __syncthreads();
-            if (warp == 0) {
-                float v = lane < kWarps ? s_rv[lane] : -INFINITY;
-                int i = lane < kWarps ? s_ri[lane] : 0x7fffffff;
-                warp_argmax(v, i);
-                if (lane == 0) {
-                    s_rv[0] = v;
-                    s_ri[0] = i;
-                }
-            }
-            __syncthreads();
-            const float M = s_rv[0];
-            const int Mi = s_ri[0];
-            double csum = 0.0;
-            if (U.c2 != 0.0f) {
-                // sampled: 256-element block sums of exp2((z - M) c2)
-                float *bs = P.bsumA + (static_cast<size_t>(b) * P.R + n) * P.nblk + static_cast<size_t>(c) * (kChunkA / kBlk);
-                double wsum = 0.0;
-                for (int blk = warp; blk < nb; blk += kWarps) {
-                    float x[8];
-                    int e0 = blk * kBlk + lane * 8;
-                    int nv = load8<ES>(vz, e0, x, bad);
-                    float s = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < nv) s = __fadd_rn(s, w_exp(x[i], M, U.c2));
-                    s = warp_butterfly_sum(s);
-                    if (lane == 0) {
-                        bs[blk] = s;
-                        wsum += static_cast<double>(s);
-                    }
-                }
-                if (lane == 0) s_rd[warp] = wsum;
-                __syncthreads();
-                if (tid == 0)
-                    for (int w = 0; w < kWarps; ++w) csum += s_rd[w];
-            }
-            // ---- publish the partial; the last chunk of the row resolves it
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                const size_t ri = static_cast<size_t>(b) * P.R + n;
-                Partial pr;
-                pr.v = M;
-                pr.idx = (Mi == 0x7fffffff) ? c * kChunkA : c * kChunkA + Mi;
-                pr.s = csum;
-                P.partial[ri * P.nca + c] = pr;
-                uint32_t old = atom_add_acqrel(P.row_done + ri, 1u);
-                s_flag[0] = (old == static_cast<uint32_t>(P.nca - 1));
-                atomicAdd(P.stats + 0, 1ull);
-                atomicAdd(P.stats + 4, static_cast<unsigned long long>(U.bytes));
-            }
-            __syncthreads();
-            if (s_flag[0] && warp == 0) {
-                // ---------------- row resolution (one warp)
-                const size_t ri = static_cast<size_t>(b) * P.R + n;
-                const Partial *pp = P.partial + ri * P.nca;
-                uint32_t rsv;
-                if (U.c2 == 0.0f) {
-                    float v = -INFINITY;
-                    int i = 0x7fffffff;
-                    for (int q = lane; q < P.nca; q += 32) argmax_merge(v, i, __ldcg(&pp[q].v), __ldcg(&pp[q].idx));
-                    warp_argmax(v, i);
-                    if (i < 0 || i >= P.V) i = 0;
-                    rsv = kResolved | static_cast<uint32_t>(i);
-                } else {
-                    float m = -INFINITY;
-                    for (int q = lane; q < P.nca; q += 32) m = fmaxf(m, __ldcg(&pp[q].v));
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                    double S = 0.0;
-                    for (int q = lane; q < P.nca; q += 32) {
-                        float Mc = __ldcg(&pp[q].v);
-                        S += __ldcg(&pp[q].s) * static_cast<double>(ex2(__fmul_rn(__fsub_rn(Mc, m), U.c2)));
-                    }
-                    S = warp_sum_d(S);
-                    uint32_t acc = 0;
-                    if (lane == 0) {
-                        RowStat st;
-                        st.m = m;
-                        st.pad = 0.0f;
-                        st.S = S;
-                        P.rowstat[ri] = st;
-                        if (n < P.R - 1) {
-                            // accept test of the draft token checked by this row
-                            int x = node_token(P, b, n + 1);
-                            if (x < 0 || x >= P.V) {
-                                set_status(P, SPEC_STATUS_TOKEN_RANGE);
-                            } else {
-                                float zx = logit_global(P, ri * P.V + x);
-                                double ph = static_cast<double>(ex2(__fmul_rn(__fsub_rn(zx, m), U.c2))) / S;
-                                float qh = __ldg(P.q + (static_cast<size_t>(b) * (P.R - 1) + n) * P.V + x);
-                                if (qh == 0.0f) {
-                                    acc = 1;
-                                } else {
-                                    double ua = static_cast<double>(__ldg(P.u_accept + static_cast<size_t>(b) * (P.R - 1) + n));
-                                    acc = ua < ph / static_cast<double>(qh);
-                                }
-                            }
-                        }
-                    }
-                    rsv = kResolved | __shfl_sync(0xffffffffu, acc, 0);
-                }
-                if (lane == 0) {
-                    __threadfence();
-                    st_release(P.rowstate + ri, rsv);
-                }
-            }
-        } else if (kind == kBLoad) {
-            // ---------------- B unit: residual block sums of one chunk of row a
-            View vq{stage + kQOff + U.shq, U.gq, U.cnt, U.tailq, U.shq == 0};
-            const int nb = (U.cnt + kBlk - 1) / kBlk;
-            float *bs = P.bsumB + static_cast<size_t>(b) * P.nblk + static_cast<size_t>(c) * (kChunkB / kBlk);
-            uint32_t qbad = 0;
-            for (int blk = warp; blk < nb; blk += kWarps) {
-                float x[8], y[8];
-                int e0 = blk * kBlk + lane * 8;
-                int nv = load8<ES>(vz, e0, x, bad);
-                load8<4>(vq, e0, y, qbad);
-                float s = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (i < nv) s = __fadd_rn(s, w_res(x[i], y[i], U.m, U.c2, U.invS));
-                s = warp_butterfly_sum(s);
-                if (lane == 0) bs[blk] = s;
-            }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                uint32_t old = atom_add_acqrel(P.res_done + b, 1u);
-                s_flag[0] = (old == static_cast<uint32_t>(P.ncb - 1));
-                atomicAdd(P.stats + 2, 1ull);
-                atomicAdd(P.stats + 4, static_cast<unsigned long long>(U.bytes));
-            }
-            __syncthreads();
-            if (s_flag[0] && warp == 0) {
-                // ---------------- residual sample of request b at row a (one warp)
-                __threadfence();
-                const int a = U.n;
-                double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + a));
-                int tok = sample_row(P, b, a, true, u, lane);
-                if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = tok;
-            }
-        } else if (kind == kASkip) {
-            if (tid == 0) atomicAdd(P.stats + 1, 1ull);
-        } else if (kind == kBSkip) {
-            if (tid == 0) atomicAdd(P.stats + 3, 1ull);
-        }
-
-        // ---- request completion (A units only, loaded or skipped)
-        if (kind == kALoad || kind == kASkip) {
-            __syncthreads();
-            if (tid == 0) {
-                __threadfence();
-                uint32_t old = atom_add_acqrel(P.req_done + b, 1u);
-                s_flag[1] = (old == static_cast<uint32_t>(P.R * P.nca - 1));
-            }
-            __syncthreads();
-            if (s_flag[1]) {
-                // ---------------- finalize request b
-                __threadfence();
-                int range_bad = 0;
-                for (int i = tid; i < P.R; i += kThreads) {
-                    s_rs[i] = *reinterpret_cast<volatile const uint32_t *>(P.rowstate + static_cast<size_t>(b) * P.R + i);
-                    s_tok[i] = i > 0 ? node_token(P, b, i) : -1;
-                    if (i > 0 && (s_tok[i] < 0 || s_tok[i] >= P.V)) range_bad = 1;
-                }
-                if (__any_sync(0xffffffffu, range_bad) && lane == 0) set_status(P, SPEC_STATUS_TOKEN_RANGE);
-                __syncthreads();
-                if (tid == 0) {
-                    const float T = P.temperature ? P.temperature[b] : 0.0f;
-                    const bool greedy = !(T > 0.0f);
-                    s_acc[0] = 1;
-                    int best = 0;
-                    for (int i = 1; i < P.R; ++i) {
-                        int p = parent_of(P, i);
-                        bool ok = s_acc[p] && edge_ok(s_rs[p], greedy, s_tok[i]);
-                        s_acc[i] = ok;
-                        int di = P.tree ? P.depth[i] : i;
-                        int db = P.tree ? P.depth[best] : best;
-                        if (ok && di > db) best = i;
-                    }
-                    const int d = P.tree ? P.depth[best] : best;
-                    int32_t *ot = P.out_tokens + static_cast<size_t>(b) * (P.D + 1);
-                    // path (root first) into s_ri as scratch-free walk
-                    int node = best;
-                    for (int i = d; i >= 1; --i) {
-                        ot[i - 1] = s_tok[node];
-                        if (P.out_path) P.out_path[static_cast<size_t>(b) * (P.D + 1) + i] = node;
-                        node = parent_of(P, node);
-                    }
-                    if (P.out_path) {
-                        P.out_path[static_cast<size_t>(b) * (P.D + 1)] = 0;
-                        for (int i = d + 1; i <= P.D; ++i) P.out_path[static_cast<size_t>(b) * (P.D + 1) + i] = -1;
-                    }
-                    for (int i = d + 1; i <= P.D; ++i) ot[i] = -1;
-                    uint32_t st = kDecided;
-                    if (greedy) {
-                        uint32_t rs = s_rs[best];
-                        ot[d] = (rs & kResolved) ? static_cast<int>(rs & kIdxMask) : 0;
-                    } else if (d < P.R - 1) {
-                        st |= kNeedsResidual | static_cast<uint32_t>(d);
-                        ot[d] = -1;   // written by the residual pass
-                    }
-                    P.out_count[b] = P.tree ? d + 1 : d;
-                    s_flag[2] = (!greedy && d == P.R - 1) ? 1 : 0;
-                    s_flag[3] = static_cast<int>(st);
-                }
-                __syncthreads();
-                if (s_flag[2] && warp == 0) {
-                    // bonus token: every draft accepted, sample from p at the last row
-                    const int a = P.R - 1;
-                    double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + a));
-                    int tok = sample_row(P, b, a, false, u, lane);
-                    if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = tok;
-                }
-                if (tid == 0) {
-                    __threadfence();
-                    st_release(P.req_state + b, static_cast<uint32_t>(s_flag[3]));
-                }
-            }
-        }
-        __syncthreads();
-        cur = nxt;
-    }
-
-    // ---- report data problems, then the last block out clears the counters
     bad = __any_sync(0xffffffffu, bad != 0);
     if (lane == 0 && bad) set_status(P, SPEC_STATUS_NONFINITE);
     __syncthreads();
     if (tid == 0) {
+        if (*reinterpret_cast<volatile int *>(&S.abort_flag)) {
+            // Let copies still in flight land before the block's memory is reused.
+            for (int it = S.consumed; it < S.issued; ++it) {
+                uint64_t *bar = &S.full[it % kStages];
+                unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(bar, static_cast<uint32_t>((it / kStages) & 1)))
+                    if (globaltimer() - t0 > kWaitLimitNs) break;
+            }
+        }
         __threadfence();
         uint32_t old = atom_add_acqrel(P.ctrl + 1, 1u);
-        s_flag[0] = (old == gridDim.x - 1);
+        S.last_flag = (old == gridDim.x - 1);
     }
     __syncthreads();
-    if (s_flag[0]) {
+    if (S.last_flag) {
         __threadfence();
         for (uint32_t i = tid; i < P.reset_words; i += kThreads) P.reset_base[i] = 0u;
         __threadfence();
@@ -993,16 +1162,18 @@ spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "") {
 }
 
 struct Layout {
-    size_t stats, reset, reset_bytes, ctrl, row_done, rowstate, req_done, req_state, res_done;
-    size_t rowstat, partial, bsumA, bsumB, total;
-    int nca, ncb, nblk;
+    size_t stats, reset, reset_bytes, ctrl, row_ctr, rowstate, req_ctr, req_state, res_ctr;
+    size_t rowstat, partial, bmaxA, bsumA, bsumB, total;
+    int esub, nsub, ncb, nblk;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-bool make_layout(int B, int R, int V, Layout &L) {
+bool make_layout(int B, int R, int V, spec_dtype_t dtype, Layout &L) {
     if (B < 1 || R < 1 || R > kMaxRows || V < 1 || V >= (1 << 30)) return false;
-    L.nca = (V + kChunkA - 1) / kChunkA;
+    if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return false;
+    L.esub = kSubBytes / (dtype == SPEC_BF16 ? 2 : 4);
+    L.nsub = (V + L.esub - 1) / L.esub;
     L.ncb = (V + kChunkB - 1) / kChunkB;
     L.nblk = (V + kBlk - 1) / kBlk;
     const size_t BR = static_cast<size_t>(B) * R;
@@ -1012,22 +1183,24 @@ bool make_layout(int B, int R, int V, Layout &L) {
     L.reset = off;
     L.ctrl = off;
     off += 32 * 4;
-    L.row_done = off;
+    L.row_ctr = off;
     off += BR * 4;
     L.rowstate = off;
     off += BR * 4;
-    L.req_done = off;
+    L.req_ctr = off;
     off += static_cast<size_t>(B) * 4;
     L.req_state = off;
     off += static_cast<size_t>(B) * 4;
-    L.res_done = off;
+    L.res_ctr = off;
     off += static_cast<size_t>(B) * 4;
     off = up256(off);
     L.reset_bytes = off - L.reset;
     L.rowstat = off;
     off = up256(off + BR * sizeof(RowStat));
     L.partial = off;
-    off = up256(off + BR * L.nca * sizeof(Partial));
+    off = up256(off + BR * L.nsub * sizeof(Partial));
+    L.bmaxA = off;
+    off = up256(off + BR * L.nblk * 4);
     L.bsumA = off;
     off = up256(off + BR * L.nblk * 4);
     L.bsumB = off;
@@ -1046,6 +1219,10 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 
+constexpr size_t kSmemBytes = ((sizeof(Smem) + 127) & ~static_cast<size_t>(127)) +
+                              static_cast<size_t>(kStages) * kStageBytes;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block exceeds the sm_103 limit");
+
 spec_status_t device_info(DeviceInfo *&out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1063,14 +1240,20 @@ spec_status_t device_info(DeviceInfo *&out) {
             return fail(SPEC_ERR_UNSUPPORTED, "needs compute capability 10.3 (sm_103a), device is %s", buf);
         }
         cudaDeviceGetAttribute(&D.sms, cudaDevAttrMultiProcessorCount, dev);
-        e = cudaFuncSetAttribute(verify_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+        e = cudaFuncSetAttribute(verify_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(verify_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+            e = cudaFuncSetAttribute(verify_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes));
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[0], verify_kernel<2>, kThreads, kStageBytes);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[0], verify_kernel<2>, kThreads,
+                                                              kSmemBytes);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[1], verify_kernel<4>, kThreads, kStageBytes);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[1], verify_kernel<4>, kThreads,
+                                                              kSmemBytes);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel setup: %s", cudaGetErrorString(e));
+        if (D.blocks_per_sm[0] < 1 || D.blocks_per_sm[1] < 1)
+            return fail(SPEC_ERR_UNSUPPORTED, "the verify kernel does not fit on this device%s");
         D.ok = 1;
     }
     out = &D;
@@ -1079,9 +1262,23 @@ spec_status_t device_info(DeviceInfo *&out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Splits per row: whole rows when the batch gives every SM about two rows,
+// otherwise finer splits (down to one 16 KiB stage) so small batches still
+// spread over the GPU.  SPEC_VERIFY_SPLITS overrides the choice (tuning).
+int choose_splits(int rows_total, int nsub, int sms) {
+    int ns = (2 * sms + rows_total - 1) / rows_total;
+    if (const char *env = getenv("SPEC_VERIFY_SPLITS")) {
+        int v = atoi(env);
+        if (v > 0) ns = v;
+    }
+    if (ns < 1) ns = 1;
+    if (ns > nsub) ns = nsub;
+    return ns;
+}
+
 spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size_t ws_bytes, void *stream) {
     Layout L;
-    if (!make_layout(P.B, P.R, P.V, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
+    if (!make_layout(P.B, P.R, P.V, dtype, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
     if (!workspace || ws_bytes < L.total)
         return fail(SPEC_ERR_INVALID_ARG, "workspace missing or smaller than spec_workspace_bytes()%s");
     if (!aligned16(workspace)) return fail(SPEC_ERR_INVALID_ARG, "workspace must be 16-byte aligned%s");
@@ -1091,38 +1288,45 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     P.stats = reinterpret_cast<unsigned long long *>(ws + L.stats);
     P.ctrl = reinterpret_cast<uint32_t *>(ws + L.ctrl);
-    P.row_done = reinterpret_cast<uint32_t *>(ws + L.row_done);
+    P.row_ctr = reinterpret_cast<uint32_t *>(ws + L.row_ctr);
     P.rowstate = reinterpret_cast<uint32_t *>(ws + L.rowstate);
-    P.req_done = reinterpret_cast<uint32_t *>(ws + L.req_done);
+    P.req_ctr = reinterpret_cast<uint32_t *>(ws + L.req_ctr);
     P.req_state = reinterpret_cast<uint32_t *>(ws + L.req_state);
-    P.res_done = reinterpret_cast<uint32_t *>(ws + L.res_done);
+    P.res_ctr = reinterpret_cast<uint32_t *>(ws + L.res_ctr);
     P.reset_base = reinterpret_cast<uint32_t *>(ws + L.reset);
     P.reset_words = static_cast<uint32_t>(L.reset_bytes / 4);
     P.rowstat = reinterpret_cast<RowStat *>(ws + L.rowstat);
     P.partial = reinterpret_cast<Partial *>(ws + L.partial);
+    P.bmaxA = reinterpret_cast<float *>(ws + L.bmaxA);
     P.bsumA = reinterpret_cast<float *>(ws + L.bsumA);
     P.bsumB = reinterpret_cast<float *>(ws + L.bsumB);
     P.esize = dtype == SPEC_BF16 ? 2 : 4;
-    P.nca = L.nca;
+    P.esub = L.esub;
+    P.nsub = L.nsub;
     P.ncb = L.ncb;
     P.nblk = L.nblk;
-    const long long ua = static_cast<long long>(P.B) * P.R * L.nca;
+    const long long rows_total = static_cast<long long>(P.B) * P.R;
+    int ns = choose_splits(rows_total > (1 << 30) ? (1 << 30) : static_cast<int>(rows_total), L.nsub, D->sms);
+    P.sps = (L.nsub + ns - 1) / ns;
+    P.ns = (L.nsub + P.sps - 1) / P.sps;
+    const long long ua = rows_total * P.ns;
     const long long ub = P.q ? static_cast<long long>(P.B) * L.ncb : 0;
-    if (ua + ub >= (1ll << 31) - 1024) return fail(SPEC_ERR_INVALID_ARG, "batch too large%s");
+    if (ua + ub >= (1ll << 31) - (1 << 20)) return fail(SPEC_ERR_INVALID_ARG, "batch too large%s");
     P.units_a = static_cast<int>(ua);
     P.units_total = static_cast<int>(ua + ub);
     const size_t zbytes = static_cast<size_t>(P.B) * P.R * static_cast<size_t>(P.V) * P.esize;
     P.logits_end = reinterpret_cast<unsigned long long>(P.logits) + zbytes;
-    P.q_end = P.q ? reinterpret_cast<unsigned long long>(P.q) + static_cast<size_t>(P.B) * (P.R - 1) * static_cast<size_t>(P.V) * 4 : 0;
-    const int per_sm = D->blocks_per_sm[dtype == SPEC_BF16 ? 0 : 1];
-    long long grid = static_cast<long long>(D->sms) * (per_sm > 0 ? per_sm : 1);
+    P.q_end = P.q ? reinterpret_cast<unsigned long long>(P.q) +
+                        static_cast<size_t>(P.B) * (P.R - 1) * static_cast<size_t>(P.V) * 4
+                  : 0;
+    long long grid = static_cast<long long>(D->sms) * D->blocks_per_sm[dtype == SPEC_BF16 ? 0 : 1];
     if (grid > P.units_total) grid = P.units_total;
     if (grid < 1) grid = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == SPEC_BF16)
-        verify_kernel<2><<<static_cast<unsigned>(grid), kThreads, kStageBytes, st>>>(P);
+        verify_kernel<2><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(P);
     else
-        verify_kernel<4><<<static_cast<unsigned>(grid), kThreads, kStageBytes, st>>>(P);
+        verify_kernel<4><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
@@ -1161,9 +1365,9 @@ spec_status_t noalloc_scratch_ptr(uint8_t *&out) {
 using namespace sv;
 
 extern "C" size_t spec_workspace_bytes(int B, int rows, int V, spec_dtype_t dtype) {
-    (void)dtype;
+
     Layout L;
-    if (!make_layout(B, rows, V, L)) return 0;
+    if (!make_layout(B, rows, V, dtype, L)) return 0;
     return L.total;
 }
 
@@ -1341,7 +1545,7 @@ extern "C" spec_status_t spec_verify_chain_noalloc(const void *target_logits, sp
     if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
         return fail(SPEC_ERR_INVALID_ARG, "target_logits and draft_probs must be 16-byte aligned%s");
     Layout L;
-    if (!make_layout(B, k + 1, V, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
+    if (!make_layout(B, k + 1, V, dtype, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
     if (L.total > kNoAllocScratchBytes) {
         char buf[160];
         snprintf(buf, sizeof buf, "these sizes need %zu bytes of scratch; the static scratch holds %zu bytes",
