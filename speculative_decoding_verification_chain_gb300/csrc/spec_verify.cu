@@ -50,15 +50,13 @@
 namespace sv {
 
 // ---------------------------------------------------------------- config --
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumerLanes = 32 * kConsumerWarps;
 constexpr int kThreads = 32 * (2 + kConsumerWarps);   // producer, epilogue, consumers
-constexpr int kStages = 12;
-constexpr int kSubBytes = 16384;                       // logits bytes per A stage
+constexpr int kStages = 8;
+constexpr int kSubBytes = 24576;                       // data bytes per stage
 constexpr int kStageBytes = kSubBytes + 128;
-constexpr int kQOff = 8192 + 64;                        // q area of a B stage
-constexpr int kSubB = 2048;                             // elements per B stage
-constexpr int kSubPerB = 8;                             // B stages per B unit
-constexpr int kChunkB = kSubB * kSubPerB;               // elements per B unit
+constexpr int kSubPerB = 4;                             // B stages per B unit
 constexpr int kResSlots = 4;
 constexpr int kBlk = 256;                               // canonical block: 32 lanes x 8 elements
 constexpr int kMaxRows = SPEC_MAX_ROWS;
@@ -78,9 +76,9 @@ struct RowStat {
     double S;     // sum_j 2^((z_j - m) * c2)
 };
 
-struct Partial {  // greedy split result
+struct Partial {  // greedy split result: max value and first 8-element group holding it
     float v;
-    int32_t idx;
+    int32_t grp;
 };
 
 struct Params {
@@ -113,8 +111,11 @@ struct Params {
     unsigned long long q_end;
     int B, R, V, D;
     int esize;
-    int esub;                    // elements per A stage (16 KiB of logits)
+    int esub;                    // elements per A stage (24 KiB of logits)
     int nsub;                    // A stages per row
+    int esb;                     // elements per B stage (24 KiB of logits + q)
+    int ecb;                     // elements per B unit
+    int qoff;                    // byte offset of the q area in a B stage
     int ns;                      // splits per row
     int sps;                     // A stages per split
     int ncb, nblk;
@@ -127,6 +128,7 @@ struct Params {
 struct StageInfo {
     int kind;
     int last;            // last stage of its unit
+    int fast;            // aligned, every element in shared memory, whole 8-element groups
     int b, n, j;         // request, row, split (A) / chunk (B)
     int e0, cnt;         // element offset within the row, element count
     int sh, tail;        // z: byte shift of element 0; elements [tail, cnt) come from global
@@ -368,6 +370,61 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// Maxima that propagate NaN (so a NaN logit surfaces in the row max).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Max of the 8 bf16 values in a 16-byte word, by packed bf16x2 maxima.
+__device__ __forceinline__ float vmax8_bf16(uint4 w) {
+    uint32_t a = bmax2_nan(bmax2_nan(w.x, w.y), bmax2_nan(w.z, w.w));
+    return fmax_nan(bf16_lo(a), bf16_hi(a));
+}
+
+__device__ __forceinline__ float vmax8_f32(uint4 a, uint4 b) {
+    float m0 = fmax_nan(__uint_as_float(a.x), __uint_as_float(a.y));
+    float m1 = fmax_nan(__uint_as_float(a.z), __uint_as_float(a.w));
+    float m2 = fmax_nan(__uint_as_float(b.x), __uint_as_float(b.y));
+    float m3 = fmax_nan(__uint_as_float(b.z), __uint_as_float(b.w));
+    return fmax_nan(fmax_nan(m0, m1), fmax_nan(m2, m3));
+}
+
+// Warp max of a float through an order-preserving integer key and redux.
+__device__ __forceinline__ int fkey(float f) {
+    int b = __float_as_int(f);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
+
+__device__ __forceinline__ float warp_max_redux(float v) {
+    int k = __reduce_max_sync(0xffffffffu, fkey(v));
+    return __int_as_float(k ^ ((k >> 31) & 0x7fffffff));
+}
+
+// (value, group) candidates: larger value wins, then the lower group.
+__device__ __forceinline__ void cand_merge(float &v, int &g, float ov, int og) {
+    if (ov > v || (ov == v && static_cast<unsigned>(og) < static_cast<unsigned>(g))) {
+        v = ov;
+        g = og;
+    }
+}
+
+__device__ __forceinline__ void warp_cand(float &v, int &g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        int og = __shfl_xor_sync(0xffffffffu, g, off);
+        cand_merge(v, g, ov, og);
+    }
+}
+
 // Canonical block sum: lane partials combined by an xor butterfly; lane 0's
 // value is the block's sum.
 __device__ __forceinline__ float warp_butterfly_sum(float s) {
@@ -389,6 +446,17 @@ __device__ __forceinline__ double warp_incl_scan_d(double s, int lane) {
         if (lane >= off) s += o;
     }
     return s;
+}
+
+// Warp-wide: index of the first element of 8-element group grp of row ri
+// equal to v (the row's max); the group's first element if none matches.
+__device__ int first_in_group(const Params &P, size_t ri, int grp, float v, int lane) {
+    if (grp < 0 || static_cast<long long>(grp) * 8 >= P.V) return 0;
+    const int e = grp * 8 + lane;
+    bool hit = false;
+    if (lane < 8 && e < P.V) hit = (logit_global(P, ri * P.V + e) == v);
+    unsigned m = __ballot_sync(0xffffffffu, hit);
+    return m ? grp * 8 + (__ffs(m) - 1) : grp * 8;
 }
 
 // ------------------------------------------------------------ topology --
@@ -625,12 +693,13 @@ __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) 
 // Warp-wide: resolve row n of request b from its finished splits.  Greedy:
 // (v, idx) is the whole row's argmax.  Sampled: m and S from the block data,
 // then the accept test of child n+1.
-__device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, int lane) {
+__device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
     uint32_t rsv;
     if (greedy) {
         int g = (gidx < 0 || gidx >= P.V) ? 0 : gidx;
         rsv = kResolved | static_cast<uint32_t>(g);
+        if (lane == 0 && !isfinite(gmax)) set_status(P, SPEC_STATUS_NONFINITE);
     } else {
         const float *bm = P.bmaxA + ri * P.nblk;
         const float *bs = P.bsumA + ri * P.nblk;
@@ -644,6 +713,7 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
         Ssum = warp_sum_d(Ssum);
         uint32_t acc = 0;
         if (lane == 0) {
+            if (!isfinite(m) || !isfinite(Ssum)) set_status(P, SPEC_STATUS_NONFINITE);
             RowStat st;
             st.m = m;
             st.pad = 0.0f;
@@ -790,6 +860,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     const uint8_t *src;
                     uint32_t nb;
                     copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
+                    I.fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
                     loaded_bytes += nb;
                     fence_proxy_async();
                     if (nb) {
@@ -832,9 +903,9 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const float c2 = kLog2e / __ldg(P.temperature + b);
             const size_t rowe = ri * static_cast<size_t>(P.V);
             const size_t qrowe = (static_cast<size_t>(b) * (P.R - 1) + a) * static_cast<size_t>(P.V);
-            const int e_begin = c * kChunkB;
-            const int e_end = min(P.V, e_begin + kChunkB);
-            for (int e = e_begin; e < e_end; e += kSubB) {
+            const int e_begin = c * P.ecb;
+            const int e_end = min(P.V, e_begin + P.ecb);
+            for (int e = e_begin; e < e_end; e += P.esb) {
                 int st;
                 if (!acquire_stage(st)) {
                     aborted = true;
@@ -843,12 +914,12 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 if (lane == 0) {
                     StageInfo &I = S.info[st];
                     I.kind = kB;
-                    I.last = (e + kSubB >= e_end);
+                    I.last = (e + P.esb >= e_end);
                     I.b = b;
                     I.n = a;
                     I.j = c;
                     I.e0 = e;
-                    I.cnt = min(kSubB, P.V - e);
+                    I.cnt = min(P.esb, P.V - e);
                     I.c2 = c2;
                     I.m = m;
                     I.invS = static_cast<float>(1.0 / Srow);
@@ -858,13 +929,14 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     uint32_t nz, nq;
                     copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, sz, nz);
                     copy_geom(I.gq, I.cnt, 4, P.q_end, I.shq, I.tailq, sq, nq);
+                    I.fast = (I.sh == 0 && I.tail == I.cnt && I.shq == 0 && I.tailq == I.cnt && (I.cnt & 7) == 0);
                     loaded_bytes += nz + nq;
                     fence_proxy_async();
                     uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
                     if (nz + nq) {
                         mbar_expect_tx(&S.full[st], nz + nq);
                         if (nz) bulk_g2s(dst, sz, nz, &S.full[st]);
-                        if (nq) bulk_g2s(dst + kQOff, sq, nq, &S.full[st]);
+                        if (nq) bulk_g2s(dst + P.qoff, sq, nq, &S.full[st]);
                     } else {
                         mbar_arrive(&S.full[st]);
                     }
@@ -895,11 +967,51 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
 }
 
 template <int ES>
+__device__ __forceinline__ float group_max(const View &v, int g, bool fast, uint32_t &bad) {
+    if (fast) {
+        if (ES == 2) return vmax8_bf16(*reinterpret_cast<const uint4 *>(v.s + 16 * g));
+        const uint4 *p = reinterpret_cast<const uint4 *>(v.s + 32 * g);
+        return vmax8_f32(p[0], p[1]);
+    }
+    float m = -INFINITY;
+    const int e0 = 8 * g;
+    const int nv = min(8, v.cnt - e0);
+    for (int i = 0; i < nv; ++i) m = fmax_nan(m, ld_one<ES>(v, e0 + i, bad));
+    return m;
+}
+
+// Loads the 8 elements of lane `lane` in block blk of a stage.
+template <int ES>
+__device__ __forceinline__ int load_block8(const View &v, int blk, int lane, bool fast, float x[8], uint32_t &bad) {
+    const int e = blk * kBlk + lane * 8;
+    if (fast) {
+        if (ES == 2) {
+            uint4 w = *reinterpret_cast<const uint4 *>(v.s + 2 * e);
+            x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x);
+            x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+            x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z);
+            x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+        } else {
+            uint4 w0 = *reinterpret_cast<const uint4 *>(v.s + 4 * e);
+            uint4 w1 = *reinterpret_cast<const uint4 *>(v.s + 4 * e + 16);
+            x[0] = __uint_as_float(w0.x); x[1] = __uint_as_float(w0.y);
+            x[2] = __uint_as_float(w0.z); x[3] = __uint_as_float(w0.w);
+            x[4] = __uint_as_float(w1.x); x[5] = __uint_as_float(w1.y);
+            x[6] = __uint_as_float(w1.z); x[7] = __uint_as_float(w1.w);
+        }
+        return max(0, min(8, v.cnt - e));
+    }
+    return load8<ES>(v, e, x, bad);
+}
+
+template <int ES>
 __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, int lane, uint32_t &bad) {
     int it = 0;      // stages consumed
     int uc = 0;      // units handed to the epilogue
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    float best = -INFINITY;   // greedy: running max of this lane
+    int bgrp = -1;            // greedy: first 8-element group of the row holding it
+    float mx = -INFINITY;     // greedy: NaN-propagating max (non-finite detection)
+    constexpr int kBPW = (kSubBytes / ES / kBlk + kConsumerWarps - 1) / kConsumerWarps;   // blocks per warp
     while (true) {
         const int st = it % kStages;
         if (!wait_bar(P, S, &S.full[st], static_cast<uint32_t>((it / kStages) & 1))) break;
@@ -918,61 +1030,81 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             break;
         }
         const uint8_t *stage = ring + static_cast<size_t>(st) * kStageBytes;
+        const bool fast = I.fast != 0;
         const View vz{stage + I.sh, I.gz, I.cnt, I.tail, I.sh == 0};
-        const int nb = (I.cnt + kBlk - 1) / kBlk;
-        const int beta0 = I.e0 / kBlk;
+        const int cnt = I.cnt;
         const int b = I.b, n = I.n, j = I.j, last = I.last;
         const float c2 = I.c2;
         if (kind == kA) {
             if (c2 == 0.0f) {
-                for (int blk = cw; blk < nb; blk += kConsumerWarps) {
-                    float x[8];
-                    const int e = blk * kBlk + lane * 8;
-                    const int nv = load8<ES>(vz, e, x, bad);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < nv && x[i] > bv) {
-                            bv = x[i];
-                            bi = I.e0 + e + i;
-                        }
+                // ---- greedy: running (max, first group) over 8-element groups
+                const int ng = (cnt + 7) >> 3;
+                const int g0 = I.e0 >> 3;
+#pragma unroll 3
+                for (int g = cw * 32 + lane; g < ng; g += kConsumerLanes) {
+                    const float m = group_max<ES>(vz, g, fast, bad);
+                    mx = fmax_nan(mx, m);
+                    if (m > best) {
+                        best = m;
+                        bgrp = g0 + g;
+                    }
                 }
             } else {
-                const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + beta0;
-                for (int blk = cw; blk < nb; blk += kConsumerWarps) {
-                    float x[8];
-                    const int e = blk * kBlk + lane * 8;
-                    const int nv = load8<ES>(vz, e, x, bad);
-                    float lm = -INFINITY;
+                // ---- sampled: per 256-element block its max M and sum of 2^((z - M) c2)
+                const int nb = (cnt + kBlk - 1) / kBlk;
+                const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + I.e0 / kBlk;
+                float x[kBPW][8];
+                int nv[kBPW];
+                float M[kBPW];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < nv) lm = fmaxf(lm, x[i]);
-                    const float M = warp_max(lm);
-                    float s = 0.0f;
+                for (int t = 0; t < kBPW; ++t) {
+                    const int blk = cw + t * kConsumerWarps;
+                    nv[t] = 0;
+                    if (blk < nb) nv[t] = load_block8<ES>(vz, blk, lane, fast, x[t], bad);
+                }
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < nv) s = __fadd_rn(s, w_exp(x[i], M, c2));
-                    s = warp_butterfly_sum(s);
-                    if (lane == 0) {
-                        P.bmaxA[rb + blk] = M;
-                        P.bsumA[rb + blk] = s;
+                for (int t = 0; t < kBPW; ++t) {
+                    const int blk = cw + t * kConsumerWarps;
+                    if (blk < nb) {
+                        float lm = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (i < nv[t]) lm = fmax_nan(lm, x[t][i]);
+                        M[t] = warp_max_redux(lm);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kBPW; ++t) {
+                    const int blk = cw + t * kConsumerWarps;
+                    if (blk < nb) {
+                        float s = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (i < nv[t]) s = __fadd_rn(s, w_exp(x[t][i], M[t], c2));
+                        s = warp_butterfly_sum(s);
+                        if (lane == 0) {
+                            P.bmaxA[rb + blk] = M[t];
+                            P.bsumA[rb + blk] = s;
+                        }
                     }
                 }
             }
         } else {
-            const View vq{stage + kQOff + I.shq, I.gq, I.cnt, I.tailq, I.shq == 0};
+            // ---- residual: per 256-element block the sum of max(0, p - q)
+            const View vq{stage + P.qoff + I.shq, I.gq, cnt, I.tailq, I.shq == 0};
+            const int nb = (cnt + kBlk - 1) / kBlk;
             const float m = I.m, invS = I.invS;
             uint32_t qbad = 0;
             for (int blk = cw; blk < nb; blk += kConsumerWarps) {
                 float x[8], y[8];
-                const int e = blk * kBlk + lane * 8;
-                const int nv = load8<ES>(vz, e, x, bad);
-                load8<4>(vq, e, y, qbad);
+                const int nvz = load_block8<ES>(vz, blk, lane, fast, x, bad);
+                load_block8<4>(vq, blk, lane, fast, y, qbad);
                 float s = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (i < nv) s = __fadd_rn(s, w_res(x[i], y[i], m, c2, invS));
+                    if (i < nvz) s = __fadd_rn(s, w_res(x[i], y[i], m, c2, invS));
                 s = warp_butterfly_sum(s);
-                if (lane == 0) P.bsumB[static_cast<size_t>(b) * P.nblk + beta0 + blk] = s;
+                if (lane == 0) P.bsumB[static_cast<size_t>(b) * P.nblk + I.e0 / kBlk + blk] = s;
             }
         }
         __syncwarp();
@@ -983,13 +1115,22 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             const int slot = uc % kResSlots;
             if (uc >= kResSlots && !wait_bar(P, S, &S.res_empty[slot], static_cast<uint32_t>((uc / kResSlots - 1) & 1)))
                 break;
-            float v = bv;
-            int i = bi;
-            if (kind == kA && c2 == 0.0f) warp_argmax(v, i);
+            float v = best;
+            int g = bgrp;
+            if (kind == kA && c2 == 0.0f) {
+                warp_cand(v, g);
+                mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                // NaN or +inf seen by this warp (a warp that saw no element keeps -inf)
+                if (lane == 0 && (mx != mx || mx == INFINITY)) set_status(P, SPEC_STATUS_NONFINITE);
+            }
             if (lane == 0) {
                 ResSlot &R = S.res[slot];
                 R.v[cw] = v;
-                R.idx[cw] = i;
+                R.idx[cw] = g;
                 if (cw == 0) {
                     R.kind = kind;
                     R.b = b;
@@ -1000,8 +1141,9 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 mbar_arrive(&S.res_full[slot]);
             }
             ++uc;
-            bv = -INFINITY;
-            bi = 0x7fffffff;
+            best = -INFINITY;
+            bgrp = -1;
+            mx = -INFINITY;
         }
     }
     if (lane == 0 && cw == 0) S.consumed = it;
@@ -1018,16 +1160,17 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
         const int b = R.b, n = R.n, j = R.j;
         const float c2 = R.c2;
         float v = lane < kConsumerWarps ? R.v[lane] : -INFINITY;
-        int idx = lane < kConsumerWarps ? R.idx[lane] : 0x7fffffff;
+        int grp = lane < kConsumerWarps ? R.idx[lane] : -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.res_empty[slot]);
         ++uc;
         if (kind == kA) {
             const bool greedy = (c2 == 0.0f);
-            if (greedy) warp_argmax(v, idx);
+            if (greedy) warp_cand(v, grp);
             const size_t ri = static_cast<size_t>(b) * P.R + n;
             if (P.ns == 1) {
-                resolve_row(P, b, n, greedy, c2, idx, lane);
+                int gi = greedy ? first_in_group(P, ri, grp, v, lane) : 0;
+                resolve_row(P, b, n, greedy, c2, gi, v, lane);
                 settle_row(P, S, 1, b, lane);
             } else {
                 uint32_t old = 0;
@@ -1035,7 +1178,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
                     if (greedy) {
                         Partial pr;
                         pr.v = v;
-                        pr.idx = idx;
+                        pr.grp = grp;
                         P.partial[ri * P.ns + j] = pr;
                     }
                     __threadfence();
@@ -1045,16 +1188,17 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
                 if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) {
                     if ((old >> 16) == 0u) {
                         // every split loaded: resolve the row
-                        int gi = 0x7fffffff;
+                        float gv = -INFINITY;
+                        int gg = -1;
                         if (greedy) {
-                            float gv = -INFINITY;
                             for (int q = lane; q < P.ns; q += 32) {
                                 const Partial *pp = P.partial + ri * P.ns + q;
-                                argmax_merge(gv, gi, __ldcg(&pp->v), __ldcg(&pp->idx));
+                                cand_merge(gv, gg, __ldcg(&pp->v), __ldcg(&pp->grp));
                             }
-                            warp_argmax(gv, gi);
+                            warp_cand(gv, gg);
                         }
-                        resolve_row(P, b, n, greedy, c2, gi, lane);
+                        int gi = greedy ? first_in_group(P, ri, gg, gv, lane) : 0;
+                        resolve_row(P, b, n, greedy, c2, gi, gv, lane);
                     }
                     settle_row(P, S, 1, b, lane);
                 }
@@ -1164,7 +1308,7 @@ spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "") {
 struct Layout {
     size_t stats, reset, reset_bytes, ctrl, row_ctr, rowstate, req_ctr, req_state, res_ctr;
     size_t rowstat, partial, bmaxA, bsumA, bsumB, total;
-    int esub, nsub, ncb, nblk;
+    int esub, nsub, esb, ecb, qoff, ncb, nblk;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1172,9 +1316,13 @@ size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 bool make_layout(int B, int R, int V, spec_dtype_t dtype, Layout &L) {
     if (B < 1 || R < 1 || R > kMaxRows || V < 1 || V >= (1 << 30)) return false;
     if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return false;
-    L.esub = kSubBytes / (dtype == SPEC_BF16 ? 2 : 4);
+    const int es = dtype == SPEC_BF16 ? 2 : 4;
+    L.esub = kSubBytes / es;
     L.nsub = (V + L.esub - 1) / L.esub;
-    L.ncb = (V + kChunkB - 1) / kChunkB;
+    L.esb = (kSubBytes / (es + 4)) & ~(kBlk - 1);
+    L.ecb = L.esb * kSubPerB;
+    L.qoff = ((L.esb * es + 16) + 15) & ~15;
+    L.ncb = (V + L.ecb - 1) / L.ecb;
     L.nblk = (V + kBlk - 1) / kBlk;
     const size_t BR = static_cast<size_t>(B) * R;
     size_t off = 0;
@@ -1303,6 +1451,9 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     P.esize = dtype == SPEC_BF16 ? 2 : 4;
     P.esub = L.esub;
     P.nsub = L.nsub;
+    P.esb = L.esb;
+    P.ecb = L.ecb;
+    P.qoff = L.qoff;
     P.ncb = L.ncb;
     P.nblk = L.nblk;
     const long long rows_total = static_cast<long long>(P.B) * P.R;
