@@ -273,6 +273,8 @@ class ChainCase:
                 self._step(c, self.with_fixup)
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize(self.dev)
+        # one graph per copy (for remainders) and one graph that runs one step
+        # on every copy in turn, so the host launches one graph per ncopy steps
         self.graphs_step, self.graphs_verify = [], []
         for c in self.copies:
             g = torch.cuda.CUDAGraph()
@@ -283,13 +285,25 @@ class ChainCase:
             with torch.cuda.graph(g2):
                 self._verify(c)
             self.graphs_verify.append(g2)
+        self.round_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.round_step):
+            for c in self.copies:
+                self._step(c, self.with_fixup)
+        self.round_verify = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.round_verify):
+            for c in self.copies:
+                self._verify(c)
         torch.cuda.synchronize(self.dev)
 
     def run(self, steps, verify_only=False):
+        """Exactly `steps` steps, rotating over the copies."""
         gs = self.graphs_verify if verify_only else self.graphs_step
+        rg = self.round_verify if verify_only else self.round_step
         n = len(gs)
-        for i in range(steps):
-            gs[i % n].replay()
+        for _ in range(steps // n):
+            rg.replay()
+        for i in range(steps % n):
+            gs[i].replay()
 
     def launches_per_step(self):
         return 2 if self.with_fixup else 1

@@ -50,7 +50,7 @@
 namespace sv {
 
 // ---------------------------------------------------------------- config --
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 12;
 constexpr int kConsumerLanes = 32 * kConsumerWarps;
 constexpr int kThreads = 32 * (2 + kConsumerWarps);   // producer, epilogue, consumers
 constexpr int kStages = 8;
@@ -76,9 +76,9 @@ struct RowStat {
     double S;     // sum_j 2^((z_j - m) * c2)
 };
 
-struct Partial {  // greedy split result: max value and first 8-element group holding it
+struct Partial {  // greedy split result: max value and the row index of its first occurrence
     float v;
-    int32_t grp;
+    int32_t idx;
 };
 
 struct Params {
@@ -192,6 +192,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the thread sleep (up to hint_ns) until the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -226,6 +239,8 @@ __device__ __forceinline__ uint32_t atom_add_acqrel(uint32_t *p, uint32_t v) {
     return old;
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -248,7 +263,7 @@ __device__ __forceinline__ void set_status(const Params &P, int bits) {
 __device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
         if (*reinterpret_cast<volatile int *>(&S.abort_flag)) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *reinterpret_cast<volatile int *>(&S.abort_flag) = 1;
@@ -448,17 +463,6 @@ __device__ __forceinline__ double warp_incl_scan_d(double s, int lane) {
     return s;
 }
 
-// Warp-wide: index of the first element of 8-element group grp of row ri
-// equal to v (the row's max); the group's first element if none matches.
-__device__ int first_in_group(const Params &P, size_t ri, int grp, float v, int lane) {
-    if (grp < 0 || static_cast<long long>(grp) * 8 >= P.V) return 0;
-    const int e = grp * 8 + lane;
-    bool hit = false;
-    if (lane < 8 && e < P.V) hit = (logit_global(P, ri * P.V + e) == v);
-    unsigned m = __ballot_sync(0xffffffffu, hit);
-    return m ? grp * 8 + (__ffs(m) - 1) : grp * 8;
-}
-
 // ------------------------------------------------------------ topology --
 __device__ __forceinline__ int parent_of(const Params &P, int n) { return P.tree ? P.parent[n] : n - 1; }
 __device__ __forceinline__ int depth_of(const Params &P, int n) { return P.tree ? P.depth[n] : n; }
@@ -622,10 +626,9 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
     uint32_t *rs = S.fin_rs[slot];
     int *tok = S.fin_tok[slot];
     uint8_t *acc = S.fin_acc[slot];
-    __threadfence();
     int range_bad = 0;
     for (int i = lane; i < P.R; i += 32) {
-        rs[i] = ld_relaxed(P.rowstate + static_cast<size_t>(b) * P.R + i);
+        rs[i] = ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
         tok[i] = i > 0 ? node_token(P, b, i) : -1;
         if (i > 0 && (tok[i] < 0 || tok[i] >= P.V)) range_bad = 1;
     }
@@ -675,10 +678,7 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
         int t = sample_row(P, b, a, false, u, lane);
         if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = t;
     }
-    if (lane == 0) {
-        __threadfence();
-        st_release(P.req_state + b, decision);
-    }
+    if (lane == 0) st_release(P.req_state + b, decision);   // orders this lane's output writes
     __syncwarp();
 }
 
@@ -739,7 +739,9 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
         rsv = kResolved | __shfl_sync(0xffffffffu, acc, 0);
     }
     if (lane == 0) {
-        __threadfence();
+        // Sampled rows: the block data written by other threads of the block must
+        // be visible wherever this row state is seen.
+        if (!greedy) fence_acq_rel_gpu();
         st_release(P.rowstate + ri, rsv);
     }
     __syncwarp();
@@ -796,8 +798,8 @@ __device__ __forceinline__ void copy_geom(const uint8_t *g, int cnt, int es, uns
 template <int ES>
 __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     int it = 0;   // stages issued
-    int u_next = 0;
-    if (lane == 0) u_next = static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+    int u_next = static_cast<int>(blockIdx.x);   // first unit without a claim
+    const int claim_base = static_cast<int>(gridDim.x);
     bool aborted = false;
     unsigned long long loaded_bytes = 0;
     int a_loaded = 0, a_skipped = 0, b_loaded = 0, b_skipped = 0;
@@ -814,7 +816,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     while (!aborted) {
         int u = __shfl_sync(0xffffffffu, u_next, 0);
         if (u < 0 || u >= P.units_total) break;
-        if (lane == 0) u_next = static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+        if (lane == 0) u_next = claim_base + static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
         if (u < P.units_a) {
             // ---------------- A unit: split j of row n of request b
             const int per_node = P.B * P.ns;
@@ -966,18 +968,89 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     }
 }
 
+// Eight logits of a 16-byte (bf16) or 32-byte (fp32) register pair as floats.
 template <int ES>
-__device__ __forceinline__ float group_max(const View &v, int g, bool fast, uint32_t &bad) {
-    if (fast) {
-        if (ES == 2) return vmax8_bf16(*reinterpret_cast<const uint4 *>(v.s + 16 * g));
-        const uint4 *p = reinterpret_cast<const uint4 *>(v.s + 32 * g);
-        return vmax8_f32(p[0], p[1]);
+__device__ __forceinline__ void unpack8(const uint4 a, const uint4 c, float x[8]) {
+    if (ES == 2) {
+        x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x);
+        x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+        x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z);
+        x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+    } else {
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+        x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+        x[4] = __uint_as_float(c.x); x[5] = __uint_as_float(c.y);
+        x[6] = __uint_as_float(c.z); x[7] = __uint_as_float(c.w);
     }
-    float m = -INFINITY;
+}
+
+// Greedy step over one 8-element group already in registers (row index of its
+// first element: e_first).
+template <int ES>
+__device__ __forceinline__ void greedy_regs(const uint4 a, const uint4 c, int e_first, float &best, int &bidx,
+                                            float &mx) {
+    const float m = (ES == 2) ? vmax8_bf16(a) : vmax8_f32(a, c);
+    mx = fmax_nan(mx, m);
+    if (m > best) {
+        best = m;
+        float x[8];
+        unpack8<ES>(a, c, x);
+        int i = 7;
+#pragma unroll
+        for (int q = 7; q >= 0; --q)
+            if (x[q] == m) i = q;
+        bidx = e_first + i;
+    }
+}
+
+// Greedy step over one 8-element group: NaN-propagating max into mx, and if
+// the group's max beats `best`, the group's first element equal to it.
+template <int ES>
+__device__ __forceinline__ void group_step(const View &v, int g, int e_row0, bool fast, float &best, int &bidx,
+                                           float &mx, uint32_t &bad) {
+    if (fast) {
+        if (ES == 2) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(v.s + 16 * g);
+            const float m = vmax8_bf16(w);
+            mx = fmax_nan(mx, m);
+            if (m > best) {
+                best = m;
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                int i = 7;
+#pragma unroll
+                for (int q = 3; q >= 0; --q) {
+                    if (bf16_hi(ww[q]) == m) i = 2 * q + 1;
+                    if (bf16_lo(ww[q]) == m) i = 2 * q;
+                }
+                bidx = e_row0 + 8 * g + i;
+            }
+        } else {
+            const uint4 *p = reinterpret_cast<const uint4 *>(v.s + 32 * g);
+            const uint4 a = p[0], c = p[1];
+            const float m = vmax8_f32(a, c);
+            mx = fmax_nan(mx, m);
+            if (m > best) {
+                best = m;
+                const uint32_t ww[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+                int i = 7;
+#pragma unroll
+                for (int q = 7; q >= 0; --q)
+                    if (__uint_as_float(ww[q]) == m) i = q;
+                bidx = e_row0 + 8 * g + i;
+            }
+        }
+        return;
+    }
     const int e0 = 8 * g;
     const int nv = min(8, v.cnt - e0);
-    for (int i = 0; i < nv; ++i) m = fmax_nan(m, ld_one<ES>(v, e0 + i, bad));
-    return m;
+    for (int i = 0; i < nv; ++i) {
+        const float x = ld_one<ES>(v, e0 + i, bad);
+        mx = fmax_nan(mx, x);
+        if (x > best) {
+            best = x;
+            bidx = e_row0 + e0 + i;
+        }
+    }
 }
 
 // Loads the 8 elements of lane `lane` in block blk of a stage.
@@ -1009,7 +1082,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
     int it = 0;      // stages consumed
     int uc = 0;      // units handed to the epilogue
     float best = -INFINITY;   // greedy: running max of this lane
-    int bgrp = -1;            // greedy: first 8-element group of the row holding it
+    int bidx = -1;            // greedy: row index of its first occurrence
     float mx = -INFINITY;     // greedy: NaN-propagating max (non-finite detection)
     constexpr int kBPW = (kSubBytes / ES / kBlk + kConsumerWarps - 1) / kConsumerWarps;   // blocks per warp
     while (true) {
@@ -1033,82 +1106,143 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
         const bool fast = I.fast != 0;
         const View vz{stage + I.sh, I.gz, I.cnt, I.tail, I.sh == 0};
         const int cnt = I.cnt;
+        const int e0 = I.e0;
         const int b = I.b, n = I.n, j = I.j, last = I.last;
         const float c2 = I.c2;
-        if (kind == kA) {
-            if (c2 == 0.0f) {
-                // ---- greedy: running (max, first group) over 8-element groups
-                const int ng = (cnt + 7) >> 3;
-                const int g0 = I.e0 >> 3;
-#pragma unroll 3
-                for (int g = cw * 32 + lane; g < ng; g += kConsumerLanes) {
-                    const float m = group_max<ES>(vz, g, fast, bad);
-                    mx = fmax_nan(mx, m);
-                    if (m > best) {
-                        best = m;
-                        bgrp = g0 + g;
+        const float m_row = I.m, invS = I.invS;
+        const View vq{stage + P.qoff + I.shq, I.gq, cnt, I.tailq, I.shq == 0};
+        // Fast stages are copied to registers and released before any arithmetic,
+        // so the producer can refill the stage while this warp computes.
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[st]);
+        };
+        if (kind == kA && c2 == 0.0f) {
+            // ---- greedy: running (max, first index) over 8-element groups
+            const int ng = (cnt + 7) >> 3;
+            if (fast) {
+                constexpr int kGPL = (kSubBytes / ES / 8 + kConsumerLanes - 1) / kConsumerLanes;
+                uint4 ra[kGPL], rc[kGPL];
+#pragma unroll
+                for (int t = 0; t < kGPL; ++t) {
+                    const int g = cw * 32 + lane + t * kConsumerLanes;
+                    if (g < ng) {
+                        ra[t] = *reinterpret_cast<const uint4 *>(stage + g * 8 * ES);
+                        if (ES == 4) rc[t] = *reinterpret_cast<const uint4 *>(stage + g * 32 + 16);
                     }
                 }
+                release();
+#pragma unroll
+                for (int t = 0; t < kGPL; ++t) {
+                    const int g = cw * 32 + lane + t * kConsumerLanes;
+                    if (g < ng) greedy_regs<ES>(ra[t], rc[t], e0 + 8 * g, best, bidx, mx);
+                }
             } else {
-                // ---- sampled: per 256-element block its max M and sum of 2^((z - M) c2)
-                const int nb = (cnt + kBlk - 1) / kBlk;
-                const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + I.e0 / kBlk;
-                float x[kBPW][8];
-                int nv[kBPW];
-                float M[kBPW];
+                for (int g = cw * 32 + lane; g < ng; g += kConsumerLanes)
+                    group_step<ES>(vz, g, e0, false, best, bidx, mx, bad);
+                release();
+            }
+        } else if (kind == kA) {
+            // ---- sampled: per 256-element block its max M and sum of 2^((z - M) c2)
+            const int nb = (cnt + kBlk - 1) / kBlk;
+            const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + e0 / kBlk;
+            float x[kBPW][8];
+            int nv[kBPW];
+            float M[kBPW];
+            if (fast) {
+                uint4 ra[kBPW], rc[kBPW];
+#pragma unroll
+                for (int t = 0; t < kBPW; ++t) {
+                    const int blk = cw + t * kConsumerWarps;
+                    if (blk < nb) {
+                        const int e = blk * kBlk + lane * 8;
+                        ra[t] = *reinterpret_cast<const uint4 *>(stage + e * ES);
+                        if (ES == 4) rc[t] = *reinterpret_cast<const uint4 *>(stage + e * 4 + 16);
+                    }
+                }
+                release();
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = cw + t * kConsumerWarps;
                     nv[t] = 0;
-                    if (blk < nb) nv[t] = load_block8<ES>(vz, blk, lane, fast, x[t], bad);
-                }
-#pragma unroll
-                for (int t = 0; t < kBPW; ++t) {
-                    const int blk = cw + t * kConsumerWarps;
                     if (blk < nb) {
-                        float lm = -INFINITY;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (i < nv[t]) lm = fmax_nan(lm, x[t][i]);
-                        M[t] = warp_max_redux(lm);
+                        nv[t] = max(0, min(8, cnt - (blk * kBlk + lane * 8)));
+                        unpack8<ES>(ra[t], rc[t], x[t]);
                     }
                 }
+            } else {
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = cw + t * kConsumerWarps;
-                    if (blk < nb) {
-                        float s = 0.0f;
+                    nv[t] = 0;
+                    if (blk < nb) nv[t] = load8<ES>(vz, blk * kBlk + lane * 8, x[t], bad);
+                }
+                release();
+            }
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (i < nv[t]) s = __fadd_rn(s, w_exp(x[t][i], M[t], c2));
-                        s = warp_butterfly_sum(s);
-                        if (lane == 0) {
-                            P.bmaxA[rb + blk] = M[t];
-                            P.bsumA[rb + blk] = s;
-                        }
+            for (int t = 0; t < kBPW; ++t) {
+                const int blk = cw + t * kConsumerWarps;
+                if (blk < nb) {
+                    float lm = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i < nv[t]) lm = fmax_nan(lm, x[t][i]);
+                    M[t] = warp_max_redux(lm);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kBPW; ++t) {
+                const int blk = cw + t * kConsumerWarps;
+                if (blk < nb) {
+                    float s = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i < nv[t]) s = __fadd_rn(s, w_exp(x[t][i], M[t], c2));
+                    s = warp_butterfly_sum(s);
+                    if (lane == 0) {
+                        P.bmaxA[rb + blk] = M[t];
+                        P.bsumA[rb + blk] = s;
                     }
                 }
             }
         } else {
             // ---- residual: per 256-element block the sum of max(0, p - q)
-            const View vq{stage + P.qoff + I.shq, I.gq, cnt, I.tailq, I.shq == 0};
-            const int nb = (cnt + kBlk - 1) / kBlk;
-            const float m = I.m, invS = I.invS;
-            uint32_t qbad = 0;
-            for (int blk = cw; blk < nb; blk += kConsumerWarps) {
-                float x[8], y[8];
-                const int nvz = load_block8<ES>(vz, blk, lane, fast, x, bad);
-                load_block8<4>(vq, blk, lane, fast, y, qbad);
+            const int nb = (cnt + kBlk - 1) / kBlk;   // at most one block per warp
+            const int blk = cw;
+            float x[8], y[8];
+            int nvz = 0;
+            if (fast) {
+                uint4 za, zc, qa, qc;
+                if (blk < nb) {
+                    const int e = blk * kBlk + lane * 8;
+                    za = *reinterpret_cast<const uint4 *>(stage + e * ES);
+                    if (ES == 4) zc = *reinterpret_cast<const uint4 *>(stage + e * 4 + 16);
+                    qa = *reinterpret_cast<const uint4 *>(stage + P.qoff + e * 4);
+                    qc = *reinterpret_cast<const uint4 *>(stage + P.qoff + e * 4 + 16);
+                }
+                release();
+                if (blk < nb) {
+                    nvz = max(0, min(8, cnt - (blk * kBlk + lane * 8)));
+                    unpack8<ES>(za, zc, x);
+                    unpack8<4>(qa, qc, y);
+                }
+            } else {
+                uint32_t qbad = 0;
+                if (blk < nb) {
+                    nvz = load8<ES>(vz, blk * kBlk + lane * 8, x, bad);
+                    load8<4>(vq, blk * kBlk + lane * 8, y, qbad);
+                }
+                release();
+            }
+            if (blk < nb) {
                 float s = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (i < nvz) s = __fadd_rn(s, w_res(x[i], y[i], m, c2, invS));
+                    if (i < nvz) s = __fadd_rn(s, w_res(x[i], y[i], m_row, c2, invS));
                 s = warp_butterfly_sum(s);
-                if (lane == 0) P.bsumB[static_cast<size_t>(b) * P.nblk + I.e0 / kBlk + blk] = s;
+                if (lane == 0) P.bsumB[static_cast<size_t>(b) * P.nblk + e0 / kBlk + blk] = s;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[st]);
         ++it;
         if (last) {
             // hand the unit to the epilogue
@@ -1116,7 +1250,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             if (uc >= kResSlots && !wait_bar(P, S, &S.res_empty[slot], static_cast<uint32_t>((uc / kResSlots - 1) & 1)))
                 break;
             float v = best;
-            int g = bgrp;
+            int g = bidx;
             if (kind == kA && c2 == 0.0f) {
                 warp_cand(v, g);
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -1142,7 +1276,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             }
             ++uc;
             best = -INFINITY;
-            bgrp = -1;
+            bidx = -1;
             mx = -INFINITY;
         }
     }
@@ -1169,8 +1303,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
             if (greedy) warp_cand(v, grp);
             const size_t ri = static_cast<size_t>(b) * P.R + n;
             if (P.ns == 1) {
-                int gi = greedy ? first_in_group(P, ri, grp, v, lane) : 0;
-                resolve_row(P, b, n, greedy, c2, gi, v, lane);
+                resolve_row(P, b, n, greedy, c2, grp, v, lane);
                 settle_row(P, S, 1, b, lane);
             } else {
                 uint32_t old = 0;
@@ -1178,10 +1311,11 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
                     if (greedy) {
                         Partial pr;
                         pr.v = v;
-                        pr.grp = grp;
+                        pr.idx = grp;
                         P.partial[ri * P.ns + j] = pr;
+                    } else {
+                        fence_acq_rel_gpu();   // block data written by the consumers
                     }
-                    __threadfence();
                     old = atom_add_acqrel(P.row_ctr + ri, 1u);
                 }
                 old = __shfl_sync(0xffffffffu, old, 0) + 1u;
@@ -1193,12 +1327,11 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
                         if (greedy) {
                             for (int q = lane; q < P.ns; q += 32) {
                                 const Partial *pp = P.partial + ri * P.ns + q;
-                                cand_merge(gv, gg, __ldcg(&pp->v), __ldcg(&pp->grp));
+                                cand_merge(gv, gg, __ldcg(&pp->v), __ldcg(&pp->idx));
                             }
                             warp_cand(gv, gg);
                         }
-                        int gi = greedy ? first_in_group(P, ri, gg, gv, lane) : 0;
-                        resolve_row(P, b, n, greedy, c2, gi, gv, lane);
+                        resolve_row(P, b, n, greedy, c2, gg, gv, lane);
                     }
                     settle_row(P, S, 1, b, lane);
                 }
@@ -1207,12 +1340,12 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
             // B unit: the last chunk of a request's residual draws the token
             uint32_t old = 0;
             if (lane == 0) {
-                __threadfence();
+                fence_acq_rel_gpu();   // residual block sums written by the consumers
                 old = atom_add_acqrel(P.res_ctr + b, 1u);
             }
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == static_cast<uint32_t>(P.ncb - 1)) {
-                __threadfence();
+                fence_acq_rel_gpu();
                 double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + n));
                 int t = sample_row(P, b, n, true, u, lane);
                 if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + n] = t;
@@ -1223,7 +1356,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
 
 // --------------------------------------------------------------- kernel --
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 1) verify_kernel(const __grid_constant__ Params P) {
+__global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     uint8_t *ring = smem_raw + ((sizeof(Smem) + 127) & ~static_cast<size_t>(127));
@@ -1265,15 +1398,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const __grid_consta
                     if (globaltimer() - t0 > kWaitLimitNs) break;
             }
         }
-        __threadfence();
         uint32_t old = atom_add_acqrel(P.ctrl + 1, 1u);
         S.last_flag = (old == gridDim.x - 1);
     }
     __syncthreads();
     if (S.last_flag) {
-        __threadfence();
+        // every other block has finished with the counters: clear them for the next call
         for (uint32_t i = tid; i < P.reset_words; i += kThreads) P.reset_base[i] = 0u;
-        __threadfence();
     }
 }
 
@@ -1319,7 +1450,8 @@ bool make_layout(int B, int R, int V, spec_dtype_t dtype, Layout &L) {
     const int es = dtype == SPEC_BF16 ? 2 : 4;
     L.esub = kSubBytes / es;
     L.nsub = (V + L.esub - 1) / L.esub;
-    L.esb = (kSubBytes / (es + 4)) & ~(kBlk - 1);
+    L.esb = kConsumerWarps * kBlk;   // one 256-element block per consumer warp
+    static_assert(kConsumerWarps * kBlk * (4 + 4) + 64 <= kSubBytes + 128, "B stage does not fit");
     L.ecb = L.esb * kSubPerB;
     L.qoff = ((L.esb * es + 16) + 15) & ~15;
     L.ncb = (V + L.ecb - 1) / L.ecb;
@@ -1400,8 +1532,15 @@ spec_status_t device_info(DeviceInfo *&out) {
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[1], verify_kernel<4>, kThreads,
                                                               kSmemBytes);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel setup: %s", cudaGetErrorString(e));
-        if (D.blocks_per_sm[0] < 1 || D.blocks_per_sm[1] < 1)
-            return fail(SPEC_ERR_UNSUPPORTED, "the verify kernel does not fit on this device%s");
+        if (D.blocks_per_sm[0] < 1 || D.blocks_per_sm[1] < 1) {
+            cudaFuncAttributes fa;
+            memset(&fa, 0, sizeof fa);
+            cudaFuncGetAttributes(&fa, verify_kernel<2>);
+            char buf[200];
+            snprintf(buf, sizeof buf, " (%d registers, max %d threads, %zu B static + %zu B dynamic shared, %d threads)",
+                     fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes, kSmemBytes, kThreads);
+            return fail(SPEC_ERR_UNSUPPORTED, "the verify kernel does not fit on this device%s", buf);
+        }
         D.ok = 1;
     }
     out = &D;
