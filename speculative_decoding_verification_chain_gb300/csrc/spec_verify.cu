@@ -76,9 +76,10 @@ struct RowStat {
     double S;     // sum_j 2^((z_j - m) * c2)
 };
 
-struct Partial {  // greedy split result: max value and the row index of its first occurrence
-    float v;
-    int32_t idx;
+struct Partial {  // result of one split of a row
+    float v;      // greedy: max value; sampled: max logit m
+    int32_t idx;  // greedy: row index of the first occurrence of v
+    double s;     // sampled: sum of 2^((z - m) c2) over the split
 };
 
 struct Params {
@@ -135,6 +136,8 @@ struct StageInfo {
     int shq, tailq;      // q (B)
     float c2;            // log2(e)/T, 0 for greedy
     float m, invS;       // row statistics (B)
+    int xtok;            // sampled A, last stage: token of node n+1 (-1 if none or out of range)
+    float zx, qx, ux;    // ... and its logit, its draft probability, its accept uniform
     const uint8_t *gz;
     const uint8_t *gq;
 };
@@ -142,8 +145,11 @@ struct StageInfo {
 struct ResSlot {
     int kind, b, n, j;
     float c2;
-    float v[kConsumerWarps];
-    int idx[kConsumerWarps];
+    int xtok;
+    float zx, qx, ux;
+    float v[kConsumerWarps];    // greedy: lane-reduced max; sampled: warp max M_w
+    int idx[kConsumerWarps];    // greedy: first index of the max
+    float s[kConsumerWarps];    // sampled: warp sum of 2^((z - M_w) c2)
 };
 
 struct Smem {
@@ -501,47 +507,54 @@ __device__ __forceinline__ double block_weight(const BlockSource &S, int beta) {
 
 // Warp-wide: total weight and the block holding t = u * total.  Returns the
 // total; beta/base receive the block and the weight before it (all lanes).
+// Lane l owns blocks [l*per, (l+1)*per); the lane whose range holds t is then
+// scanned by the whole warp, one block per lane.
 __device__ double locate_block(const BlockSource &S, int nblk, double u, int lane, int &beta, double &base) {
     const int per = (nblk + 31) / 32;
     const int lo = lane * per;
     const int hi = min(nblk, lo + per);
     double s = 0.0;
     for (int i = lo; i < hi; ++i) s += block_weight(S, i);
-    double incl = warp_incl_scan_d(s, lane);
-    double excl = incl - s;
-    double total = __shfl_sync(0xffffffffu, incl, 31);
-    double t = u * total;
-    unsigned over = __ballot_sync(0xffffffffu, incl > t && hi > lo);
-    unsigned nonzero = __ballot_sync(0xffffffffu, s > 0.0);
-    int L;
-    if (over) L = __ffs(over) - 1;
-    else L = nonzero ? 31 - __clz(nonzero) : 0;
+    const double incl = warp_incl_scan_d(s, lane);
+    const double excl = incl - s;
+    const double total = __shfl_sync(0xffffffffu, incl, 31);
+    const double t = u * total;
+    const unsigned over = __ballot_sync(0xffffffffu, incl > t && hi > lo);
+    const unsigned nonzero = __ballot_sync(0xffffffffu, s > 0.0);
+    const int L = over ? (__ffs(over) - 1) : (nonzero ? 31 - __clz(nonzero) : 0);
+    const int Llo = L * per;
+    const int Lhi = min(nblk, Llo + per);
+    const double Lexcl = __shfl_sync(0xffffffffu, excl, L);
     int bsel = -1;
-    double bbase = 0.0;
-    if (lane == L) {
-        double run = excl;
-        int last_pos = -1;
-        double last_base = excl;
-        for (int i = lo; i < hi; ++i) {
-            double w = block_weight(S, i);
-            if (w > 0.0) {
-                last_pos = i;
-                last_base = run;
+    double bbase = Lexcl;
+    int last_sel = -1;            // last block with weight seen (clamp when rounding leaves t past the end)
+    double last_base = Lexcl;
+    for (int c0 = Llo; c0 < Lhi && bsel < 0; c0 += 32) {
+        const int i = c0 + lane;
+        const double w = (i < Lhi) ? block_weight(S, i) : 0.0;
+        const double wi = warp_incl_scan_d(w, lane);
+        const double run = bbase + (wi - w);
+        const unsigned cross = __ballot_sync(0xffffffffu, i < Lhi && w > 0.0 && run + w > t);
+        const unsigned pos = __ballot_sync(0xffffffffu, i < Lhi && w > 0.0);
+        if (cross) {
+            const int q = __ffs(cross) - 1;
+            bsel = c0 + q;
+            bbase = __shfl_sync(0xffffffffu, run, q);
+        } else {
+            if (pos) {
+                const int q = 31 - __clz(pos);
+                last_sel = c0 + q;
+                last_base = __shfl_sync(0xffffffffu, run, q);
             }
-            if (run + w > t && w > 0.0) {
-                bsel = i;
-                bbase = run;
-                break;
-            }
-            run += w;
-        }
-        if (bsel < 0) {
-            bsel = last_pos >= 0 ? last_pos : lo;
-            bbase = last_base;
+            bbase += __shfl_sync(0xffffffffu, wi, 31);
         }
     }
-    beta = __shfl_sync(0xffffffffu, bsel, L);
-    base = __shfl_sync(0xffffffffu, bbase, L);
+    if (bsel < 0) {
+        bsel = last_sel >= 0 ? last_sel : (Llo < nblk ? Llo : 0);
+        bbase = last_sel >= 0 ? last_base : Lexcl;
+    }
+    beta = bsel;
+    base = bbase;
     return total;
 }
 
@@ -690,58 +703,41 @@ __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) 
     if (old == static_cast<uint32_t>(P.R - 1)) finalize_request(P, S, slot, b, lane);
 }
 
-// Warp-wide: resolve row n of request b from its finished splits.  Greedy:
-// (v, idx) is the whole row's argmax.  Sampled: m and S from the block data,
-// then the accept test of child n+1.
-__device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, int lane) {
+// Warp-wide: resolve row n of request b once all its splits are in.
+// Greedy: gidx is the row's argmax (first index), gmax its value.  Sampled:
+// (m, Srow) are the row statistics and (xtok, zx, qx, ux) the operands of the
+// accept test of node n+1 (xtok < 0: no child, or its token is out of range).
+__device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
+                            double Srow, int xtok, float zx, float qx, float ux, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
-    uint32_t rsv;
-    if (greedy) {
-        int g = (gidx < 0 || gidx >= P.V) ? 0 : gidx;
-        rsv = kResolved | static_cast<uint32_t>(g);
-        if (lane == 0 && !isfinite(gmax)) set_status(P, SPEC_STATUS_NONFINITE);
-    } else {
-        const float *bm = P.bmaxA + ri * P.nblk;
-        const float *bs = P.bsumA + ri * P.nblk;
-        float m = -INFINITY;
-        for (int i = lane; i < P.nblk; i += 32) m = fmaxf(m, __ldcg(bm + i));
-        m = warp_max(m);
-        double Ssum = 0.0;
-        for (int i = lane; i < P.nblk; i += 32)
-            Ssum += static_cast<double>(__ldcg(bs + i)) *
-                    static_cast<double>(ex2(__fmul_rn(__fsub_rn(__ldcg(bm + i), m), c2)));
-        Ssum = warp_sum_d(Ssum);
-        uint32_t acc = 0;
-        if (lane == 0) {
-            if (!isfinite(m) || !isfinite(Ssum)) set_status(P, SPEC_STATUS_NONFINITE);
+    if (lane == 0) {
+        uint32_t rsv;
+        if (greedy) {
+            const int g = (gidx < 0 || gidx >= P.V) ? 0 : gidx;
+            rsv = kResolved | static_cast<uint32_t>(g);
+            if (!isfinite(gmax)) set_status(P, SPEC_STATUS_NONFINITE);
+        } else {
+            if (!isfinite(m) || !isfinite(Srow)) set_status(P, SPEC_STATUS_NONFINITE);
             RowStat st;
             st.m = m;
             st.pad = 0.0f;
-            st.S = Ssum;
+            st.S = Srow;
             P.rowstat[ri] = st;
+            uint32_t acc = 0;
             if (n < P.R - 1) {
-                int x = node_token(P, b, n + 1);
-                if (x < 0 || x >= P.V) {
+                if (xtok < 0) {
                     set_status(P, SPEC_STATUS_TOKEN_RANGE);
+                } else if (qx == 0.0f) {
+                    acc = 1;
                 } else {
-                    float zx = logit_global(P, ri * P.V + x);
-                    double ph = static_cast<double>(ex2(__fmul_rn(__fsub_rn(zx, m), c2))) / Ssum;
-                    float qh = __ldg(P.q + (static_cast<size_t>(b) * (P.R - 1) + n) * P.V + x);
-                    if (qh == 0.0f) {
-                        acc = 1;
-                    } else {
-                        double ua = static_cast<double>(__ldg(P.u_accept + static_cast<size_t>(b) * (P.R - 1) + n));
-                        acc = ua < ph / static_cast<double>(qh);
-                    }
+                    const double ph = static_cast<double>(ex2(__fmul_rn(__fsub_rn(zx, m), c2))) / Srow;
+                    acc = static_cast<double>(ux) < ph / static_cast<double>(qx);
                 }
             }
+            rsv = kResolved | acc;
+            // the block data the consumers wrote must be visible wherever this state is seen
+            fence_acq_rel_gpu();
         }
-        rsv = kResolved | __shfl_sync(0xffffffffu, acc, 0);
-    }
-    if (lane == 0) {
-        // Sampled rows: the block data written by other threads of the block must
-        // be visible wherever this row state is seen.
-        if (!greedy) fence_acq_rel_gpu();
         st_release(P.rowstate + ri, rsv);
     }
     __syncwarp();
@@ -842,6 +838,19 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             }
             ++a_loaded;
             const size_t rowe = (static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V);
+            // accept-test operands of node n+1 (sampled rows): loaded now, used by the
+            // epilogue after the whole row has streamed
+            int xtok = -1;
+            float zx = 0.0f, qx = 0.0f, ux = 0.0f;
+            if (lane == 0 && !greedy && n < P.R - 1) {
+                const int x = node_token(P, b, n + 1);
+                ux = __ldg(P.u_accept + static_cast<size_t>(b) * (P.R - 1) + n);
+                if (x >= 0 && x < P.V) {
+                    xtok = x;
+                    zx = logit_global(P, rowe + x);
+                    qx = __ldg(P.q + (static_cast<size_t>(b) * (P.R - 1) + n) * P.V + x);
+                }
+            }
             for (int s = s0; s < s1; ++s) {
                 int st;
                 if (!acquire_stage(st)) {
@@ -858,6 +867,12 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     I.e0 = s * P.esub;
                     I.cnt = min(P.esub, P.V - I.e0);
                     I.c2 = c2;
+                    I.xtok = xtok;
+                    if (I.last) {
+                        I.zx = zx;
+                        I.qx = qx;
+                        I.ux = ux;
+                    }
                     I.gz = P.logits + (rowe + I.e0) * ES;
                     const uint8_t *src;
                     uint32_t nb;
@@ -1084,6 +1099,8 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
     float best = -INFINITY;   // greedy: running max of this lane
     int bidx = -1;            // greedy: row index of its first occurrence
     float mx = -INFINITY;     // greedy: NaN-propagating max (non-finite detection)
+    float Mw = -INFINITY;     // sampled: running max of this warp's blocks
+    float Sw = 0.0f, Sc = 0.0f;   // sampled: compensated sum of 2^((z - Mw) c2)
     constexpr int kBPW = (kSubBytes / ES / kBlk + kConsumerWarps - 1) / kConsumerWarps;   // blocks per warp
     while (true) {
         const int st = it % kStages;
@@ -1110,6 +1127,8 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
         const int b = I.b, n = I.n, j = I.j, last = I.last;
         const float c2 = I.c2;
         const float m_row = I.m, invS = I.invS;
+        const int xtok = I.xtok;
+        const float zx = I.zx, qx = I.qx, ux = I.ux;
         const View vq{stage + P.qoff + I.shq, I.gq, cnt, I.tailq, I.shq == 0};
         // Fast stages are copied to registers and released before any arithmetic,
         // so the producer can refill the stage while this warp computes.
@@ -1146,9 +1165,29 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             // ---- sampled: per 256-element block its max M and sum of 2^((z - M) c2)
             const int nb = (cnt + kBlk - 1) / kBlk;
             const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + e0 / kBlk;
-            float x[kBPW][8];
-            int nv[kBPW];
-            float M[kBPW];
+            // Fold one finished block (max M, canonical sum s in lane 0) into the
+            // block data and this warp's running statistics.
+            auto fold = [&](int blk, float M, float s) {
+                if (lane == 0) {
+                    P.bmaxA[rb + blk] = M;
+                    P.bsumA[rb + blk] = s;
+                }
+                const float sb = __shfl_sync(0xffffffffu, s, 0);
+                float add;
+                if (M > Mw) {
+                    const float f = ex2(__fmul_rn(__fsub_rn(Mw, M), c2));
+                    Sw = __fmul_rn(Sw, f);
+                    Sc = __fmul_rn(Sc, f);
+                    Mw = M;
+                    add = sb;
+                } else {
+                    add = __fmul_rn(sb, ex2(__fmul_rn(__fsub_rn(M, Mw), c2)));
+                }
+                const float tsum = __fadd_rn(Sw, add);   // Neumaier compensation
+                if (fabsf(Sw) >= fabsf(add)) Sc = __fadd_rn(Sc, __fadd_rn(__fsub_rn(Sw, tsum), add));
+                else Sc = __fadd_rn(Sc, __fadd_rn(__fsub_rn(add, tsum), Sw));
+                Sw = tsum;
+            };
             if (fast) {
                 uint4 ra[kBPW], rc[kBPW];
 #pragma unroll
@@ -1161,49 +1200,46 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                     }
                 }
                 release();
+                // cnt is a multiple of 8 here: a lane's 8 elements are all valid or all past the end
+                float M[kBPW], sm[kBPW];
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = cw + t * kConsumerWarps;
-                    nv[t] = 0;
                     if (blk < nb) {
-                        nv[t] = max(0, min(8, cnt - (blk * kBlk + lane * 8)));
-                        unpack8<ES>(ra[t], rc[t], x[t]);
+                        const bool valid = blk * kBlk + lane * 8 < cnt;
+                        const float lm = valid ? (ES == 2 ? vmax8_bf16(ra[t]) : vmax8_f32(ra[t], rc[t])) : -INFINITY;
+                        M[t] = warp_max_redux(lm);
                     }
                 }
-            } else {
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = cw + t * kConsumerWarps;
-                    nv[t] = 0;
-                    if (blk < nb) nv[t] = load8<ES>(vz, blk * kBlk + lane * 8, x[t], bad);
+                    if (blk < nb) {
+                        float s = 0.0f;
+                        if (blk * kBlk + lane * 8 < cnt) {
+                            float x[8];
+                            unpack8<ES>(ra[t], rc[t], x);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) s = __fadd_rn(s, w_exp(x[i], M[t], c2));
+                        }
+                        sm[t] = warp_butterfly_sum(s);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kBPW; ++t)
+                    if (cw + t * kConsumerWarps < nb) fold(cw + t * kConsumerWarps, M[t], sm[t]);
+            } else {
+                for (int blk = cw; blk < nb; blk += kConsumerWarps) {
+                    float x[8];
+                    const int nv = load8<ES>(vz, blk * kBlk + lane * 8, x, bad);
+                    float lm = -INFINITY;
+                    for (int i = 0; i < nv; ++i) lm = fmax_nan(lm, x[i]);
+                    const float M = warp_max_redux(lm);
+                    float s = 0.0f;
+                    for (int i = 0; i < nv; ++i) s = __fadd_rn(s, w_exp(x[i], M, c2));
+                    fold(blk, M, warp_butterfly_sum(s));
                 }
                 release();
-            }
-#pragma unroll
-            for (int t = 0; t < kBPW; ++t) {
-                const int blk = cw + t * kConsumerWarps;
-                if (blk < nb) {
-                    float lm = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < nv[t]) lm = fmax_nan(lm, x[t][i]);
-                    M[t] = warp_max_redux(lm);
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < kBPW; ++t) {
-                const int blk = cw + t * kConsumerWarps;
-                if (blk < nb) {
-                    float s = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < nv[t]) s = __fadd_rn(s, w_exp(x[t][i], M[t], c2));
-                    s = warp_butterfly_sum(s);
-                    if (lane == 0) {
-                        P.bmaxA[rb + blk] = M[t];
-                        P.bsumA[rb + blk] = s;
-                    }
-                }
             }
         } else {
             // ---- residual: per 256-element block the sum of max(0, p - q)
@@ -1263,14 +1299,23 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             }
             if (lane == 0) {
                 ResSlot &R = S.res[slot];
-                R.v[cw] = v;
-                R.idx[cw] = g;
+                if (kind == kA && c2 != 0.0f) {
+                    R.v[cw] = Mw;
+                    R.s[cw] = __fadd_rn(Sw, Sc);
+                } else {
+                    R.v[cw] = v;
+                    R.idx[cw] = g;
+                }
                 if (cw == 0) {
                     R.kind = kind;
                     R.b = b;
                     R.n = n;
                     R.j = j;
                     R.c2 = c2;
+                    R.xtok = xtok;
+                    R.zx = zx;
+                    R.qx = qx;
+                    R.ux = ux;
                 }
                 mbar_arrive(&S.res_full[slot]);
             }
@@ -1278,6 +1323,9 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             best = -INFINITY;
             bidx = -1;
             mx = -INFINITY;
+            Mw = -INFINITY;
+            Sw = 0.0f;
+            Sc = 0.0f;
         }
     }
     if (lane == 0 && cw == 0) S.consumed = it;
@@ -1293,45 +1341,71 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
         if (kind == kEnd) break;
         const int b = R.b, n = R.n, j = R.j;
         const float c2 = R.c2;
+        const int xtok = R.xtok;
+        const float zx = R.zx, qx = R.qx, ux = R.ux;
         float v = lane < kConsumerWarps ? R.v[lane] : -INFINITY;
         int grp = lane < kConsumerWarps ? R.idx[lane] : -1;
+        const float sw = lane < kConsumerWarps ? R.s[lane] : 0.0f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.res_empty[slot]);
         ++uc;
         if (kind == kA) {
             const bool greedy = (c2 == 0.0f);
-            if (greedy) warp_cand(v, grp);
+            float um = 0.0f;
+            double uS = 0.0;
+            if (greedy) {
+                warp_cand(v, grp);
+            } else {
+                // combine the consumer warps' (M_w, S_w) into the unit's (m, S)
+                um = warp_max(v);
+                double t = 0.0;
+                if (lane < kConsumerWarps && sw != 0.0f)
+                    t = static_cast<double>(sw) * static_cast<double>(ex2(__fmul_rn(__fsub_rn(v, um), c2)));
+                uS = warp_sum_d(t);
+            }
             const size_t ri = static_cast<size_t>(b) * P.R + n;
             if (P.ns == 1) {
-                resolve_row(P, b, n, greedy, c2, grp, v, lane);
+                resolve_row(P, b, n, greedy, c2, grp, v, um, uS, xtok, zx, qx, ux, lane);
                 settle_row(P, S, 1, b, lane);
             } else {
                 uint32_t old = 0;
                 if (lane == 0) {
-                    if (greedy) {
-                        Partial pr;
-                        pr.v = v;
-                        pr.idx = grp;
-                        P.partial[ri * P.ns + j] = pr;
-                    } else {
-                        fence_acq_rel_gpu();   // block data written by the consumers
-                    }
+                    Partial pr;
+                    pr.v = greedy ? v : um;
+                    pr.idx = grp;
+                    pr.s = uS;
+                    P.partial[ri * P.ns + j] = pr;
+                    if (!greedy) fence_acq_rel_gpu();   // block data written by the consumers
                     old = atom_add_acqrel(P.row_ctr + ri, 1u);
                 }
                 old = __shfl_sync(0xffffffffu, old, 0) + 1u;
                 if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) {
                     if ((old >> 16) == 0u) {
-                        // every split loaded: resolve the row
+                        // every split loaded: combine the splits and resolve the row
                         float gv = -INFINITY;
                         int gg = -1;
+                        float rm = 0.0f;
+                        double rS = 0.0;
                         if (greedy) {
                             for (int q = lane; q < P.ns; q += 32) {
                                 const Partial *pp = P.partial + ri * P.ns + q;
                                 cand_merge(gv, gg, __ldcg(&pp->v), __ldcg(&pp->idx));
                             }
                             warp_cand(gv, gg);
+                        } else {
+                            float lm = -INFINITY;
+                            for (int q = lane; q < P.ns; q += 32) lm = fmaxf(lm, __ldcg(&P.partial[ri * P.ns + q].v));
+                            rm = warp_max(lm);
+                            double t = 0.0;
+                            for (int q = lane; q < P.ns; q += 32) {
+                                const Partial *pp = P.partial + ri * P.ns + q;
+                                const double ps = __ldcg(&pp->s);
+                                if (ps != 0.0)
+                                    t += ps * static_cast<double>(ex2(__fmul_rn(__fsub_rn(__ldcg(&pp->v), rm), c2)));
+                            }
+                            rS = warp_sum_d(t);
                         }
-                        resolve_row(P, b, n, greedy, c2, gg, gv, lane);
+                        resolve_row(P, b, n, greedy, c2, gg, gv, rm, rS, xtok, zx, qx, ux, lane);
                     }
                     settle_row(P, S, 1, b, lane);
                 }
