@@ -126,15 +126,16 @@ struct Params {
     uint8_t depth[kMaxRows];
 };
 
-struct StageInfo {
-    int kind;
-    int last;            // last stage of its unit
-    int fast;            // aligned, every element in shared memory, whole 8-element groups
+// Stage descriptor.  The first 16 bytes are what every consumer reads per stage.
+struct __align__(16) StageInfo {
+    int flags;           // kind | last << 4 (last stage of its unit) | fast << 5
+                         // (aligned, every element in shared memory, whole 8-element groups)
+    int cnt;             // element count
+    int e0;              // element offset within the row
+    float c2;            // log2(e)/T, 0 for greedy
     int b, n, j;         // request, row, split (A) / chunk (B)
-    int e0, cnt;         // element offset within the row, element count
     int sh, tail;        // z: byte shift of element 0; elements [tail, cnt) come from global
     int shq, tailq;      // q (B)
-    float c2;            // log2(e)/T, 0 for greedy
     float m, invS;       // row statistics (B)
     int xtok;            // sampled A, last stage: token of node n+1 (-1 if none or out of range)
     float zx, qx, ux;    // ... and its logit, its draft probability, its accept uniform
@@ -233,6 +234,10 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
@@ -635,6 +640,7 @@ __device__ int sample_row(const Params &P, int b, int row, bool residual, double
 // Warp-wide.  Every row of request b is settled: walk the tree, write the
 // outputs, publish the decision (and draw the bonus token of a sampled
 // request that accepted every draft).
+template <bool SMP>
 __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int lane) {
     uint32_t *rs = S.fin_rs[slot];
     int *tok = S.fin_tok[slot];
@@ -647,7 +653,7 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
     }
     if (__any_sync(0xffffffffu, range_bad) && lane == 0) set_status(P, SPEC_STATUS_TOKEN_RANGE);
     __syncwarp();
-    const bool greedy = is_greedy(P, b);
+    const bool greedy = !SMP || is_greedy(P, b);
     int bonus = 0;
     uint32_t decision = kDecided;
     if (lane == 0) {
@@ -685,34 +691,41 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
         P.out_count[b] = P.tree ? d + 1 : d;
     }
     bonus = __shfl_sync(0xffffffffu, bonus, 0);
-    if (bonus) {
+    if (SMP && bonus) {
         const int a = P.R - 1;
         double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + a));
         int t = sample_row(P, b, a, false, u, lane);
         if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = t;
     }
-    if (lane == 0) st_release(P.req_state + b, decision);   // orders this lane's output writes
+    if (lane == 0) {
+        // Residual units read the decision and then this request's row data:
+        // publish with release.  Without residual units nobody waits on it.
+        if (P.units_total > P.units_a) st_release(P.req_state + b, decision);
+        else st_relaxed(P.req_state + b, decision);
+    }
     __syncwarp();
 }
 
 // One more row of request b is settled (resolved or known dead).
+template <bool SMP>
 __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) {
     uint32_t old = 0;
     if (lane == 0) old = atom_add_acqrel(P.req_ctr + b, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == static_cast<uint32_t>(P.R - 1)) finalize_request(P, S, slot, b, lane);
+    if (old == static_cast<uint32_t>(P.R - 1)) finalize_request<SMP>(P, S, slot, b, lane);
 }
 
 // Warp-wide: resolve row n of request b once all its splits are in.
 // Greedy: gidx is the row's argmax (first index), gmax its value.  Sampled:
 // (m, Srow) are the row statistics and (xtok, zx, qx, ux) the operands of the
 // accept test of node n+1 (xtok < 0: no child, or its token is out of range).
+template <bool SMP>
 __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
                             double Srow, int xtok, float zx, float qx, float ux, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
     if (lane == 0) {
         uint32_t rsv;
-        if (greedy) {
+        if (!SMP || greedy) {
             const int g = (gidx < 0 || gidx >= P.V) ? 0 : gidx;
             rsv = kResolved | static_cast<uint32_t>(g);
             if (!isfinite(gmax)) set_status(P, SPEC_STATUS_NONFINITE);
@@ -738,7 +751,9 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
             // the block data the consumers wrote must be visible wherever this state is seen
             fence_acq_rel_gpu();
         }
-        st_release(P.rowstate + ri, rsv);
+        // Relaxed: skip checks need only the value, and the settle atomic that
+        // follows (acq_rel, same thread) publishes it to the request's finaliser.
+        st_relaxed(P.rowstate + ri, rsv);
     }
     __syncwarp();
 }
@@ -791,7 +806,7 @@ __device__ __forceinline__ void copy_geom(const uint8_t *g, int cnt, int es, uns
     src = reinterpret_cast<const uint8_t *>(lo);
 }
 
-template <int ES>
+template <int ES, bool SMP>
 __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     int it = 0;   // stages issued
     int u_next = static_cast<int>(blockIdx.x);   // first unit without a claim
@@ -820,19 +835,19 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const int rem = u - n * per_node;
             const int b = rem / P.ns;
             const int j = rem - b * P.ns;
-            const bool greedy = is_greedy(P, b);
+            const bool greedy = !SMP || is_greedy(P, b);
             const float c2 = greedy ? 0.0f : kLog2e / __ldg(P.temperature + b);
             const int s0 = j * P.sps;
             const int s1 = min(P.nsub, s0 + P.sps);
             if (node_dead(P, b, n, greedy, lane)) {
                 ++a_skipped;
                 if (P.ns == 1) {
-                    settle_row(P, S, 0, b, lane);
+                    settle_row<SMP>(P, S, 0, b, lane);
                 } else {
                     uint32_t old = 0;
                     if (lane == 0) old = atom_add_acqrel(P.row_ctr + static_cast<size_t>(b) * P.R + n, kSkipInc);
                     old = __shfl_sync(0xffffffffu, old, 0) + kSkipInc;
-                    if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) settle_row(P, S, 0, b, lane);
+                    if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) settle_row<SMP>(P, S, 0, b, lane);
                 }
                 continue;
             }
@@ -842,7 +857,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             // epilogue after the whole row has streamed
             int xtok = -1;
             float zx = 0.0f, qx = 0.0f, ux = 0.0f;
-            if (lane == 0 && !greedy && n < P.R - 1) {
+            if (SMP && lane == 0 && !greedy && n < P.R - 1) {
                 const int x = node_token(P, b, n + 1);
                 ux = __ldg(P.u_accept + static_cast<size_t>(b) * (P.R - 1) + n);
                 if (x >= 0 && x < P.V) {
@@ -859,8 +874,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 }
                 if (lane == 0) {
                     StageInfo &I = S.info[st];
-                    I.kind = kA;
-                    I.last = (s == s1 - 1);
+                    const int last = (s == s1 - 1);
                     I.b = b;
                     I.n = n;
                     I.j = j;
@@ -868,7 +882,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     I.cnt = min(P.esub, P.V - I.e0);
                     I.c2 = c2;
                     I.xtok = xtok;
-                    if (I.last) {
+                    if (last) {
                         I.zx = zx;
                         I.qx = qx;
                         I.ux = ux;
@@ -877,7 +891,8 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     const uint8_t *src;
                     uint32_t nb;
                     copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
-                    I.fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
+                    const int fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
+                    I.flags = kA | (last << 4) | (fast << 5);
                     loaded_bytes += nb;
                     fence_proxy_async();
                     if (nb) {
@@ -889,7 +904,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 }
                 ++it;
             }
-        } else {
+        } else if (SMP) {
             // ---------------- B unit: chunk c of the rejected row of request b
             const int v = u - P.units_a;
             const int b = v / P.ncb;
@@ -930,8 +945,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 }
                 if (lane == 0) {
                     StageInfo &I = S.info[st];
-                    I.kind = kB;
-                    I.last = (e + P.esb >= e_end);
+                    const int last = (e + P.esb >= e_end);
                     I.b = b;
                     I.n = a;
                     I.j = c;
@@ -946,7 +960,8 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     uint32_t nz, nq;
                     copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, sz, nz);
                     copy_geom(I.gq, I.cnt, 4, P.q_end, I.shq, I.tailq, sq, nq);
-                    I.fast = (I.sh == 0 && I.tail == I.cnt && I.shq == 0 && I.tailq == I.cnt && (I.cnt & 7) == 0);
+                    const int fast = (I.sh == 0 && I.tail == I.cnt && I.shq == 0 && I.tailq == I.cnt && (I.cnt & 7) == 0);
+                    I.flags = kB | (last << 4) | (fast << 5);
                     loaded_bytes += nz + nq;
                     fence_proxy_async();
                     uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
@@ -967,7 +982,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
         int st;
         if (acquire_stage(st)) {
             if (lane == 0) {
-                S.info[st].kind = kEnd;
+                S.info[st].flags = kEnd;
                 mbar_arrive(&S.full[st]);
             }
             ++it;
@@ -981,6 +996,24 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
         if (b_skipped) atomicAdd(P.stats + 3, static_cast<unsigned long long>(b_skipped));
         if (loaded_bytes) atomicAdd(P.stats + 4, loaded_bytes);
     }
+}
+
+// Does either bf16 half of a exceed the matching half of b?  (NaN: no.)
+__device__ __forceinline__ bool bf16x2_any_gt(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("{\n\t.reg .pred p, q;\n\t"
+        "setp.gt.bf16x2 p|q, %1, %2;\n\t"
+        "or.pred p, p, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(b));
+    return r != 0;
+}
+
+// A bf16 value (given as its exact float) in both halves of a word.
+__device__ __forceinline__ uint32_t bf16_pair(float m) {
+    const uint32_t h = __float_as_uint(m) >> 16;
+    return h | (h << 16);
 }
 
 // Eight logits of a 16-byte (bf16) or 32-byte (fp32) register pair as floats.
@@ -1092,13 +1125,15 @@ __device__ __forceinline__ int load_block8(const View &v, int blk, int lane, boo
     return load8<ES>(v, e, x, bad);
 }
 
-template <int ES>
+template <int ES, bool SMP>
 __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, int lane, uint32_t &bad) {
     int it = 0;      // stages consumed
     int uc = 0;      // units handed to the epilogue
     float best = -INFINITY;   // greedy: running max of this lane
     int bidx = -1;            // greedy: row index of its first occurrence
     float mx = -INFINITY;     // greedy: NaN-propagating max (non-finite detection)
+    uint32_t best2 = 0xff80ff80u;   // greedy bf16: best in both halves (starts at -inf)
+    uint32_t pmx = 0xff80ff80u;     // greedy bf16: packed NaN-propagating max
     float Mw = -INFINITY;     // sampled: running max of this warp's blocks
     float Sw = 0.0f, Sc = 0.0f;   // sampled: compensated sum of 2^((z - Mw) c2)
     constexpr int kBPW = (kSubBytes / ES / kBlk + kConsumerWarps - 1) / kConsumerWarps;   // blocks per warp
@@ -1106,7 +1141,8 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
         const int st = it % kStages;
         if (!wait_bar(P, S, &S.full[st], static_cast<uint32_t>((it / kStages) & 1))) break;
         const StageInfo &I = S.info[st];
-        const int kind = I.kind;
+        const uint4 hot = *reinterpret_cast<const uint4 *>(&S.info[st]);
+        const int kind = static_cast<int>(hot.x & 15u);
         if (kind == kEnd) {
             // forward the end marker to the epilogue
             const int slot = uc % kResSlots;
@@ -1120,16 +1156,23 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             break;
         }
         const uint8_t *stage = ring + static_cast<size_t>(st) * kStageBytes;
-        const bool fast = I.fast != 0;
-        const View vz{stage + I.sh, I.gz, I.cnt, I.tail, I.sh == 0};
-        const int cnt = I.cnt;
-        const int e0 = I.e0;
-        const int b = I.b, n = I.n, j = I.j, last = I.last;
-        const float c2 = I.c2;
-        const float m_row = I.m, invS = I.invS;
-        const int xtok = I.xtok;
-        const float zx = I.zx, qx = I.qx, ux = I.ux;
-        const View vq{stage + P.qoff + I.shq, I.gq, cnt, I.tailq, I.shq == 0};
+        const int last = static_cast<int>((hot.x >> 4) & 1u);
+        const bool fast = ((hot.x >> 5) & 1u) != 0;
+        const int cnt = static_cast<int>(hot.y);
+        const int e0 = static_cast<int>(hot.z);
+        const float c2 = SMP ? __uint_as_float(hot.w) : 0.0f;
+        // unit identity, needed at the end of a unit (read before the stage is released)
+        int b = 0, n = 0, j = 0, xtok = -1;
+        float zx = 0.0f, qx = 0.0f, ux = 0.0f;
+        if (last || kind == kB || c2 != 0.0f) {
+            b = I.b;
+            n = I.n;
+            j = I.j;
+            xtok = I.xtok;
+            zx = I.zx;
+            qx = I.qx;
+            ux = I.ux;
+        }
         // Fast stages are copied to registers and released before any arithmetic,
         // so the producer can refill the stage while this warp computes.
         auto release = [&]() {
@@ -1139,7 +1182,37 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
         if (kind == kA && c2 == 0.0f) {
             // ---- greedy: running (max, first index) over 8-element groups
             const int ng = (cnt + 7) >> 3;
-            if (fast) {
+            if (ES == 2 && fast) {
+                // bf16: packed maxima; a group is unpacked only when it beats the running best
+                constexpr int kGPL = (kSubBytes / 2 / 8 + kConsumerLanes - 1) / kConsumerLanes;
+                uint4 ra[kGPL];
+#pragma unroll
+                for (int t = 0; t < kGPL; ++t) {
+                    const int g = cw * 32 + lane + t * kConsumerLanes;
+                    if (g < ng) ra[t] = *reinterpret_cast<const uint4 *>(stage + g * 16);
+                }
+                release();
+#pragma unroll
+                for (int t = 0; t < kGPL; ++t) {
+                    const int g = cw * 32 + lane + t * kConsumerLanes;
+                    if (g < ng) {
+                        const uint32_t a = bmax2_nan(bmax2_nan(ra[t].x, ra[t].y), bmax2_nan(ra[t].z, ra[t].w));
+                        pmx = bmax2_nan(pmx, a);
+                        if (bf16x2_any_gt(a, best2)) {
+                            const float m = fmaxf(bf16_lo(a), bf16_hi(a));
+                            float x[8];
+                            unpack8<2>(ra[t], ra[t], x);
+                            int i = 7;
+#pragma unroll
+                            for (int q = 7; q >= 0; --q)
+                                if (x[q] == m) i = q;
+                            best = m;
+                            best2 = bf16_pair(m);
+                            bidx = e0 + 8 * g + i;
+                        }
+                    }
+                }
+            } else if (fast) {
                 constexpr int kGPL = (kSubBytes / ES / 8 + kConsumerLanes - 1) / kConsumerLanes;
                 uint4 ra[kGPL], rc[kGPL];
 #pragma unroll
@@ -1157,12 +1230,14 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                     if (g < ng) greedy_regs<ES>(ra[t], rc[t], e0 + 8 * g, best, bidx, mx);
                 }
             } else {
+                const View vz{stage + I.sh, I.gz, cnt, I.tail, I.sh == 0};
                 for (int g = cw * 32 + lane; g < ng; g += kConsumerLanes)
                     group_step<ES>(vz, g, e0, false, best, bidx, mx, bad);
                 release();
             }
-        } else if (kind == kA) {
+        } else if (SMP && kind == kA) {
             // ---- sampled: per 256-element block its max M and sum of 2^((z - M) c2)
+            const View vz{stage + I.sh, I.gz, cnt, I.tail, I.sh == 0};
             const int nb = (cnt + kBlk - 1) / kBlk;
             const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + e0 / kBlk;
             // Fold one finished block (max M, canonical sum s in lane 0) into the
@@ -1241,8 +1316,11 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 }
                 release();
             }
-        } else {
+        } else if (SMP) {
             // ---- residual: per 256-element block the sum of max(0, p - q)
+            const View vz{stage + I.sh, I.gz, cnt, I.tail, I.sh == 0};
+            const View vq{stage + P.qoff + I.shq, I.gq, cnt, I.tailq, I.shq == 0};
+            const float m_row = I.m, invS = I.invS;
             const int nb = (cnt + kBlk - 1) / kBlk;   // at most one block per warp
             const int blk = cw;
             float x[8], y[8];
@@ -1289,6 +1367,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             int g = bidx;
             if (kind == kA && c2 == 0.0f) {
                 warp_cand(v, g);
+                mx = fmax_nan(mx, fmax_nan(bf16_lo(pmx), bf16_hi(pmx)));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
@@ -1323,6 +1402,8 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             best = -INFINITY;
             bidx = -1;
             mx = -INFINITY;
+            best2 = 0xff80ff80u;
+            pmx = 0xff80ff80u;
             Mw = -INFINITY;
             Sw = 0.0f;
             Sc = 0.0f;
@@ -1331,6 +1412,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
     if (lane == 0 && cw == 0) S.consumed = it;
 }
 
+template <bool SMP>
 __device__ void epilogue(const Params &P, Smem &S, int lane) {
     int uc = 0;
     while (true) {
@@ -1350,7 +1432,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
         if (lane == 0) mbar_arrive(&S.res_empty[slot]);
         ++uc;
         if (kind == kA) {
-            const bool greedy = (c2 == 0.0f);
+            const bool greedy = !SMP || (c2 == 0.0f);
             float um = 0.0f;
             double uS = 0.0;
             if (greedy) {
@@ -1365,8 +1447,8 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
             }
             const size_t ri = static_cast<size_t>(b) * P.R + n;
             if (P.ns == 1) {
-                resolve_row(P, b, n, greedy, c2, grp, v, um, uS, xtok, zx, qx, ux, lane);
-                settle_row(P, S, 1, b, lane);
+                resolve_row<SMP>(P, b, n, greedy, c2, grp, v, um, uS, xtok, zx, qx, ux, lane);
+                settle_row<SMP>(P, S, 1, b, lane);
             } else {
                 uint32_t old = 0;
                 if (lane == 0) {
@@ -1405,12 +1487,12 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
                             }
                             rS = warp_sum_d(t);
                         }
-                        resolve_row(P, b, n, greedy, c2, gg, gv, rm, rS, xtok, zx, qx, ux, lane);
+                        resolve_row<SMP>(P, b, n, greedy, c2, gg, gv, rm, rS, xtok, zx, qx, ux, lane);
                     }
-                    settle_row(P, S, 1, b, lane);
+                    settle_row<SMP>(P, S, 1, b, lane);
                 }
             }
-        } else {
+        } else if (SMP) {
             // B unit: the last chunk of a request's residual draws the token
             uint32_t old = 0;
             if (lane == 0) {
@@ -1429,7 +1511,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
 }
 
 // --------------------------------------------------------------- kernel --
-template <int ES>
+template <int ES, bool SMP>
 __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
@@ -1455,9 +1537,9 @@ __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P)
     }
     __syncthreads();
 
-    if (warp == 0) producer<ES>(P, S, ring, lane);
-    else if (warp == 1) epilogue(P, S, lane);
-    else consumer<ES>(P, S, ring, warp - 2, lane, bad);
+    if (warp == 0) producer<ES, SMP>(P, S, ring, lane);
+    else if (warp == 1) epilogue<SMP>(P, S, lane);
+    else consumer<ES, SMP>(P, S, ring, warp - 2, lane, bad);
 
     bad = __any_sync(0xffffffffu, bad != 0);
     if (lane == 0 && bad) set_status(P, SPEC_STATUS_NONFINITE);
@@ -1594,22 +1676,22 @@ spec_status_t device_info(DeviceInfo *&out) {
             return fail(SPEC_ERR_UNSUPPORTED, "needs compute capability 10.3 (sm_103a), device is %s", buf);
         }
         cudaDeviceGetAttribute(&D.sms, cudaDevAttrMultiProcessorCount, dev);
-        e = cudaFuncSetAttribute(verify_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(verify_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const void *kernels[4] = {reinterpret_cast<const void *>(verify_kernel<2, false>),
+                                  reinterpret_cast<const void *>(verify_kernel<4, false>),
+                                  reinterpret_cast<const void *>(verify_kernel<2, true>),
+                                  reinterpret_cast<const void *>(verify_kernel<4, true>)};
+        for (int q = 0; q < 4 && e == cudaSuccess; ++q) {
+            e = cudaFuncSetAttribute(kernels[q], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes));
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[0], verify_kernel<2>, kThreads,
-                                                              kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&D.blocks_per_sm[1], verify_kernel<4>, kThreads,
-                                                              kSmemBytes);
+            int nb = 0;
+            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernels[q], kThreads, kSmemBytes);
+            if (e == cudaSuccess && (q < 2 || nb < D.blocks_per_sm[q & 1])) D.blocks_per_sm[q & 1] = nb;
+        }
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "kernel setup: %s", cudaGetErrorString(e));
         if (D.blocks_per_sm[0] < 1 || D.blocks_per_sm[1] < 1) {
             cudaFuncAttributes fa;
             memset(&fa, 0, sizeof fa);
-            cudaFuncGetAttributes(&fa, verify_kernel<2>);
+            cudaFuncGetAttributes(&fa, verify_kernel<2, true>);
             char buf[200];
             snprintf(buf, sizeof buf, " (%d registers, max %d threads, %zu B static + %zu B dynamic shared, %d threads)",
                      fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes, kSmemBytes, kThreads);
@@ -1687,10 +1769,16 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     if (grid > P.units_total) grid = P.units_total;
     if (grid < 1) grid = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == SPEC_BF16)
-        verify_kernel<2><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(P);
-    else
-        verify_kernel<4><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(P);
+    // Calls without draft probabilities are greedy only: a leaner instantiation
+    // without the sampling and residual code.
+    const dim3 g3(static_cast<unsigned>(grid));
+    if (P.q) {
+        if (dtype == SPEC_BF16) verify_kernel<2, true><<<g3, kThreads, kSmemBytes, st>>>(P);
+        else verify_kernel<4, true><<<g3, kThreads, kSmemBytes, st>>>(P);
+    } else {
+        if (dtype == SPEC_BF16) verify_kernel<2, false><<<g3, kThreads, kSmemBytes, st>>>(P);
+        else verify_kernel<4, false><<<g3, kThreads, kSmemBytes, st>>>(P);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
