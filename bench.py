@@ -444,7 +444,7 @@ def reference_main(args, world, rank):
     value = nreq * x.k * args.steps / dt
     sample = "first %d of %d requests per step (whole requests, all rows)" % (nreq, x.B)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, "global_batch": x.B, "k": x.k, "V": x.V,
