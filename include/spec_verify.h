@@ -62,7 +62,9 @@ typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype_t;
 
 /* Bits OR-ed into the device status word. */
 #define SPEC_STATUS_TOKEN_RANGE 1  /* a draft token outside [0, V): treated as a rejection */
-#define SPEC_STATUS_NONFINITE 2    /* a NaN or infinite logit was read (results undefined) */
+#define SPEC_STATUS_NONFINITE 2    /* a NaN or +inf logit was read, or a row was -inf throughout
+                                      (results undefined).  A -inf logit alone is a masked
+                                      token: probability 0, never the argmax of a finite row. */
 #define SPEC_STATUS_WAIT_TIMEOUT 4 /* an inter-block wait gave up (results of that request undefined) */
 
 /* Largest rows per request (k+1 for chains, N+1 for trees). */

@@ -287,25 +287,57 @@ __device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parit
 
 // ------------------------------------------------------------ weights --
 // Per-element weights of the inverse CDF, written with explicit rounding
-// intrinsics so every call site evaluates them bit-identically.
-__device__ __forceinline__ float w_exp(float z, float M, float c2) {
-    return ex2(__fmul_rn(__fsub_rn(z, M), c2));
+// intrinsics so every call site evaluates them bit-identically.  The exponent
+// z*c2 - M*c2 is one fused multiply-add with nMc2 = RN(-M*c2).
+// A reference max of -inf (every element -inf, e.g. a masked block) gives
+// weights 2^-inf = 0 through nMc2 = 0 instead of inf - inf.
+__device__ __forceinline__ float neg_mc2(float M, float c2) { return M == -INFINITY ? 0.0f : __fmul_rn(-M, c2); }
+
+__device__ __forceinline__ float w_exp(float z, float nMc2, float c2) { return ex2(__fmaf_rn(z, c2, nMc2)); }
+
+__device__ __forceinline__ float w_res(float z, float qv, float nmc2, float c2, float invS) {
+    const float p = __fmul_rn(ex2(__fmaf_rn(z, c2, nmc2)), invS);
+    return fmaxf(__fsub_rn(p, qv), 0.0f);
 }
 
-__device__ __forceinline__ float w_res(float z, float qv, float m, float c2, float invS) {
-    float p = __fmul_rn(ex2(__fmul_rn(__fsub_rn(z, m), c2)), invS);
-    return fmaxf(__fsub_rn(p, qv), 0.0f);
+// Canonical lane partial of 8 weights: the even and the odd positions summed
+// in order, then added (the order packed f32x2 accumulation produces).
+__device__ __forceinline__ float lane_sum8(const float w[8]) {
+    const float e = __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[2]), w[4]), w[6]);
+    const float o = __fadd_rn(__fadd_rn(__fadd_rn(w[1], w[3]), w[5]), w[7]);
+    return __fadd_rn(e, o);
+}
+
+// Packed fp32 pairs (two IEEE operations per instruction).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 __device__ __forceinline__ uint32_t nonfinite_bf16x2(uint32_t w) {
-    return __vcmpeq2(w & 0x7f807f80u, 0x7f807f80u);
+    return __vcmpeq2(w & 0x7f807f80u, 0x7f807f80u) & ~__vcmpeq2(w, 0xff80ff80u);
 }
 
 __device__ __forceinline__ uint32_t nonfinite_f32(uint32_t w) {
-    return (w & 0x7f800000u) == 0x7f800000u;
+    return (w & 0x7f800000u) == 0x7f800000u && w != 0xff800000u;
 }
 
 // Element view of one stage: elements [0, tail) live in shared memory at s,
@@ -322,7 +354,7 @@ __device__ __forceinline__ float ld_one(const View &v, int e, uint32_t &bad) {
     if (ES == 2) {
         uint16_t h = (e < v.tail) ? *reinterpret_cast<const uint16_t *>(v.s + 2 * e)
                                   : __ldg(reinterpret_cast<const unsigned short *>(v.g + 2 * e));
-        bad |= ((h & 0x7f80u) == 0x7f80u);
+        bad |= ((h & 0x7f80u) == 0x7f80u && h != 0xff80u);
         return __uint_as_float(static_cast<uint32_t>(h) << 16);
     } else {
         uint32_t w = (e < v.tail) ? *reinterpret_cast<const uint32_t *>(v.s + 4 * e)
@@ -571,8 +603,7 @@ __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row,
     const size_t rowz = (static_cast<size_t>(b) * P.R + row) * static_cast<size_t>(P.V);
     const int e0 = beta * kBlk + lane * 8;
     float w[8];
-    float s = 0.0f;
-    float Mb = residual ? 0.0f : __ldcg(S.bmax + beta);
+    const float nMc2 = neg_mc2(residual ? S.m : __ldcg(S.bmax + beta), S.c2);
     double fac = residual ? 1.0 : block_factor(S, beta);
     const float *qrow =
         residual ? P.q + (static_cast<size_t>(b) * (P.R - 1) + row) * static_cast<size_t>(P.V) : nullptr;
@@ -582,11 +613,11 @@ __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row,
         float wi = 0.0f;
         if (e < P.V) {
             float z = logit_global(P, rowz + e);
-            wi = residual ? w_res(z, __ldg(qrow + e), S.m, S.c2, invS) : w_exp(z, Mb, S.c2);
+            wi = residual ? w_res(z, __ldg(qrow + e), nMc2, S.c2, invS) : w_exp(z, nMc2, S.c2);
         }
         w[i] = wi;
-        s = __fadd_rn(s, wi);
     }
+    const float s = lane_sum8(w);
     double ls = static_cast<double>(s) * fac;
     double incl = warp_incl_scan_d(ls, lane);
     double lbase = base + (incl - ls);
@@ -998,6 +1029,26 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     }
 }
 
+// Fold a finished sum s (relative to reference max M) into a warp's running
+// (Mw, Sw + Sc) statistics, with Neumaier compensation.
+__device__ __forceinline__ void fold_stats(float M, float s, float c2, float &Mw, float &Sw, float &Sc) {
+    if (M == -INFINITY) return;   // an all -inf stretch adds nothing
+    float add;
+    if (M > Mw) {
+        const float f = ex2(__fmul_rn(__fsub_rn(Mw, M), c2));
+        Sw = __fmul_rn(Sw, f);
+        Sc = __fmul_rn(Sc, f);
+        Mw = M;
+        add = s;
+    } else {
+        add = __fmul_rn(s, ex2(__fmul_rn(__fsub_rn(M, Mw), c2)));
+    }
+    const float tsum = __fadd_rn(Sw, add);
+    if (fabsf(Sw) >= fabsf(add)) Sc = __fadd_rn(Sc, __fadd_rn(__fsub_rn(Sw, tsum), add));
+    else Sc = __fadd_rn(Sc, __fadd_rn(__fsub_rn(add, tsum), Sw));
+    Sw = tsum;
+}
+
 // Does either bf16 half of a exceed the matching half of b?  (NaN: no.)
 __device__ __forceinline__ bool bf16x2_any_gt(uint32_t a, uint32_t b) {
     uint32_t r;
@@ -1240,29 +1291,6 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             const View vz{stage + I.sh, I.gz, cnt, I.tail, I.sh == 0};
             const int nb = (cnt + kBlk - 1) / kBlk;
             const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + e0 / kBlk;
-            // Fold one finished block (max M, canonical sum s in lane 0) into the
-            // block data and this warp's running statistics.
-            auto fold = [&](int blk, float M, float s) {
-                if (lane == 0) {
-                    P.bmaxA[rb + blk] = M;
-                    P.bsumA[rb + blk] = s;
-                }
-                const float sb = __shfl_sync(0xffffffffu, s, 0);
-                float add;
-                if (M > Mw) {
-                    const float f = ex2(__fmul_rn(__fsub_rn(Mw, M), c2));
-                    Sw = __fmul_rn(Sw, f);
-                    Sc = __fmul_rn(Sc, f);
-                    Mw = M;
-                    add = sb;
-                } else {
-                    add = __fmul_rn(sb, ex2(__fmul_rn(__fsub_rn(M, Mw), c2)));
-                }
-                const float tsum = __fadd_rn(Sw, add);   // Neumaier compensation
-                if (fabsf(Sw) >= fabsf(add)) Sc = __fadd_rn(Sc, __fadd_rn(__fsub_rn(Sw, tsum), add));
-                else Sc = __fadd_rn(Sc, __fadd_rn(__fsub_rn(add, tsum), Sw));
-                Sw = tsum;
-            };
             if (fast) {
                 uint4 ra[kBPW], rc[kBPW];
 #pragma unroll
@@ -1275,17 +1303,21 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                     }
                 }
                 release();
-                // cnt is a multiple of 8 here: a lane's 8 elements are all valid or all past the end
-                float M[kBPW], sm[kBPW];
+                // One reference max M for all of this warp's blocks in the stage (any M at
+                // or above a block's max works; it is stored with each block's sum).
+                // cnt is a multiple of 8 here: a lane's 8 elements are all valid or none.
+                float lm = -INFINITY;
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = cw + t * kConsumerWarps;
-                    if (blk < nb) {
-                        const bool valid = blk * kBlk + lane * 8 < cnt;
-                        const float lm = valid ? (ES == 2 ? vmax8_bf16(ra[t]) : vmax8_f32(ra[t], rc[t])) : -INFINITY;
-                        M[t] = warp_max_redux(lm);
-                    }
+                    if (blk < nb && blk * kBlk + lane * 8 < cnt)
+                        lm = fmax_nan(lm, ES == 2 ? vmax8_bf16(ra[t]) : vmax8_f32(ra[t], rc[t]));
                 }
+                const float M = warp_max_redux(lm);
+                const float nMc2 = neg_mc2(M, c2);
+                const float2 c22 = make_float2(c2, c2), nm2 = make_float2(nMc2, nMc2);
+                float stage_sum = 0.0f;
+                bool any = false;
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = cw + t * kConsumerWarps;
@@ -1294,15 +1326,25 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                         if (blk * kBlk + lane * 8 < cnt) {
                             float x[8];
                             unpack8<ES>(ra[t], rc[t], x);
+                            float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) s = __fadd_rn(s, w_exp(x[i], M[t], c2));
+                            for (int k = 0; k < 4; ++k) {
+                                const float2 a = fma2(make_float2(x[2 * k], x[2 * k + 1]), c22, nm2);
+                                const float2 wv = make_float2(ex2(a.x), ex2(a.y));
+                                acc = (k == 0) ? wv : add2(acc, wv);
+                            }
+                            s = __fadd_rn(acc.x, acc.y);
                         }
-                        sm[t] = warp_butterfly_sum(s);
+                        s = warp_butterfly_sum(s);
+                        if (lane == 0) {
+                            P.bmaxA[rb + blk] = M;
+                            P.bsumA[rb + blk] = s;
+                        }
+                        stage_sum = __fadd_rn(stage_sum, __shfl_sync(0xffffffffu, s, 0));
+                        any = true;
                     }
                 }
-#pragma unroll
-                for (int t = 0; t < kBPW; ++t)
-                    if (cw + t * kConsumerWarps < nb) fold(cw + t * kConsumerWarps, M[t], sm[t]);
+                if (any) fold_stats(M, stage_sum, c2, Mw, Sw, Sc);
             } else {
                 for (int blk = cw; blk < nb; blk += kConsumerWarps) {
                     float x[8];
@@ -1310,9 +1352,16 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                     float lm = -INFINITY;
                     for (int i = 0; i < nv; ++i) lm = fmax_nan(lm, x[i]);
                     const float M = warp_max_redux(lm);
-                    float s = 0.0f;
-                    for (int i = 0; i < nv; ++i) s = __fadd_rn(s, w_exp(x[i], M, c2));
-                    fold(blk, M, warp_butterfly_sum(s));
+                    const float nMc2 = neg_mc2(M, c2);
+                    float w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[i] = (i < nv) ? w_exp(x[i], nMc2, c2) : 0.0f;
+                    const float sblk = warp_butterfly_sum(lane_sum8(w));
+                    if (lane == 0) {
+                        P.bmaxA[rb + blk] = M;
+                        P.bsumA[rb + blk] = sblk;
+                    }
+                    fold_stats(M, __shfl_sync(0xffffffffu, sblk, 0), c2, Mw, Sw, Sc);
                 }
                 release();
             }
@@ -1349,11 +1398,11 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 release();
             }
             if (blk < nb) {
-                float s = 0.0f;
+                const float nmc2 = neg_mc2(m_row, c2);
+                float w[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (i < nvz) s = __fadd_rn(s, w_res(x[i], y[i], m_row, c2, invS));
-                s = warp_butterfly_sum(s);
+                for (int i = 0; i < 8; ++i) w[i] = (i < nvz) ? w_res(x[i], y[i], nmc2, c2, invS) : 0.0f;
+                const float s = warp_butterfly_sum(lane_sum8(w));
                 if (lane == 0) P.bsumB[static_cast<size_t>(b) * P.nblk + e0 / kBlk + blk] = s;
             }
         }

@@ -116,6 +116,58 @@ def test_nonfinite_logit_sets_status(sv, dev):
     assert int(st.item()) & sv.STATUS_NONFINITE
 
 
+def _mask_vocab(x, V):
+    """-inf over whole 256-element blocks, a ragged stretch and the row tail
+    (a masked vocabulary: those tokens have probability 0)."""
+    neg = np.uint16(0xFF80) if x.dtype == W.BF16 else np.float32(-np.inf)
+    spans = [(256, 256 + 3 * 256), (3000, 3000 + 777), (V - 1100, V)]
+    for lo, hi in spans:
+        x.logits[:, :, lo:hi] = neg
+    return x
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.FP32], ids=["bf16", "fp32"])
+def test_masked_vocabulary_greedy(sv, O, dev, dtype):
+    import torch
+    x = _mask_vocab(W.chain_greedy(seed=43, B=12, k=4, V=20011, p_match=0.8, dtype=dtype), 20011)
+    x.draft_tokens[0, 0] = 300     # a masked draft token is rejected
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    got_t, got_a = run_chain(sv, x, dev, status=st)
+    ref = oracle_chain(O, x)
+    assert int(st.item()) == 0
+    assert (got_a == ref["num_accepted"]).all() and (got_t == ref["out_tokens"]).all()
+    assert got_a[0] == 0
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.FP32], ids=["bf16", "fp32"])
+def test_masked_vocabulary_sampled(sv, O, dev, dtype):
+    import torch
+    V = 20011
+    x = _mask_vocab(W.chain_sampled(seed=44, B=12, k=4, V=V, temperature=0.8, lam=0.3, dtype=dtype), V)
+    x.draft_tokens[0, 0] = 300     # p = 0 at a masked token: always rejected
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    got_t, got_a = run_chain(sv, x, dev, status=st)
+    ref = oracle_chain(O, x)
+    assert int(st.item()) == 0
+    compare_chain(got_t, got_a, ref)
+    masked = np.zeros(V, bool)
+    for lo, hi in [(256, 1024), (3000, 3777), (V - 1100, V)]:
+        masked[lo:hi] = True
+    # no emitted token (accepted draft, residual or bonus sample) is masked
+    emitted = got_t[got_t >= 0]
+    assert not masked[emitted].any()
+    assert got_a[0] == 0
+
+
+def test_all_masked_row_sets_status(sv, dev):
+    import torch
+    x = W.chain_sampled(seed=45, B=3, k=2, V=3000, temperature=1.0, lam=0.3, dtype=W.FP32)
+    x.logits[2, 1, :] = -np.inf
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    run_chain(sv, x, dev, status=st)
+    assert int(st.item()) & sv.STATUS_NONFINITE
+
+
 # ----------------------------------------------------------------- sampled --
 SAMPLED = [
     dict(B=16, k=4, V=5000, temperature=0.7, lam=0.3),
