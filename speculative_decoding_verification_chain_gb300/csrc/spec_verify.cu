@@ -53,8 +53,12 @@ namespace sv {
 constexpr int kConsumerWarps = 12;
 constexpr int kConsumerLanes = 32 * kConsumerWarps;
 constexpr int kThreads = 32 * (2 + kConsumerWarps);   // producer, epilogue, consumers
-constexpr int kStages = 8;
-constexpr int kSubBytes = 24576;                       // data bytes per stage
+// The bulk-copy engine of an SM completes about one copy at a time, so the
+// per-SM stream rate grows with the copy size: three 64 KiB stages, each one
+// copy, consumed in passes of 24 KiB (the consumers' register tiles).
+constexpr int kStages = 3;
+constexpr int kSubBytes = 65536;                       // data bytes per stage (at most)
+constexpr int kPassBytes = 24576;                      // bytes per consumer pass
 constexpr int kStageBytes = kSubBytes + 128;
 constexpr int kSubPerB = 4;                             // B stages per B unit
 constexpr int kResSlots = 4;
@@ -67,6 +71,10 @@ constexpr uint32_t kNeedsResidual = 0x40000000u;
 constexpr uint32_t kSkipInc = 0x10000u;                 // split counter: skipped splits count here
 constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kEarlyMax = 4;                            // children per node given an early-rejection check
+constexpr uint32_t kFirstF = 1u << 6;                   // stage flag: first stage of its unit
+constexpr int kThrOff = kSubBytes + 64;                 // A stage: 16-byte chunks holding the children's logits
+static_assert(kThrOff + 16 * kEarlyMax <= kStageBytes, "threshold chunks do not fit in the stage");
 
 enum Kind : int { kEnd = 0, kA = 1, kB = 2 };
 
@@ -101,6 +109,7 @@ struct Params {
     uint32_t *req_ctr;           // [B] settled rows
     uint32_t *req_state;         // [B] decision
     uint32_t *res_ctr;           // [B] residual units done
+    uint32_t *early;             // [B*R] node known rejected before its parent row resolved
     uint32_t *reset_base;
     uint32_t reset_words;
     RowStat *rowstat;            // [B*R]
@@ -122,8 +131,11 @@ struct Params {
     int ncb, nblk;
     int units_a, units_total;
     int tree;
+    int ahead;                   // stages the producer may have in flight
     int16_t parent[kMaxRows];
     uint8_t depth[kMaxRows];
+    uint8_t kid_off[kMaxRows + 1];   // tree: children of n are kid_list[kid_off[n] .. kid_off[n+1])
+    uint8_t kid_list[kMaxRows];
 };
 
 // Stage descriptor.  The first 16 bytes are what every consumer reads per stage.
@@ -139,6 +151,10 @@ struct __align__(16) StageInfo {
     float m, invS;       // row statistics (B)
     int xtok;            // sampled A, last stage: token of node n+1 (-1 if none or out of range)
     float zx, qx, ux;    // ... and its logit, its draft probability, its accept uniform
+    int nk;              // greedy A, first stage: children with an early-rejection check
+    int ktok[kEarlyMax]; // ... their draft tokens
+    int kofs[kEarlyMax]; // ... byte offset of the token's logit in its chunk at kThrOff + 16 c
+                         //     (-1: token out of range, -2: not copied, read from global)
     const uint8_t *gz;
     const uint8_t *gq;
 };
@@ -791,6 +807,7 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
 
 // --------------------------------------------------------------- roles --
 // Producer (warp 0): is node n of request b already known to be rejected?
+// (An edge on its path rejected by a resolved parent row, or flagged early.)
 __device__ bool node_dead(const Params &P, int b, int n, bool greedy, int lane) {
     if (n == 0) return false;
     const int d = depth_of(P, n);
@@ -806,8 +823,10 @@ __device__ bool node_dead(const Params &P, int b, int n, bool greedy, int lane) 
                 child = n - i;
             }
             int par = parent_of(P, child);
-            uint32_t rs = ld_relaxed(P.rowstate + static_cast<size_t>(b) * P.R + par);
-            if (rs & kResolved) bad = !edge_ok(rs, greedy, node_token(P, b, child));
+            const size_t rb = static_cast<size_t>(b) * P.R;
+            const uint32_t ef = ld_relaxed(P.early + rb + child);
+            const uint32_t rs = ld_relaxed(P.rowstate + rb + par);
+            bad = ef != 0u || ((rs & kResolved) && !edge_ok(rs, greedy, node_token(P, b, child)));
         }
         dead = __any_sync(0xffffffffu, bad);
     }
@@ -846,11 +865,14 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     unsigned long long loaded_bytes = 0;
     int a_loaded = 0, a_skipped = 0, b_loaded = 0, b_skipped = 0;
 
-    // Reserve the next stage (wait until the consumers released its previous use).
+    // Reserve the next stage: at most P.ahead stages are issued and not yet
+    // released (stage it - ahead released; consumers release in order, so its
+    // slot's previous use, stage it - kStages, is free too).
     auto acquire_stage = [&](int &st) -> bool {
         st = it % kStages;
-        if (it >= kStages) {
-            if (!wait_bar(P, S, &S.empty[st], static_cast<uint32_t>((it / kStages - 1) & 1))) return false;
+        if (it >= P.ahead) {
+            const int r = it - P.ahead;
+            if (!wait_bar(P, S, &S.empty[r % kStages], static_cast<uint32_t>((r / kStages) & 1))) return false;
         }
         return true;
     };
@@ -870,6 +892,20 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const float c2 = greedy ? 0.0f : kLog2e / __ldg(P.temperature + b);
             const int s0 = j * P.sps;
             const int s1 = min(P.nsub, s0 + P.sps);
+            // Greedy rows: draft tokens of (up to kEarlyMax) children, for the
+            // consumers' early-rejection check (loaded alongside the dead check).
+            int nk = 0, ktok = -1;
+            if (greedy) {
+                int k0 = 0;
+                if (P.tree) {
+                    k0 = P.kid_off[n];
+                    nk = P.kid_off[n + 1] - k0;
+                } else {
+                    nk = n < P.R - 1 ? 1 : 0;
+                }
+                nk = min(nk, kEarlyMax);
+                if (lane < nk) ktok = node_token(P, b, P.tree ? static_cast<int>(P.kid_list[k0 + lane]) : n + 1);
+            }
             if (node_dead(P, b, n, greedy, lane)) {
                 ++a_skipped;
                 if (P.ns == 1) {
@@ -884,6 +920,9 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             }
             ++a_loaded;
             const size_t rowe = (static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V);
+            int kt[kEarlyMax];
+#pragma unroll
+            for (int c = 0; c < kEarlyMax; ++c) kt[c] = __shfl_sync(0xffffffffu, ktok, c);
             // accept-test operands of node n+1 (sampled rows): loaded now, used by the
             // epilogue after the whole row has streamed
             int xtok = -1;
@@ -918,17 +957,48 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                         I.qx = qx;
                         I.ux = ux;
                     }
+                    // first stage: the children's logits travel with the stage
+                    uint32_t extra = 0;
+                    const uint8_t *ksrc[kEarlyMax];
+                    if (s == s0) {
+                        I.nk = nk;
+#pragma unroll
+                        for (int c = 0; c < kEarlyMax; ++c) {
+                            I.ktok[c] = kt[c];
+                            int ko = -1;
+                            ksrc[c] = nullptr;
+                            if (c < nk && kt[c] >= 0 && kt[c] < P.V) {
+                                const unsigned long long a = reinterpret_cast<unsigned long long>(P.logits) +
+                                                             (rowe + static_cast<size_t>(kt[c])) * ES;
+                                const unsigned long long ch = a & ~15ull;
+                                if (ch + 16 <= P.logits_end) {
+                                    ko = static_cast<int>(a - ch);
+                                    ksrc[c] = reinterpret_cast<const uint8_t *>(ch);
+                                    extra += 16;
+                                } else {
+                                    ko = -2;
+                                }
+                            }
+                            I.kofs[c] = ko;
+                        }
+                    }
                     I.gz = P.logits + (rowe + I.e0) * ES;
                     const uint8_t *src;
                     uint32_t nb;
                     copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
                     const int fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
-                    I.flags = kA | (last << 4) | (fast << 5);
+                    I.flags = kA | (last << 4) | (fast << 5) | (s == s0 ? kFirstF : 0u);
                     loaded_bytes += nb;
                     fence_proxy_async();
-                    if (nb) {
-                        mbar_expect_tx(&S.full[st], nb);
-                        bulk_g2s(ring + static_cast<size_t>(st) * kStageBytes, src, nb, &S.full[st]);
+                    uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
+                    if (nb + extra) {
+                        mbar_expect_tx(&S.full[st], nb + extra);
+                        if (nb) bulk_g2s(dst, src, nb, &S.full[st]);
+                        if (extra) {
+#pragma unroll
+                            for (int c = 0; c < kEarlyMax; ++c)
+                                if (ksrc[c]) bulk_g2s(dst + kThrOff + 16 * c, ksrc[c], 16, &S.full[st]);
+                        }
                     } else {
                         mbar_arrive(&S.full[st]);
                     }
@@ -1061,6 +1131,19 @@ __device__ __forceinline__ bool bf16x2_any_gt(uint32_t a, uint32_t b) {
     return r != 0;
 }
 
+// Packed running maximum of the two bf16 halves with the row index of the
+// group that first set each half's record (branch-free): the half of `a`
+// that beats the record moves it to group start ge.  NaN freezes both.
+__device__ __forceinline__ void bf16x2_record(uint32_t a, uint32_t &pk, int ge, int &glo, int &ghi) {
+    asm("{\n\t.reg .pred plo, phi;\n\t"
+        "setp.gt.bf16x2 plo|phi, %3, %2;\n\t"
+        "selp.s32 %0, %4, %0, plo;\n\t"
+        "selp.s32 %1, %4, %1, phi;\n\t}"
+        : "+r"(glo), "+r"(ghi)
+        : "r"(pk), "r"(a), "r"(ge));
+    pk = bmax2_nan(pk, a);
+}
+
 // A bf16 value (given as its exact float) in both halves of a word.
 __device__ __forceinline__ uint32_t bf16_pair(float m) {
     const uint32_t h = __float_as_uint(m) >> 16;
@@ -1183,11 +1266,16 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
     float best = -INFINITY;   // greedy: running max of this lane
     int bidx = -1;            // greedy: row index of its first occurrence
     float mx = -INFINITY;     // greedy: NaN-propagating max (non-finite detection)
-    uint32_t best2 = 0xff80ff80u;   // greedy bf16: best in both halves (starts at -inf)
-    uint32_t pmx = 0xff80ff80u;     // greedy bf16: packed NaN-propagating max
+    uint32_t pk = 0xff80ff80u;      // greedy bf16: per-half NaN-propagating max (starts at -inf)
+    int glo = -1, ghi = -1;         // ... row index of the group that first set each half's max
     float Mw = -INFINITY;     // sampled: running max of this warp's blocks
     float Sw = 0.0f, Sc = 0.0f;   // sampled: compensated sum of 2^((z - Mw) c2)
-    constexpr int kBPW = (kSubBytes / ES / kBlk + kConsumerWarps - 1) / kConsumerWarps;   // blocks per warp
+    uint32_t epend = 0;       // greedy: children (lanes) not yet shown rejected
+    float ethr = 0.0f;        // ... lane c: the logit of child c's draft token in this row
+    int eidx = 0;             // ... lane c: b * R + child c
+    constexpr int kPB = kPassBytes / ES / kBlk;                 // sampled: blocks per pass
+    constexpr int kBPW = kPB / kConsumerWarps;                  // ... per warp
+    static_assert(kPB % kConsumerWarps == 0, "pass blocks must split evenly over the consumer warps");
     while (true) {
         const int st = it % kStages;
         if (!wait_bar(P, S, &S.full[st], static_cast<uint32_t>((it / kStages) & 1))) break;
@@ -1232,53 +1320,70 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
         };
         if (kind == kA && c2 == 0.0f) {
             // ---- greedy: running (max, first index) over 8-element groups
+            if (hot.x & kFirstF) {
+                // A child whose draft token's logit is beaten by any element of
+                // this row is not the argmax: rejected, whatever the rest holds.
+                const int nk = I.nk;
+                epend = __ballot_sync(0xffffffffu, lane < nk);
+                if (lane < nk) {
+                    const int ko = I.kofs[lane];
+                    const int bb = I.b, nn = I.n;
+                    const int kid = P.tree ? static_cast<int>(P.kid_list[P.kid_off[nn] + lane]) : nn + 1;
+                    eidx = bb * P.R + kid;
+                    if (ko >= 0) {
+                        const uint8_t *pz = stage + kThrOff + 16 * lane + ko;
+                        ethr = ES == 2 ? __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(pz)) << 16)
+                                       : *reinterpret_cast<const float *>(pz);
+                    } else if (ko == -2) {
+                        ethr = logit_global(P, (static_cast<size_t>(bb) * P.R + nn) * static_cast<size_t>(P.V) + I.ktok[lane]);
+                    } else {
+                        ethr = -INFINITY;
+                    }
+                }
+            }
             const int ng = (cnt + 7) >> 3;
             if (ES == 2 && fast) {
-                // bf16: packed maxima; a group is unpacked only when it beats the running best
-                constexpr int kGPL = (kSubBytes / 2 / 8 + kConsumerLanes - 1) / kConsumerLanes;
-                uint4 ra[kGPL];
+                // bf16: packed per-half maxima with branch-free records, one pass at a time
+                constexpr int kPG = kPassBytes / 16;   // groups per pass
+                constexpr int kGPL = kPG / kConsumerLanes;
+                static_assert(kPG % kConsumerLanes == 0, "pass must split evenly over the consumer lanes");
+                for (int p0 = 0; p0 < ng; p0 += kPG) {
+                    uint4 ra[kGPL];
 #pragma unroll
-                for (int t = 0; t < kGPL; ++t) {
-                    const int g = cw * 32 + lane + t * kConsumerLanes;
-                    if (g < ng) ra[t] = *reinterpret_cast<const uint4 *>(stage + g * 16);
-                }
-                release();
+                    for (int t = 0; t < kGPL; ++t) {
+                        const int g = p0 + cw * 32 + lane + t * kConsumerLanes;
+                        if (g < ng) ra[t] = *reinterpret_cast<const uint4 *>(stage + g * 16);
+                    }
+                    if (p0 + kPG >= ng) release();
 #pragma unroll
-                for (int t = 0; t < kGPL; ++t) {
-                    const int g = cw * 32 + lane + t * kConsumerLanes;
-                    if (g < ng) {
-                        const uint32_t a = bmax2_nan(bmax2_nan(ra[t].x, ra[t].y), bmax2_nan(ra[t].z, ra[t].w));
-                        pmx = bmax2_nan(pmx, a);
-                        if (bf16x2_any_gt(a, best2)) {
-                            const float m = fmaxf(bf16_lo(a), bf16_hi(a));
-                            float x[8];
-                            unpack8<2>(ra[t], ra[t], x);
-                            int i = 7;
-#pragma unroll
-                            for (int q = 7; q >= 0; --q)
-                                if (x[q] == m) i = q;
-                            best = m;
-                            best2 = bf16_pair(m);
-                            bidx = e0 + 8 * g + i;
+                    for (int t = 0; t < kGPL; ++t) {
+                        const int g = p0 + cw * 32 + lane + t * kConsumerLanes;
+                        if (g < ng) {
+                            const uint32_t a = bmax2_nan(bmax2_nan(ra[t].x, ra[t].y), bmax2_nan(ra[t].z, ra[t].w));
+                            bf16x2_record(a, pk, e0 + 8 * g, glo, ghi);
                         }
                     }
                 }
             } else if (fast) {
-                constexpr int kGPL = (kSubBytes / ES / 8 + kConsumerLanes - 1) / kConsumerLanes;
-                uint4 ra[kGPL], rc[kGPL];
+                constexpr int kPG = kPassBytes / (8 * ES);
+                constexpr int kGPL = kPG / kConsumerLanes;
+                static_assert(kPG % kConsumerLanes == 0, "pass must split evenly over the consumer lanes");
+                for (int p0 = 0; p0 < ng; p0 += kPG) {
+                    uint4 ra[kGPL], rc[kGPL];
 #pragma unroll
-                for (int t = 0; t < kGPL; ++t) {
-                    const int g = cw * 32 + lane + t * kConsumerLanes;
-                    if (g < ng) {
-                        ra[t] = *reinterpret_cast<const uint4 *>(stage + g * 8 * ES);
-                        if (ES == 4) rc[t] = *reinterpret_cast<const uint4 *>(stage + g * 32 + 16);
+                    for (int t = 0; t < kGPL; ++t) {
+                        const int g = p0 + cw * 32 + lane + t * kConsumerLanes;
+                        if (g < ng) {
+                            ra[t] = *reinterpret_cast<const uint4 *>(stage + g * 8 * ES);
+                            if (ES == 4) rc[t] = *reinterpret_cast<const uint4 *>(stage + g * 32 + 16);
+                        }
                     }
-                }
-                release();
+                    if (p0 + kPG >= ng) release();
 #pragma unroll
-                for (int t = 0; t < kGPL; ++t) {
-                    const int g = cw * 32 + lane + t * kConsumerLanes;
-                    if (g < ng) greedy_regs<ES>(ra[t], rc[t], e0 + 8 * g, best, bidx, mx);
+                    for (int t = 0; t < kGPL; ++t) {
+                        const int g = p0 + cw * 32 + lane + t * kConsumerLanes;
+                        if (g < ng) greedy_regs<ES>(ra[t], rc[t], e0 + 8 * g, best, bidx, mx);
+                    }
                 }
             } else {
                 const View vz{stage + I.sh, I.gz, cnt, I.tail, I.sh == 0};
@@ -1286,30 +1391,37 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                     group_step<ES>(vz, g, e0, false, best, bidx, mx, bad);
                 release();
             }
+            if (epend) {
+                const float wm = warp_max_redux(fmaxf(best, fmaxf(bf16_lo(pk), bf16_hi(pk))));
+                const uint32_t hit = __ballot_sync(0xffffffffu, ((epend >> lane) & 1u) && wm > ethr);
+                if ((hit >> lane) & 1u) st_relaxed(P.early + eidx, 1u);
+                epend &= ~hit;
+            }
         } else if (SMP && kind == kA) {
             // ---- sampled: per 256-element block its max M and sum of 2^((z - M) c2)
             const View vz{stage + I.sh, I.gz, cnt, I.tail, I.sh == 0};
             const int nb = (cnt + kBlk - 1) / kBlk;
             const size_t rb = (static_cast<size_t>(b) * P.R + n) * P.nblk + e0 / kBlk;
             if (fast) {
+              for (int p0 = 0; p0 < nb; p0 += kPB) {
                 uint4 ra[kBPW], rc[kBPW];
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
-                    const int blk = cw + t * kConsumerWarps;
+                    const int blk = p0 + cw + t * kConsumerWarps;
                     if (blk < nb) {
                         const int e = blk * kBlk + lane * 8;
                         ra[t] = *reinterpret_cast<const uint4 *>(stage + e * ES);
                         if (ES == 4) rc[t] = *reinterpret_cast<const uint4 *>(stage + e * 4 + 16);
                     }
                 }
-                release();
-                // One reference max M for all of this warp's blocks in the stage (any M at
+                if (p0 + kPB >= nb) release();
+                // One reference max M for all of this warp's blocks in the pass (any M at
                 // or above a block's max works; it is stored with each block's sum).
                 // cnt is a multiple of 8 here: a lane's 8 elements are all valid or none.
                 float lm = -INFINITY;
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
-                    const int blk = cw + t * kConsumerWarps;
+                    const int blk = p0 + cw + t * kConsumerWarps;
                     if (blk < nb && blk * kBlk + lane * 8 < cnt)
                         lm = fmax_nan(lm, ES == 2 ? vmax8_bf16(ra[t]) : vmax8_f32(ra[t], rc[t]));
                 }
@@ -1320,7 +1432,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 bool any = false;
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
-                    const int blk = cw + t * kConsumerWarps;
+                    const int blk = p0 + cw + t * kConsumerWarps;
                     if (blk < nb) {
                         float s = 0.0f;
                         if (blk * kBlk + lane * 8 < cnt) {
@@ -1345,6 +1457,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                     }
                 }
                 if (any) fold_stats(M, stage_sum, c2, Mw, Sw, Sc);
+              }
             } else {
                 for (int blk = cw; blk < nb; blk += kConsumerWarps) {
                     float x[8];
@@ -1416,7 +1529,29 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             int g = bidx;
             if (kind == kA && c2 == 0.0f) {
                 warp_cand(v, g);
-                mx = fmax_nan(mx, fmax_nan(bf16_lo(pmx), bf16_hi(pmx)));
+                if (ES == 2) {
+                    // packed records: the lane's max, the first group holding it, the
+                    // warp's winner, then its first element from the row in memory
+                    const float mlo = bf16_lo(pk), mhi = bf16_hi(pk);
+                    float pv = fmaxf(mlo, mhi);
+                    int pg = mlo > mhi ? glo : (mhi > mlo ? ghi : min(static_cast<unsigned>(glo), static_cast<unsigned>(ghi)));
+                    if (!(pv > -INFINITY)) pg = -1;
+                    warp_cand(pv, pg);
+                    int pidx = -1;
+                    if (pg >= 0 && pg + 8 <= P.V) {
+                        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(
+                            P.logits + ((static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V) + pg) * 2));
+                        float x[8];
+                        unpack8<2>(w, w, x);
+                        int i = 7;
+#pragma unroll
+                        for (int q = 7; q >= 0; --q)
+                            if (x[q] == pv) i = q;
+                        pidx = pg + i;
+                    }
+                    cand_merge(v, g, pv, pidx);
+                }
+                mx = fmax_nan(mx, fmax_nan(bf16_lo(pk), bf16_hi(pk)));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
@@ -1451,11 +1586,13 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
             best = -INFINITY;
             bidx = -1;
             mx = -INFINITY;
-            best2 = 0xff80ff80u;
-            pmx = 0xff80ff80u;
+            pk = 0xff80ff80u;
+            glo = -1;
+            ghi = -1;
             Mw = -INFINITY;
             Sw = 0.0f;
             Sc = 0.0f;
+            epend = 0;
         }
     }
     if (lane == 0 && cw == 0) S.consumed = it;
@@ -1642,7 +1779,7 @@ spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "") {
 }
 
 struct Layout {
-    size_t stats, reset, reset_bytes, ctrl, row_ctr, rowstate, req_ctr, req_state, res_ctr;
+    size_t stats, reset, reset_bytes, ctrl, row_ctr, rowstate, req_ctr, req_state, res_ctr, early;
     size_t rowstat, partial, bmaxA, bsumA, bsumB, total;
     int esub, nsub, esb, ecb, qoff, ncb, nblk;
 };
@@ -1653,8 +1790,10 @@ bool make_layout(int B, int R, int V, spec_dtype_t dtype, Layout &L) {
     if (B < 1 || R < 1 || R > kMaxRows || V < 1 || V >= (1 << 30)) return false;
     if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return false;
     const int es = dtype == SPEC_BF16 ? 2 : 4;
-    L.esub = kSubBytes / es;
-    L.nsub = (V + L.esub - 1) / L.esub;
+    // stages of a row balanced in size, each a whole number of 256-element blocks
+    const int emax = kSubBytes / es;
+    L.nsub = (V + emax - 1) / emax;
+    L.esub = (((V + L.nsub - 1) / L.nsub) + kBlk - 1) / kBlk * kBlk;
     L.esb = kConsumerWarps * kBlk;   // one 256-element block per consumer warp
     static_assert(kConsumerWarps * kBlk * (4 + 4) + 64 <= kSubBytes + 128, "B stage does not fit");
     L.ecb = L.esb * kSubPerB;
@@ -1678,6 +1817,8 @@ bool make_layout(int B, int R, int V, spec_dtype_t dtype, Layout &L) {
     off += static_cast<size_t>(B) * 4;
     L.res_ctr = off;
     off += static_cast<size_t>(B) * 4;
+    L.early = off;
+    off += BR * 4;
     off = up256(off);
     L.reset_bytes = off - L.reset;
     L.rowstat = off;
@@ -1768,6 +1909,18 @@ int choose_splits(int rows_total, int nsub, int sms) {
     return ns;
 }
 
+// Stages the producer keeps in flight: the whole ring.  SPEC_VERIFY_AHEAD
+// (2..ring size) overrides it (tuning: fewer stages in flight let a row that
+// turns out not to be needed stop sooner).
+int choose_ahead() {
+    int a = kStages;
+    if (const char *env = getenv("SPEC_VERIFY_AHEAD")) {
+        int v = atoi(env);
+        if (v >= 2 && v <= kStages) a = v;
+    }
+    return a;
+}
+
 spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size_t ws_bytes, void *stream) {
     Layout L;
     if (!make_layout(P.B, P.R, P.V, dtype, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
@@ -1785,6 +1938,7 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     P.req_ctr = reinterpret_cast<uint32_t *>(ws + L.req_ctr);
     P.req_state = reinterpret_cast<uint32_t *>(ws + L.req_state);
     P.res_ctr = reinterpret_cast<uint32_t *>(ws + L.res_ctr);
+    P.early = reinterpret_cast<uint32_t *>(ws + L.early);
     P.reset_base = reinterpret_cast<uint32_t *>(ws + L.reset);
     P.reset_words = static_cast<uint32_t>(L.reset_bytes / 4);
     P.rowstat = reinterpret_cast<RowStat *>(ws + L.rowstat);
@@ -1803,6 +1957,7 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     const long long rows_total = static_cast<long long>(P.B) * P.R;
     int ns = choose_splits(rows_total > (1 << 30) ? (1 << 30) : static_cast<int>(rows_total), L.nsub, D->sms);
     P.sps = (L.nsub + ns - 1) / ns;
+    P.ahead = choose_ahead();
     P.ns = (L.nsub + P.sps - 1) / P.sps;
     const long long ua = rows_total * P.ns;
     const long long ub = P.q ? static_cast<long long>(P.B) * L.ncb : 0;
@@ -1941,6 +2096,17 @@ extern "C" spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_
         if (P.depth[n] > maxd) maxd = P.depth[n];
     }
     if (max_depth < maxd) return fail(SPEC_ERR_INVALID_ARG, "max_depth is smaller than the tree depth%s");
+    // children lists, in node order (counting sort by parent)
+    int cnt[kMaxRows + 1] = {0};
+    for (int n = 1; n <= N; ++n) ++cnt[parent[n]];
+    int off = 0;
+    for (int n = 0; n <= N; ++n) {
+        P.kid_off[n] = static_cast<uint8_t>(off);
+        off += cnt[n];
+        cnt[n] = P.kid_off[n];
+    }
+    P.kid_off[N + 1] = static_cast<uint8_t>(off);
+    for (int n = 1; n <= N; ++n) P.kid_list[cnt[parent[n]]++] = static_cast<uint8_t>(n);
     P.logits = static_cast<const uint8_t *>(target_logits);
     P.q = nullptr;
     P.tokens = node_tokens;

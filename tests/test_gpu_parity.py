@@ -336,3 +336,43 @@ def test_workspace_is_left_clean_between_calls(sv, O, dev):
                 assert (got_t == ref["out_tokens"]).all()
         path, toks, ln = sv.verify_tree(cuda(t.logits, dev), cuda(t.node_tokens, dev), t.parent)
         assert (toks.cpu().numpy() == tref["tokens"]).all()
+
+
+# ------------------------------------------- skipped rows, producer run-ahead --
+@pytest.mark.parametrize("ahead", [2, 3])
+def test_results_do_not_depend_on_producer_run_ahead(sv, O, dev, ahead, monkeypatch):
+    """How many stages the producer keeps in flight changes the timing of
+    claims and so which rows are skipped; the answers must not change."""
+    monkeypatch.setenv("SPEC_VERIFY_AHEAD", str(ahead))
+    x = W.chain_greedy(seed=61 + ahead, B=16, k=5, V=128256, p_match=0.5)
+    got_t, got_a = run_chain(sv, x, dev)
+    ref = oracle_chain(O, x)
+    assert (got_a == ref["num_accepted"]).all() and (got_t == ref["out_tokens"]).all()
+    t = W.tree_greedy(seed=62 + ahead, B=4, V=50000)
+    path, toks, ln = sv.verify_tree(cuda(t.logits, dev), cuda(t.node_tokens, dev), t.parent)
+    r = O.verify_tree(t.logits, t.dtype, t.node_tokens, t.parent)
+    assert (ln.cpu().numpy() == r["length"]).all()
+    assert (path.cpu().numpy() == r["path"]).all() and (toks.cpu().numpy() == r["tokens"]).all()
+    xs = W.chain_sampled(seed=63 + ahead, B=8, k=4, V=30000, temperature=0.8, lam=0.3)
+    got_t, got_a = run_chain(sv, xs, dev)
+    compare_chain(got_t, got_a, oracle_chain(O, xs))
+
+
+def test_rejected_first_drafts_skip_later_rows(sv, O, dev, monkeypatch):
+    """Every first draft wrong: rows 1..k are never needed.  Many are skipped
+    at claim (the first stage of row 0 already shows the rejection), and the
+    counters stay consistent."""
+    import torch
+    monkeypatch.setenv("SPEC_VERIFY_AHEAD", "3")
+    x = W.chain_greedy(seed=64, B=32, k=5, V=128256, p_match=0.0)
+    z, tok = cuda(x.logits, dev), cuda(x.draft_tokens, dev)
+    ws = torch.zeros(sv.workspace_bytes(x.B, x.k + 1, x.V), dtype=torch.uint8, device=dev)
+    ot, na = sv.verify_chain(z, tok, workspace=ws)
+    c = sv.workspace_counters(ws)
+    ref = oracle_chain(O, x)
+    assert (na.cpu().numpy() == 0).all()
+    assert (na.cpu().numpy() == ref["num_accepted"]).all() and (ot.cpu().numpy() == ref["out_tokens"]).all()
+    units = c["a_loaded"] + c["a_skipped"]   # rows x splits per row
+    assert units >= x.B * (x.k + 1) and units % (x.B * (x.k + 1)) == 0
+    assert c["a_skipped"] > 0
+    print("counters", c)
