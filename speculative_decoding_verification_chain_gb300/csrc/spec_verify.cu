@@ -203,6 +203,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
+// Raise the expected transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -877,6 +883,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
         return true;
     };
 
+    bool first = true;   // the block's first unit: no row can be resolved or flagged yet, no check
     while (!aborted) {
         int u = __shfl_sync(0xffffffffu, u_next, 0);
         if (u < 0 || u >= P.units_total) break;
@@ -906,7 +913,9 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 nk = min(nk, kEarlyMax);
                 if (lane < nk) ktok = node_token(P, b, P.tree ? static_cast<int>(P.kid_list[k0 + lane]) : n + 1);
             }
-            if (node_dead(P, b, n, greedy, lane)) {
+            const bool check = !first;
+            first = false;
+            if (check && node_dead(P, b, n, greedy, lane)) {
                 ++a_skipped;
                 if (P.ns == 1) {
                     settle_row<SMP>(P, S, 0, b, lane);
@@ -920,9 +929,6 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             }
             ++a_loaded;
             const size_t rowe = (static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V);
-            int kt[kEarlyMax];
-#pragma unroll
-            for (int c = 0; c < kEarlyMax; ++c) kt[c] = __shfl_sync(0xffffffffu, ktok, c);
             // accept-test operands of node n+1 (sampled rows): loaded now, used by the
             // epilogue after the whole row has streamed
             int xtok = -1;
@@ -957,10 +963,40 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                         I.qx = qx;
                         I.ux = ux;
                     }
-                    // first stage: the children's logits travel with the stage
-                    uint32_t extra = 0;
-                    const uint8_t *ksrc[kEarlyMax];
-                    if (s == s0) {
+                    I.gz = P.logits + (rowe + I.e0) * ES;
+                    const uint8_t *src;
+                    uint32_t nb;
+                    copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
+                    const int fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
+                    I.flags = kA | (last << 4) | (fast << 5) | (s == s0 ? kFirstF : 0u);
+                    loaded_bytes += nb;
+                    fence_proxy_async();
+                    uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
+                    if (s != s0) {
+                        if (nb) {
+                            mbar_expect_tx(&S.full[st], nb);
+                            bulk_g2s(dst, src, nb, &S.full[st]);
+                        } else {
+                            mbar_arrive(&S.full[st]);
+                        }
+                    } else if (nb) {
+                        // first stage: the row's copy goes out at once; the stage
+                        // completes only after the arrive below
+                        mbar_expect_tx_only(&S.full[st], nb);
+                        bulk_g2s(dst, src, nb, &S.full[st]);
+                    }
+                }
+                if (s == s0) {
+                    // the children's logits travel with the first stage (their tokens
+                    // may still be in flight when the row's copy has gone out)
+                    int kt[kEarlyMax];
+#pragma unroll
+                    for (int c = 0; c < kEarlyMax; ++c) kt[c] = __shfl_sync(0xffffffffu, ktok, c);
+                    if (lane == 0) {
+                        StageInfo &I = S.info[st];
+                        uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
+                        uint32_t extra = 0;
+                        const uint8_t *ksrc[kEarlyMax];
                         I.nk = nk;
 #pragma unroll
                         for (int c = 0; c < kEarlyMax; ++c) {
@@ -981,26 +1017,14 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                             }
                             I.kofs[c] = ko;
                         }
-                    }
-                    I.gz = P.logits + (rowe + I.e0) * ES;
-                    const uint8_t *src;
-                    uint32_t nb;
-                    copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
-                    const int fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
-                    I.flags = kA | (last << 4) | (fast << 5) | (s == s0 ? kFirstF : 0u);
-                    loaded_bytes += nb;
-                    fence_proxy_async();
-                    uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
-                    if (nb + extra) {
-                        mbar_expect_tx(&S.full[st], nb + extra);
-                        if (nb) bulk_g2s(dst, src, nb, &S.full[st]);
                         if (extra) {
+                            mbar_expect_tx(&S.full[st], extra);
 #pragma unroll
                             for (int c = 0; c < kEarlyMax; ++c)
                                 if (ksrc[c]) bulk_g2s(dst + kThrOff + 16 * c, ksrc[c], 16, &S.full[st]);
+                        } else {
+                            mbar_arrive(&S.full[st]);
                         }
-                    } else {
-                        mbar_arrive(&S.full[st]);
                     }
                 }
                 ++it;
