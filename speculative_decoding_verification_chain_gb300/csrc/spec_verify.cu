@@ -52,7 +52,8 @@ namespace sv {
 // ---------------------------------------------------------------- config --
 constexpr int kConsumerWarps = 12;
 constexpr int kConsumerLanes = 32 * kConsumerWarps;
-constexpr int kThreads = 32 * (2 + kConsumerWarps);   // producer, epilogue, consumers
+constexpr int kEpilogueWarps = 2;
+constexpr int kThreads = 32 * (1 + kEpilogueWarps + kConsumerWarps);   // producer, epilogues, consumers
 // The bulk-copy engine of an SM completes about one copy at a time, so the
 // per-SM stream rate grows with the copy size: three 64 KiB stages, each one
 // copy, consumed in passes of 24 KiB (the consumers' register tiles).
@@ -73,8 +74,10 @@ constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kEarlyMax = 4;                            // children per node given an early-rejection check
 constexpr uint32_t kFirstF = 1u << 6;                   // stage flag: first stage of its unit
+constexpr uint32_t kSkipF = 1u << 7;                    // stage flag: empty, the unit's row is not needed
 constexpr int kThrOff = kSubBytes + 64;                 // A stage: 16-byte chunks holding the children's logits
 static_assert(kThrOff + 16 * kEarlyMax <= kStageBytes, "threshold chunks do not fit in the stage");
+static_assert(kResSlots % kEpilogueWarps == 0, "result slots must split evenly over the epilogue warps");
 
 enum Kind : int { kEnd = 0, kA = 1, kB = 2 };
 
@@ -161,6 +164,7 @@ struct __align__(16) StageInfo {
 
 struct ResSlot {
     int kind, b, n, j;
+    int skip;                   // the unit was skipped (empty stage): account only
     float c2;
     int xtok;
     float zx, qx, ux;
@@ -176,9 +180,9 @@ struct Smem {
     uint64_t res_empty[kResSlots];
     StageInfo info[kStages];
     ResSlot res[kResSlots];
-    uint32_t fin_rs[2][kMaxRows];   // request finalisation scratch, per finalising warp
-    int fin_tok[2][kMaxRows];
-    uint8_t fin_acc[2][kMaxRows];
+    uint32_t fin_rs[kEpilogueWarps][kMaxRows];   // request finalisation scratch, per epilogue warp
+    int fin_tok[kEpilogueWarps][kMaxRows];
+    uint8_t fin_acc[kEpilogueWarps][kMaxRows];
     int abort_flag;
     int issued;                     // stages issued by the producer
     int consumed;                   // stages released by the consumers
@@ -887,7 +891,13 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     while (!aborted) {
         int u = __shfl_sync(0xffffffffu, u_next, 0);
         if (u < 0 || u >= P.units_total) break;
-        if (lane == 0) u_next = claim_base + static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+        // The following unit is claimed late (two stages before this one ends) so a
+        // block never holds a claimed unit long while others run out of work.
+        bool claimed = false;
+        auto claim_next = [&]() {
+            if (lane == 0) u_next = claim_base + static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+            claimed = true;
+        };
         if (u < P.units_a) {
             // ---------------- A unit: split j of row n of request b
             const int per_node = P.B * P.ns;
@@ -916,15 +926,30 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const bool check = !first;
             first = false;
             if (check && node_dead(P, b, n, greedy, lane)) {
+                // not needed: an empty stage carries the unit to the epilogue for its accounting
                 ++a_skipped;
-                if (P.ns == 1) {
-                    settle_row<SMP>(P, S, 0, b, lane);
-                } else {
-                    uint32_t old = 0;
-                    if (lane == 0) old = atom_add_acqrel(P.row_ctr + static_cast<size_t>(b) * P.R + n, kSkipInc);
-                    old = __shfl_sync(0xffffffffu, old, 0) + kSkipInc;
-                    if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) settle_row<SMP>(P, S, 0, b, lane);
+                int st;
+                if (!acquire_stage(st)) {
+                    aborted = true;
+                    break;
                 }
+                if (lane == 0) {
+                    StageInfo &I = S.info[st];
+                    I.b = b;
+                    I.n = n;
+                    I.j = j;
+                    I.e0 = 0;
+                    I.cnt = 0;
+                    I.c2 = c2;
+                    I.xtok = -1;
+                    I.sh = 0;
+                    I.tail = 0;
+                    I.gz = P.logits;
+                    I.flags = kA | (1 << 4) | kSkipF;
+                    mbar_arrive(&S.full[st]);
+                }
+                ++it;
+                claim_next();
                 continue;
             }
             ++a_loaded;
@@ -1028,9 +1053,12 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     }
                 }
                 ++it;
+                if (s == max(s0, s1 - 2)) claim_next();
             }
+            if (!claimed) claim_next();
         } else if (SMP) {
             // ---------------- B unit: chunk c of the rejected row of request b
+            claim_next();
             const int v = u - P.units_a;
             const int b = v / P.ncb;
             const int c = v - b * P.ncb;
@@ -1307,13 +1335,19 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
         const uint4 hot = *reinterpret_cast<const uint4 *>(&S.info[st]);
         const int kind = static_cast<int>(hot.x & 15u);
         if (kind == kEnd) {
-            // forward the end marker to the epilogue
-            const int slot = uc % kResSlots;
-            if (uc >= kResSlots && !wait_bar(P, S, &S.res_empty[slot], static_cast<uint32_t>((uc / kResSlots - 1) & 1)))
-                break;
-            if (lane == 0) {
-                if (cw == 0) S.res[slot].kind = kEnd;
-                mbar_arrive(&S.res_full[slot]);
+            // forward the end marker to every epilogue warp (the next kEpilogueWarps slots)
+            bool ok = true;
+            for (int q = 0; q < kEpilogueWarps && ok; ++q, ++uc) {
+                const int slot = uc % kResSlots;
+                if (uc >= kResSlots &&
+                    !wait_bar(P, S, &S.res_empty[slot], static_cast<uint32_t>((uc / kResSlots - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    if (cw == 0) S.res[slot].kind = kEnd;
+                    mbar_arrive(&S.res_full[slot]);
+                }
             }
             ++it;
             break;
@@ -1595,6 +1629,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 }
                 if (cw == 0) {
                     R.kind = kind;
+                    R.skip = (hot.x & kSkipF) != 0u;
                     R.b = b;
                     R.n = n;
                     R.j = j;
@@ -1623,8 +1658,8 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
 }
 
 template <bool SMP>
-__device__ void epilogue(const Params &P, Smem &S, int lane) {
-    int uc = 0;
+__device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
+    int uc = e;   // this warp takes units e, e + kEpilogueWarps, ...
     while (true) {
         const int slot = uc % kResSlots;
         if (!wait_bar(P, S, &S.res_full[slot], static_cast<uint32_t>((uc / kResSlots) & 1))) break;
@@ -1635,13 +1670,24 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
         const float c2 = R.c2;
         const int xtok = R.xtok;
         const float zx = R.zx, qx = R.qx, ux = R.ux;
+        const bool skip = R.skip != 0;
         float v = lane < kConsumerWarps ? R.v[lane] : -INFINITY;
         int grp = lane < kConsumerWarps ? R.idx[lane] : -1;
         const float sw = lane < kConsumerWarps ? R.s[lane] : 0.0f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.res_empty[slot]);
-        ++uc;
-        if (kind == kA) {
+        uc += kEpilogueWarps;
+        if (kind == kA && skip) {
+            // skipped row: counts as a skipped split, the row stays unresolved
+            if (P.ns == 1) {
+                settle_row<SMP>(P, S, e, b, lane);
+            } else {
+                uint32_t old = 0;
+                if (lane == 0) old = atom_add_acqrel(P.row_ctr + static_cast<size_t>(b) * P.R + n, kSkipInc);
+                old = __shfl_sync(0xffffffffu, old, 0) + kSkipInc;
+                if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) settle_row<SMP>(P, S, e, b, lane);
+            }
+        } else if (kind == kA) {
             const bool greedy = !SMP || (c2 == 0.0f);
             float um = 0.0f;
             double uS = 0.0;
@@ -1658,7 +1704,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
             const size_t ri = static_cast<size_t>(b) * P.R + n;
             if (P.ns == 1) {
                 resolve_row<SMP>(P, b, n, greedy, c2, grp, v, um, uS, xtok, zx, qx, ux, lane);
-                settle_row<SMP>(P, S, 1, b, lane);
+                settle_row<SMP>(P, S, e, b, lane);
             } else {
                 uint32_t old = 0;
                 if (lane == 0) {
@@ -1699,7 +1745,7 @@ __device__ void epilogue(const Params &P, Smem &S, int lane) {
                         }
                         resolve_row<SMP>(P, b, n, greedy, c2, gg, gv, rm, rS, xtok, zx, qx, ux, lane);
                     }
-                    settle_row<SMP>(P, S, 1, b, lane);
+                    settle_row<SMP>(P, S, e, b, lane);
                 }
             }
         } else if (SMP) {
@@ -1748,8 +1794,8 @@ __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P)
     __syncthreads();
 
     if (warp == 0) producer<ES, SMP>(P, S, ring, lane);
-    else if (warp == 1) epilogue<SMP>(P, S, lane);
-    else consumer<ES, SMP>(P, S, ring, warp - 2, lane, bad);
+    else if (warp <= kEpilogueWarps) epilogue<SMP>(P, S, warp - 1, lane);
+    else consumer<ES, SMP>(P, S, ring, warp - 1 - kEpilogueWarps, lane, bad);
 
     bad = __any_sync(0xffffffffu, bad != 0);
     if (lane == 0 && bad) set_status(P, SPEC_STATUS_NONFINITE);
