@@ -517,6 +517,35 @@ __device__ __forceinline__ float warp_butterfly_sum(float s) {
     return s;
 }
 
+// Sums of N = 2 or 4 per-lane values over the warp, scattered: afterwards lane
+// l holds the total of value q(l) = bits (4, 3) of l (N = 4) or bit 4 (N = 2);
+// 5 dependent steps for all N values instead of 5 per value.
+template <int N>
+__device__ __forceinline__ float warp_sum_scatter(const float (&v)[N], int lane) {
+    static_assert(N == 2 || N == 4, "2 or 4 values");
+    const bool h16 = (lane & 16) != 0;
+    float c;
+    if constexpr (N == 4) {
+        float k0 = h16 ? v[2] : v[0], k1 = h16 ? v[3] : v[1];
+        const float d0 = h16 ? v[0] : v[2], d1 = h16 ? v[1] : v[3];
+        k0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, d0, 16));
+        k1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, d1, 16));
+        const bool h8 = (lane & 8) != 0;
+        c = h8 ? k1 : k0;
+        const float d = h8 ? k0 : k1;
+        c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, d, 8));
+    } else {
+        c = h16 ? v[1] : v[0];
+        const float d = h16 ? v[0] : v[1];
+        c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, d, 16));
+        c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, 8));
+    }
+    c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, 4));
+    c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, 2));
+    c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, 1));
+    return c;
+}
+
 __device__ __forceinline__ double warp_sum_d(double s) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -1486,35 +1515,39 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 const float M = warp_max_redux(lm);
                 const float nMc2 = neg_mc2(M, c2);
                 const float2 c22 = make_float2(c2, c2), nm2 = make_float2(nMc2, nMc2);
-                float stage_sum = 0.0f;
-                bool any = false;
+                float sl[kBPW];   // this lane's partial of each of the warp's blocks
 #pragma unroll
                 for (int t = 0; t < kBPW; ++t) {
                     const int blk = p0 + cw + t * kConsumerWarps;
-                    if (blk < nb) {
-                        float s = 0.0f;
-                        if (blk * kBlk + lane * 8 < cnt) {
-                            float x[8];
-                            unpack8<ES>(ra[t], rc[t], x);
-                            float2 acc = make_float2(0.0f, 0.0f);
+                    float s = 0.0f;
+                    if (blk < nb && blk * kBlk + lane * 8 < cnt) {
+                        float x[8];
+                        unpack8<ES>(ra[t], rc[t], x);
+                        float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const float2 a = fma2(make_float2(x[2 * k], x[2 * k + 1]), c22, nm2);
-                                const float2 wv = make_float2(ex2(a.x), ex2(a.y));
-                                acc = (k == 0) ? wv : add2(acc, wv);
-                            }
-                            s = __fadd_rn(acc.x, acc.y);
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 a = fma2(make_float2(x[2 * k], x[2 * k + 1]), c22, nm2);
+                            const float2 wv = make_float2(ex2(a.x), ex2(a.y));
+                            acc = (k == 0) ? wv : add2(acc, wv);
                         }
-                        s = warp_butterfly_sum(s);
-                        if (lane == 0) {
-                            P.bmaxA[rb + blk] = M;
-                            P.bsumA[rb + blk] = s;
-                        }
-                        stage_sum = __fadd_rn(stage_sum, __shfl_sync(0xffffffffu, s, 0));
-                        any = true;
+                        s = __fadd_rn(acc.x, acc.y);
                     }
+                    sl[t] = s;
                 }
-                if (any) fold_stats(M, stage_sum, c2, Mw, Sw, Sc);
+                // block totals, scattered over the lanes: lane l holds block q(l)
+                const float tb = warp_sum_scatter<kBPW>(sl, lane);
+                constexpr int kGroup = 32 / kBPW;   // lanes holding the same block
+                const int q = kBPW == 4 ? (((lane >> 4) & 1) * 2 + ((lane >> 3) & 1)) : ((lane >> 4) & 1);
+                const int bq = p0 + cw + q * kConsumerWarps;
+                if ((lane & (kGroup - 1)) == 0 && bq < nb) {
+                    P.bmaxA[rb + bq] = M;
+                    P.bsumA[rb + bq] = tb;
+                }
+                // the pass total: the block totals summed across the groups
+                float pt = tb;
+#pragma unroll
+                for (int off = kGroup; off < 32; off <<= 1) pt = __fadd_rn(pt, __shfl_xor_sync(0xffffffffu, pt, off));
+                if (p0 + cw < nb) fold_stats(M, pt, c2, Mw, Sw, Sc);
               }
             } else {
                 for (int blk = cw; blk < nb; blk += kConsumerWarps) {
