@@ -769,8 +769,9 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
             uint32_t r = rs[best];
             ot[d] = (r & kResolved) ? static_cast<int>(r & kIdxMask) : 0;
         } else if (d < P.R - 1) {
+            // ot[d] is the residual pass's (which may already have run: the decision
+            // can be published as soon as the rejecting row resolves)
             decision |= kNeedsResidual | static_cast<uint32_t>(d);
-            ot[d] = -1;   // written by the residual pass
         } else {
             bonus = 1;
         }
@@ -798,7 +799,10 @@ __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) 
     uint32_t old = 0;
     if (lane == 0) old = atom_add_acqrel(P.req_ctr + b, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == static_cast<uint32_t>(P.R - 1)) finalize_request<SMP>(P, S, slot, b, lane);
+    if (old == static_cast<uint32_t>(P.R - 1)) {
+        __syncwarp();   // the whole warp reads after lane 0's acquire
+        finalize_request<SMP>(P, S, slot, b, lane);
+    }
 }
 
 // Warp-wide: resolve row n of request b once all its splits are in.
@@ -809,6 +813,7 @@ template <bool SMP>
 __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
                             double Srow, int xtok, float zx, float qx, float ux, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
+    uint32_t rejected = 0;   // sampled row with a child whose draft was rejected
     if (lane == 0) {
         uint32_t rsv;
         if (!SMP || greedy) {
@@ -832,16 +837,34 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
                     const double ph = static_cast<double>(ex2(__fmul_rn(__fsub_rn(zx, m), c2))) / Srow;
                     acc = static_cast<double>(ux) < ph / static_cast<double>(qx);
                 }
+                rejected = acc == 0;
             }
             rsv = kResolved | acc;
-            // the block data the consumers wrote must be visible wherever this state is seen
-            fence_acq_rel_gpu();
         }
-        // Relaxed: skip checks need only the value, and the settle atomic that
-        // follows (acq_rel, same thread) publishes it to the request's finaliser.
+        // Relaxed: skip checks and the early decision use only the value.  Readers
+        // of the row's data (block sums and maxima, statistics) synchronise through
+        // the settle atomic that follows (acq_rel, same thread, cumulative over the
+        // consumers' writes this warp observed at the stage barrier) or through the
+        // decision this thread publishes with release.
         st_relaxed(P.rowstate + ri, rsv);
     }
     __syncwarp();
+    // Sampled chain: a rejection at row n decides the request once every earlier
+    // draft is known to be accepted.  Publish the decision now, so the residual
+    // pass need not wait for the later rows (the finaliser writes the same value).
+    if (SMP && !P.tree && P.units_total > P.units_a && __shfl_sync(0xffffffffu, rejected, 0)) {
+        bool all = true;
+        for (int base = 0; base < n && all; base += 32) {
+            const int i = base + lane;
+            bool ok = true;
+            if (i < n) {
+                const uint32_t rs = ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
+                ok = (rs & kResolved) && (rs & 1u);
+            }
+            all = __all_sync(0xffffffffu, ok);
+        }
+        if (all && lane == 0) st_release(P.req_state + b, kDecided | kNeedsResidual | static_cast<uint32_t>(n));
+    }
 }
 
 // --------------------------------------------------------------- roles --
@@ -1746,7 +1769,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                     pr.idx = grp;
                     pr.s = uS;
                     P.partial[ri * P.ns + j] = pr;
-                    if (!greedy) fence_acq_rel_gpu();   // block data written by the consumers
+                    // acq_rel: publishes the partial and the consumers' block data
                     old = atom_add_acqrel(P.row_ctr + ri, 1u);
                 }
                 old = __shfl_sync(0xffffffffu, old, 0) + 1u;
@@ -1784,13 +1807,12 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
         } else if (SMP) {
             // B unit: the last chunk of a request's residual draws the token
             uint32_t old = 0;
-            if (lane == 0) {
-                fence_acq_rel_gpu();   // residual block sums written by the consumers
-                old = atom_add_acqrel(P.res_ctr + b, 1u);
-            }
+            // acq_rel: publishes this chunk's residual block sums; the last chunk's
+            // acquire sees every chunk's (the warp then reads them after a warp sync)
+            if (lane == 0) old = atom_add_acqrel(P.res_ctr + b, 1u);
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == static_cast<uint32_t>(P.ncb - 1)) {
-                fence_acq_rel_gpu();
+                __syncwarp();
                 double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + n));
                 int t = sample_row(P, b, n, true, u, lane);
                 if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + n] = t;
