@@ -170,7 +170,8 @@ struct ResSlot {
     float zx, qx, ux;
     float v[kConsumerWarps];    // greedy: lane-reduced max; sampled: warp max M_w
     int idx[kConsumerWarps];    // greedy: first index of the max
-    float s[kConsumerWarps];    // sampled: warp sum of 2^((z - M_w) c2)
+    float s[kConsumerWarps];    // sampled: warp sum of 2^((z - M_w) c2); greedy bf16: packed-record max
+    int pg[kConsumerWarps];     // greedy bf16: row index of the first 8-element group holding it
 };
 
 struct Smem {
@@ -1641,29 +1642,19 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 break;
             float v = best;
             int g = bidx;
+            float pv = -INFINITY;   // greedy bf16: packed-record candidate (value, group)
+            int pgw = -1;
             if (kind == kA && c2 == 0.0f) {
                 warp_cand(v, g);
                 if (ES == 2) {
-                    // packed records: the lane's max, the first group holding it, the
-                    // warp's winner, then its first element from the row in memory
+                    // packed records: the lane's max and the first group holding it, then
+                    // the warp's winner (the epilogue finds its first element in memory,
+                    // off the consumers' path)
                     const float mlo = bf16_lo(pk), mhi = bf16_hi(pk);
-                    float pv = fmaxf(mlo, mhi);
-                    int pg = mlo > mhi ? glo : (mhi > mlo ? ghi : min(static_cast<unsigned>(glo), static_cast<unsigned>(ghi)));
-                    if (!(pv > -INFINITY)) pg = -1;
-                    warp_cand(pv, pg);
-                    int pidx = -1;
-                    if (pg >= 0 && pg + 8 <= P.V) {
-                        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(
-                            P.logits + ((static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V) + pg) * 2));
-                        float x[8];
-                        unpack8<2>(w, w, x);
-                        int i = 7;
-#pragma unroll
-                        for (int q = 7; q >= 0; --q)
-                            if (x[q] == pv) i = q;
-                        pidx = pg + i;
-                    }
-                    cand_merge(v, g, pv, pidx);
+                    pv = fmaxf(mlo, mhi);
+                    pgw = mlo > mhi ? glo : (mhi > mlo ? ghi : min(static_cast<unsigned>(glo), static_cast<unsigned>(ghi)));
+                    if (!(pv > -INFINITY)) pgw = -1;
+                    warp_cand(pv, pgw);
                 }
                 mx = fmax_nan(mx, fmax_nan(bf16_lo(pk), bf16_hi(pk)));
                 mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -1682,6 +1673,8 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 } else {
                     R.v[cw] = v;
                     R.idx[cw] = g;
+                    R.s[cw] = pv;
+                    R.pg[cw] = pgw;
                 }
                 if (cw == 0) {
                     R.kind = kind;
@@ -1730,6 +1723,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
         float v = lane < kConsumerWarps ? R.v[lane] : -INFINITY;
         int grp = lane < kConsumerWarps ? R.idx[lane] : -1;
         const float sw = lane < kConsumerWarps ? R.s[lane] : 0.0f;
+        int pgr = lane < kConsumerWarps ? R.pg[lane] : -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.res_empty[slot]);
         uc += kEpilogueWarps;
@@ -1749,6 +1743,25 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
             double uS = 0.0;
             if (greedy) {
                 warp_cand(v, grp);
+                if (P.esize == 2) {
+                    // packed records: the winning group's first element equal to its max
+                    float pv = (lane < kConsumerWarps) ? sw : -INFINITY;
+                    warp_cand(pv, pgr);
+                    int pidx = -1;
+                    if (pgr >= 0 && pgr + 8 <= P.V) {
+                        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(
+                            P.logits + ((static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V) + pgr) * 2));
+                        int i = 7;
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 3; q >= 0; --q) {
+                            if (bf16_hi(ww[q]) == pv) i = 2 * q + 1;
+                            if (bf16_lo(ww[q]) == pv) i = 2 * q;
+                        }
+                        pidx = pgr + i;
+                    }
+                    cand_merge(v, grp, pv, pidx);
+                }
             } else {
                 // combine the consumer warps' (M_w, S_w) into the unit's (m, S)
                 um = warp_max(v);
