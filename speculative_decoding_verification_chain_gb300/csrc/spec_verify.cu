@@ -842,29 +842,39 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
             }
             rsv = kResolved | acc;
         }
-        // Relaxed: skip checks and the early decision use only the value.  Readers
+        // Relaxed: skip checks and the early decisions use only the value; readers
         // of the row's data (block sums and maxima, statistics) synchronise through
         // the settle atomic that follows (acq_rel, same thread, cumulative over the
-        // consumers' writes this warp observed at the stage barrier) or through the
+        // consumers' writes this warp observed at the stage barrier) or through a
         // decision this thread publishes with release.
         st_relaxed(P.rowstate + ri, rsv);
     }
     __syncwarp();
-    // Sampled chain: a rejection at row n decides the request once every earlier
-    // draft is known to be accepted.  Publish the decision now, so the residual
-    // pass need not wait for the later rows (the finaliser writes the same value).
-    if (SMP && !P.tree && P.units_total > P.units_a && __shfl_sync(0xffffffffu, rejected, 0)) {
-        bool all = true;
-        for (int base = 0; base < n && all; base += 32) {
+    // Sampled chain: publish the decision as soon as it is known, so the residual
+    // pass need not wait for the later rows (the finaliser writes the same value
+    // and covers every case left here): a rejection at this row with every
+    // earlier draft accepted (this thread wrote the row statistics the residual
+    // pass reads), or every draft accepted (no residual pass: its units can leave).
+    if (SMP && !greedy && !P.tree && P.units_total > P.units_a) {
+        const uint32_t rej_n = __shfl_sync(0xffffffffu, rejected, 0);
+        int f = -1;   // first draft not known accepted
+        bool rej = false;
+        for (int base = 0; base < P.R - 1 && f < 0; base += 32) {
             const int i = base + lane;
-            bool ok = true;
-            if (i < n) {
-                const uint32_t rs = ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
-                ok = (rs & kResolved) && (rs & 1u);
+            uint32_t rs = 0;
+            if (i < P.R - 1) rs = (i == n) ? (kResolved | (rej_n ? 0u : 1u))
+                                          : ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
+            const unsigned notacc = __ballot_sync(0xffffffffu, i < P.R - 1 && !((rs & kResolved) && (rs & 1u)));
+            if (notacc) {
+                const int l = __ffs(notacc) - 1;
+                f = base + l;
+                rej = __shfl_sync(0xffffffffu, (rs & kResolved) != 0u, l);
             }
-            all = __all_sync(0xffffffffu, ok);
         }
-        if (all && lane == 0) st_release(P.req_state + b, kDecided | kNeedsResidual | static_cast<uint32_t>(n));
+        if (lane == 0) {
+            if (f < 0) st_release(P.req_state + b, kDecided);   // every draft accepted: bonus, no residual
+            else if (rej && f == n) st_release(P.req_state + b, kDecided | kNeedsResidual | static_cast<uint32_t>(f));
+        }
     }
 }
 
