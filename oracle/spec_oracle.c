@@ -279,7 +279,8 @@ int oracle_verify_chain(const void *logits, int dtype, const float *draft_probs,
                         int32_t *out_tokens, int32_t *out_num_accepted, int32_t *flag_accept,
                         int32_t *flag_sample, double *b_alg, double *accept_ratio, int nthreads)
 {
-    if (B < 0 || k < 1 || V < 1 || !logits || !draft_tokens || !temperature || !u_sample ||
+    /* k = 0 (a request with no drafts) emits the bonus token of row 0 */
+    if (B < 0 || k < 0 || V < 1 || !logits || (k > 0 && !draft_tokens) || !temperature || !u_sample ||
         !out_tokens || !out_num_accepted)
         return 1;
     for (int b = 0; b < B; ++b)

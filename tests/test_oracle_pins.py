@@ -178,6 +178,27 @@ def test_bonus_sampler_is_inverse_cdf(oracle_mod):
         assert (r["out_tokens"][b, :k] == tok[b]).all()
 
 
+def test_zero_drafts_emit_the_row0_token(oracle_mod):
+    """A request with no drafts (k = 0, ragged batches) accepts nothing and emits
+    the bonus token of row 0: numpy argmax when greedy, else the inverse CDF of
+    p_0 (numpy cumsum + searchsorted) at u_sample[b, 0]."""
+    g = np.random.default_rng(26)
+    B, V, T = 64, 333, 0.9
+    z = (g.standard_normal((B, 1, V)) * 2).astype(np.float32)
+    us = W.method_uniforms(g, (B, 1))
+    tok = np.zeros((B, 0), np.int32)
+    r = oracle_mod.verify_chain(z, W.FP32, tok, np.zeros(B, np.float32), us)
+    assert (r["num_accepted"] == 0).all()
+    assert (r["out_tokens"][:, 0] == np.argmax(z[:, 0], axis=-1)).all()
+    r = oracle_mod.verify_chain(z, W.FP32, tok, np.full(B, T, np.float32), us, np.zeros((B, 0, V), np.float32),
+                                np.zeros((B, 0), np.float32))
+    assert (r["num_accepted"] == 0).all()
+    for b in range(B):
+        c = np.cumsum(_softmax64(z[b, 0], T))
+        j = int(np.searchsorted(c, float(us[b, 0]) * c[-1], side="right"))
+        assert r["flag_sample"][b] or r["out_tokens"][b, 0] == j
+
+
 def _lossless_case(seed, V=8, k=4, T=1.0):
     g = np.random.default_rng(seed)
     zp = (g.standard_normal((k + 1, V)) * 1.2).astype(np.float32)
