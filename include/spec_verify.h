@@ -66,6 +66,9 @@ typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype_t;
                                       (results undefined).  A -inf logit alone is a masked
                                       token: probability 0, never the argmax of a finite row. */
 #define SPEC_STATUS_WAIT_TIMEOUT 4 /* an inter-block wait gave up (results of that request undefined) */
+#define SPEC_STATUS_BAD_OFFSETS 8  /* ragged chains: cu_num_draft_tokens not non-decreasing within
+                                      [0, total_drafts] or a count above max_k (clamped; results of
+                                      the requests involved undefined) */
 
 /* Largest rows per request (k+1 for chains, N+1 for trees). */
 #define SPEC_MAX_ROWS 256
@@ -122,6 +125,40 @@ spec_status_t spec_verify_chain(const void *target_logits, spec_dtype_t dtype,
                                 void *stream);
 
 /*
+ * Ragged chain verification: a different number of drafts per request, packed
+ * (the vLLM speculative-decoding walkthrough's per-step metadata:
+ * cu_num_draft_tokens offsets into packed draft and target rows).  Greedy and
+ * sampled requests may be mixed, as in spec_verify_chain.
+ *
+ *  cu_num_draft_tokens [B+1] int32 device, non-decreasing, cu[0] = 0,
+ *      cu[B] = total_drafts: request b has k_b = cu[b+1] - cu[b] drafts
+ *      (0 <= k_b <= max_k).
+ *  target_logits [total_drafts + B, V] device: request b's k_b + 1 rows start
+ *      at row cu[b] + b (row i of the request as in spec_verify_chain).
+ *  draft_probs   [total_drafts, V] fp32 device or NULL: request b's rows start
+ *      at row cu[b].
+ *  draft_tokens, u_accept [total_drafts] packed the same way (u_accept NULL when
+ *      every request is greedy).
+ *  u_sample      [total_drafts + B], packed like the logits rows.
+ *  temperature   [B], as in spec_verify_chain.
+ *  out_tokens    [B, max_k+1] int32 device (padded, -1 after the emitted tokens).
+ *  out_num_accepted [B] int32 device: a_b in [0, k_b].
+ *  workspace: spec_workspace_bytes(B, max_k+1, V, dtype).
+ *  Offsets that break the rules above are clamped so nothing is read outside
+ *  the packed inputs, and SPEC_STATUS_BAD_OFFSETS is set.
+ *  Sizes: 1 <= B, 0 <= max_k <= SPEC_MAX_ROWS-1, 1 <= V < 2^30,
+ *  0 <= total_drafts <= B * max_k.
+ */
+spec_status_t spec_verify_chain_ragged(const void *target_logits, spec_dtype_t dtype,
+                                       const float *draft_probs, const int32_t *draft_tokens,
+                                       const int32_t *cu_num_draft_tokens, int total_drafts,
+                                       const float *temperature, const float *u_accept,
+                                       const float *u_sample, int B, int max_k, int V,
+                                       int32_t *out_tokens, int32_t *out_num_accepted,
+                                       int32_t *d_status, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/*
  * Greedy token-tree verification (EAGLE-style tree, one verification forward).
  *
  *  target_logits [B, N+1, V] device, bf16 or fp32, 16-byte aligned.  Row n is
@@ -160,6 +197,16 @@ spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_t dtype,
 spec_status_t spec_fixup_slots(int64_t *slot_mapping, int B, int P, const int32_t *num_accepted,
                                const int32_t *path, int path_stride, int64_t padding_slot_id,
                                void *stream);
+
+/*
+ * Slot_mapping fix-up for ragged chains, in place on packed int64 device
+ * memory of total_drafts + B entries: request b's k_b + 1 slots start at
+ * cu_num_draft_tokens[b] + b, and slot j of request b keeps its value iff
+ * j <= num_accepted[b]; the others become padding_slot_id.
+ */
+spec_status_t spec_fixup_slots_ragged(int64_t *slot_mapping, int B, const int32_t *cu_num_draft_tokens,
+                                      int total_drafts, const int32_t *num_accepted,
+                                      int64_t padding_slot_id, void *stream);
 
 /*
  * Host helper (no device work): tree_choices -> parent[] and level metadata,

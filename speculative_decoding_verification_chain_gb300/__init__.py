@@ -23,11 +23,12 @@ from typing import Optional, Sequence, Tuple
 
 __all__ = ["verify_chain", "verify_tree", "fixup_slots", "tree_from_choices", "workspace_bytes",
            "SpecError", "PADDING_SLOT_ID", "STATUS_TOKEN_RANGE", "STATUS_NONFINITE",
-           "STATUS_WAIT_TIMEOUT", "library_path", "load_library", "verify_chain_noalloc"]
+           "STATUS_WAIT_TIMEOUT", "STATUS_BAD_OFFSETS", "library_path", "load_library", "verify_chain_noalloc",
+           "verify_chain_ragged", "fixup_slots_ragged"]
 
 PADDING_SLOT_ID = -1
 SPEC_BF16, SPEC_FP32 = 0, 1
-STATUS_TOKEN_RANGE, STATUS_NONFINITE, STATUS_WAIT_TIMEOUT = 1, 2, 4
+STATUS_TOKEN_RANGE, STATUS_NONFINITE, STATUS_WAIT_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8
 MAX_ROWS = 256
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +70,10 @@ def load_library():
         lib.spec_workspace_init.restype = I
         lib.spec_verify_chain.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, P, Z, P]
         lib.spec_verify_chain.restype = I
+        lib.spec_verify_chain_ragged.argtypes = [P, I, P, P, P, I, P, P, P, I, I, I, P, P, P, P, Z, P]
+        lib.spec_verify_chain_ragged.restype = I
+        lib.spec_fixup_slots_ragged.argtypes = [P, I, P, I, P, ctypes.c_int64, P]
+        lib.spec_fixup_slots_ragged.restype = I
         lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
         lib.spec_verify_tree.restype = I
         lib.spec_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64, P]
@@ -220,6 +225,76 @@ def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u
                                _ptr(out_num_accepted), _ptr(status), _ptr(ws), ws.numel(), sh)
     _check("spec_verify_chain", rc)
     return out_tokens, out_num_accepted
+
+
+def verify_chain_ragged(target_logits, draft_tokens, cu_num_draft_tokens, max_k: int, temperature=None,
+                        u_accept=None, u_sample=None, draft_probs=None, *, out_tokens=None,
+                        out_num_accepted=None, status=None, workspace=None, stream=None) -> Tuple[object, object]:
+    """Chain verify-and-accept with a different number of drafts per request.
+
+    cu_num_draft_tokens [B+1] int32 CUDA (cu[0] = 0, non-decreasing): request b
+    has k_b = cu[b+1] - cu[b] <= max_k drafts.  target_logits [cu[B] + B, V]
+    packed rows (request b's k_b + 1 rows from row cu[b] + b); draft_tokens and
+    u_accept [cu[B]], draft_probs [cu[B], V] packed from row cu[b]; u_sample
+    [cu[B] + B] packed like the logits rows; temperature [B].  Returns
+    (out_tokens [B, max_k+1] int32 padded with -1, num_accepted [B] int32).
+    """
+    torch = _torch()
+    lib = load_library()
+    z = target_logits
+    if z.dim() != 2 or z.device.type != "cuda" or not z.is_contiguous():
+        raise ValueError("target_logits must be a contiguous [rows, V] CUDA tensor")
+    rows, V = z.shape
+    dev = z.device
+    cu = cu_num_draft_tokens
+    if cu.dtype != torch.int32 or cu.dim() != 1 or cu.device != dev or not cu.is_contiguous():
+        raise ValueError("cu_num_draft_tokens must be a contiguous [B+1] int32 tensor on the logits' device")
+    B = cu.shape[0] - 1
+    total = rows - B
+    if B < 1 or total < 0:
+        raise ValueError("target_logits must hold cu[B] + B rows")
+    code = _dtype_code(z)
+    _need(draft_tokens, "draft_tokens", torch.int32, (total,), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(u_accept, "u_accept", torch.float32, (total,), dev)
+    _need(u_sample, "u_sample", torch.float32, (total + B,), dev)
+    _need(draft_probs, "draft_probs", torch.float32, (total, V), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, max_k + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, max_k + 1), dev)
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    sh = _stream_handle(dev, stream)
+    nbytes = workspace_bytes(B, max_k + 1, V, code)
+    ws = workspace if workspace is not None else _workspace(dev, sh, nbytes, ("chain", B, max_k + 1, V, code))
+    rc = lib.spec_verify_chain_ragged(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(cu), total,
+                                      _ptr(temperature), _ptr(u_accept), _ptr(u_sample), B, max_k, V,
+                                      _ptr(out_tokens), _ptr(out_num_accepted), _ptr(status), _ptr(ws),
+                                      ws.numel(), sh)
+    _check("spec_verify_chain_ragged", rc)
+    return out_tokens, out_num_accepted
+
+
+def fixup_slots_ragged(slot_mapping, cu_num_draft_tokens, num_accepted, padding_slot_id: int = PADDING_SLOT_ID,
+                       stream=None):
+    """In-place fix-up of packed slots ([cu[B] + B] int64 CUDA): request b's
+    slots start at cu[b] + b; slot j is kept iff j <= num_accepted[b]."""
+    torch = _torch()
+    lib = load_library()
+    cu = cu_num_draft_tokens
+    if slot_mapping.dtype != torch.int64 or slot_mapping.dim() != 1 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous 1-D int64 tensor")
+    dev = slot_mapping.device
+    if cu.dtype != torch.int32 or cu.dim() != 1 or cu.device != dev:
+        raise ValueError("cu_num_draft_tokens must be a [B+1] int32 tensor on the slots' device")
+    B = cu.shape[0] - 1
+    total = slot_mapping.shape[0] - B
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    rc = lib.spec_fixup_slots_ragged(_ptr(slot_mapping), B, _ptr(cu), total, _ptr(num_accepted),
+                                     int(padding_slot_id), _stream_handle(dev, stream))
+    _check("spec_fixup_slots_ragged", rc)
+    return slot_mapping
 
 
 def verify_tree(target_logits, node_tokens, parent: Sequence[int], max_depth: Optional[int] = None, *,

@@ -134,6 +134,8 @@ struct Params {
     int ncb, nblk;
     int units_a, units_total;
     int tree;
+    const int32_t *cu;           // ragged chains: request b has cu[b+1] - cu[b] drafts (null: R - 1 each)
+    int total_drafts;            // ragged chains: cu[B] (packed draft rows; logit rows add one per request)
     int ahead;                   // stages the producer may have in flight
     int16_t parent[kMaxRows];
     uint8_t depth[kMaxRows];
@@ -566,8 +568,53 @@ __device__ __forceinline__ double warp_incl_scan_d(double s, int lane) {
 __device__ __forceinline__ int parent_of(const Params &P, int n) { return P.tree ? P.parent[n] : n - 1; }
 __device__ __forceinline__ int depth_of(const Params &P, int n) { return P.tree ? P.depth[n] : n; }
 
+// Request b's first draft slot in the packed per-draft inputs (tokens, accept
+// uniforms, q rows) and its number of drafts.  Padded batches: b * (R - 1) and
+// R - 1.  Ragged chains read the offsets; offsets outside [0, total] or a count
+// above R - 1 are clamped (and flagged) so no read leaves the inputs.
+__device__ __forceinline__ void draft_span(const Params &P, int b, int &first, int &count) {
+    if (!P.cu) {
+        first = b * (P.R - 1);
+        count = P.R - 1;
+        return;
+    }
+    int lo = __ldg(P.cu + b), hi = __ldg(P.cu + b + 1);
+    const int lo0 = lo, hi0 = hi;
+    lo = min(max(lo, 0), P.total_drafts);
+    hi = min(max(hi, lo), P.total_drafts);
+    hi = min(hi, lo + P.R - 1);
+    if (lo != lo0 || hi != hi0) set_status(P, SPEC_STATUS_BAD_OFFSETS);
+    first = lo;
+    count = hi - lo;
+}
+
+// Rows (nodes) of request b: drafts + 1.
+__device__ __forceinline__ int rows_of(const Params &P, int b) {
+    if (!P.cu) return P.R;
+    int first, count;
+    draft_span(P, b, first, count);
+    return count + 1;
+}
+
+// Input row of node n of request b in the logits (packed: each request's rows
+// follow its drafts' offsets, one extra row per request).
+__device__ __forceinline__ size_t in_row(const Params &P, int b, int n) {
+    if (!P.cu) return static_cast<size_t>(b) * P.R + n;
+    int first, count;
+    draft_span(P, b, first, count);
+    return static_cast<size_t>(first) + b + n;
+}
+
+// Per-draft input index of draft slot i (node i + 1) of request b.
+__device__ __forceinline__ size_t in_draft(const Params &P, int b, int i) {
+    if (!P.cu) return static_cast<size_t>(b) * (P.R - 1) + i;
+    int first, count;
+    draft_span(P, b, first, count);
+    return static_cast<size_t>(first) + i;
+}
+
 __device__ __forceinline__ int node_token(const Params &P, int b, int n) {
-    return __ldg(P.tokens + static_cast<size_t>(b) * (P.R - 1) + (n - 1));
+    return __ldg(P.tokens + in_draft(P, b, n - 1));
 }
 
 // Edge parent -> child accepted, given the parent's resolved row state.
@@ -656,13 +703,13 @@ __device__ double locate_block(const BlockSource &S, int nblk, double u, int lan
 // block max, scaled by the block factor; residual == true: max(0, p - q).
 __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, double base, double t,
                           bool residual, float invS, int lane) {
-    const size_t rowz = (static_cast<size_t>(b) * P.R + row) * static_cast<size_t>(P.V);
+    const size_t rowz = in_row(P, b, row) * static_cast<size_t>(P.V);
     const int e0 = beta * kBlk + lane * 8;
     float w[8];
     const float nMc2 = neg_mc2(residual ? S.m : __ldcg(S.bmax + beta), S.c2);
     double fac = residual ? 1.0 : block_factor(S, beta);
     const float *qrow =
-        residual ? P.q + (static_cast<size_t>(b) * (P.R - 1) + row) * static_cast<size_t>(P.V) : nullptr;
+        residual ? P.q + in_draft(P, b, row) * static_cast<size_t>(P.V) : nullptr;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         int e = e0 + i;
@@ -732,8 +779,9 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
     uint32_t *rs = S.fin_rs[slot];
     int *tok = S.fin_tok[slot];
     uint8_t *acc = S.fin_acc[slot];
+    const int Rb = rows_of(P, b);
     int range_bad = 0;
-    for (int i = lane; i < P.R; i += 32) {
+    for (int i = lane; i < Rb; i += 32) {
         rs[i] = ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
         tok[i] = i > 0 ? node_token(P, b, i) : -1;
         if (i > 0 && (tok[i] < 0 || tok[i] >= P.V)) range_bad = 1;
@@ -746,7 +794,7 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
     if (lane == 0) {
         acc[0] = 1;
         int best = 0;
-        for (int i = 1; i < P.R; ++i) {
+        for (int i = 1; i < Rb; ++i) {
             int p = parent_of(P, i);
             bool ok = acc[p] && edge_ok(rs[p], greedy, tok[i]);
             acc[i] = ok;
@@ -769,7 +817,7 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
         if (greedy) {
             uint32_t r = rs[best];
             ot[d] = (r & kResolved) ? static_cast<int>(r & kIdxMask) : 0;
-        } else if (d < P.R - 1) {
+        } else if (d < Rb - 1) {
             // ot[d] is the residual pass's (which may already have run: the decision
             // can be published as soon as the rejecting row resolves)
             decision |= kNeedsResidual | static_cast<uint32_t>(d);
@@ -780,8 +828,8 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
     }
     bonus = __shfl_sync(0xffffffffu, bonus, 0);
     if (SMP && bonus) {
-        const int a = P.R - 1;
-        double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + a));
+        const int a = Rb - 1;
+        double u = static_cast<double>(__ldg(P.u_sample + in_row(P, b, a)));
         int t = sample_row(P, b, a, false, u, lane);
         if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = t;
     }
@@ -800,7 +848,7 @@ __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) 
     uint32_t old = 0;
     if (lane == 0) old = atom_add_acqrel(P.req_ctr + b, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == static_cast<uint32_t>(P.R - 1)) {
+    if (old == static_cast<uint32_t>(rows_of(P, b) - 1)) {
         __syncwarp();   // the whole warp reads after lane 0's acquire
         finalize_request<SMP>(P, S, slot, b, lane);
     }
@@ -814,6 +862,7 @@ template <bool SMP>
 __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
                             double Srow, int xtok, float zx, float qx, float ux, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
+    const int Rb = rows_of(P, b);
     uint32_t rejected = 0;   // sampled row with a child whose draft was rejected
     if (lane == 0) {
         uint32_t rsv;
@@ -829,7 +878,7 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
             st.S = Srow;
             P.rowstat[ri] = st;
             uint32_t acc = 0;
-            if (n < P.R - 1) {
+            if (n < Rb - 1) {
                 if (xtok < 0) {
                     set_status(P, SPEC_STATUS_TOKEN_RANGE);
                 } else if (qx == 0.0f) {
@@ -859,12 +908,12 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
         const uint32_t rej_n = __shfl_sync(0xffffffffu, rejected, 0);
         int f = -1;   // first draft not known accepted
         bool rej = false;
-        for (int base = 0; base < P.R - 1 && f < 0; base += 32) {
+        for (int base = 0; base < Rb - 1 && f < 0; base += 32) {
             const int i = base + lane;
             uint32_t rs = 0;
-            if (i < P.R - 1) rs = (i == n) ? (kResolved | (rej_n ? 0u : 1u))
-                                          : ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
-            const unsigned notacc = __ballot_sync(0xffffffffu, i < P.R - 1 && !((rs & kResolved) && (rs & 1u)));
+            if (i < Rb - 1) rs = (i == n) ? (kResolved | (rej_n ? 0u : 1u))
+                                         : ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
+            const unsigned notacc = __ballot_sync(0xffffffffu, i < Rb - 1 && !((rs & kResolved) && (rs & 1u)));
             if (notacc) {
                 const int l = __ffs(notacc) - 1;
                 f = base + l;
@@ -968,6 +1017,10 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const int rem = u - n * per_node;
             const int b = rem / P.ns;
             const int j = rem - b * P.ns;
+            if (P.cu && n >= rows_of(P, b)) {   // ragged: this request has fewer rows
+                claim_next();
+                continue;
+            }
             const bool greedy = !SMP || is_greedy(P, b);
             const float c2 = greedy ? 0.0f : kLog2e / __ldg(P.temperature + b);
             const int s0 = j * P.sps;
@@ -981,7 +1034,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     k0 = P.kid_off[n];
                     nk = P.kid_off[n + 1] - k0;
                 } else {
-                    nk = n < P.R - 1 ? 1 : 0;
+                    nk = n < rows_of(P, b) - 1 ? 1 : 0;
                 }
                 nk = min(nk, kEarlyMax);
                 if (lane < nk) ktok = node_token(P, b, P.tree ? static_cast<int>(P.kid_list[k0 + lane]) : n + 1);
@@ -1016,18 +1069,18 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 continue;
             }
             ++a_loaded;
-            const size_t rowe = (static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V);
+            const size_t rowe = in_row(P, b, n) * static_cast<size_t>(P.V);
             // accept-test operands of node n+1 (sampled rows): loaded now, used by the
             // epilogue after the whole row has streamed
             int xtok = -1;
             float zx = 0.0f, qx = 0.0f, ux = 0.0f;
-            if (SMP && lane == 0 && !greedy && n < P.R - 1) {
+            if (SMP && lane == 0 && !greedy && n < rows_of(P, b) - 1) {
                 const int x = node_token(P, b, n + 1);
-                ux = __ldg(P.u_accept + static_cast<size_t>(b) * (P.R - 1) + n);
+                ux = __ldg(P.u_accept + in_draft(P, b, n));
                 if (x >= 0 && x < P.V) {
                     xtok = x;
                     zx = logit_global(P, rowe + x);
-                    qx = __ldg(P.q + (static_cast<size_t>(b) * (P.R - 1) + n) * P.V + x);
+                    qx = __ldg(P.q + in_draft(P, b, n) * P.V + x);
                 }
             }
             for (int s = s0; s < s1; ++s) {
@@ -1140,7 +1193,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             }
             stv = __shfl_sync(0xffffffffu, stv, 0);
             const int a = static_cast<int>(stv & kIdxMask);
-            if (!(stv & kDecided) || !(stv & kNeedsResidual) || a >= P.R - 1) {
+            if (!(stv & kDecided) || !(stv & kNeedsResidual) || a >= rows_of(P, b) - 1) {
                 ++b_skipped;
                 continue;
             }
@@ -1149,8 +1202,8 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const float m = __ldcg(&P.rowstat[ri].m);
             const double Srow = __ldcg(&P.rowstat[ri].S);
             const float c2 = kLog2e / __ldg(P.temperature + b);
-            const size_t rowe = ri * static_cast<size_t>(P.V);
-            const size_t qrowe = (static_cast<size_t>(b) * (P.R - 1) + a) * static_cast<size_t>(P.V);
+            const size_t rowe = in_row(P, b, a) * static_cast<size_t>(P.V);
+            const size_t qrowe = in_draft(P, b, a) * static_cast<size_t>(P.V);
             const int e_begin = c * P.ecb;
             const int e_end = min(P.V, e_begin + P.ecb);
             for (int e = e_begin; e < e_end; e += P.esb) {
@@ -1456,7 +1509,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                         ethr = ES == 2 ? __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(pz)) << 16)
                                        : *reinterpret_cast<const float *>(pz);
                     } else if (ko == -2) {
-                        ethr = logit_global(P, (static_cast<size_t>(bb) * P.R + nn) * static_cast<size_t>(P.V) + I.ktok[lane]);
+                        ethr = logit_global(P, in_row(P, bb, nn) * static_cast<size_t>(P.V) + I.ktok[lane]);
                     } else {
                         ethr = -INFINITY;
                     }
@@ -1760,7 +1813,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                     int pidx = -1;
                     if (pgr >= 0 && pgr + 8 <= P.V) {
                         const uint4 w = __ldg(reinterpret_cast<const uint4 *>(
-                            P.logits + ((static_cast<size_t>(b) * P.R + n) * static_cast<size_t>(P.V) + pgr) * 2));
+                            P.logits + (in_row(P, b, n) * static_cast<size_t>(P.V) + pgr) * 2));
                         int i = 7;
                         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -1836,7 +1889,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == static_cast<uint32_t>(P.ncb - 1)) {
                 __syncwarp();
-                double u = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * P.R + n));
+                double u = static_cast<double>(__ldg(P.u_sample + in_row(P, b, n)));
                 int t = sample_row(P, b, n, true, u, lane);
                 if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + n] = t;
             }
@@ -1899,6 +1952,22 @@ __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P)
 }
 
 // ------------------------------------------------------------ slot fix-up --
+// Ragged chains: request b's slots are packed at cu[b] + b .. cu[b+1] + b (its
+// drafts plus one); one warp per request keeps j <= num_accepted[b].
+__global__ void fixup_ragged_kernel(int64_t *slots, int B, const int32_t *cu, int total, const int32_t *num_acc,
+                                    int64_t pad) {
+    const int w = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= B) return;
+    int lo = __ldg(cu + w), hi = __ldg(cu + w + 1);
+    lo = min(max(lo, 0), total);
+    hi = min(max(hi, lo), total);
+    const int a = __ldg(num_acc + w);
+    int64_t *sb = slots + static_cast<size_t>(lo) + w;
+    for (int j = lane; j <= hi - lo; j += 32)
+        if (j > a) sb[j] = pad;
+}
+
 __global__ void fixup_kernel(int64_t *slots, int B, int P, const int32_t *num_acc, const int32_t *path,
                              int stride, int64_t pad) {
     const long long total = static_cast<long long>(B) * P;
@@ -2102,29 +2171,31 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     P.qoff = L.qoff;
     P.ncb = L.ncb;
     P.nblk = L.nblk;
-    const long long rows_total = static_cast<long long>(P.B) * P.R;
+    // rows actually present (ragged chains: one more than the drafts per request)
+    const long long rows_total = P.cu ? static_cast<long long>(P.total_drafts) + P.B : static_cast<long long>(P.B) * P.R;
     int ns = choose_splits(rows_total > (1 << 30) ? (1 << 30) : static_cast<int>(rows_total), L.nsub, D->sms);
     P.sps = (L.nsub + ns - 1) / ns;
     P.ahead = choose_ahead();
     P.ns = (L.nsub + P.sps - 1) / P.sps;
-    const long long ua = rows_total * P.ns;
+    // units span the padded (node, request, split) space; ragged requests' missing
+    // nodes are dropped by the producer without work
+    const long long ua = static_cast<long long>(P.B) * P.R * P.ns;
     const long long ub = P.q ? static_cast<long long>(P.B) * L.ncb : 0;
     if (ua + ub >= (1ll << 31) - (1 << 20)) return fail(SPEC_ERR_INVALID_ARG, "batch too large%s");
     P.units_a = static_cast<int>(ua);
     P.units_total = static_cast<int>(ua + ub);
-    const size_t zbytes = static_cast<size_t>(P.B) * P.R * static_cast<size_t>(P.V) * P.esize;
-    P.logits_end = reinterpret_cast<unsigned long long>(P.logits) + zbytes;
-    P.q_end = P.q ? reinterpret_cast<unsigned long long>(P.q) +
-                        static_cast<size_t>(P.B) * (P.R - 1) * static_cast<size_t>(P.V) * 4
-                  : 0;
+    const size_t zrows = static_cast<size_t>(rows_total);
+    const size_t qrows = P.cu ? static_cast<size_t>(P.total_drafts) : static_cast<size_t>(P.B) * (P.R - 1);
+    P.logits_end = reinterpret_cast<unsigned long long>(P.logits) + zrows * static_cast<size_t>(P.V) * P.esize;
+    P.q_end = P.q ? reinterpret_cast<unsigned long long>(P.q) + qrows * static_cast<size_t>(P.V) * 4 : 0;
     long long grid = static_cast<long long>(D->sms) * D->blocks_per_sm[dtype == SPEC_BF16 ? 0 : 1];
     if (grid > P.units_total) grid = P.units_total;
     if (grid < 1) grid = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Calls without draft probabilities are greedy only: a leaner instantiation
-    // without the sampling and residual code.
+    // Calls without temperatures are greedy only: a leaner instantiation without
+    // the sampling and residual code.
     const dim3 g3(static_cast<unsigned>(grid));
-    if (P.q) {
+    if (P.q || P.temperature) {
         if (dtype == SPEC_BF16) verify_kernel<2, true><<<g3, kThreads, kSmemBytes, st>>>(P);
         else verify_kernel<4, true><<<g3, kThreads, kSmemBytes, st>>>(P);
     } else {
@@ -2219,6 +2290,51 @@ extern "C" spec_status_t spec_verify_chain(const void *target_logits, spec_dtype
     return launch_verify(P, dtype, workspace, workspace_bytes, stream);
 }
 
+extern "C" spec_status_t spec_verify_chain_ragged(const void *target_logits, spec_dtype_t dtype,
+                                                  const float *draft_probs, const int32_t *draft_tokens,
+                                                  const int32_t *cu_num_draft_tokens, int total_drafts,
+                                                  const float *temperature, const float *u_accept,
+                                                  const float *u_sample, int B, int max_k, int V,
+                                                  int32_t *out_tokens, int32_t *out_num_accepted, int32_t *d_status,
+                                                  void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype%s");
+    if (B < 1 || max_k < 0 || max_k > kMaxRows - 1 || V < 1 || V >= (1 << 30) || total_drafts < 0 ||
+        static_cast<long long>(total_drafts) > static_cast<long long>(B) * max_k)
+        return fail(SPEC_ERR_INVALID_ARG,
+                    "sizes out of range (1<=B, 0<=max_k<=255, 1<=V<2^30, 0<=total_drafts<=B*max_k)%s");
+    if (!target_logits || !cu_num_draft_tokens || !out_tokens || !out_num_accepted ||
+        (total_drafts > 0 && !draft_tokens))
+        return fail(SPEC_ERR_INVALID_ARG, "a required pointer is NULL%s");
+    // with no drafts at all, sampled requests need only temperature and u_sample
+    const bool sampled = draft_probs || u_accept || u_sample || temperature;
+    if (sampled && (!u_sample || !temperature || (total_drafts > 0 && (!draft_probs || !u_accept))))
+        return fail(SPEC_ERR_INVALID_ARG,
+                    "draft_probs, temperature, u_accept and u_sample must be all given or all NULL%s");
+    if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
+        return fail(SPEC_ERR_INVALID_ARG, "target_logits and draft_probs must be 16-byte aligned%s");
+    Params P;
+    memset(&P, 0, sizeof P);
+    P.logits = static_cast<const uint8_t *>(target_logits);
+    P.q = draft_probs;
+    P.tokens = draft_tokens;
+    P.temperature = temperature;
+    P.u_accept = u_accept;
+    P.u_sample = u_sample;
+    P.out_tokens = out_tokens;
+    P.out_count = out_num_accepted;
+    P.out_path = nullptr;
+    P.status = d_status;
+    P.B = B;
+    P.R = max_k + 1;
+    P.V = V;
+    P.D = max_k;
+    P.tree = 0;
+    P.cu = cu_num_draft_tokens;
+    P.total_drafts = total_drafts;
+    return launch_verify(P, dtype, workspace, workspace_bytes, stream);
+}
+
 extern "C" spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_t dtype, const int32_t *node_tokens,
                                           const int32_t *parent, int B, int N, int V, int max_depth,
                                           int32_t *out_path, int32_t *out_tokens, int32_t *out_len,
@@ -2285,6 +2401,22 @@ extern "C" spec_status_t spec_fixup_slots(int64_t *slot_mapping, int B, int P, c
     if (blocks > 4096) blocks = 4096;
     fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         slot_mapping, B, P, num_accepted, path, path_stride, padding_slot_id);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "fixup launch: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+extern "C" spec_status_t spec_fixup_slots_ragged(int64_t *slot_mapping, int B, const int32_t *cu_num_draft_tokens,
+                                                 int total_drafts, const int32_t *num_accepted,
+                                                 int64_t padding_slot_id, void *stream) {
+    g_err[0] = 0;
+    if (B < 0 || total_drafts < 0) return fail(SPEC_ERR_INVALID_ARG, "negative size%s");
+    if (B == 0) return SPEC_OK;
+    if (!slot_mapping || !cu_num_draft_tokens || !num_accepted)
+        return fail(SPEC_ERR_INVALID_ARG, "a required pointer is NULL%s");
+    const long long threads = static_cast<long long>(B) * 32;
+    fixup_ragged_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        slot_mapping, B, cu_num_draft_tokens, total_drafts, num_accepted, padding_slot_id);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "fixup launch: %s", cudaGetErrorString(e));
     return SPEC_OK;

@@ -302,6 +302,73 @@ def chain_mixed(seed: int, B: int, k: int, V: int, dtype: int = BF16,
 # ----------------------------------------------------------------------------
 # tree workloads
 # ----------------------------------------------------------------------------
+@dataclass
+class RaggedChainInputs:
+    """Chains with a different number of drafts per request, packed as the
+    vLLM walkthrough's per-step metadata lays them out: request b's k_b drafts
+    at cu[b] .. cu[b+1]-1 and its k_b + 1 target rows at cu[b] + b .. cu[b+1] + b."""
+    logits: np.ndarray               # [cu[B] + B, V] uint16 (bf16 bits) or float32
+    dtype: int
+    cu: np.ndarray                   # [B+1] int32 cu_num_draft_tokens
+    draft_tokens: np.ndarray         # [cu[B]] int32
+    temperature: np.ndarray          # [B] float32, 0 = greedy
+    u_sample: np.ndarray             # [cu[B] + B] float32
+    draft_probs: Optional[np.ndarray]   # [cu[B], V] float32 (None: every request greedy)
+    u_accept: Optional[np.ndarray]      # [cu[B]] float32
+    slot_mapping: np.ndarray         # [cu[B] + B] int64
+    parts: list                      # the per-request ChainInputs (B = 1 each)
+    name: str = "chain_ragged"
+
+    @property
+    def B(self) -> int:
+        return self.cu.shape[0] - 1
+
+    @property
+    def V(self) -> int:
+        return self.logits.shape[1]
+
+    @property
+    def max_k(self) -> int:
+        return int(np.max(np.diff(self.cu))) if self.B else 0
+
+
+def chain_ragged(seed: int, B: int, max_k: int, V: int, mode: str = "greedy", dtype: int = BF16,
+                 temperature: float = 0.8, lam: float = 0.3, p_match: float = 0.8,
+                 min_k: int = 0) -> RaggedChainInputs:
+    """Per-request k_b uniform in [min_k, max_k]; each request drawn by the
+    greedy or sampled chain recipe (mode "greedy", "sampled" or "mixed": half
+    of the requests greedy, at random), then packed."""
+    rng = np.random.default_rng(seed)
+    ks = rng.integers(min_k, max_k + 1, size=B)
+    greedy = np.ones(B, bool) if mode == "greedy" else (np.zeros(B, bool) if mode == "sampled"
+                                                        else rng.random(B) < 0.5)
+    parts = []
+    for b in range(B):
+        s = seed * 7919 + 13 * b + 1
+        if greedy[b]:
+            parts.append(chain_greedy(seed=s, B=1, k=int(ks[b]), V=V, p_match=p_match, dtype=dtype))
+        else:
+            parts.append(chain_sampled(seed=s, B=1, k=int(ks[b]), V=V, temperature=temperature, lam=lam,
+                                       dtype=dtype))
+    cu = np.zeros(B + 1, np.int32)
+    cu[1:] = np.cumsum(ks)
+    total = int(cu[-1])
+    logits = np.concatenate([x.logits[0] for x in parts], axis=0)
+    tokens = np.concatenate([x.draft_tokens[0] for x in parts]).astype(np.int32) if total else np.zeros(0, np.int32)
+    sampled = not greedy.all()
+    q = ua = None
+    if sampled:
+        q = np.concatenate([x.draft_probs[0] if x.draft_probs is not None else np.zeros((x.k, V), np.float32)
+                            for x in parts], axis=0) if total else np.zeros((0, V), np.float32)
+        ua = np.concatenate([x.u_accept[0] if x.u_accept is not None else np.zeros(x.k, np.float32)
+                             for x in parts]).astype(np.float32) if total else np.zeros(0, np.float32)
+    us = np.concatenate([x.u_sample[0] for x in parts]).astype(np.float32)
+    T = np.array([x.temperature[0] for x in parts], np.float32)
+    slots = np.concatenate([x.slot_mapping[0] + 100000 * b for b, x in enumerate(parts)]).astype(np.int64)
+    return RaggedChainInputs(logits=logits, dtype=dtype, cu=cu, draft_tokens=tokens, temperature=T,
+                             u_sample=us, draft_probs=q, u_accept=ua, slot_mapping=slots, parts=parts)
+
+
 def level_tree_choices(children_per_level: Sequence[int]) -> list:
     """tree_choices (list of index tuples, level order) for a tree in which every
     node of level L-1 has children_per_level[L] children (level 0 = root)."""

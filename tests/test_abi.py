@@ -63,6 +63,33 @@ def test_chain_host_checks_reject_bad_arguments(lib, bad):
     assert lib.spec_last_error() != b""
 
 
+def _ragged(lib, **kw):
+    args = dict(z=0x10000, dtype=0, q=None, tok=0x20000, cu=0x28000, total=5, T=None, ua=None, us=None, B=2,
+                max_k=3, V=100, out=0x30000, na=0x40000, st=None, ws=0x50000, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return lib.spec_verify_chain_ragged(args["z"], args["dtype"], args["q"], args["tok"], args["cu"], args["total"],
+                                        args["T"], args["ua"], args["us"], args["B"], args["max_k"], args["V"],
+                                        args["out"], args["na"], args["st"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(B=0), dict(max_k=-1), dict(max_k=256), dict(V=0), dict(total=-1), dict(total=7),   # 7 > B * max_k
+    dict(cu=None), dict(tok=None), dict(z=None), dict(out=None), dict(z=0x10008), dict(dtype=3),
+    dict(T=0x60000), dict(ws=None), dict(wsb=16),
+])
+def test_ragged_host_checks_reject_bad_arguments(lib, bad):
+    assert _ragged(lib, **bad) == 1
+    assert lib.spec_last_error() != b""
+
+
+def test_ragged_fixup_host_checks(lib):
+    assert lib.spec_fixup_slots_ragged(None, 2, 0x1000, 3, 0x2000, -1, None) == 1
+    assert lib.spec_fixup_slots_ragged(0x3000, 2, None, 3, 0x2000, -1, None) == 1
+    assert lib.spec_fixup_slots_ragged(0x3000, 2, 0x1000, 3, None, -1, None) == 1
+    assert lib.spec_fixup_slots_ragged(0x3000, -1, 0x1000, 3, 0x2000, -1, None) == 1
+    assert lib.spec_fixup_slots_ragged(None, 0, None, 0, None, -1, None) == 0
+
+
 def test_tree_host_checks(lib):
     par = np.array([-1, 0, 0, 1], np.int32)
     bad_par = np.array([-1, 0, 2, 1], np.int32)
