@@ -559,6 +559,7 @@ def others(sv, W, dev, dist, peak, args):
     x = W.chain_sampled(seed=5, B=args.sweep_b, k=8, V=152064, temperature=1.0, lam=0.3)
     out.append(_other_chain(sv, x, dev, dist, peak, "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % args.sweep_b))
     out.append(_other_tree(sv, W, dev, dist, peak))
+    out.append(_other_ragged(sv, W, dev, dist, peak))
     return out
 
 
@@ -661,6 +662,62 @@ def _other_tree(sv, W, dev, dist, peak, target_s=0.5):
             "frac_alg": ach / peak, "frac_dense": b_dense / (us * 1e-6) / 1e9 / peak,
             "bytes_per_launch": {"algorithmic": b_alg, "dense": b_dense,
                                  "streamed_by_kernel": (c1["bytes_loaded"] - c0["bytes_loaded"]) / n}}
+
+
+def _other_ragged(sv, W, dev, dist, peak, target_s=0.5):
+    """Ragged greedy chain: B = 64 requests with k_b uniform in [1, 8] drafts,
+    V = 128256 bf16, packed by cu_num_draft_tokens (the headline recipe per
+    request)."""
+    import torch
+    x = W.chain_ragged(seed=7, B=64, max_k=8, V=128256, mode="greedy", min_k=1)
+    per_copy = x.logits.nbytes
+    ncopy = min(64, max(2, int(np.ceil(4 * l2_bytes(dev) / per_copy)) + 1))
+    zs = [to_dev(x.logits, dev) for _ in range(ncopy)]
+    tok, cu = to_dev(x.draft_tokens, dev), to_dev(x.cu, dev)
+    mk = x.max_k
+    outs = [(torch.empty((x.B, mk + 1), dtype=torch.int32, device=dev), torch.empty((x.B,), dtype=torch.int32, device=dev))
+            for _ in range(ncopy)]
+    ws = torch.zeros(sv.workspace_bytes(x.B, mk + 1, x.V, 0), dtype=torch.uint8, device=dev)
+
+    def call(i):
+        sv.verify_chain_ragged(zs[i], tok, cu, mk, out_tokens=outs[i][0], out_num_accepted=outs[i][1], workspace=ws)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for i in range(ncopy):
+            call(i)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    graphs = []
+    for i in range(ncopy):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call(i)
+        graphs.append(g)
+
+    class _C:
+        def run(self, steps, verify_only=False):
+            for j in range(steps):
+                graphs[j % ncopy].replay()
+    case = _C()
+    case.run(20)
+    ms = time_steps(case, 200, dev, dist)
+    n = max(200, int(200 * target_s / max(ms / 1e3, 1e-6)))
+    c0 = sv.workspace_counters(ws)
+    ms = time_steps(case, n, dev, dist)
+    c1 = sv.workspace_counters(ws)
+    us = ms * 1e3 / n
+    a = outs[0][1].cpu().numpy().astype(np.int64)
+    ks = np.diff(x.cu).astype(np.int64)
+    b_alg = float(((np.minimum(a, ks) + 1) * x.V * 2).sum())
+    b_dense = float(x.logits.nbytes)
+    ach = b_alg / (us * 1e-6) / 1e9
+    return {"workload": "ragged greedy chain B=64 k_b uniform in [1, 8] (sum %d) V=128256 bf16" % int(ks.sum()),
+            "positions_per_s": float(ks.sum()) / (us * 1e-6), "kernel_us": us, "achieved_gbs_alg": ach,
+            "frac_alg": ach / peak, "frac_dense": b_dense / (us * 1e-6) / 1e9 / peak,
+            "bytes_per_launch": {"algorithmic": b_alg, "dense": b_dense,
+                                 "streamed_by_kernel": (c1["bytes_loaded"] - c0["bytes_loaded"]) / n},
+            "mean_accepted": float(a.mean())}
 
 
 if __name__ == "__main__":
