@@ -48,6 +48,8 @@ def _bind(lib):
     lib.oracle_verify_tree.restype = I
     lib.oracle_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64]
     lib.oracle_fixup_slots.restype = I
+    lib.oracle_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P]
+    lib.oracle_ngram_propose.restype = I
     return lib
 
 
@@ -124,6 +126,23 @@ def verify_tree(logits: np.ndarray, dtype: int, node_tokens: np.ndarray, parent:
                                 _ptr(out["b_alg"]))
     if rc != 0:
         raise ValueError("oracle_verify_tree rejected its arguments")
+    return out
+
+
+def ngram_propose(tokens: np.ndarray, lengths: np.ndarray, n_min: int, n_max: int, k: int, lib=None) -> dict:
+    """n-gram lookup drafts.  tokens [B, Lmax] int32, lengths [B].  Returns
+    draft [B, k] (-1 padded), count [B], match_len [B], match_end [B]."""
+    lib = _load(lib)
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, Lmax = t.shape
+    ln = _c(lengths, np.int32)
+    out = dict(draft=np.empty((B, k), np.int32), count=np.empty(B, np.int32),
+               match_len=np.empty(B, np.int32), match_end=np.empty(B, np.int32))
+    rc = lib.oracle_ngram_propose(_ptr(t), _ptr(ln), B, Lmax, int(n_min), int(n_max), int(k),
+                                  _ptr(out["draft"]), _ptr(out["count"]), _ptr(out["match_len"]),
+                                  _ptr(out["match_end"]))
+    if rc != 0:
+        raise ValueError("oracle_ngram_propose rejected its arguments")
     return out
 
 

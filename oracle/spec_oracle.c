@@ -23,6 +23,9 @@
  *    rejected positions' slot_mapping entries become PADDING_SLOT_ID.
  *  - serving-book chapter, "acceptance rule preserving the output
  *    distribution": temperature 0 means greedy.
+ *  - serving-book chapter, table of draft sources, row "n-gram lookup": find,
+ *    in the prompt or the text generated so far, a span equal to the current
+ *    ending and propose what follows it (no model).
  *
  * Readings where the pages are silent (the same list is kept in the design
  * notes): ties in argmax go to the lowest vocabulary index; q is used as given
@@ -425,6 +428,59 @@ int oracle_fixup_slots(int64_t *slot_mapping, int B, int P, const int32_t *num_a
             if (!keep)
                 slot_mapping[(size_t)b * P + j] = pad;
         }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------- n-gram lookup -- */
+
+/* For each sequence s[0..L-1] (row b of tokens, L = lengths[b]): the longest
+ * n in [n_min, n_max] for which the ending s[L-n..L-1] also occurs ending at
+ * an earlier position e < L-1 (s[e-n+1..e] == s[L-n..L-1]); among the
+ * occurrences of that length the latest (largest e).  The draft is the tokens
+ * after it, s[e+1..], at most k of them (fewer if the text ends first).
+ * No such n: no draft (count 0, match_len 0, match_end -1).  Readings (the
+ * page is silent): longest n first, then the most recent occurrence. */
+int oracle_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int Lmax, int n_min, int n_max,
+                         int k, int32_t *out_draft, int32_t *out_count, int32_t *out_match_len,
+                         int32_t *out_match_end)
+{
+    if (B < 0 || Lmax < 0 || n_min < 1 || n_max < n_min || k < 0 || !out_draft || !out_count)
+        return 1;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *s = tokens + (size_t)b * Lmax;
+        int L = lengths[b];
+        if (L < 0 || L > Lmax)
+            return 1;
+        int best_n = 0, best_e = -1;
+        for (int n = n_max; n >= n_min && best_e < 0; --n) {
+            if (n > L - 1)
+                continue;  /* the ending and an earlier copy need n + 1 tokens at least */
+            for (int e = L - 2; e >= n - 1; --e) {
+                int same = 1;
+                for (int t = 0; t < n && same; ++t)
+                    same = s[e - t] == s[L - 1 - t];
+                if (same) {
+                    best_n = n;
+                    best_e = e;
+                    break;
+                }
+            }
+        }
+        int count = 0;
+        for (int j = 0; j < k; ++j) {
+            int32_t v = -1;
+            if (best_e >= 0 && best_e + 1 + j < L) {
+                v = s[best_e + 1 + j];
+                ++count;
+            }
+            out_draft[(size_t)b * k + j] = v;
+        }
+        out_count[b] = count;
+        if (out_match_len)
+            out_match_len[b] = best_n;
+        if (out_match_end)
+            out_match_end[b] = best_e;
     }
     return 0;
 }

@@ -369,6 +369,34 @@ def chain_ragged(seed: int, B: int, max_k: int, V: int, mode: str = "greedy", dt
                              u_sample=us, draft_probs=q, u_accept=ua, slot_mapping=slots, parts=parts)
 
 
+def ngram_texts(seed: int, B: int, Lmax: int, V: int = 128256, copy_frac: float = 0.5,
+                span: Tuple[int, int] = (4, 48), min_len: int = 1) -> Tuple[np.ndarray, np.ndarray]:
+    """Token texts for n-gram lookup: a random prompt of half the length, then
+    text in which spans copied from earlier (lengths uniform in `span`) make up
+    about `copy_frac` of the tokens, the rest drawn at random (the copy-heavy
+    tasks the lookup suits: summarising, editing code).  Lengths uniform in
+    [min_len, Lmax]; tokens past a row's length are 0.  Returns (tokens
+    [B, Lmax] int32, lengths [B] int32)."""
+    rng = np.random.default_rng(seed)
+    tokens = np.zeros((B, Lmax), np.int32)
+    lengths = rng.integers(min_len, Lmax + 1, size=B).astype(np.int32)
+    for b in range(B):
+        L = int(lengths[b])
+        t = rng.integers(0, V, size=L, dtype=np.int64).astype(np.int32)
+        pos = max(1, L // 2)
+        while pos < L:
+            if rng.random() < copy_frac and pos > 1:
+                n = int(rng.integers(span[0], span[1] + 1))
+                src = int(rng.integers(0, pos))
+                n = min(n, L - pos, pos - src)
+                t[pos:pos + n] = t[src:src + n]
+                pos += max(1, n)
+            else:
+                pos += int(rng.integers(1, span[1] + 1))
+        tokens[b, :L] = t
+    return tokens, lengths
+
+
 def level_tree_choices(children_per_level: Sequence[int]) -> list:
     """tree_choices (list of index tuples, level order) for a tree in which every
     node of level L-1 has children_per_level[L] children (level 0 = root)."""

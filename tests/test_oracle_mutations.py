@@ -105,6 +105,21 @@ def _tree_mismatches(O, lib):
     return bad
 
 
+def _ngram_mismatches(O, lib):
+    import test_oracle_ngram as ng
+    g = np.random.default_rng(72)
+    B, Lmax = 200, 50
+    t = g.integers(0, 3, size=(B, Lmax)).astype(np.int32)
+    ln = g.integers(0, Lmax + 1, size=B).astype(np.int32)
+    r = O.ngram_propose(t, ln, 1, 5, 4, lib=lib)
+    bad = 0
+    for b in range(B):
+        s = t[b, :ln[b]]
+        n, e = ng._numpy_search(s, 1, 5)
+        bad += int((r["match_len"][b], r["match_end"][b]) != (n, e))
+    return bad
+
+
 CASES = [
     ("residual_sign", "double d = p[j] - (double)qi[j];", "double d = (double)qi[j] - p[j];",
      lambda O, lib: _lossless(O, lib) < 1e-6),
@@ -124,6 +139,12 @@ CASES = [
      "acc[n] = x == g[parent[n]];", lambda O, lib: _tree_mismatches(O, lib) > 0),
     ("tree_parent_row", "acc[n] = acc[parent[n]] && x == g[parent[n]];",
      "acc[n] = acc[parent[n]] && x == g[n];", lambda O, lib: _tree_mismatches(O, lib) > 0),
+    ("ngram_earliest", "for (int e = L - 2; e >= n - 1; --e) {", "for (int e = n - 1; e <= L - 2; ++e) {",
+     lambda O, lib: _ngram_mismatches(O, lib) > 0),
+    ("ngram_shortest_first", "for (int n = n_max; n >= n_min && best_e < 0; --n) {",
+     "for (int n = n_min; n <= n_max && best_e < 0; ++n) {", lambda O, lib: _ngram_mismatches(O, lib) > 0),
+    ("ngram_self_match", "for (int e = L - 2; e >= n - 1; --e) {", "for (int e = L - 1; e >= n - 1; --e) {",
+     lambda O, lib: _ngram_mismatches(O, lib) > 0),
 ]
 
 
@@ -136,6 +157,7 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _accept_rate_z(O, lib) < 4
     assert _tie_ok(O, lib)
     assert _tree_mismatches(O, lib) == 0
+    assert _ngram_mismatches(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
