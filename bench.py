@@ -550,7 +550,8 @@ def main():
 
 def others(sv, W, dev, dist, peak, args):
     """Secondary workloads (kernel-only device time): sampled chain, greedy
-    tree, and the k = 8, V = 152064 sampled sweep."""
+    tree, the k = 8, V = 152064 sampled sweep, the ragged greedy chain and
+    n-gram lookup drafting."""
     import torch
     out = []
     # sampled chain, B=32 k=4 V=128256 T=0.7, lambda = 0.3
@@ -560,6 +561,7 @@ def others(sv, W, dev, dist, peak, args):
     out.append(_other_chain(sv, x, dev, dist, peak, "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % args.sweep_b))
     out.append(_other_tree(sv, W, dev, dist, peak))
     out.append(_other_ragged(sv, W, dev, dist, peak))
+    out.append(_other_ngram(sv, W, dev, dist, peak))
     return out
 
 
@@ -718,6 +720,54 @@ def _other_ragged(sv, W, dev, dist, peak, target_s=0.5):
             "bytes_per_launch": {"algorithmic": b_alg, "dense": b_dense,
                                  "streamed_by_kernel": (c1["bytes_loaded"] - c0["bytes_loaded"]) / n},
             "mean_accepted": float(a.mean())}
+
+
+def _other_ngram(sv, W, dev, dist, peak, target_s=0.5):
+    """n-gram lookup drafting: B = 64 copy-heavy texts, lengths uniform in
+    [1, 8192], n in [2, 8], k = 8 (the draft length of the chain workloads).
+    Input copies rotate so the token buffers together exceed L2 four times."""
+    import torch
+    t, ln = W.ngram_texts(seed=11, B=64, Lmax=8192, V=128256)
+    n_min, n_max, k = 2, 8, 8
+    ncopy = min(256, max(2, int(np.ceil(4 * l2_bytes(dev) / t.nbytes)) + 1))
+    ts = [to_dev(t, dev) for _ in range(ncopy)]
+    lt = to_dev(ln, dev)
+    outs = [tuple(torch.empty(shape, dtype=torch.int32, device=dev) for shape in ((64, k), (64,), (64,), (64,)))
+            for _ in range(ncopy)]
+
+    def call(i):
+        o = outs[i]
+        sv.ngram_propose(ts[i], lt, n_min, n_max, k, out_draft=o[0], out_count=o[1], out_match_len=o[2],
+                         out_match_end=o[3])
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for i in range(ncopy):
+            call(i)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(ncopy):
+            call(i)
+
+    class _C:
+        def run(self, steps, verify_only=False):
+            for _ in range(steps):
+                g.replay()
+    case = _C()
+    case.run(3)
+    ms = time_steps(case, 10, dev, dist)
+    n = max(10, int(10 * target_s / max(ms / 1e3, 1e-6)))
+    ms = time_steps(case, n, dev, dist)
+    us = ms * 1e3 / (n * ncopy)
+    b_alg = float(ln.astype(np.int64).sum() * 4 + 64 * 4 + 64 * (k + 3) * 4)
+    ach = b_alg / (us * 1e-6) / 1e9
+    cnt = outs[0][1].cpu().numpy()
+    return {"workload": "n-gram lookup B=64 copy-heavy texts L uniform in [1, 8192] (sum %d) n in [2, 8] k=8"
+            % int(ln.sum()), "sequences_per_s": 64 / (us * 1e-6), "kernel_us": us, "achieved_gbs_alg": ach,
+            "frac_alg": ach / peak, "bytes_per_launch": {"algorithmic": b_alg},
+            "mean_draft_len": float(cnt.mean())}
 
 
 if __name__ == "__main__":

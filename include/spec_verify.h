@@ -209,6 +209,27 @@ spec_status_t spec_fixup_slots_ragged(int64_t *slot_mapping, int B, const int32_
                                       int64_t padding_slot_id, void *stream);
 
 /*
+ * n-gram lookup drafting (serving-book chapter, table of draft sources, row
+ * "n-gram lookup": find, in the prompt or the text generated so far, a span
+ * equal to the current ending and use what follows it as the draft; no model).
+ *
+ *  tokens  [B, Lmax] int32 device: row b holds sequence b (prompt + generated)
+ *      in its first lengths[b] entries.
+ *  lengths [B] int32 device (values outside [0, Lmax] are clamped).
+ *  For each sequence s of length L: the longest n in [n_min, n_max] such that
+ *  the ending s[L-n..L-1] also occurs ending at some e < L-1, and among those
+ *  occurrences the latest e; the draft is s[e+1..], at most k tokens.
+ *  out_draft [B, k] int32 device: the draft, -1 padded.
+ *  out_count [B] int32 device: draft length (0 when nothing matches).
+ *  out_match_len, out_match_end [B] int32 device, may be NULL: n and e
+ *      (0 and -1 when nothing matches).
+ *  Sizes: B, Lmax >= 0; 1 <= n_min <= n_max <= 64; k >= 0.
+ */
+spec_status_t spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int Lmax, int n_min,
+                                 int n_max, int k, int32_t *out_draft, int32_t *out_count,
+                                 int32_t *out_match_len, int32_t *out_match_end, void *stream);
+
+/*
  * Host helper (no device work): tree_choices -> parent[] and level metadata,
  * following the vLLM EAGLE walkthrough ("tree drafting in detail").
  *  flat / lens / n: the n tuples of tree_choices, concatenated in `flat`,

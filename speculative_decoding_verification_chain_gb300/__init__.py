@@ -24,7 +24,7 @@ from typing import Optional, Sequence, Tuple
 __all__ = ["verify_chain", "verify_tree", "fixup_slots", "tree_from_choices", "workspace_bytes",
            "SpecError", "PADDING_SLOT_ID", "STATUS_TOKEN_RANGE", "STATUS_NONFINITE",
            "STATUS_WAIT_TIMEOUT", "STATUS_BAD_OFFSETS", "library_path", "load_library", "verify_chain_noalloc",
-           "verify_chain_ragged", "fixup_slots_ragged"]
+           "verify_chain_ragged", "fixup_slots_ragged", "ngram_propose"]
 
 PADDING_SLOT_ID = -1
 SPEC_BF16, SPEC_FP32 = 0, 1
@@ -74,6 +74,8 @@ def load_library():
         lib.spec_verify_chain_ragged.restype = I
         lib.spec_fixup_slots_ragged.argtypes = [P, I, P, I, P, ctypes.c_int64, P]
         lib.spec_fixup_slots_ragged.restype = I
+        lib.spec_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
+        lib.spec_ngram_propose.restype = I
         lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
         lib.spec_verify_tree.restype = I
         lib.spec_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64, P]
@@ -295,6 +297,30 @@ def fixup_slots_ragged(slot_mapping, cu_num_draft_tokens, num_accepted, padding_
                                      int(padding_slot_id), _stream_handle(dev, stream))
     _check("spec_fixup_slots_ragged", rc)
     return slot_mapping
+
+
+def ngram_propose(tokens, lengths, n_min: int, n_max: int, k: int, *, out_draft=None, out_count=None,
+                  out_match_len=None, out_match_end=None, stream=None):
+    """n-gram lookup drafts.  tokens [B, Lmax] int32 CUDA (row b's first
+    lengths[b] entries are its text), lengths [B] int32 CUDA.  Returns
+    (draft [B, k] int32 -1 padded, count [B], match_len [B], match_end [B])."""
+    torch = _torch()
+    lib = load_library()
+    if tokens.dtype != torch.int32 or tokens.dim() != 2 or tokens.device.type != "cuda" or not tokens.is_contiguous():
+        raise ValueError("tokens must be a contiguous [B, Lmax] int32 CUDA tensor")
+    B, Lmax = tokens.shape
+    dev = tokens.device
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    mk = lambda t, shape: t if t is not None else torch.empty(shape, dtype=torch.int32, device=dev)
+    out_draft, out_count = mk(out_draft, (B, k)), mk(out_count, (B,))
+    out_match_len, out_match_end = mk(out_match_len, (B,)), mk(out_match_end, (B,))
+    for t, name, shape in ((out_draft, "out_draft", (B, k)), (out_count, "out_count", (B,)),
+                           (out_match_len, "out_match_len", (B,)), (out_match_end, "out_match_end", (B,))):
+        _need(t, name, torch.int32, shape, dev)
+    rc = lib.spec_ngram_propose(_ptr(tokens), _ptr(lengths), B, Lmax, int(n_min), int(n_max), int(k), _ptr(out_draft),
+                                _ptr(out_count), _ptr(out_match_len), _ptr(out_match_end), _stream_handle(dev, stream))
+    _check("spec_ngram_propose", rc)
+    return out_draft, out_count, out_match_len, out_match_end
 
 
 def verify_tree(target_logits, node_tokens, parent: Sequence[int], max_depth: Optional[int] = None, *,

@@ -90,6 +90,16 @@ def test_ragged_fixup_host_checks(lib):
     assert lib.spec_fixup_slots_ragged(None, 0, None, 0, None, -1, None) == 0
 
 
+def test_ngram_host_checks(lib):
+    def call(B=2, Lmax=10, nmin=1, nmax=4, k=3, tok=0x1000, ln=0x2000, d=0x3000, c=0x4000):
+        return lib.spec_ngram_propose(tok, ln, B, Lmax, nmin, nmax, k, d, c, None, None, None)
+    for bad in (dict(B=-1), dict(Lmax=-1), dict(nmin=0), dict(nmax=0), dict(nmin=3, nmax=2), dict(nmax=65),
+                dict(k=-1), dict(tok=None), dict(ln=None), dict(d=None), dict(c=None)):
+        assert call(**bad) == 1, bad
+        assert lib.spec_last_error() != b""
+    assert call(B=0, tok=None, ln=None, d=None, c=None) == 0
+
+
 def test_tree_host_checks(lib):
     par = np.array([-1, 0, 0, 1], np.int32)
     bad_par = np.array([-1, 0, 2, 1], np.int32)
