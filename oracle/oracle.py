@@ -49,6 +49,8 @@ def _bind(lib):
     lib.oracle_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64]
     lib.oracle_fixup_slots.restype = I
     lib.oracle_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P]
+    lib.oracle_verify_tree_sampled.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, P]
+    lib.oracle_verify_tree_sampled.restype = I
     lib.oracle_ngram_propose.restype = I
     return lib
 
@@ -126,6 +128,37 @@ def verify_tree(logits: np.ndarray, dtype: int, node_tokens: np.ndarray, parent:
                                 _ptr(out["b_alg"]))
     if rc != 0:
         raise ValueError("oracle_verify_tree rejected its arguments")
+    return out
+
+
+def verify_tree_sampled(logits: np.ndarray, dtype: int, node_tokens: np.ndarray, parent: np.ndarray,
+                        temperature: np.ndarray, u_accept: np.ndarray, u_sample: np.ndarray,
+                        draft_probs: np.ndarray, max_depth: Optional[int] = None, lib=None) -> dict:
+    """Sampled tree verify (sequential over siblings with residual updates).
+    logits [B, N+1, V]; draft_probs [B, N+1, V] (row c: the distribution the
+    children of node c were drawn from); node_tokens, u_accept [B, N];
+    u_sample [B, N+1] (indexed by the node the walk ends at); temperature [B] > 0.
+    Returns path [B, D+1], tokens [B, D+1], length [B], flag_accept [B, N],
+    flag_sample [B], b_alg [B]."""
+    lib = _load(lib)
+    B, n1, V = logits.shape
+    N = n1 - 1
+    par = _c(parent, np.int32)
+    if max_depth is None:
+        max_depth = int(tree_depths(par).max()) if N > 0 else 0
+    z = np.ascontiguousarray(logits, dtype=np.uint16 if dtype == BF16 else np.float32)
+    toks = _c(node_tokens if N > 0 else np.zeros((B, 0), np.int32), np.int32)
+    ua = _c(u_accept if N > 0 else np.zeros((B, 0), np.float32), np.float32)
+    q = _c(draft_probs, np.float32)
+    out = dict(path=np.empty((B, max_depth + 1), np.int32), tokens=np.empty((B, max_depth + 1), np.int32),
+               length=np.empty(B, np.int32), flag_accept=np.empty((B, N), np.int32),
+               flag_sample=np.empty(B, np.int32), b_alg=np.empty(B, np.float64))
+    rc = lib.oracle_verify_tree_sampled(
+        _ptr(z), dtype, _ptr(q), _ptr(toks), _ptr(par), _ptr(_c(temperature, np.float32)), _ptr(ua),
+        _ptr(_c(u_sample, np.float32)), B, N, V, int(max_depth), _ptr(out["path"]), _ptr(out["tokens"]),
+        _ptr(out["length"]), _ptr(out["flag_accept"]), _ptr(out["flag_sample"]), _ptr(out["b_alg"]))
+    if rc != 0:
+        raise ValueError("oracle_verify_tree_sampled rejected its arguments")
     return out
 
 

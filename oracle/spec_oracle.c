@@ -404,6 +404,176 @@ int oracle_verify_tree(const void *logits, int dtype, const int32_t *node_tokens
     return bad ? 1 : 0;
 }
 
+/* ------------------------------------------------------ the sampled tree -- */
+
+/* Sampled token tree (EAGLE-3 review, "EAGLE-3 inference" step 4: sampling
+ * keeps min(1, p/q) acceptance with residual correction; the pages give no
+ * rule for siblings).  Reading taken: walk from the root; at node c the target
+ * distribution is p' = softmax(z_c / T); the children of c are tested in index
+ * order, child n with token x accepted iff q_c(x) == 0 or u_accept[n] <
+ * p'(x) / q_c(x), where q_c (row c of draft_probs) is the distribution the
+ * children of c were drawn from.  An accepted child becomes the next node; a
+ * rejected one replaces p' by norm(max(0, p' - q_c)) (unchanged if that has
+ * zero mass) before the next sibling.  When no child is accepted, or c is a
+ * leaf, one token is drawn from p' by inverse CDF with u_sample[c].  A child
+ * token outside [0, V) is rejected (p'(x) = 0).  With children drawn i.i.d.
+ * from q_c this emits each token with law p (the chain's identity applied once
+ * per sibling).
+ *
+ * Flag windows: the accept test's ratio and the inverse CDF's edges carry the
+ * rounding of every term that went into them before the clip, so the windows
+ * scale with g, the running "gross" value that starts at p and becomes
+ * (g + q_c) / Z wherever a residual step keeps a positive entry (Z the
+ * residual's mass): |u - ratio| < 1e-6 * max(1, g(x) / q_c(x)) flags a test,
+ * and t within 1e-5 of the gross prefix sum of a bucket edge flags a draw.
+ * With no residual step (g = p) these are the chain's windows. */
+int oracle_verify_tree_sampled(const void *logits, int dtype, const float *draft_probs,
+                               const int32_t *node_tokens, const int32_t *parent, const float *temperature,
+                               const float *u_accept, const float *u_sample, int B, int N, int V,
+                               int max_depth, int32_t *out_path, int32_t *out_tokens, int32_t *out_len,
+                               int32_t *flag_accept, int32_t *flag_sample, double *b_alg)
+{
+    if (B < 0 || N < 0 || V < 1 || max_depth < 0 || !logits || !parent || !temperature || !u_sample ||
+        !out_path || !out_tokens || !out_len)
+        return 1;
+    if (N > 0 && (!node_tokens || !draft_probs || !u_accept))
+        return 1;
+    if (parent[0] != -1)
+        return 1;
+    for (int b = 0; b < B; ++b)
+        if (!(temperature[b] > 0.0f))
+            return 1;
+    int *depth = (int *)malloc(sizeof(int) * (size_t)(N + 1));
+    int bad = 0;
+    depth[0] = 0;
+    for (int n = 1; n <= N; ++n) {
+        if (parent[n] < 0 || parent[n] >= n) {
+            bad = 1;
+            break;
+        }
+        depth[n] = depth[parent[n]] + 1;
+        if (depth[n] > max_depth)
+            bad = 1;
+    }
+    if (bad) {
+        free(depth);
+        return 1;
+    }
+    const size_t zs = (dtype == OR_BF16) ? 2 : 4;
+    const size_t row = (size_t)V;
+    double *w = (double *)malloc(sizeof(double) * row);
+    double *g = (double *)malloc(sizeof(double) * row);
+    for (int b = 0; b < B; ++b) {
+        const size_t zbase = (size_t)b * (size_t)(N + 1) * row;
+        const double T = (double)temperature[b];
+        int32_t *path = out_path + (size_t)b * (size_t)(max_depth + 1);
+        int32_t *tok = out_tokens + (size_t)b * (size_t)(max_depth + 1);
+        for (int i = 0; i <= max_depth; ++i) {
+            path[i] = -1;
+            tok[i] = -1;
+        }
+        if (flag_accept)
+            for (int n = 0; n < N; ++n)
+                flag_accept[(size_t)b * N + n] = 0;
+        double bytes = 0.0;
+        int c = 0, d = 0;
+        path[0] = 0;
+        for (;;) {
+            row_softmax(logits, dtype, zbase + (size_t)c * row, V, T, w);
+            bytes += (double)row * (double)zs;
+            for (size_t j = 0; j < row; ++j)
+                g[j] = w[j];
+            const float *qc = draft_probs ? draft_probs + ((size_t)b * (size_t)(N + 1) + (size_t)c) * row : NULL;
+            int next = -1, q_read = 0;
+            for (int n = c + 1; n <= N && next < 0; ++n) {
+                if (parent[n] != c)
+                    continue;
+                const int x = node_tokens[(size_t)b * N + (n - 1)];
+                int accept = 0;
+                if (x >= 0 && x < V) {
+                    const double qh = (double)qc[x];
+                    bytes += 4.0;
+                    if (qh == 0.0) {
+                        accept = 1;
+                    } else {
+                        const double ratio = w[x] / qh;
+                        const double u = (double)u_accept[(size_t)b * N + (n - 1)];
+                        accept = ratio > u;
+                        double scale = g[x] / qh;
+                        if (scale < 1.0)
+                            scale = 1.0;
+                        if (flag_accept && fabs(u - ratio) < OR_ACCEPT_WINDOW * scale)
+                            flag_accept[(size_t)b * N + (n - 1)] = 1;
+                    }
+                }
+                if (accept) {
+                    next = n;
+                    break;
+                }
+                /* p' <- norm(max(0, p' - q_c)); kept as it is if the residual has no mass */
+                if (!q_read) {
+                    bytes += (double)row * 4.0;
+                    q_read = 1;
+                }
+                double Z = 0.0;
+                for (size_t j = 0; j < row; ++j) {
+                    const double r = w[j] - (double)qc[j];
+                    Z += r > 0.0 ? r : 0.0;
+                }
+                if (Z > 0.0)
+                    for (size_t j = 0; j < row; ++j) {
+                        const double r = w[j] - (double)qc[j];
+                        if (r > 0.0) {
+                            w[j] = r / Z;
+                            g[j] = (g[j] + (double)qc[j]) / Z;
+                        } else {
+                            w[j] = 0.0;
+                            g[j] = 0.0;
+                        }
+                    }
+            }
+            if (next < 0)
+                break;
+            tok[d] = node_tokens[(size_t)b * N + (next - 1)];
+            ++d;
+            path[d] = next;
+            c = next;
+        }
+        /* one draw from p' of the last node: smallest j with prefix above t */
+        const double u = (double)u_sample[(size_t)b * (size_t)(N + 1) + (size_t)c];
+        double total = 0.0;
+        for (size_t j = 0; j < row; ++j)
+            total += w[j];
+        const double t = u * total;
+        double cw = 0.0, cg = 0.0;
+        int pick = -1, last_pos = -1, edge = 1;
+        for (int j = 0; j < V; ++j) {
+            const double lo = cw, glo = cg;
+            cw += w[j];
+            cg += g[j];
+            if (w[j] > 0.0)
+                last_pos = j;
+            if (cw > t) {
+                edge = (lo > 0.0 && t - lo <= OR_EDGE_WINDOW * glo) || (cw - t <= OR_EDGE_WINDOW * cg);
+                pick = j;
+                break;
+            }
+        }
+        if (pick < 0)
+            pick = last_pos < 0 ? V - 1 : last_pos;
+        tok[d] = pick;
+        out_len[b] = d + 1;
+        if (flag_sample)
+            flag_sample[b] = edge;
+        if (b_alg)
+            b_alg[b] = bytes;
+    }
+    free(w);
+    free(g);
+    free(depth);
+    return 0;
+}
+
 /* ------------------------------------------------------------ slot fix-up -- */
 
 /* Chain mode (path == NULL): entries j > num_accepted[b] become pad.

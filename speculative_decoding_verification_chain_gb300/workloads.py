@@ -106,6 +106,11 @@ class TreeInputs:
     slot_mapping: Optional[np.ndarray] = None  # [B, N+1] int64
     name: str = ""
     meta: dict = field(default_factory=dict)
+    # sampled trees only
+    draft_probs: Optional[np.ndarray] = None   # [B, N+1, V] f32, row c: law of c's children
+    temperature: Optional[np.ndarray] = None   # [B] f32 > 0
+    u_accept: Optional[np.ndarray] = None      # [B, N] f32, node n at column n-1
+    u_sample: Optional[np.ndarray] = None      # [B, N+1] f32, by the node the walk ends at
 
     @property
     def B(self) -> int:
@@ -462,6 +467,46 @@ def tree_greedy(seed: int = 4, B: int = 16, V: int = 128256,
         logits=logits, dtype=dtype, node_tokens=toks, parent=parent,
         tree_choices=choices, slot_mapping=slot_map(g[3], B, N + 1), name="tree_greedy",
         meta=dict(p_match=p_match, children_per_level=tuple(children_per_level)))
+
+
+def tree_sampled(seed: int = 6, B: int = 16, V: int = 128256,
+                 children_per_level: Sequence[int] = (4, 2, 2, 1, 1), temperature: float = 0.7,
+                 lam: float = 0.3, dtype: int = BF16, parent: Optional[np.ndarray] = None) -> TreeInputs:
+    """Sampled token tree: Zipf-shaped logits per node (as the sampled chain);
+    row c of draft_probs is q_c = softmax(((1-lam) z_c + lam n_c) / T) with n_c
+    an independent Zipf-shaped draw; the children of c are drawn i.i.d. from q_c
+    (with replacement, so siblings may repeat a token)."""
+    g = _streams(seed)
+    if parent is None:
+        parent = parents_in_order(children_per_level)
+        choices = level_tree_choices(children_per_level)
+    else:
+        parent = np.asarray(parent, dtype=np.int32)
+        choices = []
+    N = parent.shape[0] - 1
+    logits = np.empty((B, N + 1, V), dtype=np.uint16 if dtype == BF16 else np.float32)
+    q = np.empty((B, N + 1, V), dtype=np.float32)
+    toks = np.empty((B, N), dtype=np.int32)
+    T = np.float32(temperature)
+    for b in range(B):
+        z = _zipf_rows(g[0], N + 1, V)
+        if dtype == BF16:
+            bits = f32_to_bf16_bits(z)
+            logits[b] = bits
+            zv = bf16_bits_to_f32(bits)
+        else:
+            logits[b] = z
+            zv = z
+        n = _zipf_rows(g[4], N + 1, V)
+        q[b] = _softmax_rows_f32((np.float32(1.0 - lam) * zv + np.float32(lam) * n) / T)
+        if N > 0:
+            toks[b] = _draw_from_rows(g[1], q[b][parent[1:]])
+    return TreeInputs(
+        logits=logits, dtype=dtype, node_tokens=toks, parent=parent, tree_choices=choices,
+        slot_mapping=slot_map(g[3], B, N + 1), name="tree_sampled",
+        meta=dict(lam=lam, children_per_level=tuple(children_per_level)),
+        draft_probs=q, temperature=np.full(B, temperature, dtype=np.float32),
+        u_accept=method_uniforms(g[2], (B, N)), u_sample=method_uniforms(g[2], (B, N + 1)))
 
 
 # ----------------------------------------------------------------------------

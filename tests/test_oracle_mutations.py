@@ -120,6 +120,23 @@ def _ngram_mismatches(O, lib):
     return bad
 
 
+def _tree_law(O, lib):
+    import test_oracle_tree_sampled as ts
+    c = ts.law_case(seed=52, trials=200_000)
+    pv = ts.law_pvalues(c, ts.run(O, c, lib=lib))
+    return min(pv["first"], pv["sibling"], pv["second"])
+
+
+def _tree_closed_form(O, lib):
+    import test_oracle_tree_sampled as ts
+    return ts.closed_form_residual_mismatches(O, lib)[0]
+
+
+def _tree_q_equal_p(O, lib):
+    import test_oracle_tree_sampled as ts
+    return ts.q_equal_p_mismatches(O, lib)
+
+
 CASES = [
     ("residual_sign", "double d = p[j] - (double)qi[j];", "double d = (double)qi[j] - p[j];",
      lambda O, lib: _lossless(O, lib) < 1e-6),
@@ -145,6 +162,18 @@ CASES = [
      "for (int n = n_min; n <= n_max && best_e < 0; ++n) {", lambda O, lib: _ngram_mismatches(O, lib) > 0),
     ("ngram_self_match", "for (int e = L - 2; e >= n - 1; --e) {", "for (int e = L - 1; e >= n - 1; --e) {",
      lambda O, lib: _ngram_mismatches(O, lib) > 0),
+    ("tree_sampled_no_normalise", "w[j] = r / Z;", "w[j] = r;", lambda O, lib: _tree_closed_form(O, lib) > 10),
+    ("tree_sampled_no_clip", "Z += r > 0.0 ? r : 0.0;", "Z += r;", lambda O, lib: _tree_closed_form(O, lib) > 10),
+    ("tree_sampled_first_sibling_only",
+     "                        }\n                    }\n            }\n            if (next < 0)\n",
+     "                        }\n                    }\n                n = N;\n            }\n            if (next < 0)\n",
+     lambda O, lib: _tree_law(O, lib) < 1e-6),
+    ("tree_sampled_child_q_row", "+ (size_t)c) * row : NULL;", "+ (size_t)(c < N ? c + 1 : c)) * row : NULL;",
+     lambda O, lib: _tree_law(O, lib) < 1e-6),
+    ("tree_sampled_accept_reversed", "accept = ratio > u;", "accept = ratio < u;",
+     lambda O, lib: _tree_law(O, lib) < 1e-6),
+    ("tree_sampled_uniform_index", "u_sample[(size_t)b * (size_t)(N + 1) + (size_t)c]",
+     "u_sample[(size_t)b * (size_t)(N + 1)]", lambda O, lib: _tree_q_equal_p(O, lib) > 10),
 ]
 
 
@@ -158,6 +187,9 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _tie_ok(O, lib)
     assert _tree_mismatches(O, lib) == 0
     assert _ngram_mismatches(O, lib) == 0
+    assert _tree_law(O, lib) > 0.01
+    assert _tree_closed_form(O, lib) == 0
+    assert _tree_q_equal_p(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
