@@ -69,6 +69,9 @@ typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype_t;
 #define SPEC_STATUS_BAD_OFFSETS 8  /* ragged chains: cu_num_draft_tokens not non-decreasing within
                                       [0, total_drafts] or a count above max_k (clamped; results of
                                       the requests involved undefined) */
+#define SPEC_STATUS_BAD_TEMPERATURE 16 /* sampled trees: a temperature that is not finite and > 0 (that
+                                          request is walked with T = 1; greedy trees go through
+                                          spec_verify_tree) */
 
 /* Largest rows per request (k+1 for chains, N+1 for trees). */
 #define SPEC_MAX_ROWS 256
@@ -183,6 +186,45 @@ spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_t dtype,
                                int V, int max_depth, int32_t *out_path, int32_t *out_tokens,
                                int32_t *out_len, int32_t *d_status, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/*
+ * Sampled token-tree verification (EAGLE-3 review, "EAGLE-3 inference" step
+ * 4: with sampling, min(1, p/q) acceptance and residual correction keep the
+ * target distribution).  The pages give no rule for siblings; this one walks
+ * from the root and tests the children of the current node c in index order:
+ * child n with token x is accepted iff q_c(x) == 0 or u_accept[b, n-1] <
+ * p'(x) / q_c(x), where p' starts as softmax(z_c / T) and, after each rejected
+ * sibling, becomes norm(max(0, p' - q_c)) (unchanged if that has no mass).
+ * An accepted child becomes the current node.  When no child of c is
+ * accepted, or c is a leaf, one token is drawn from p' by inverse CDF with
+ * u_sample[b, c] (the smallest j whose prefix mass exceeds u * total).  With
+ * the children of c drawn i.i.d. from q_c this emits tokens with the target's
+ * law.  A child token outside [0, V) is rejected (SPEC_STATUS_TOKEN_RANGE).
+ *
+ *  target_logits [B, N+1, V] device, bf16 or fp32, 16-byte aligned: row n is
+ *      the target distribution after the path root..n.
+ *  draft_probs   [B, N+1, V] fp32 device, 16-byte aligned: row c is the
+ *      distribution the children of node c were drawn from (rows of leaves
+ *      are not read).  NULL allowed only when N == 0.
+ *  node_tokens   [B, N] int32 device, column n-1 = node n's token.
+ *  parent        [N+1] int32 HOST, parent[0] = -1, 0 <= parent[n] < n.
+ *  temperature   [B] fp32 device, T > 0 (otherwise SPEC_STATUS_BAD_TEMPERATURE
+ *      and T = 1 for that request).
+ *  u_accept      [B, N] fp32 device in [0, 1), column n-1 for node n's test.
+ *  u_sample      [B, N+1] fp32 device in [0, 1), indexed by the node where the
+ *      walk stops.
+ *  out_path / out_tokens [B, max_depth+1] int32 device and out_len [B], as in
+ *      spec_verify_tree: the walk's nodes from the root, the accepted tokens
+ *      then the drawn one, -1 padded; out_len = accepted + 1.
+ *  d_status      one int32 device word or NULL (SPEC_STATUS_* bits).
+ *  No workspace.  Sizes: 1 <= B, 0 <= N <= SPEC_MAX_ROWS-1, 1 <= V <= 409600,
+ *  max_depth at least the tree's depth.
+ */
+spec_status_t spec_verify_tree_sampled(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                       const int32_t *node_tokens, const int32_t *parent, const float *temperature,
+                                       const float *u_accept, const float *u_sample, int B, int N, int V,
+                                       int max_depth, int32_t *out_path, int32_t *out_tokens, int32_t *out_len,
+                                       int32_t *d_status, void *stream);
 
 /*
  * KV slot_mapping fix-up, in place on [B, P] int64 device memory.

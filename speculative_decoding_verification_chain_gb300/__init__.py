@@ -23,12 +23,13 @@ from typing import Optional, Sequence, Tuple
 
 __all__ = ["verify_chain", "verify_tree", "fixup_slots", "tree_from_choices", "workspace_bytes",
            "SpecError", "PADDING_SLOT_ID", "STATUS_TOKEN_RANGE", "STATUS_NONFINITE",
-           "STATUS_WAIT_TIMEOUT", "STATUS_BAD_OFFSETS", "library_path", "load_library", "verify_chain_noalloc",
+           "STATUS_WAIT_TIMEOUT", "STATUS_BAD_OFFSETS", "STATUS_BAD_TEMPERATURE", "verify_tree_sampled", "library_path", "load_library", "verify_chain_noalloc",
            "verify_chain_ragged", "fixup_slots_ragged", "ngram_propose"]
 
 PADDING_SLOT_ID = -1
 SPEC_BF16, SPEC_FP32 = 0, 1
 STATUS_TOKEN_RANGE, STATUS_NONFINITE, STATUS_WAIT_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8
+STATUS_BAD_TEMPERATURE = 16
 MAX_ROWS = 256
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +78,7 @@ def load_library():
         lib.spec_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
         lib.spec_ngram_propose.restype = I
         lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
+        lib.spec_verify_tree_sampled.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P]
         lib.spec_verify_tree.restype = I
         lib.spec_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64, P]
         lib.spec_fixup_slots.restype = I
@@ -367,6 +369,56 @@ def verify_tree(target_logits, node_tokens, parent: Sequence[int], max_depth: Op
                               _ptr(out_path), _ptr(out_tokens), _ptr(out_len), _ptr(status), _ptr(ws),
                               ws.numel(), sh)
     _check("spec_verify_tree", rc)
+    return out_path, out_tokens, out_len
+
+
+def verify_tree_sampled(target_logits, draft_probs, node_tokens, parent: Sequence[int], temperature, u_accept,
+                        u_sample, max_depth: Optional[int] = None, *, out_path=None, out_tokens=None, out_len=None,
+                        status=None, stream=None):
+    """Sampled token-tree verify on the GPU (children tested in index order,
+    residual after each rejected sibling, one draw where the walk stops).
+
+    target_logits [B, N+1, V] bf16/fp32 CUDA; draft_probs [B, N+1, V] fp32
+    CUDA (row c: the law of c's children); node_tokens [B, N] int32;
+    temperature [B] fp32 (> 0); u_accept [B, N] and u_sample [B, N+1] fp32;
+    parent: N+1 host integers.  Returns (out_path, out_tokens, out_len)."""
+    torch = _torch()
+    import numpy as np
+    lib = load_library()
+    z = target_logits
+    if z.dim() != 3:
+        raise ValueError("target_logits must be [B, N+1, V]")
+    B, n1, V = z.shape
+    N = n1 - 1
+    dev = z.device
+    if dev.type != "cuda" or not z.is_contiguous():
+        raise ValueError("target_logits must be a contiguous CUDA tensor")
+    code = _dtype_code(z)
+    par = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    if par.shape != (N + 1,):
+        raise ValueError("parent must hold N+1 = %d entries" % (N + 1))
+    if max_depth is None:
+        d = np.zeros(N + 1, np.int64)
+        for n in range(1, N + 1):
+            d[n] = d[par[n]] + 1 if 0 <= par[n] < n else 0
+        max_depth = int(d.max())
+    _need(draft_probs, "draft_probs", torch.float32, (B, N + 1, V), dev)
+    _need(node_tokens, "node_tokens", torch.int32, (B, N), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(u_accept, "u_accept", torch.float32, (B, N), dev)
+    _need(u_sample, "u_sample", torch.float32, (B, N + 1), dev)
+    D1 = max_depth + 1
+    if out_path is None:
+        out_path = torch.empty((B, D1), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, D1), dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    rc = lib.spec_verify_tree_sampled(_ptr(z), code, _ptr(draft_probs), _ptr(node_tokens), par.ctypes.data,
+                                      _ptr(temperature), _ptr(u_accept), _ptr(u_sample), B, N, V, int(max_depth),
+                                      _ptr(out_path), _ptr(out_tokens), _ptr(out_len), _ptr(status),
+                                      _stream_handle(dev, stream))
+    _check("spec_verify_tree_sampled", rc)
     return out_path, out_tokens, out_len
 
 

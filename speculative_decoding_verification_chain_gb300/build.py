@@ -7,8 +7,9 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "spec_verify.cu")
-HDR = os.path.join(ROOT, "include", "spec_verify.h")
+SRCS = [os.path.join(PKG, "csrc", f) for f in ("spec_verify.cu", "tree_sampled.cu")]
+HDRS = [os.path.join(ROOT, "include", "spec_verify.h"), os.path.join(PKG, "csrc", "common.h")]
+SRC = SRCS[0]
 LIB = os.path.join(PKG, "libspecverify.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -30,22 +31,41 @@ def cuda_lib_dir() -> str:
     return os.path.join(home, "lib64")
 
 
-def command(out: str = LIB, verbose_ptxas: bool = False) -> list:
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-cudart", "shared", "-Xlinker", "-rpath," + cuda_lib_dir(),
-           "-I", os.path.join(ROOT, "include"), "-o", out, SRC]
+def _flags() -> list:
+    return [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
+
+
+def compile_command(src: str, obj: str, verbose_ptxas: bool = False) -> list:
+    cmd = [nvcc(), *_flags(), "-c", "-o", obj, src]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     return cmd
 
 
+def link_command(objs: list, out: str) -> list:
+    return [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath," + cuda_lib_dir(), "-o", out, *objs]
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile the CUDA library if it is missing or older than its sources."""
-    newest = max(os.path.getmtime(SRC), os.path.getmtime(HDR))
+    """Compile the CUDA library if it is missing or older than its sources.
+    The translation units compile in parallel, then link into one .so."""
+    newest = max(os.path.getmtime(f) for f in SRCS + HDRS)
     if force or verbose_ptxas or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call(command(tmp, verbose_ptxas))
-        os.replace(tmp, LIB)
+        tag = "%d" % os.getpid()
+        objs = [os.path.join(PKG, "csrc", os.path.basename(f) + ".%s.o" % tag) for f in SRCS]
+        procs = [subprocess.Popen(compile_command(s, o, verbose_ptxas)) for s, o in zip(SRCS, objs)]
+        rcs = [p.wait() for p in procs]
+        try:
+            for rc, s in zip(rcs, SRCS):
+                if rc != 0:
+                    raise subprocess.CalledProcessError(rc, "nvcc " + os.path.basename(s))
+            tmp = LIB + ".tmp" + tag
+            subprocess.check_call(link_command(objs, tmp))
+            os.replace(tmp, LIB)
+        finally:
+            for o in objs:
+                if os.path.exists(o):
+                    os.remove(o)
     return LIB
 
 

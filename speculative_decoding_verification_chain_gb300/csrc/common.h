@@ -1,0 +1,16 @@
+// Host helpers shared by the translation units of libspecverify.
+#pragma once
+
+#include "spec_verify.h"
+
+namespace sv {
+
+// Records the message (fmt with one %s for detail) for spec_last_error() and
+// returns s.
+spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "");
+
+// SPEC_OK when the current device is compute capability 10.3; fills *sms with
+// its SM count.
+spec_status_t require_sm103(int *sms);
+
+}  // namespace sv

@@ -45,6 +45,7 @@
 
 #include <mutex>
 
+#include "common.h"
 #include "spec_verify.h"
 
 namespace sv {
@@ -2063,7 +2064,7 @@ __global__ void fixup_kernel(int64_t *slots, int B, int P, const int32_t *num_ac
 // =================================================================== host ==
 thread_local char g_err[512] = "";
 
-spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "") {
+spec_status_t fail(spec_status_t s, const char *fmt, const char *detail) {
     snprintf(g_err, sizeof g_err, fmt, detail);
     return s;
 }
@@ -2181,6 +2182,13 @@ spec_status_t device_info(DeviceInfo *&out) {
     }
     out = &D;
     return SPEC_OK;
+}
+
+spec_status_t require_sm103(int *sms) {
+    DeviceInfo *D = nullptr;
+    spec_status_t st = device_info(D);
+    if (st == SPEC_OK && sms) *sms = D->sms;
+    return st;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -90,6 +90,23 @@ def test_ragged_fixup_host_checks(lib):
     assert lib.spec_fixup_slots_ragged(None, 0, None, 0, None, -1, None) == 0
 
 
+def test_tree_sampled_host_checks(lib):
+    import ctypes
+    par = (ctypes.c_int32 * 4)(-1, 0, 0, 1)
+    bad_par = (ctypes.c_int32 * 4)(-1, 0, 3, 1)
+
+    def call(B=2, N=3, V=100, depth=2, z=0x1000, q=0x2000, tok=0x3000, parent=par, T=0x4000, ua=0x5000,
+             us=0x6000, op=0x7000, ot=0x8000, ol=0x9000, dtype=0):
+        return lib.spec_verify_tree_sampled(z, dtype, q, tok, parent, T, ua, us, B, N, V, depth, op, ot, ol,
+                                            None, None)
+    for bad in (dict(B=0), dict(N=-1), dict(N=256), dict(V=0), dict(V=409601), dict(depth=1), dict(depth=-1),
+                dict(parent=bad_par), dict(z=None), dict(q=None), dict(tok=None), dict(T=None), dict(ua=None),
+                dict(us=None), dict(op=None), dict(ot=None), dict(ol=None), dict(z=0x1008), dict(q=0x2004),
+                dict(dtype=7)):
+        assert call(**bad) == 1, bad
+        assert lib.spec_last_error() != b""
+
+
 def test_ngram_host_checks(lib):
     def call(B=2, Lmax=10, nmin=1, nmax=4, k=3, tok=0x1000, ln=0x2000, d=0x3000, c=0x4000):
         return lib.spec_ngram_propose(tok, ln, B, Lmax, nmin, nmax, k, d, c, None, None, None)

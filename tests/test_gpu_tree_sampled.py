@@ -1,0 +1,175 @@
+"""Sampled token trees on the GPU against the oracle.
+
+Paths, lengths and tokens are compared request by request; where they differ,
+the first difference must sit at a decision the oracle flags (an accept test
+within its window among the children of the node where the walks part, or
+the final draw near a bucket edge).  The output and sibling laws are checked
+on the GPU path itself by chi-square.  Every call goes through the C ABI via
+the binding.
+"""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_chain_gb300 import workloads as W
+
+from helpers import cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for gpu-marked tests")
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def O(oracle_mod):
+    return oracle_mod
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_decoding_verification_chain_gb300 as m
+    m.load_library()
+    return m
+
+
+def _logits_dev(x, dev):
+    import torch
+    t = cuda(x.logits, dev)
+    return t.view(torch.bfloat16) if x.dtype == W.BF16 else t
+
+
+def run_gpu(sv, dev, x, status=None):
+    import torch
+    p, t, n = sv.verify_tree_sampled(_logits_dev(x, dev), cuda(x.draft_probs, dev), cuda(x.node_tokens, dev),
+                                     x.parent, cuda(x.temperature, dev), cuda(x.u_accept, dev),
+                                     cuda(x.u_sample, dev), status=status)
+    torch.cuda.synchronize(dev)
+    return dict(path=p.cpu().numpy(), tokens=t.cpu().numpy(), length=n.cpu().numpy())
+
+
+def run_oracle(O, x):
+    return O.verify_tree_sampled(x.logits, x.dtype, x.node_tokens, x.parent, x.temperature, x.u_accept,
+                                 x.u_sample, x.draft_probs)
+
+
+def compare(x, got, ref):
+    """(exact requests, flagged differences, unexplained differences)."""
+    exact = flagged = bad = 0
+    par = np.asarray(x.parent)
+    for b in range(x.B):
+        if ((got["path"][b] == ref["path"][b]).all() and (got["tokens"][b] == ref["tokens"][b]).all()
+                and got["length"][b] == ref["length"][b]):
+            exact += 1
+            continue
+        L = int(ref["length"][b])
+        i = 1
+        while i < L and got["path"][b, i] == ref["path"][b, i]:
+            i += 1
+        node = int(ref["path"][b, i - 1])        # the walks agree up to this node
+        kids = np.flatnonzero(par == node)
+        ok = bool(ref["flag_accept"][b, kids - 1].any()) if kids.size else False
+        if i == L and got["length"][b] == L and (got["path"][b] == ref["path"][b]).all():
+            ok = ok or bool(ref["flag_sample"][b])   # same walk, different draw
+        if ok:
+            flagged += 1
+        else:
+            bad += 1
+    return exact, flagged, bad
+
+
+@pytest.mark.parametrize("dtype", [W.FP32, W.BF16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("V", [1000, 4099, 32000])
+def test_parity_level_tree(sv, O, dev, dtype, V):
+    x = W.tree_sampled(seed=900 + V, B=64, V=V, dtype=dtype)
+    got, ref = run_gpu(sv, dev, x), run_oracle(O, x)
+    exact, flagged, bad = compare(x, got, ref)
+    assert bad == 0, (exact, flagged, bad)
+    assert exact >= 60
+
+
+@pytest.mark.parametrize("lam,T", [(0.1, 1.0), (0.6, 0.7), (0.9, 0.5)])
+def test_parity_acceptance_regimes(sv, O, dev, lam, T):
+    x = W.tree_sampled(seed=910, B=48, V=5003, children_per_level=(3, 3, 2), temperature=T, lam=lam)
+    got, ref = run_gpu(sv, dev, x), run_oracle(O, x)
+    exact, flagged, bad = compare(x, got, ref)
+    assert bad == 0 and exact >= 44, (exact, flagged, bad)
+
+
+def test_parity_full_size_bf16(sv, O, dev):
+    x = W.tree_sampled(seed=920, B=16, V=128256)
+    got, ref = run_gpu(sv, dev, x), run_oracle(O, x)
+    exact, flagged, bad = compare(x, got, ref)
+    assert bad == 0 and exact >= 15, (exact, flagged, bad)
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 9, 152064, 262144])
+def test_parity_vocabulary_edges(sv, O, dev, V):
+    """Tiny vocabularies (one CTA, partial chunks), the sweep vocabulary, and a
+    vocabulary that needs a 16-CTA cluster."""
+    B = 24 if V < 100000 else 4
+    x = W.tree_sampled(seed=930 + V, B=B, V=V, children_per_level=(2, 2), dtype=W.FP32)
+    got, ref = run_gpu(sv, dev, x), run_oracle(O, x)
+    exact, flagged, bad = compare(x, got, ref)
+    assert bad == 0 and exact >= B - 2, (exact, flagged, bad)
+
+
+def test_root_only_tree_draws_from_root(sv, O, dev):
+    x = W.tree_sampled(seed=940, B=32, V=3000, parent=np.array([-1], np.int32))
+    got, ref = run_gpu(sv, dev, x), run_oracle(O, x)
+    assert (got["length"] == 1).all() and (got["path"][:, 0] == 0).all()
+    exact, flagged, bad = compare(x, got, ref)
+    assert bad == 0 and exact >= 30
+
+
+def test_irregular_tree(sv, O, dev):
+    parent = np.array([-1, 0, 0, 1, 1, 1, 2, 3, 3, 6, 7, 7, 7, 9], np.int32)
+    x = W.tree_sampled(seed=941, B=64, V=2048, parent=parent, lam=0.6)
+    got, ref = run_gpu(sv, dev, x), run_oracle(O, x)
+    exact, flagged, bad = compare(x, got, ref)
+    assert bad == 0 and exact >= 60, (exact, flagged, bad)
+
+
+def test_status_bits(sv, O, dev):
+    import torch
+    x = W.tree_sampled(seed=942, B=8, V=500, children_per_level=(2,))
+    x.node_tokens[:, 0] = 500                 # out of range: rejected
+    x.node_tokens[0, 1] = -3
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = run_gpu(sv, dev, x, status=st)
+    assert int(st.item()) & sv.STATUS_TOKEN_RANGE
+    ref = run_oracle(O, x)
+    assert compare(x, got, ref)[2] == 0
+    x.temperature[3] = 0.0
+    st.zero_()
+    run_gpu(sv, dev, x, status=st)
+    assert int(st.item()) & sv.STATUS_BAD_TEMPERATURE
+
+
+def test_law_on_gpu(sv, O, dev):
+    """The GPU path's own output law and sibling law (chi-square, as for the oracle)."""
+    import test_oracle_tree_sampled as ts
+    c = ts.law_case(seed=52, trials=200_000)
+    x = W.TreeInputs(logits=c["z"], dtype=W.FP32, node_tokens=c["toks"], parent=c["parent"], tree_choices=[],
+                     draft_probs=c["q"], temperature=c["T"], u_accept=c["ua"], u_sample=c["us"])
+    got = run_gpu(sv, dev, x)
+    pv = ts.law_pvalues(c, got)
+    assert pv["first"] > 0.01 and pv["sibling"] > 0.01, pv
+    assert pv["second"] > 0.01 / pv["n_second"], pv
+
+
+def test_host_checks(sv, dev):
+    import torch
+    x = W.tree_sampled(seed=943, B=2, V=64, children_per_level=(2,))
+    with pytest.raises(Exception):
+        sv.verify_tree_sampled(_logits_dev(x, dev), cuda(x.draft_probs, dev), cuda(x.node_tokens, dev),
+                               [-1, 0, 2], cuda(x.temperature, dev), cuda(x.u_accept, dev), cuda(x.u_sample, dev))
+    with pytest.raises(Exception):
+        sv.verify_tree_sampled(_logits_dev(x, dev), cuda(x.draft_probs, dev), cuda(x.node_tokens, dev),
+                               x.parent, cuda(x.temperature, dev), cuda(x.u_accept, dev), cuda(x.u_sample, dev),
+                               max_depth=0)
+    assert torch.cuda.is_available()
