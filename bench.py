@@ -550,8 +550,8 @@ def main():
 
 def others(sv, W, dev, dist, peak, args):
     """Secondary workloads (kernel-only device time): sampled chain, greedy
-    tree, the k = 8, V = 152064 sampled sweep, the ragged greedy chain and
-    n-gram lookup drafting."""
+    tree, the k = 8, V = 152064 sampled sweep, the ragged greedy chain,
+    n-gram lookup drafting and the sampled tree."""
     import torch
     out = []
     # sampled chain, B=32 k=4 V=128256 T=0.7, lambda = 0.3
@@ -562,6 +562,7 @@ def others(sv, W, dev, dist, peak, args):
     out.append(_other_tree(sv, W, dev, dist, peak))
     out.append(_other_ragged(sv, W, dev, dist, peak))
     out.append(_other_ngram(sv, W, dev, dist, peak))
+    out.append(_other_tree_sampled(sv, W, dev, dist, peak))
     return out
 
 
@@ -768,6 +769,92 @@ def _other_ngram(sv, W, dev, dist, peak, target_s=0.5):
             % int(ln.sum()), "sequences_per_s": 64 / (us * 1e-6), "kernel_us": us, "achieved_gbs_alg": ach,
             "frac_alg": ach / peak, "bytes_per_launch": {"algorithmic": b_alg},
             "mean_draft_len": float(cnt.mean())}
+
+
+def tree_sampled_bytes(parent, path, length, V, zbytes):
+    """Algorithmic bytes of one sampled-tree walk, from its path: the logits
+    row of every node on the path; the q row of a node where a child was
+    rejected (the next node is not its first child, or the walk stopped at a
+    node with children); 4 bytes per q(x) gather (one per child tested)."""
+    par = np.asarray(parent)
+    kids = [np.flatnonzero(par == c) for c in range(par.shape[0])]
+    total = 0.0
+    for b in range(path.shape[0]):
+        L = int(length[b])
+        nodes = [int(v) for v in path[b, :L]]
+        total += L * V * zbytes
+        for i, c in enumerate(nodes):
+            ch = kids[c]
+            if i + 1 < L:
+                tested = int(np.flatnonzero(ch == nodes[i + 1])[0]) + 1
+                rejected = tested > 1
+            else:
+                tested = ch.size
+                rejected = ch.size > 0
+            total += 4.0 * tested + (V * 4.0 if rejected else 0.0)
+    return total
+
+
+def _other_tree_sampled(sv, W, dev, dist, peak, target_s=0.5):
+    """Sampled tree: B = 16 requests, the 60-node tree of the greedy tree
+    workload, V = 128256 bf16 logits and fp32 q rows, T = 0.7, lambda = 0.3.
+    Input copies rotate so the rows the walks read never come from L2."""
+    import torch
+    x = W.tree_sampled(seed=13, B=16, V=128256)
+    per_copy = x.logits.nbytes + x.draft_probs.nbytes
+    z0 = to_dev(x.logits, dev)
+    q0 = to_dev(x.draft_probs, dev)
+    small = dict(tok=to_dev(x.node_tokens, dev), T=to_dev(x.temperature, dev), ua=to_dev(x.u_accept, dev),
+                 us=to_dev(x.u_sample, dev))
+    ncopy = 8
+    zs = [z0] + [z0.clone() for _ in range(ncopy - 1)]
+    qs = [q0] + [q0.clone() for _ in range(ncopy - 1)]
+    D1 = int(tree_depth(x.parent)) + 1
+    outs = [tuple(torch.empty(sh, dtype=torch.int32, device=dev) for sh in ((x.B, D1), (x.B, D1), (x.B,)))
+            for _ in range(ncopy)]
+
+    def call(i):
+        o = outs[i]
+        sv.verify_tree_sampled(zs[i], qs[i], small["tok"], x.parent, small["T"], small["ua"], small["us"],
+                               out_path=o[0], out_tokens=o[1], out_len=o[2])
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for i in range(ncopy):
+            call(i)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(ncopy):
+            call(i)
+
+    class _C:
+        def run(self, steps, verify_only=False):
+            for _ in range(steps):
+                g.replay()
+    case = _C()
+    case.run(3)
+    ms = time_steps(case, 10, dev, dist)
+    n = max(10, int(10 * target_s / max(ms / 1e3, 1e-6)))
+    ms = time_steps(case, n, dev, dist)
+    us = ms * 1e3 / (n * ncopy)
+    path, length = outs[0][0].cpu().numpy(), outs[0][2].cpu().numpy()
+    b_alg = tree_sampled_bytes(x.parent, path, length, x.V, 2)
+    ach = b_alg / (us * 1e-6) / 1e9
+    return {"workload": "sampled tree B=16 N=60 levels (4,8,16,16,16) V=128256 bf16 T=0.7 lambda=0.3 (Zipf)",
+            "positions_per_s": float(x.B * x.N) / (us * 1e-6), "tokens_per_s": float(length.sum()) / (us * 1e-6),
+            "kernel_us": us, "achieved_gbs_alg": ach, "frac_alg": ach / peak,
+            "bytes_per_launch": {"algorithmic": b_alg, "dense_inputs": float(per_copy)},
+            "mean_tokens_per_request": float(length.mean())}
+
+
+def tree_depth(parent):
+    par = np.asarray(parent)
+    d = np.zeros(par.shape[0], np.int64)
+    for n in range(1, par.shape[0]):
+        d[n] = d[par[n]] + 1
+    return d.max()
 
 
 if __name__ == "__main__":

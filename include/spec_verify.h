@@ -217,8 +217,8 @@ spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_t dtype,
  *      spec_verify_tree: the walk's nodes from the root, the accepted tokens
  *      then the drawn one, -1 padded; out_len = accepted + 1.
  *  d_status      one int32 device word or NULL (SPEC_STATUS_* bits).
- *  No workspace.  Sizes: 1 <= B, 0 <= N <= SPEC_MAX_ROWS-1, 1 <= V <= 409600,
- *  max_depth at least the tree's depth.
+ *  No workspace.  Sizes: 1 <= B, 0 <= N <= SPEC_MAX_ROWS-1, max_depth at least
+ *  the tree's depth, 1 <= V <= 360448 (bf16) or 300288 (fp32).
  */
 spec_status_t spec_verify_tree_sampled(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
                                        const int32_t *node_tokens, const int32_t *parent, const float *temperature,

@@ -18,11 +18,17 @@
 // then one pass over p and q of the row, both held in shared memory.
 //
 // Layout: one thread-block cluster per request; CTA r of the cluster holds
-// columns [r * slice, (r + 1) * slice) of the current node's row (e = exp2 of
-// the scaled logits, then q) in shared memory.  Scalars (row max, sums,
-// masses, prefix sums) are combined across the cluster through distributed
-// shared memory after a cluster barrier; every CTA runs the same control flow
-// on the same combined values, so all of them take the same decisions.
+// columns [r * slice, (r + 1) * slice) of the current node's row in shared
+// memory: the logits as stored (one bulk-async copy), e = 2^((z - M) log2e/T)
+// in fp32, and q (a second bulk copy, issued with the first whenever the node
+// has children).  Row max, sums, residual masses and prefix sums are combined
+// across the cluster through distributed shared memory after one cluster
+// barrier each; thread 0 of every CTA combines the ranks' values in rank
+// order, so every CTA holds the same numbers and takes the same decisions.
+// All arithmetic is fp32: per-thread sums are compensated (Kahan) and every
+// combination beyond a thread is two-float (about 44 significant bits); FP64
+// issue is scarce on this part and its latency sits on the walk's critical
+// path.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -32,6 +38,7 @@
 #include <climits>
 
 #include "common.h"
+#include "ptx.cuh"
 #include "spec_verify.h"
 
 namespace cg = cooperative_groups;
@@ -41,10 +48,14 @@ namespace ts {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxNodes = SPEC_MAX_ROWS;       // N + 1
+constexpr int kMaxNodes = SPEC_MAX_ROWS;            // N + 1
 constexpr int kMaxCluster = 16;
-constexpr int kSliceCap = 25600;               // columns per CTA: e and q (fp32) in 200 KiB
+constexpr int kSmemBudget = 220 * 1024;             // dynamic: e, q (fp32) and the logits slice as stored
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Columns per CTA for a logits element of es bytes (8 + es bytes a column).
+__host__ __device__ constexpr int slice_cap(int es) { return (kSmemBudget / (8 + es)) & ~7; }
 
 struct Params {
     const void *logits;        // [B, N+1, V] bf16 bits or fp32
@@ -57,363 +68,525 @@ struct Params {
     int32_t *out_tokens;       // [B, D+1]
     int32_t *out_len;          // [B]
     int32_t *status;           // one word or null
-    int bf16, B, N, V, max_depth, slice, cluster, vec_z, vec_q;
+    int bf16, B, N, V, max_depth, slice, cluster;
+    int zbulk, qbulk;          // rows start on 16-byte boundaries: bulk copies allowed
     uint16_t child_off[kMaxNodes + 1];  // children of c: child_list[child_off[c] .. child_off[c+1])
     uint8_t child_list[kMaxNodes];
 };
 
 struct Shared {
-    double slot[2][2];          // cluster exchange, double-buffered by reduction parity
-    double wsum[kWarps];
+    uint64_t bar;                          // the current node's row copies
+    float4 slot[2][kMaxCluster];           // pushed by every rank, double-buffered by exchange parity
+    float ws[kWarps], wc[kWarps];          // warp partials (two-float)
+    float wxs[kWarps], wxc[kWarps];        // warp exclusive prefixes (two-float, final draw)
+    float tot[2];                          // block total (final draw)
     float wmax[kWarps];
-    int wint[2][kWarps];
+    int wint[kWarps];
     int dec;
+    int pick;
+    int32_t tok[kMaxNodes];                // node tokens of this request (node n at n-1)
+    float ua[kMaxNodes];                   // u_accept of this request (node n at n-1)
+    float qx[kMaxNodes];                   // q_c(x) of the current node's children, in child order
+    float ex[kMaxNodes];                   // e(x) of the same, on its owner's scale
+    uint8_t exo[kMaxNodes];                // owner rank of each child's column
 };
 
 // ---------------------------------------------------------------- helpers --
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-// Compensated (Neumaier) running sum in fp32: s + c is the sum to ~1 ulp of
-// the terms' magnitude, whatever the chunk length.
-__device__ __forceinline__ void nadd(float &s, float &c, float v) {
-    const float t = s + v;
-    const bool big = fabsf(s) >= fabsf(v);
-    c += big ? (s - t) + v : (v - t) + s;
+// 2^x by the SFU approximation (relative error about 2^-22).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Kahan running sum of non-negative terms: s - c carries the sum to about one
+// ulp of its magnitude, whatever the chunk length.
+__device__ __forceinline__ void kadd(float &s, float &c, float v) {
+    const float y = v - c;
+    const float t = s + y;
+    c = (t - s) - y;
     s = t;
 }
 
-__device__ __forceinline__ double block_sum(double v, Shared &sh) {
+// s + e == a + b exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// (hi, lo) += (bh, bl) as two-float numbers (about 44 significant bits).
+__device__ __forceinline__ void tf_add(float &hi, float &lo, float bh, float bl) {
+    float s, e;
+    two_sum(hi, bh, s, e);
+    e += lo + bl;
+    hi = s + e;
+    lo = e - (hi - s);
+}
+
+// (hi, lo) = (ah, al) * f, two-float times float.
+__device__ __forceinline__ void tf_mul(float ah, float al, float f, float &hi, float &lo) {
+    const float p = ah * f;
+    const float e = fmaf(ah, f, -p) + al * f;
+    hi = p + e;
+    lo = e - (hi - p);
+}
+
+// Block sum of the threads' two-float values; warp 0 combines the warps; the
+// result reaches every thread.
+__device__ __forceinline__ void block_sum2(float &hi, float &lo, Shared &sh) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) sh.wsum[w] = v;
+    for (int o = 16; o > 0; o >>= 1)
+        tf_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        sh.ws[w] = hi;
+        sh.wc[w] = lo;
+    }
     __syncthreads();
-    double r = 0.0;
-    for (int i = 0; i < kWarps; ++i) r += sh.wsum[i];
+    if (w == 0) {
+        hi = lane < kWarps ? sh.ws[lane] : 0.0f;
+        lo = lane < kWarps ? sh.wc[lane] : 0.0f;
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1)
+            tf_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+        if (lane == 0) {
+            sh.tot[0] = hi;
+            sh.tot[1] = lo;
+        }
+    }
     __syncthreads();
-    return r;
+    hi = sh.tot[0];
+    lo = sh.tot[1];
 }
 
 __device__ __forceinline__ float block_max(float v, Shared &sh) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) sh.wmax[w] = v;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sh.wmax[w] = v;
     __syncthreads();
-    float r = -INFINITY;
-    for (int i = 0; i < kWarps; ++i) r = fmaxf(r, sh.wmax[i]);
-    __syncthreads();
-    return r;
-}
-
-// Block minimum of a and maximum of b (ints).
-__device__ __forceinline__ void block_minmax(int &a, int &b, Shared &sh) {
+    v = sh.wmax[lane & (kWarps - 1)];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
-        b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
-    }
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        sh.wint[0][w] = a;
-        sh.wint[1][w] = b;
-    }
-    __syncthreads();
-    a = INT_MAX;
-    b = -1;
-    for (int i = 0; i < kWarps; ++i) {
-        a = min(a, sh.wint[0][i]);
-        b = max(b, sh.wint[1][i]);
-    }
-    __syncthreads();
+    for (int o = kWarps / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
 }
 
-// Exclusive prefix over the block's threads (thread order) of v; *total gets
-// the block sum.
-__device__ __forceinline__ double block_excl_scan(double v, double *total, Shared &sh) {
+// Block maximum of an int, to every thread.
+__device__ __forceinline__ int block_imax(int v, Shared &sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sh.wint[w] = v;
+    __syncthreads();
+    v = sh.wint[lane & (kWarps - 1)];
+#pragma unroll
+    for (int o = kWarps / 2; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Exclusive and inclusive prefixes, in thread order, of the threads'
+// two-float values.  Consecutive threads' boundaries are the same numbers (the
+// same operations in the same order), and so is the last inclusive prefix and
+// the block total, which goes to (th, tl).
+__device__ __forceinline__ void block_scan2(float s, float c, float &exh, float &exl, float &inh, float &inl,
+                                            float &th, float &tl, Shared &sh) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    double x = v;
+    float is = s, ic = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const float ys = __shfl_up_sync(0xffffffffu, is, o), yc = __shfl_up_sync(0xffffffffu, ic, o);
+        if (lane >= o) {
+            float h = ys, l = yc;
+            tf_add(h, l, is, ic);
+            is = h;
+            ic = l;
+        }
     }
-    if (lane == 31) sh.wsum[w] = x;
-    __syncthreads();
-    double before = 0.0, all = 0.0;
-    for (int i = 0; i < kWarps; ++i) {
-        if (i < w) before += sh.wsum[i];
-        all += sh.wsum[i];
+    float es = __shfl_up_sync(0xffffffffu, is, 1), ec = __shfl_up_sync(0xffffffffu, ic, 1);
+    if (lane == 0) es = ec = 0.0f;
+    if (lane == 31) {
+        sh.ws[w] = is;
+        sh.wc[w] = ic;
     }
     __syncthreads();
-    *total = all;
-    return before + x - v;
+    if (threadIdx.x == 0) {
+        float h = 0.0f, l = 0.0f;
+        for (int i = 0; i < kWarps; ++i) {
+            sh.wxs[i] = h;
+            sh.wxc[i] = l;
+            tf_add(h, l, sh.ws[i], sh.wc[i]);
+        }
+        sh.tot[0] = h;
+        sh.tot[1] = l;
+    }
+    __syncthreads();
+    exh = sh.wxs[w];
+    exl = sh.wxc[w];
+    inh = exh;
+    inl = exl;
+    if (lane > 0) tf_add(exh, exl, es, ec);
+    tf_add(inh, inl, is, ic);
+    th = sh.tot[0];
+    tl = sh.tot[1];
 }
 
-// Calls f(r, a_r, b_r) for every rank r in rank order after one cluster
-// barrier; (a, b) are this CTA's values (thread 0's).  The two parity slots
-// make a second barrier unnecessary: a slot is rewritten only after every CTA
-// has passed the barrier that follows its last read of it.
-template <class F>
-__device__ __forceinline__ void cluster_each(cg::cluster_group &cl, Shared &sh, int &parity, double a, double b,
-                                             int C, F f) {
-    if (threadIdx.x == 0) {
-        sh.slot[parity][0] = a;
-        sh.slot[parity][1] = b;
-    }
+// Every CTA pushes its float4 into slot[parity][its rank] of every CTA of the
+// cluster (threads 0..C-1, one remote store each), then one cluster barrier;
+// afterwards every thread reads the C local slots.  A slot is rewritten only
+// after every CTA has passed the barrier that follows its last read (all of
+// this CTA's threads arrive at the next barrier only after reading), so one
+// barrier per exchange suffices.  Returns the slot row to read.
+__device__ __forceinline__ const float4 *cluster_exchange(cg::cluster_group &cl, Shared &sh, int &parity, int rank,
+                                                          float4 v, int C) {
+    if (static_cast<int>(threadIdx.x) < C) *cl.map_shared_rank(&sh.slot[parity][rank], static_cast<int>(threadIdx.x)) = v;
     cl.sync();
-    for (int r = 0; r < C; ++r) {
-        const double *rem = cl.map_shared_rank(&sh.slot[parity][0], r);
-        f(r, rem[0], rem[1]);
-    }
+    const float4 *row = sh.slot[parity];
     parity ^= 1;
+    return row;
 }
 
 __device__ __forceinline__ bool nonfinite(float f) { return (f != f) || f == INFINITY; }
 
-// Columns [lo, lo + n) of one logits row (element offset roff) into dst as
-// fp32; returns this thread's maximum and ORs NaN / +inf into bad.
-__device__ float load_logits(const Params &P, size_t roff, int lo, int n, float *dst, bool &bad) {
-    float m = -INFINITY;
-    if (P.bf16) {
-        const uint16_t *src = static_cast<const uint16_t *>(P.logits) + roff + lo;
-        int done = 0;
-        if (P.vec_z) {
-            const int nv = n >> 3;
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-            for (int i = threadIdx.x; i < nv; i += kThreads) {
-                const uint4 v = __ldg(s4 + i);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    f[2 * j] = __uint_as_float(w[j] << 16);
-                    f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    m = fmaxf(m, f[j]);
-                    bad |= nonfinite(f[j]);
-                }
-                float4 *d4 = reinterpret_cast<float4 *>(dst + 8 * i);
-                d4[0] = make_float4(f[0], f[1], f[2], f[3]);
-                d4[1] = make_float4(f[4], f[5], f[6], f[7]);
-            }
-            done = nv << 3;
-        }
-        for (int i = done + threadIdx.x; i < n; i += kThreads) {
-            const float f = bf16_to_f32(__ldg(src + i));
-            m = fmaxf(m, f);
-            bad |= nonfinite(f);
-            dst[i] = f;
-        }
-    } else {
-        const float *src = static_cast<const float *>(P.logits) + roff + lo;
-        int done = 0;
-        if (P.vec_z) {
-            const int nv = n >> 2;
-            const float4 *s4 = reinterpret_cast<const float4 *>(src);
-            for (int i = threadIdx.x; i < nv; i += kThreads) {
-                const float4 v = __ldg(s4 + i);
-                m = fmaxf(fmaxf(m, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
-                bad |= nonfinite(v.x) | nonfinite(v.y) | nonfinite(v.z) | nonfinite(v.w);
-                reinterpret_cast<float4 *>(dst)[i] = v;
-            }
-            done = nv << 2;
-        }
-        for (int i = done + threadIdx.x; i < n; i += kThreads) {
-            const float f = __ldg(src + i);
-            m = fmaxf(m, f);
-            bad |= nonfinite(f);
-            dst[i] = f;
-        }
-    }
-    return m;
+// Bounded wait on the row-copy barrier; false after kWaitLimitNs.
+__device__ bool wait_rows(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait_sleep(bar, parity, 100000u))
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
 }
 
-// Columns [lo, lo + n) of one q row (element offset roff) into dst.
-__device__ void load_q(const Params &P, size_t roff, int lo, int n, float *dst) {
-    const float *src = P.q + roff + lo;
-    int done = 0;
-    if (P.vec_q) {
-        const int nv = n >> 2;
-        const float4 *s4 = reinterpret_cast<const float4 *>(src);
-        for (int i = threadIdx.x; i < nv; i += kThreads) reinterpret_cast<float4 *>(dst)[i] = __ldg(s4 + i);
-        done = nv << 2;
-    }
-    for (int i = done + threadIdx.x; i < n; i += kThreads) dst[i] = __ldg(src + i);
+__device__ __forceinline__ float zval(const unsigned char *zs, bool bf16, int i) {
+    return bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t *>(zs)[i]) : reinterpret_cast<const float *>(zs)[i];
 }
 
 __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_constant__ Params P) {
-    extern __shared__ __align__(16) float dyn[];
+    extern __shared__ __align__(128) unsigned char dyn[];
     __shared__ Shared sh;
     cg::cluster_group cl = cg::this_cluster();
     const int C = P.cluster;
     const int rank = static_cast<int>(cl.block_rank());
     const int b = static_cast<int>(blockIdx.x) / C;
     const int S = P.slice, V = P.V, N = P.N, D1 = P.max_depth + 1;
-    float *ev = dyn;        // e = exp2((z - M) * log2(e) / T) of this CTA's columns
-    float *qv = dyn + S;    // q of this CTA's columns (loaded on the first rejection at a node)
+    const int tid = threadIdx.x;
+    const bool bf16 = P.bf16 != 0;
+    const int es = bf16 ? 2 : 4;
+    float *ev = reinterpret_cast<float *>(dyn);               // e of this CTA's columns
+    float *qv = ev + S;                                       // q of this CTA's columns
+    unsigned char *zs = dyn + 8 * static_cast<size_t>(S);     // logits of this CTA's columns, as stored
     const int lo = rank * S;
     const int n = max(0, min(S, V - lo));
     // Thread t owns the contiguous chunk [t*E, t*E + E) of the CTA's columns;
     // E is odd so that consecutive threads fall in different banks.
     const int E = ((n + kThreads - 1) / kThreads) | 1;
-    const int c0 = min(n, static_cast<int>(threadIdx.x) * E), c1 = min(n, c0 + E);
-    const bool lead = rank == 0 && threadIdx.x == 0;
+    const int c0 = min(n, tid * E), c1 = min(n, c0 + E);
+    const bool lead = rank == 0 && tid == 0;
+    const size_t rows = static_cast<size_t>(N) + 1;
+    // bulk parts of this CTA's slices (16-byte multiples); the rest by plain loads
+    const uint32_t zmain = P.zbulk ? static_cast<uint32_t>((n * es) & ~15) : 0u;
+    const uint32_t qmain = P.qbulk ? static_cast<uint32_t>((n * 4) & ~15) : 0u;
     int parity = 0;
-    bool bad = false;
+    uint32_t phase = 0;
+    bool bad = false, late = false;
 
+    for (int i = tid; i < N; i += kThreads) {
+        sh.tok[i] = __ldg(P.tokens + static_cast<size_t>(b) * N + i);
+        sh.ua[i] = __ldg(P.u_accept + static_cast<size_t>(b) * N + i);
+    }
+    if (tid == 0) {
+        mbar_init(&sh.bar, 1);
+        fence_proxy_async();
+    }
     float T = __ldg(P.temperature + b);
     if (!(T > 0.0f) || T == INFINITY) {
         if (lead && P.status) atomicOr(P.status, SPEC_STATUS_BAD_TEMPERATURE);
         T = 1.0f;
     }
     const float c2 = kLog2e / T;
-    const size_t rows = static_cast<size_t>(N) + 1;
     if (lead) P.out_path[static_cast<size_t>(b) * D1] = 0;
+    __syncthreads();
 
     int cur = 0, d = 0;
     for (;;) {
         const size_t roff = (static_cast<size_t>(b) * rows + cur) * static_cast<size_t>(V);
-        // row max over the cluster
-        float m = block_max(load_logits(P, roff, lo, n, ev, bad), sh);
-        float M = -INFINITY;
-        cluster_each(cl, sh, parity, static_cast<double>(m), 0.0, C,
-                     [&](int, double a, double) { M = fmaxf(M, static_cast<float>(a)); });
-        // e and its sum (rank order, so every CTA holds the same value)
-        float s = 0.0f, c = 0.0f;
-        for (int i = c0; i < c1; ++i) {
-            const float e = exp2f((ev[i] - M) * c2);
-            ev[i] = e;
-            nadd(s, c, e);
+        const int kb = P.child_off[cur], m = P.child_off[cur + 1] - kb;
+        // (1) this node's rows: logits always, q when it has children; the
+        // children's q(x) gathered while the copies run
+        const uint32_t qbytes = m > 0 ? qmain : 0u;
+        if (tid == 0 && zmain + qbytes > 0) {
+            fence_proxy_async();  // earlier reads of zs / qv come before the async writes
+            mbar_expect_tx(&sh.bar, zmain + qbytes);
+            if (zmain)
+                bulk_g2s(zs, static_cast<const unsigned char *>(P.logits) + (roff + lo) * es, zmain, &sh.bar);
+            if (qbytes) bulk_g2s(qv, P.q + roff + lo, qbytes, &sh.bar);
         }
-        const double part = block_sum(static_cast<double>(s) + static_cast<double>(c), sh);
-        double Ssum = 0.0;
-        cluster_each(cl, sh, parity, part, 0.0, C, [&](int, double a, double) { Ssum += a; });
-        if (!(Ssum > 0.0) || !(Ssum < INFINITY)) {
-            bad = true;
-            Ssum = 1.0;
+        if (bf16) {
+            const uint16_t *src = static_cast<const uint16_t *>(P.logits) + roff + lo;
+            for (int i = static_cast<int>(zmain / 2) + tid; i < n; i += kThreads)
+                reinterpret_cast<uint16_t *>(zs)[i] = __ldg(src + i);
+        } else {
+            const float *src = static_cast<const float *>(P.logits) + roff + lo;
+            for (int i = static_cast<int>(zmain / 4) + tid; i < n; i += kThreads)
+                reinterpret_cast<float *>(zs)[i] = __ldg(src + i);
         }
-        const double invS = 1.0 / Ssum;
-        const float invSf = static_cast<float>(invS);
+        if (m > 0)
+            for (int i = static_cast<int>(qmain / 4) + tid; i < n; i += kThreads) qv[i] = __ldg(P.q + roff + lo + i);
+        for (int k = tid; k < m; k += kThreads) {
+            const int x = sh.tok[P.child_list[kb + k] - 1];
+            sh.qx[k] = (x >= 0 && x < V) ? __ldg(P.q + roff + x) : 0.0f;
+        }
+        if (zmain + qbytes > 0) {
+            if (!wait_rows(&sh.bar, phase)) late = true;
+            phase ^= 1u;
+        }
+        __syncthreads();
 
-        // children in index order; (Tm, ST): p' is max(0, p - Tm q) / ST
-        double Tm = 0.0, ST = 1.0;
-        bool qloaded = false;
+        // (2) this CTA's max m_r, e = 2^((z - m_r) c2) and its sum; one cluster
+        // exchange gives M = max m_r, the scales f_r = 2^((m_r - M) c2) and
+        // S = sum_r f_r * sum_r, so p = e * f_r / S on rank r
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        {
+            int i = c0;
+            for (; i + 3 < c1; i += 4) {
+                const float z0 = zval(zs, bf16, i), z1 = zval(zs, bf16, i + 1);
+                const float z2 = zval(zs, bf16, i + 2), z3 = zval(zs, bf16, i + 3);
+                mx0 = fmaxf(mx0, z0);
+                mx1 = fmaxf(mx1, z1);
+                mx2 = fmaxf(mx2, z2);
+                mx3 = fmaxf(mx3, z3);
+                bad |= nonfinite(z0) | nonfinite(z1) | nonfinite(z2) | nonfinite(z3);
+            }
+            for (; i < c1; ++i) {
+                const float z = zval(zs, bf16, i);
+                mx0 = fmaxf(mx0, z);
+                bad |= nonfinite(z);
+            }
+        }
+        const float mr = block_max(fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)), sh);
+        const float mrs = mr == -INFINITY ? 0.0f : mr;  // an empty or all -inf slice contributes nothing
+        float sh0, sl0;
+        {
+            float s0 = 0.0f, k0 = 0.0f, s1 = 0.0f, k1 = 0.0f, s2 = 0.0f, k2 = 0.0f, s3 = 0.0f, k3 = 0.0f;
+            int i = c0;
+            for (; i + 3 < c1; i += 4) {
+                const float e0 = ex2((zval(zs, bf16, i) - mrs) * c2);
+                const float e1 = ex2((zval(zs, bf16, i + 1) - mrs) * c2);
+                const float e2 = ex2((zval(zs, bf16, i + 2) - mrs) * c2);
+                const float e3 = ex2((zval(zs, bf16, i + 3) - mrs) * c2);
+                ev[i] = e0;
+                ev[i + 1] = e1;
+                ev[i + 2] = e2;
+                ev[i + 3] = e3;
+                kadd(s0, k0, e0);
+                kadd(s1, k1, e1);
+                kadd(s2, k2, e2);
+                kadd(s3, k3, e3);
+            }
+            for (; i < c1; ++i) {
+                const float e = ex2((zval(zs, bf16, i) - mrs) * c2);
+                ev[i] = e;
+                kadd(s0, k0, e);
+            }
+            sh0 = s0;
+            sl0 = -k0;
+            tf_add(sh0, sl0, s1, -k1);
+            tf_add(sh0, sl0, s2, -k2);
+            tf_add(sh0, sl0, s3, -k3);
+        }
+        block_sum2(sh0, sl0, sh);
+        const float4 *row = cluster_exchange(cl, sh, parity, rank, make_float4(mr, sh0, sl0, 0.0f), C);
+        float M = -INFINITY;
+        for (int r = 0; r < C; ++r) M = fmaxf(M, row[r].x);
+        float Sh = 0.0f, Sl = 0.0f, fmine = 0.0f;
+        for (int r = 0; r < C; ++r) {
+            const float f = row[r].x == -INFINITY ? 0.0f : ex2((row[r].x - M) * c2);
+            if (r == rank) fmine = f;
+            float ph, pl;
+            tf_mul(row[r].y, row[r].z, f, ph, pl);
+            tf_add(Sh, Sl, ph, pl);
+        }
+        if (!(Sh > 0.0f) || !(Sh < INFINITY)) {
+            bad = true;
+            Sh = 1.0f;
+            Sl = 0.0f;
+        }
+        const float pscale = fmine / Sh;  // p = e * pscale on this rank
+        // (3) e(x) of the children, scaled to p(x) * S (every CTA is past step 2)
+        for (int k = tid; k < m; k += kThreads) {
+            const int x = sh.tok[P.child_list[kb + k] - 1];
+            float v = 0.0f;
+            if (x >= 0 && x < V) {
+                const int owner = x / S;
+                const float fo = row[owner].x == -INFINITY ? 0.0f : ex2((row[owner].x - M) * c2);
+                v = *cl.map_shared_rank(ev + (x - owner * S), owner) * fo;
+            }
+            sh.ex[k] = v;
+        }
+        __syncthreads();
+
+        // (4) children in index order; p' is max(0, p - Tm q) / ST.  Child x is
+        // accepted iff q(x) == 0 or u * ST * q(x) < p(x) - Tm * q(x), both
+        // sides multiplied through by S > 0 (no division)
+        float Tmh = 0.0f, Tml = 0.0f, STh = 1.0f, STl = 0.0f;
         int next = -1;
-        for (int k = P.child_off[cur]; k < P.child_off[cur + 1]; ++k) {
-            const int nd = P.child_list[k];
-            if (threadIdx.x == 0) {
-                const int x = __ldg(P.tokens + static_cast<size_t>(b) * N + (nd - 1));
+        for (int k = 0; k < m; ++k) {
+            if (tid == 0) {
+                const int nd = P.child_list[kb + k];
+                const int x = sh.tok[nd - 1];
                 int acc = 0;
                 if (x < 0 || x >= V) {
                     if (rank == 0 && P.status) atomicOr(P.status, SPEC_STATUS_TOKEN_RANGE);
                 } else {
-                    const int owner = x / S;
-                    const float ex = *cl.map_shared_rank(ev + (x - owner * S), owner);
-                    const double qx = static_cast<double>(__ldg(P.q + roff + x));
-                    if (qx == 0.0) {
+                    const float qx = sh.qx[k];
+                    if (qx == 0.0f) {
                         acc = 1;
                     } else {
-                        double r = static_cast<double>(ex) * invS - Tm * qx;
-                        r = r > 0.0 ? r : 0.0;
-                        const double u = static_cast<double>(__ldg(P.u_accept + static_cast<size_t>(b) * N + (nd - 1)));
-                        acc = u < r / (ST * qx);
+                        const float qS = qx * Sh;
+                        const float lhs = sh.ua[nd - 1] * (STh * qS);
+                        const float rhs = fmaf(-Tmh, qS, sh.ex[k]);
+                        acc = lhs < rhs;
                     }
                 }
                 sh.dec = acc;
             }
             __syncthreads();
-            const int acc = sh.dec;
-            __syncthreads();
-            if (acc) {
-                next = nd;
+            if (sh.dec) {  // uniform: every thread read it after the barrier
+                next = P.child_list[kb + k];
                 break;
             }
-            // rejected: p' <- norm(max(0, p' - q)), i.e. Tm <- Tm + ST and ST <- its mass
-            if (!qloaded) {
-                load_q(P, roff, lo, n, qv);
-                __syncthreads();
-                qloaded = true;
+            // rejected: Tm <- Tm + ST and ST <- the new residual's mass
+            float Tnh = Tmh, Tnl = Tml;
+            tf_add(Tnh, Tnl, STh, STl);
+            const float Tnf = Tnh;
+            float rh, rl;
+            {
+                float s0 = 0.0f, k0 = 0.0f, s1 = 0.0f, k1 = 0.0f, s2 = 0.0f, k2 = 0.0f, s3 = 0.0f, k3 = 0.0f;
+                int i = c0;
+                for (; i + 3 < c1; i += 4) {
+                    kadd(s0, k0, fmaxf(0.0f, fmaf(-Tnf, qv[i], ev[i] * pscale)));
+                    kadd(s1, k1, fmaxf(0.0f, fmaf(-Tnf, qv[i + 1], ev[i + 1] * pscale)));
+                    kadd(s2, k2, fmaxf(0.0f, fmaf(-Tnf, qv[i + 2], ev[i + 2] * pscale)));
+                    kadd(s3, k3, fmaxf(0.0f, fmaf(-Tnf, qv[i + 3], ev[i + 3] * pscale)));
+                }
+                for (; i < c1; ++i) kadd(s0, k0, fmaxf(0.0f, fmaf(-Tnf, qv[i], ev[i] * pscale)));
+                rh = s0;
+                rl = -k0;
+                tf_add(rh, rl, s1, -k1);
+                tf_add(rh, rl, s2, -k2);
+                tf_add(rh, rl, s3, -k3);
             }
-            const double Tn = Tm + ST;
-            const float Tnf = static_cast<float>(Tn);
-            s = 0.0f;
-            c = 0.0f;
-            for (int i = c0; i < c1; ++i) nadd(s, c, fmaxf(0.0f, fmaf(-Tnf, qv[i], ev[i] * invSf)));
-            const double rpart = block_sum(static_cast<double>(s) + static_cast<double>(c), sh);
-            double Sn = 0.0;
-            cluster_each(cl, sh, parity, rpart, 0.0, C, [&](int, double a, double) { Sn += a; });
-            if (Sn > 0.0) {  // a residual of no mass leaves p' as it is
-                Tm = Tn;
-                ST = Sn;
+            block_sum2(rh, rl, sh);
+            const float4 *rrow = cluster_exchange(cl, sh, parity, rank, make_float4(rh, rl, 0.0f, 0.0f), C);
+            float Snh = 0.0f, Snl = 0.0f;
+            for (int r = 0; r < C; ++r) tf_add(Snh, Snl, rrow[r].x, rrow[r].y);
+            if (Snh > 0.0f) {  // a residual of no mass leaves p' as it is
+                Tmh = Tnh;
+                Tml = Tnl;
+                STh = Snh;
+                STl = Snl;
             }
         }
         if (next < 0) {
-            // one draw from p' (weights e, or max(0, e/S - Tm q) after a
-            // rejection): the smallest column whose prefix sum exceeds
-            // t = u * (total); the prefix runs over CTAs in rank order, threads
-            // in thread order and columns in index order, all in the same
-            // compensated sums, so the total and the prefixes agree.
-            const bool resid = Tm > 0.0;
-            const float Tf = static_cast<float>(Tm);
-            s = 0.0f;
-            c = 0.0f;
+            // one draw from p' (p, or max(0, p - Tm q) after a rejection): the
+            // smallest column whose prefix exceeds t = u * total.  Prefixes run
+            // over CTAs in rank order, threads in thread order and columns in
+            // index order.  Every CTA finds the same CTA r* holding t from the
+            // exchanged totals; in r* the thread whose chunk holds t rescans it.
+            const bool resid = Tmh > 0.0f;
+            const float Tf = Tmh;
+            float s = 0.0f, k = 0.0f;
             int lastpos = -1;
             for (int i = c0; i < c1; ++i) {
-                const float w = resid ? fmaxf(0.0f, fmaf(-Tf, qv[i], ev[i] * invSf)) : ev[i];
-                nadd(s, c, w);
+                const float w = resid ? fmaxf(0.0f, fmaf(-Tf, qv[i], ev[i] * pscale)) : ev[i] * pscale;
+                kadd(s, k, w);
                 if (w > 0.0f) lastpos = lo + i;
             }
-            double btot = 0.0;
-            const double texcl = block_excl_scan(static_cast<double>(s) + static_cast<double>(c), &btot, sh);
-            double cexcl = 0.0, total = 0.0;
-            cluster_each(cl, sh, parity, btot, 0.0, C, [&](int r, double a, double) {
-                if (r < rank) cexcl += a;
-                total += a;
-            });
-            const double t = static_cast<double>(__ldg(P.u_sample + static_cast<size_t>(b) * rows + cur)) * total;
-            const double base = cexcl + texcl;
-            int cand = INT_MAX;
-            if (c1 > c0 && base <= t) {
-                float s2 = 0.0f, k2 = 0.0f;
-                for (int i = c0; i < c1; ++i) {
-                    const float w = resid ? fmaxf(0.0f, fmaf(-Tf, qv[i], ev[i] * invSf)) : ev[i];
-                    nadd(s2, k2, w);
-                    if (base + (static_cast<double>(s2) + static_cast<double>(k2)) > t) {
-                        cand = lo + i;
-                        break;
+            float exh, exl, inh, inl, th, tl;
+            block_scan2(s, -k, exh, exl, inh, inl, th, tl, sh);
+            const int clast = block_imax(lastpos, sh);
+            const float4 *trow =
+                cluster_exchange(cl, sh, parity, rank, make_float4(th, tl, __int_as_float(clast), 0.0f), C);
+            // t = u * total, then the first CTA whose running end exceeds t
+            float toth = 0.0f, totl = 0.0f;
+            for (int r = 0; r < C; ++r) tf_add(toth, totl, trow[r].x, trow[r].y);
+            const float u = __ldg(P.u_sample + static_cast<size_t>(b) * rows + cur);
+            float tth, ttl;
+            tf_mul(toth, totl, u, tth, ttl);
+            float ch = 0.0f, cl_ = 0.0f;  // running CTA prefix
+            int rstar = -1, rlast = -1;
+            float bh = 0.0f, bl = 0.0f;   // prefix before r*
+            for (int r = 0; r < C; ++r) {
+                if (__float_as_int(trow[r].z) >= 0) rlast = r;
+                float eh = ch, el = cl_;
+                tf_add(eh, el, trow[r].x, trow[r].y);
+                if (rstar < 0 && ((eh - tth) + (el - ttl)) > 0.0f) {
+                    rstar = r;
+                    bh = ch;
+                    bl = cl_;
+                }
+                ch = eh;
+                cl_ = el;
+            }
+            if (rstar < 0) rstar = rlast;  // t at or past the total after rounding: the last positive column
+            if (rank == rstar) {
+                if (tid == 0) sh.pick = -1;
+                __syncthreads();
+                // t relative to this CTA's first column (clamped at 0)
+                float trh = tth, trl = ttl;
+                tf_add(trh, trl, -bh, -bl);
+                if (trh < 0.0f) trh = trl = 0.0f;
+                const bool holds = c1 > c0 && ((exh - trh) + (exl - trl)) <= 0.0f && ((inh - trh) + (inl - trl)) > 0.0f;
+                if (holds) {
+                    float s2 = 0.0f, k2 = 0.0f;
+                    int cand = -1;
+                    for (int i = c0; i < c1; ++i) {
+                        const float w = resid ? fmaxf(0.0f, fmaf(-Tf, qv[i], ev[i] * pscale)) : ev[i] * pscale;
+                        kadd(s2, k2, w);
+                        if (w > 0.0f) {
+                            cand = lo + i;  // the last positive column so far: the answer if t is never passed
+                            float ph = exh, pl = exl;
+                            tf_add(ph, pl, s2, -k2);
+                            if (((ph - trh) + (pl - trl)) > 0.0f) break;
+                        }
                     }
+                    sh.pick = cand;
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    int pick = sh.pick;
+                    if (pick < 0) pick = __float_as_int(trow[rank].z);  // no thread holds t: this CTA's last positive
+                    if (pick < 0) pick = V - 1;
+                    P.out_tokens[static_cast<size_t>(b) * D1 + d] = pick;
                 }
             }
-            block_minmax(cand, lastpos, sh);
-            int pick = INT_MAX, last = -1;
-            cluster_each(cl, sh, parity, static_cast<double>(cand), static_cast<double>(lastpos), C,
-                         [&](int, double a, double l) {
-                             pick = min(pick, static_cast<int>(a));
-                             last = max(last, static_cast<int>(l));
-                         });
-            if (pick == INT_MAX) pick = last >= 0 ? last : V - 1;  // t at or past the total after rounding
             if (lead) {
                 int32_t *ot = P.out_tokens + static_cast<size_t>(b) * D1;
                 int32_t *op = P.out_path + static_cast<size_t>(b) * D1;
-                ot[d] = pick;
                 for (int i = d + 1; i < D1; ++i) {
                     ot[i] = -1;
                     op[i] = -1;
                 }
                 P.out_len[b] = d + 1;
+                if (rstar < 0) ot[d] = V - 1;  // nothing positive anywhere (a non-finite row)
             }
             break;
         }
         if (lead) {
-            P.out_tokens[static_cast<size_t>(b) * D1 + d] = __ldg(P.tokens + static_cast<size_t>(b) * N + (next - 1));
+            P.out_tokens[static_cast<size_t>(b) * D1 + d] = sh.tok[next - 1];
             P.out_path[static_cast<size_t>(b) * D1 + d + 1] = next;
         }
         ++d;
         cur = next;
-        cl.sync();  // every remote read of this row's e is done before any CTA loads the next row
+        __syncthreads();  // this node's reads of zs, qv and the child arrays end before the next copies
+    }
+    if (late) {
+        // a row copy outlived its wait: give it one more bounded wait so no
+        // copy lands in this CTA's shared memory after exit
+        wait_rows(&sh.bar, phase ^ 1u);
+        if (tid == 0 && P.status) atomicOr(P.status, SPEC_STATUS_WAIT_TIMEOUT);
     }
     if (bad && P.status) atomicOr(P.status, SPEC_STATUS_NONFINITE);
     cl.sync();  // keep this CTA's shared memory alive until the last remote read of it
@@ -438,8 +611,7 @@ spec_status_t ts_setup() {
     if (dev < 0 || dev >= 64) return fail(SPEC_ERR_UNSUPPORTED, "device index out of range%s");
     if (!g_ts_dev[dev].ok) {
         const void *k = reinterpret_cast<const void *>(ts::tree_sampled_kernel);
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(2 * sizeof(float) * ts::kSliceCap));
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ts::kSmemBudget);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "sampled tree kernel setup: %s", cudaGetErrorString(e));
         g_ts_dev[dev].ok = 1;
@@ -484,14 +656,22 @@ extern "C" spec_status_t spec_verify_tree_sampled(const void *target_logits, spe
     for (int c = 0; c <= N; ++c) cnt[c + 1] += cnt[c];
     for (int c = 0; c <= N + 1; ++c) P.child_off[c] = static_cast<uint16_t>(cnt[c]);
     for (int n = 1; n <= N; ++n) P.child_list[cnt[parent[n]]++] = static_cast<uint8_t>(n);  // index order per parent
-    int C = 1;
-    while (C < ts::kMaxCluster && round8((V + C - 1) / C) > ts::kSliceCap) C *= 2;
-    while (C < 8 && round8((V + C - 1) / C) > 4096) C *= 2;
-    const int S = round8((V + C - 1) / C);
-    if (S > ts::kSliceCap) return fail(SPEC_ERR_INVALID_ARG, "V is above 409600 (16 CTAs x 25600 columns)%s");
+    const int es = dtype == SPEC_BF16 ? 2 : 4;
+    const int cap = ts::slice_cap(es);
+    // fewest CTAs whose slices fit: a cluster per request must be resident
+    // at once, and small clusters pack the GPCs best
+    int C = (V + cap - 1) / cap;
+    if (C < 1) C = 1;
+    if (C > ts::kMaxCluster) C = ts::kMaxCluster;
+    int S = round8((V + C - 1) / C);
+    while (S > cap && C < ts::kMaxCluster) S = round8((V + ++C - 1) / C);
+    if (S > cap) {
+        char buf[96];
+        snprintf(buf, sizeof buf, " (at most %d for this dtype: 16 CTAs x %d columns)", ts::kMaxCluster * cap, cap);
+        return fail(SPEC_ERR_INVALID_ARG, "V is too large%s", buf);
+    }
     spec_status_t st = ts_setup();
     if (st != SPEC_OK) return st;
-    const int es = dtype == SPEC_BF16 ? 2 : 4;
     P.logits = target_logits;
     P.q = draft_probs;
     P.tokens = node_tokens;
@@ -509,13 +689,13 @@ extern "C" spec_status_t spec_verify_tree_sampled(const void *target_logits, spe
     P.max_depth = max_depth;
     P.slice = S;
     P.cluster = C;
-    P.vec_z = (static_cast<long long>(V) * es) % 16 == 0;
-    P.vec_q = V % 4 == 0;
+    P.zbulk = (static_cast<long long>(V) * es) % 16 == 0;
+    P.qbulk = V % 4 == 0;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(C));
     cfg.blockDim = dim3(ts::kThreads);
-    cfg.dynamicSmemBytes = 2 * sizeof(float) * static_cast<size_t>(S);
+    cfg.dynamicSmemBytes = static_cast<size_t>(S) * static_cast<size_t>(8 + es);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

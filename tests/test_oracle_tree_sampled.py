@@ -239,3 +239,18 @@ def test_argument_checks(oracle_mod):
     bad_parent[3] = 5
     with pytest.raises(ValueError):
         oracle_mod.verify_tree_sampled(c["z"], W.FP32, c["toks"], bad_parent, c["T"], c["ua"], c["us"], c["q"])
+
+
+def test_bench_bytes_from_path_match_the_oracle(oracle_mod):
+    """The benchmark derives a walk's algorithmic bytes from its path alone;
+    on the same walks that equals the oracle's own count."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    x = W.tree_sampled(seed=48, B=40, V=3001, children_per_level=(3, 2, 2), lam=0.5)
+    r = oracle_mod.verify_tree_sampled(x.logits, x.dtype, x.node_tokens, x.parent, x.temperature,
+                                       x.u_accept, x.u_sample, x.draft_probs)
+    for b in range(x.B):
+        got = bench.tree_sampled_bytes(x.parent, r["path"][b:b + 1], r["length"][b:b + 1], x.V, 2)
+        assert got == r["b_alg"][b], b
