@@ -51,6 +51,11 @@ def _bind(lib):
     lib.oracle_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P]
     lib.oracle_verify_tree_sampled.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, P]
     lib.oracle_verify_tree_sampled.restype = I
+    L = ctypes.c_int64
+    lib.oracle_prepare_next_step.argtypes = [P, I, P, P, P, I, I, I, I, I, P, P, L, L, P, P, P, P, P, P]
+    lib.oracle_prepare_next_step.restype = I
+    lib.oracle_compact_tree_kv.argtypes = [P, L, L, P, I, P, I, P, I, P]
+    lib.oracle_compact_tree_kv.restype = I
     lib.oracle_ngram_propose.restype = I
     return lib
 
@@ -160,6 +165,51 @@ def verify_tree_sampled(logits: np.ndarray, dtype: int, node_tokens: np.ndarray,
     if rc != 0:
         raise ValueError("oracle_verify_tree_sampled rejected its arguments")
     return out
+
+
+def prepare_next_step(out_tokens: np.ndarray, num_accepted: np.ndarray, positions: np.ndarray,
+                      block_table: np.ndarray, block_size: int, P_next: int, rows_per_req: int = 0,
+                      cu: Optional[np.ndarray] = None, hidden: Optional[np.ndarray] = None, pad: int = -1,
+                      lib=None) -> dict:
+    """Next-step inputs after verification.  Returns next_token [B],
+    next_position [B], next_slots [B, P_next] int64, last_row [B],
+    hidden_out [B, row] (when hidden is given) and status."""
+    lib = _load(lib)
+    ot = _c(out_tokens, np.int32)
+    B, stride = ot.shape
+    bt = _c(block_table, np.int32)
+    max_blocks = 0 if bt is None else bt.shape[1]
+    hid = None if hidden is None else np.ascontiguousarray(hidden)
+    row_bytes = 0 if hid is None else hid.reshape(hid.shape[0], -1).view(np.uint8).shape[1]
+    out = dict(next_token=np.empty(B, np.int32), next_position=np.empty(B, np.int32),
+               next_slots=np.empty((B, P_next), np.int64), last_row=np.empty(B, np.int32),
+               hidden_out=None if hid is None else np.empty((B,) + hid.shape[1:], hid.dtype),
+               status=np.zeros(1, np.int32))
+    rc = lib.oracle_prepare_next_step(
+        _ptr(ot), stride, _ptr(_c(num_accepted, np.int32)), _ptr(_c(positions, np.int32)), _ptr(bt), max_blocks,
+        int(block_size), B, int(P_next), int(rows_per_req), _ptr(_c(cu, np.int32)), _ptr(hid), int(row_bytes),
+        int(pad), _ptr(out["next_token"]), _ptr(out["next_position"]), _ptr(out["next_slots"]),
+        _ptr(out["last_row"]), _ptr(out["hidden_out"]), _ptr(out["status"]))
+    if rc != 0:
+        raise ValueError("oracle_prepare_next_step rejected its arguments")
+    return out
+
+
+def compact_tree_kv(kv: np.ndarray, slot_mapping: np.ndarray, path: np.ndarray, out_len: np.ndarray,
+                    lib=None) -> dict:
+    """Tree KV compaction on a copy of kv [num_slots, ...].  Returns kv, status."""
+    lib = _load(lib)
+    k = np.array(kv, copy=True, order="C")
+    num_slots = k.shape[0]
+    row_bytes = k.reshape(num_slots, -1).view(np.uint8).shape[1] if num_slots else 1
+    sm = _c(slot_mapping, np.int64)
+    pa = _c(path, np.int32)
+    st = np.zeros(1, np.int32)
+    rc = lib.oracle_compact_tree_kv(_ptr(k), num_slots, int(row_bytes), _ptr(sm), sm.shape[1], _ptr(pa),
+                                    pa.shape[1], _ptr(_c(out_len, np.int32)), sm.shape[0], _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle_compact_tree_kv rejected its arguments")
+    return dict(kv=k, status=st)
 
 
 def ngram_propose(tokens: np.ndarray, lengths: np.ndarray, n_min: int, n_max: int, k: int, lib=None) -> dict:

@@ -23,6 +23,10 @@
  *    rejected positions' slot_mapping entries become PADDING_SLOT_ID.
  *  - serving-book chapter, "acceptance rule preserving the output
  *    distribution": temperature 0 means greedy.
+ *  - vLLM EAGLE walkthrough, "slot mapping and KV-cache management" (the names
+ *    of the next-step preparation helpers) and the EAGLE-3 review, "EAGLE-3
+ *    inference" step 5 (keep only the accepted path's KV, then draft again
+ *    from the confirmed prefix): next-step inputs and tree KV compaction.
  *  - serving-book chapter, table of draft sources, row "n-gram lookup": find,
  *    in the prompt or the text generated so far, a span equal to the current
  *    ending and propose what follows it (no model).
@@ -652,5 +656,123 @@ int oracle_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, i
         if (out_match_end)
             out_match_end[b] = best_e;
     }
+    return 0;
+}
+
+/* -------------------------------------------------- next-step preparation -- */
+
+/* After verification of request b (row 0 at sequence position positions[b],
+ * rows 0..k at positions[b]..positions[b]+k, a = num_accepted[b] drafts
+ * accepted), the token emitted last, out_tokens[b][a], is the next step's
+ * first input, at position positions[b] + a + 1.  Readings (the pages give
+ * only the helpers' names): the next step writes P_next rows at positions
+ * next_position .. next_position + P_next - 1, whose KV slots come from the
+ * block table, slot = block_table[b][pos / block_size] * block_size +
+ * pos % block_size, or pad when pos / block_size is past the table or the
+ * entry is negative (status bit 1); the drafter's hidden-state input is the
+ * target's row of the last accepted position, flat row index
+ * row0(b) + a, row0(b) = b * rows_per_req (padded) or cu[b] + b (ragged);
+ * that row of hidden_in (row_bytes bytes) is copied to hidden_out[b]. */
+int oracle_prepare_next_step(const int32_t *out_tokens, int out_stride, const int32_t *num_accepted,
+                             const int32_t *positions, const int32_t *block_table, int max_blocks,
+                             int block_size, int B, int P_next, int rows_per_req, const int32_t *cu,
+                             const uint8_t *hidden_in, int64_t row_bytes, int64_t pad, int32_t *next_token,
+                             int32_t *next_position, int64_t *next_slots, int32_t *last_row,
+                             uint8_t *hidden_out, int32_t *status)
+{
+    if (B < 0 || out_stride < 1 || max_blocks < 0 || block_size < 1 || P_next < 0 || !out_tokens ||
+        !num_accepted || !positions || !next_token || !next_position)
+        return 1;
+    if (P_next > 0 && (!block_table || !next_slots))
+        return 1;
+    if (!cu && rows_per_req < 1)
+        return 1;
+    if (hidden_in && (!hidden_out || row_bytes < 1))
+        return 1;
+    int st = 0;
+    for (int b = 0; b < B; ++b) {
+        const int a = num_accepted[b];
+        if (a < 0 || a >= out_stride)
+            return 1;
+        next_token[b] = out_tokens[(size_t)b * out_stride + a];
+        const int64_t np = (int64_t)positions[b] + a + 1;
+        next_position[b] = (int32_t)np;
+        for (int j = 0; j < P_next; ++j) {
+            const int64_t pos = np + j;
+            const int64_t blk = pos / block_size;
+            int64_t slot = pad;
+            if (blk < max_blocks) {
+                const int32_t e = block_table[(size_t)b * max_blocks + blk];
+                if (e >= 0)
+                    slot = (int64_t)e * block_size + pos % block_size;
+                else
+                    st |= 1;
+            } else {
+                st |= 1;
+            }
+            next_slots[(size_t)b * P_next + j] = slot;
+        }
+        const int64_t r0 = cu ? (int64_t)cu[b] + b : (int64_t)b * rows_per_req;
+        const int64_t r = r0 + a;
+        if (last_row)
+            last_row[b] = (int32_t)r;
+        if (hidden_in)
+            memcpy(hidden_out + (size_t)b * (size_t)row_bytes, hidden_in + (size_t)r * (size_t)row_bytes,
+                   (size_t)row_bytes);
+    }
+    if (status)
+        *status |= st;
+    return 0;
+}
+
+/* Tree KV compaction: the accepted path root = n_0, n_1, ..., n_d
+ * (d = out_len[b] - 1) was verified with node n's KV in slot
+ * slot_mapping[b][n]; afterwards depth i of the path must sit where the chain
+ * keeps position i, slot_mapping[b][i].  Every destination slot receives the
+ * row its source slot held before the call (sources are read before any
+ * destination is written).  A source or destination outside [0, num_slots)
+ * is skipped with status bit 1. */
+int oracle_compact_tree_kv(uint8_t *kv, int64_t num_slots, int64_t row_bytes, const int64_t *slot_mapping,
+                           int slot_stride, const int32_t *path, int path_stride, const int32_t *out_len, int B,
+                           int32_t *status)
+{
+    if (B < 0 || num_slots < 0 || row_bytes < 1 || slot_stride < 1 || path_stride < 1 || !kv || !slot_mapping ||
+        !path || !out_len)
+        return 1;
+    int st = 0;
+    uint8_t *tmp = (uint8_t *)malloc((size_t)row_bytes * (size_t)path_stride);
+    int64_t *dst = (int64_t *)malloc(sizeof(int64_t) * (size_t)path_stride);
+    for (int b = 0; b < B; ++b) {
+        const int L = out_len[b];
+        if (L < 1 || L > path_stride || L > slot_stride) {
+            free(tmp);
+            free(dst);
+            return 1;
+        }
+        int nmove = 0;
+        for (int i = 1; i < L; ++i) {
+            const int node = path[(size_t)b * path_stride + i];
+            if (node < 0 || node >= slot_stride) {
+                st |= 1;
+                continue;
+            }
+            if (node == i)
+                continue;
+            const int64_t s_src = slot_mapping[(size_t)b * slot_stride + node];
+            const int64_t s_dst = slot_mapping[(size_t)b * slot_stride + i];
+            if (s_src < 0 || s_src >= num_slots || s_dst < 0 || s_dst >= num_slots) {
+                st |= 1;
+                continue;
+            }
+            memcpy(tmp + (size_t)nmove * (size_t)row_bytes, kv + (size_t)s_src * (size_t)row_bytes, (size_t)row_bytes);
+            dst[nmove++] = s_dst;
+        }
+        for (int i = 0; i < nmove; ++i)
+            memcpy(kv + (size_t)dst[i] * (size_t)row_bytes, tmp + (size_t)i * (size_t)row_bytes, (size_t)row_bytes);
+    }
+    free(tmp);
+    free(dst);
+    if (status)
+        *status |= st;
     return 0;
 }

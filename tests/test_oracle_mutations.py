@@ -137,6 +137,25 @@ def _tree_q_equal_p(O, lib):
     return ts.q_equal_p_mismatches(O, lib)
 
 
+def _next_step_bad(O, lib):
+    import test_oracle_next_step as ns
+    g = ns.golden_case()
+    r = O.prepare_next_step(g["out_tokens"], g["a"], g["pos"], g["bt"], 4, 3, rows_per_req=4, lib=lib)
+    return int((r["next_position"] != g["next_position"]).sum() + (r["next_slots"] != g["slots"]).any(axis=1).sum()
+               + (r["last_row"] != g["last_row"]).sum() + (r["next_token"] != g["next_token"]).sum())
+
+
+def _compaction_bad(O, lib):
+    import test_oracle_next_step as ns
+    parent = W.parents_in_order((4, 2, 2))
+    paths = np.array([[0, 2, 7, 16], [0, 3, 4, 13], [0, 1, 2, -1], [0, 4, 12, 28]], np.int32)
+    return ns.compaction_mismatches(O, paths, parent, lib=lib)
+
+
+_SNAPSHOT_LOOP = """        for (int i = 1; i < L; ++i) {
+            const int node = path[(size_t)b * path_stride + i];"""
+
+
 CASES = [
     ("residual_sign", "double d = p[j] - (double)qi[j];", "double d = (double)qi[j] - p[j];",
      lambda O, lib: _lossless(O, lib) < 1e-6),
@@ -174,6 +193,25 @@ CASES = [
      lambda O, lib: _tree_law(O, lib) < 1e-6),
     ("tree_sampled_uniform_index", "u_sample[(size_t)b * (size_t)(N + 1) + (size_t)c]",
      "u_sample[(size_t)b * (size_t)(N + 1)]", lambda O, lib: _tree_q_equal_p(O, lib) > 10),
+    ("next_position_no_bonus", "const int64_t np = (int64_t)positions[b] + a + 1;",
+     "const int64_t np = (int64_t)positions[b] + a;", lambda O, lib: _next_step_bad(O, lib) > 0),
+    ("next_block_index", "const int64_t blk = pos / block_size;", "const int64_t blk = (pos + 1) / block_size;",
+     lambda O, lib: _next_step_bad(O, lib) > 0),
+    ("next_last_row", "const int64_t r = r0 + a;", "const int64_t r = r0;", lambda O, lib: _next_step_bad(O, lib) > 0),
+    ("next_token_row", "next_token[b] = out_tokens[(size_t)b * out_stride + a];",
+     "next_token[b] = out_tokens[(size_t)b * out_stride + (a > 0 ? a - 1 : 0)];",
+     lambda O, lib: _next_step_bad(O, lib) > 0),
+    ("compaction_descending_in_place", _SNAPSHOT_LOOP,
+     """        for (int i = L - 1; i >= 1; --i) {
+            const int node = path[(size_t)b * path_stride + i];
+            if (node > 0 && node < slot_stride && node != i && slot_mapping[(size_t)b * slot_stride + node] >= 0)
+                memmove(kv + (size_t)slot_mapping[(size_t)b * slot_stride + i] * (size_t)row_bytes,
+                        kv + (size_t)slot_mapping[(size_t)b * slot_stride + node] * (size_t)row_bytes,
+                        (size_t)row_bytes);
+            continue;""", lambda O, lib: _compaction_bad(O, lib) > 0),
+    ("compaction_wrong_destination", "const int64_t s_dst = slot_mapping[(size_t)b * slot_stride + i];",
+     "const int64_t s_dst = slot_mapping[(size_t)b * slot_stride + i - 1];",
+     lambda O, lib: _compaction_bad(O, lib) > 0),
 ]
 
 
@@ -190,6 +228,8 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _tree_law(O, lib) > 0.01
     assert _tree_closed_form(O, lib) == 0
     assert _tree_q_equal_p(O, lib) == 0
+    assert _next_step_bad(O, lib) == 0
+    assert _compaction_bad(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
