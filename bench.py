@@ -551,7 +551,8 @@ def main():
 def others(sv, W, dev, dist, peak, args):
     """Secondary workloads (kernel-only device time): sampled chain, greedy
     tree, the k = 8, V = 152064 sampled sweep, the ragged greedy chain,
-    n-gram lookup drafting and the sampled tree."""
+    n-gram lookup drafting, the sampled tree, next-step preparation and tree
+    KV compaction."""
     import torch
     out = []
     # sampled chain, B=32 k=4 V=128256 T=0.7, lambda = 0.3
@@ -563,6 +564,7 @@ def others(sv, W, dev, dist, peak, args):
     out.append(_other_ragged(sv, W, dev, dist, peak))
     out.append(_other_ngram(sv, W, dev, dist, peak))
     out.append(_other_tree_sampled(sv, W, dev, dist, peak))
+    out.extend(_other_next_step(sv, W, dev, dist, peak))
     return out
 
 
@@ -847,6 +849,86 @@ def _other_tree_sampled(sv, W, dev, dist, peak, target_s=0.5):
             "kernel_us": us, "achieved_gbs_alg": ach, "frac_alg": ach / peak,
             "bytes_per_launch": {"algorithmic": b_alg, "dense_inputs": float(per_copy)},
             "mean_tokens_per_request": float(length.mean())}
+
+
+def _other_next_step(sv, W, dev, dist, peak, target_s=0.3):
+    """Post-verify work.  (1) Tree KV compaction: B = 16 requests, the 60-node
+    tree, one token's KV = 32 layers x (K, V) x 8 heads x 128 x bf16 = 128 KiB
+    a row; paths from the sampled-tree walks of the same tree; 8 slot maps over
+    a 4096-slot (512 MiB) cache rotate so consecutive launches touch different
+    rows.  (2) Next-step preparation for the greedy chain batch: B = 64, k = 5,
+    6 next slots from 64-block tables, 4096-wide bf16 hidden rows."""
+    import torch
+    res = []
+    # (1) compaction
+    x = W.tree_sampled(seed=17, B=16, V=4096)
+    p, t, n = sv.verify_tree_sampled(to_dev(x.logits, dev).view(torch.bfloat16), to_dev(x.draft_probs, dev),
+                                     to_dev(x.node_tokens, dev), x.parent, to_dev(x.temperature, dev),
+                                     to_dev(x.u_accept, dev), to_dev(x.u_sample, dev))
+    row = 32 * 2 * 8 * 128 * 2
+    num_slots = 4096
+    kv = torch.zeros((num_slots, row // 2), dtype=torch.bfloat16, device=dev)
+    g = np.random.default_rng(19)
+    nmap = 8
+    maps = [torch.from_numpy(g.permutation(num_slots)[:x.B * (x.N + 1)].reshape(x.B, x.N + 1).astype(np.int64)).to(dev)
+            for _ in range(nmap)]
+    torch.cuda.synchronize(dev)
+    lens = n.cpu().numpy()
+    moved = sum(int(np.sum(p.cpu().numpy()[b, 1:lens[b]] != np.arange(1, lens[b]))) for b in range(x.B))
+
+    gk = _graph_of(dev, lambda: [sv.compact_tree_kv(kv, maps[j], p, n) for j in range(nmap)])
+    us = _time_graph(gk, nmap, dev, dist, target_s)
+    b_alg = 2.0 * moved * row
+    res.append({"workload": "tree KV compaction B=16 N=60 (4,8,16,16,16), 128 KiB KV rows, %d rows moved" % moved,
+                "kernel_us": us, "achieved_gbs_alg": b_alg / (us * 1e-6) / 1e9,
+                "frac_alg": b_alg / (us * 1e-6) / 1e9 / peak, "bytes_per_launch": {"algorithmic": b_alg},
+                "note": "CUDA-graph replays of 8 launches, rotating slot maps"})
+    # (2) next-step preparation
+    B, k1, H = 64, 6, 4096
+    ot = torch.from_numpy(g.integers(0, 128256, size=(B, k1)).astype(np.int32)).to(dev)
+    na = torch.from_numpy(g.integers(0, k1, size=B).astype(np.int32)).to(dev)
+    pos = torch.from_numpy(g.integers(0, 900, size=B).astype(np.int32)).to(dev)
+    bt = torch.from_numpy(g.integers(0, 20000, size=(B, 64)).astype(np.int32)).to(dev)
+    hid = torch.zeros((B * k1, H), dtype=torch.bfloat16, device=dev)
+
+    gp = _graph_of(dev, lambda: [sv.prepare_next_step(ot, na, pos, bt, 16, k1, rows_per_req=k1, hidden=hid)
+                                 for _ in range(16)])
+    us = _time_graph(gp, 16, dev, dist, target_s)
+    b_alg = float(B * (2 * H * 2 + 4 * 4 + k1 * 8 + 4))
+    res.append({"workload": "next-step preparation B=64 k=5, 6 next slots, 4096-wide bf16 hidden rows",
+                "kernel_us": us, "achieved_gbs_alg": b_alg / (us * 1e-6) / 1e9,
+                "bytes_per_launch": {"algorithmic": b_alg},
+                "note": "CUDA-graph replays of 16 launches; 1.1 MB a launch, so launch latency dominates"})
+    return res
+
+
+def _graph_of(dev, fn):
+    """fn() enqueues work; warm it up on a side stream, then capture it."""
+    import torch
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _time_graph(g, launches_per_replay, dev, dist, target_s):
+    """Mean device time of one launch over graph replays (CUDA events)."""
+    class _C:
+        def run(self, steps, verify_only=False):
+            for _ in range(steps):
+                g.replay()
+    case = _C()
+    case.run(3)
+    ms = time_steps(case, 10, dev, dist)
+    n = max(10, int(10 * target_s / max(ms / 1e3, 1e-6)))
+    ms = time_steps(case, n, dev, dist)
+    return ms * 1e3 / (n * launches_per_replay)
 
 
 def tree_depth(parent):

@@ -69,6 +69,9 @@ typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype_t;
 #define SPEC_STATUS_BAD_OFFSETS 8  /* ragged chains: cu_num_draft_tokens not non-decreasing within
                                       [0, total_drafts] or a count above max_k (clamped; results of
                                       the requests involved undefined) */
+#define SPEC_STATUS_SLOT_RANGE 32  /* next-step preparation / KV compaction: a position past the block
+                                      table or a negative table entry (the slot is padded), or a KV slot
+                                      outside the cache (that row is not moved) */
 #define SPEC_STATUS_BAD_TEMPERATURE 16 /* sampled trees: a temperature that is not finite and > 0 (that
                                           request is walked with T = 1; greedy trees go through
                                           spec_verify_tree) */
@@ -225,6 +228,65 @@ spec_status_t spec_verify_tree_sampled(const void *target_logits, spec_dtype_t d
                                        const float *u_accept, const float *u_sample, int B, int N, int V,
                                        int max_depth, int32_t *out_path, int32_t *out_tokens, int32_t *out_len,
                                        int32_t *d_status, void *stream);
+
+/*
+ * Next-step preparation after verification (vLLM EAGLE walkthrough, "slot
+ * mapping and KV-cache management", which names the next-step helpers, and
+ * the EAGLE-3 review, "EAGLE-3 inference" step 5: drafting restarts from the
+ * confirmed prefix).  Request b verified rows 0..k at sequence positions
+ * positions[b]..positions[b]+k and accepted a = num_accepted[b] drafts.
+ *
+ *  out_tokens    [B, out_stride] int32 device: the verify step's output tokens.
+ *  num_accepted  [B] int32 device (for a tree: out_len - 1).  An a outside
+ *      [0, min(out_stride-1, k_b)] is clamped and sets SPEC_STATUS_BAD_OFFSETS
+ *      (k_b = rows_per_req - 1, or cu[b+1] - cu[b] when ragged).
+ *  positions     [B] int32 device: sequence position of row 0.
+ *  block_table   [B, max_blocks] int32 device (may be NULL when P_next == 0):
+ *      block ids of each request's KV cache, block_size slots a block.
+ *  rows_per_req / cu_num_draft_tokens: where request b's rows start in the
+ *      flat target rows: b * rows_per_req, or cu[b] + b when cu ([B+1] int32
+ *      device) is given.
+ *  hidden_in     [rows, row_bytes] device or NULL: the target's hidden states,
+ *      one row per verified position (all B * rows_per_req, or cu[B] + B, rows).
+ *  Outputs (device): next_token[b] = out_tokens[b][a]; next_position[b] =
+ *  positions[b] + a + 1; next_slots [B, P_next] int64: slot of position
+ *  next_position + j, block_table[b][pos / block_size] * block_size +
+ *  pos % block_size, or padding_slot_id past the table or for a negative
+ *  entry (SPEC_STATUS_SLOT_RANGE); last_row[b] (may be NULL) = the flat row of
+ *  the last accepted position, row0(b) + a; hidden_out [B, row_bytes] = that
+ *  row of hidden_in.
+ *  Sizes: B >= 0, out_stride >= 1, block_size >= 1, P_next >= 0.
+ */
+spec_status_t spec_prepare_next_step(const int32_t *out_tokens, int out_stride, const int32_t *num_accepted,
+                                     const int32_t *positions, const int32_t *block_table, int max_blocks,
+                                     int block_size, int B, int P_next, int rows_per_req,
+                                     const int32_t *cu_num_draft_tokens, const void *hidden_in, int64_t row_bytes,
+                                     int64_t padding_slot_id, int32_t *next_token, int32_t *next_position,
+                                     int64_t *next_slots, int32_t *last_row, void *hidden_out, int32_t *d_status,
+                                     void *stream);
+
+/*
+ * Tree KV compaction (EAGLE-3 review, "EAGLE-3 inference" step 5: only the
+ * accepted path's KV is kept).  After a tree verify whose node n wrote its KV
+ * row into slot slot_mapping[b][n], depth i of the accepted path
+ * (path[b][i], i = 1 .. out_len[b]-1) moves to slot_mapping[b][i], the slot
+ * of chain position i; every destination receives its source's row as it was
+ * before the call.  Afterwards the chain-mode slot fix-up with
+ * num_accepted = out_len - 1 describes the cache.
+ *
+ *  kv            [num_slots, row_bytes] device, 16-byte aligned, row_bytes a
+ *      multiple of 16 (one token's KV across the layers and heads it covers).
+ *  slot_mapping  [B, slot_stride] int64 device (slot_stride = N + 1).
+ *  path          [B, path_stride] int32 device, out_len [B] int32 device, as
+ *      spec_verify_tree / spec_verify_tree_sampled return them.  A path whose
+ *      node indices do not start at 0 and strictly increase leaves its request
+ *      untouched (SPEC_STATUS_BAD_OFFSETS); a slot outside [0, num_slots)
+ *      skips that row (SPEC_STATUS_SLOT_RANGE).
+ *  Sizes: B >= 0, 1 <= path_stride <= SPEC_MAX_ROWS.
+ */
+spec_status_t spec_compact_tree_kv(void *kv, int64_t num_slots, int64_t row_bytes, const int64_t *slot_mapping,
+                                   int slot_stride, const int32_t *path, int path_stride, const int32_t *out_len,
+                                   int B, int32_t *d_status, void *stream);
 
 /*
  * KV slot_mapping fix-up, in place on [B, P] int64 device memory.

@@ -23,13 +23,14 @@ from typing import Optional, Sequence, Tuple
 
 __all__ = ["verify_chain", "verify_tree", "fixup_slots", "tree_from_choices", "workspace_bytes",
            "SpecError", "PADDING_SLOT_ID", "STATUS_TOKEN_RANGE", "STATUS_NONFINITE",
-           "STATUS_WAIT_TIMEOUT", "STATUS_BAD_OFFSETS", "STATUS_BAD_TEMPERATURE", "verify_tree_sampled", "library_path", "load_library", "verify_chain_noalloc",
+           "STATUS_WAIT_TIMEOUT", "STATUS_BAD_OFFSETS", "STATUS_BAD_TEMPERATURE", "STATUS_SLOT_RANGE", "verify_tree_sampled", "prepare_next_step",
+           "compact_tree_kv", "library_path", "load_library", "verify_chain_noalloc",
            "verify_chain_ragged", "fixup_slots_ragged", "ngram_propose"]
 
 PADDING_SLOT_ID = -1
 SPEC_BF16, SPEC_FP32 = 0, 1
 STATUS_TOKEN_RANGE, STATUS_NONFINITE, STATUS_WAIT_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8
-STATUS_BAD_TEMPERATURE = 16
+STATUS_BAD_TEMPERATURE, STATUS_SLOT_RANGE = 16, 32
 MAX_ROWS = 256
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +80,9 @@ def load_library():
         lib.spec_ngram_propose.restype = I
         lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, P, Z, P]
         lib.spec_verify_tree_sampled.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P]
+        L = ctypes.c_int64
+        lib.spec_prepare_next_step.argtypes = [P, I, P, P, P, I, I, I, I, I, P, P, L, L, P, P, P, P, P, P, P]
+        lib.spec_compact_tree_kv.argtypes = [P, L, L, P, I, P, I, P, I, P, P]
         lib.spec_verify_tree.restype = I
         lib.spec_fixup_slots.argtypes = [P, I, I, P, P, I, ctypes.c_int64, P]
         lib.spec_fixup_slots.restype = I
@@ -420,6 +424,76 @@ def verify_tree_sampled(target_logits, draft_probs, node_tokens, parent: Sequenc
                                       _stream_handle(dev, stream))
     _check("spec_verify_tree_sampled", rc)
     return out_path, out_tokens, out_len
+
+
+def prepare_next_step(out_tokens, num_accepted, positions, block_table, block_size: int, P_next: int, *,
+                      rows_per_req: Optional[int] = None, cu_num_draft_tokens=None, hidden=None,
+                      padding_slot_id: int = PADDING_SLOT_ID, status=None, stream=None):
+    """Next-step inputs after verification (all CUDA tensors).
+
+    out_tokens [B, S] int32; num_accepted [B] int32 (out_len - 1 for trees);
+    positions [B] int32 (sequence position of row 0); block_table [B, M]
+    int32; hidden [rows, H] (any dtype) or None.  Returns (next_token [B],
+    next_position [B], next_slots [B, P_next] int64, last_row [B],
+    hidden_out [B, H] or None)."""
+    torch = _torch()
+    lib = load_library()
+    if out_tokens.dtype != torch.int32 or out_tokens.dim() != 2 or out_tokens.device.type != "cuda" \
+            or not out_tokens.is_contiguous():
+        raise ValueError("out_tokens must be a contiguous [B, S] int32 CUDA tensor")
+    B, stride = out_tokens.shape
+    dev = out_tokens.device
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    _need(positions, "positions", torch.int32, (B,), dev)
+    if block_table is None or block_table.dim() != 2:
+        raise ValueError("block_table must be a [B, max_blocks] int32 CUDA tensor")
+    _need(block_table, "block_table", torch.int32, (B, block_table.shape[1]), dev)
+    if cu_num_draft_tokens is not None:
+        _need(cu_num_draft_tokens, "cu_num_draft_tokens", torch.int32, (B + 1,), dev)
+        rpr = 0
+    else:
+        rpr = int(rows_per_req if rows_per_req is not None else stride)
+    row_bytes = 0
+    hidden_out = None
+    if hidden is not None:
+        if hidden.device != dev or not hidden.is_contiguous() or hidden.dim() < 2:
+            raise ValueError("hidden must be a contiguous [rows, ...] CUDA tensor on the same device")
+        row_bytes = hidden[0].numel() * hidden.element_size()
+        hidden_out = torch.empty((B,) + tuple(hidden.shape[1:]), dtype=hidden.dtype, device=dev)
+    mk = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+    next_token, next_position, last_row = mk((B,), torch.int32), mk((B,), torch.int32), mk((B,), torch.int32)
+    next_slots = mk((B, P_next), torch.int64)
+    rc = lib.spec_prepare_next_step(_ptr(out_tokens), stride, _ptr(num_accepted), _ptr(positions), _ptr(block_table),
+                                    block_table.shape[1], int(block_size), B, int(P_next), rpr,
+                                    _ptr(cu_num_draft_tokens), _ptr(hidden), int(row_bytes), int(padding_slot_id),
+                                    _ptr(next_token), _ptr(next_position), _ptr(next_slots), _ptr(last_row),
+                                    _ptr(hidden_out), _ptr(status), _stream_handle(dev, stream))
+    _check("spec_prepare_next_step", rc)
+    return next_token, next_position, next_slots, last_row, hidden_out
+
+
+def compact_tree_kv(kv, slot_mapping, path, out_len, *, status=None, stream=None):
+    """Tree KV compaction in place: kv [num_slots, ...] CUDA (rows a multiple of
+    16 bytes), slot_mapping [B, N+1] int64, path [B, D+1] int32, out_len [B]
+    int32 (as verify_tree / verify_tree_sampled return them)."""
+    torch = _torch()
+    lib = load_library()
+    if kv.device.type != "cuda" or not kv.is_contiguous() or kv.dim() < 1:
+        raise ValueError("kv must be a contiguous CUDA tensor [num_slots, ...]")
+    dev = kv.device
+    num_slots = kv.shape[0]
+    row_bytes = (kv[0].numel() * kv.element_size()) if num_slots else 16
+    if slot_mapping.dim() != 2 or path.dim() != 2:
+        raise ValueError("slot_mapping and path must be 2-D")
+    B = slot_mapping.shape[0]
+    _need(slot_mapping, "slot_mapping", torch.int64, tuple(slot_mapping.shape), dev)
+    _need(path, "path", torch.int32, (B, path.shape[1]), dev)
+    _need(out_len, "out_len", torch.int32, (B,), dev)
+    rc = lib.spec_compact_tree_kv(_ptr(kv), num_slots, int(row_bytes), _ptr(slot_mapping), slot_mapping.shape[1],
+                                  _ptr(path), path.shape[1], _ptr(out_len), B, _ptr(status),
+                                  _stream_handle(dev, stream))
+    _check("spec_compact_tree_kv", rc)
+    return kv
 
 
 def fixup_slots(slot_mapping, num_accepted=None, path=None, padding_slot_id: int = PADDING_SLOT_ID,

@@ -107,6 +107,29 @@ def test_tree_sampled_host_checks(lib):
         assert lib.spec_last_error() != b""
 
 
+def test_next_step_host_checks(lib):
+    def call(ot=0x1000, stride=4, na=0x2000, pos=0x3000, bt=0x4000, mb=4, bs=16, B=2, P=3, rpr=4, cu=None,
+             hid=None, rb=0, nt=0x5000, npos=0x6000, ns=0x7000):
+        return lib.spec_prepare_next_step(ot, stride, na, pos, bt, mb, bs, B, P, rpr, cu, hid, rb, -1, nt, npos,
+                                          ns, None, None, None, None)
+    for bad in (dict(B=-1), dict(stride=0), dict(mb=-1), dict(bs=0), dict(P=-1), dict(rpr=0), dict(ot=None),
+                dict(na=None), dict(pos=None), dict(nt=None), dict(npos=None), dict(bt=None), dict(ns=None),
+                dict(hid=0x8000, rb=0)):
+        assert call(**bad) == 1, bad
+        assert lib.spec_last_error() != b""
+    assert call(B=0) == 0
+
+
+def test_compact_host_checks(lib):
+    def call(kv=0x1000, ns=100, rb=64, sm=0x2000, ss=7, pa=0x3000, ps=4, ol=0x4000, B=2):
+        return lib.spec_compact_tree_kv(kv, ns, rb, sm, ss, pa, ps, ol, B, None, None)
+    for bad in (dict(B=-1), dict(ns=-1), dict(rb=8), dict(rb=40), dict(ss=0), dict(ps=0), dict(ps=257),
+                dict(kv=None), dict(sm=None), dict(pa=None), dict(ol=None), dict(kv=0x1008)):
+        assert call(**bad) == 1, bad
+        assert lib.spec_last_error() != b""
+    assert call(B=0) == 0 and call(ns=0) == 0
+
+
 def test_ngram_host_checks(lib):
     def call(B=2, Lmax=10, nmin=1, nmax=4, k=3, tok=0x1000, ln=0x2000, d=0x3000, c=0x4000):
         return lib.spec_ngram_propose(tok, ln, B, Lmax, nmin, nmax, k, d, c, None, None, None)
