@@ -42,7 +42,8 @@ METRIC = "verified draft positions/sec and achieved HBM GB/s vs GB300 peak (1 GP
 UNIT = "verified draft positions/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_chain_gb300", "csrc", "spec_verify.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_chain_gb300", "csrc", f)
+               for f in ("spec_verify.cu", "ptx.cuh")]
 
 
 # ------------------------------------------------------------------ setup --
@@ -108,8 +109,12 @@ def measured_peak():
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the sources the verify kernel is compiled from."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(name: str):
