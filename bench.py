@@ -43,7 +43,7 @@ UNIT = "verified draft positions/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_chain_gb300", "csrc", f)
-               for f in ("spec_verify.cu", "ptx.cuh")]
+               for f in ("spec_verify.cu", "ptx.cuh", "twofloat.cuh")]
 
 
 # ------------------------------------------------------------------ setup --

@@ -47,6 +47,7 @@
 
 #include "common.h"
 #include "ptx.cuh"
+#include "twofloat.cuh"
 #include "spec_verify.h"
 
 namespace sv {
@@ -84,15 +85,15 @@ static_assert(kResSlots % kEpilogueWarps == 0, "result slots must split evenly o
 enum Kind : int { kEnd = 0, kA = 1, kB = 2 };
 
 struct RowStat {
-    float m;      // row max of raw logits
+    float m;        // row max of raw logits
+    float Sh, Sl;   // sum_j 2^((z_j - m) * c2), two-float
     float pad;
-    double S;     // sum_j 2^((z_j - m) * c2)
 };
 
 struct Partial {  // result of one split of a row
     float v;      // greedy: max value; sampled: max logit m
     int32_t idx;  // greedy: row index of the first occurrence of v
-    double s;     // sampled: sum of 2^((z - m) c2) over the split
+    float sh, sl; // sampled: sum of 2^((z - m) c2) over the split, two-float
 };
 
 struct Params {
@@ -485,21 +486,6 @@ __device__ __forceinline__ float warp_sum_scatter(const float (&v)[N], int lane)
     return c;
 }
 
-__device__ __forceinline__ double warp_sum_d(double s) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    return s;
-}
-
-__device__ __forceinline__ double warp_incl_scan_d(double s, int lane) {
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        double o = __shfl_up_sync(0xffffffffu, s, off);
-        if (lane >= off) s += o;
-    }
-    return s;
-}
-
 // ------------------------------------------------------------ topology --
 __device__ __forceinline__ int parent_of(const Params &P, int n) { return P.tree ? P.parent[n] : n - 1; }
 __device__ __forceinline__ int depth_of(const Params &P, int n) { return P.tree ? P.depth[n] : n; }
@@ -572,57 +558,58 @@ struct BlockSource {
     float m, c2;
 };
 
-__device__ __forceinline__ double block_factor(const BlockSource &S, int beta) {
-    if (!S.bmax) return 1.0;
-    return static_cast<double>(ex2(__fmul_rn(__fsub_rn(__ldcg(S.bmax + beta), S.m), S.c2)));
+__device__ __forceinline__ float block_factor(const BlockSource &S, int beta) {
+    if (!S.bmax) return 1.0f;
+    return ex2(__fmul_rn(__fsub_rn(__ldcg(S.bmax + beta), S.m), S.c2));
 }
 
-__device__ __forceinline__ double block_weight(const BlockSource &S, int beta) {
-    return static_cast<double>(__ldcg(S.bsum + beta)) * block_factor(S, beta);
+__device__ __forceinline__ tf block_weight(const BlockSource &S, int beta) {
+    return tf_prod(__ldcg(S.bsum + beta), block_factor(S, beta));
 }
 
 // Warp-wide: total weight and the block holding t = u * total.  Returns the
 // total; beta/base receive the block and the weight before it (all lanes).
 // Lane l owns blocks [l*per, (l+1)*per); the lane whose range holds t is then
-// scanned by the whole warp, one block per lane.
-__device__ double locate_block(const BlockSource &S, int nblk, double u, int lane, int &beta, double &base) {
+// scanned by the whole warp, one block per lane.  Sums and prefixes are
+// two-float.
+__device__ tf locate_block(const BlockSource &S, int nblk, float u, int lane, int &beta, tf &base) {
     const int per = (nblk + 31) / 32;
     const int lo = lane * per;
     const int hi = min(nblk, lo + per);
-    double s = 0.0;
-    for (int i = lo; i < hi; ++i) s += block_weight(S, i);
-    const double incl = warp_incl_scan_d(s, lane);
-    const double excl = incl - s;
-    const double total = __shfl_sync(0xffffffffu, incl, 31);
-    const double t = u * total;
-    const unsigned over = __ballot_sync(0xffffffffu, incl > t && hi > lo);
-    const unsigned nonzero = __ballot_sync(0xffffffffu, s > 0.0);
+    tf s = tf_of(0.0f);
+    for (int i = lo; i < hi; ++i) s = tf_add(s, block_weight(S, i));
+    const tf incl = warp_incl_scan_tf(s, lane);
+    const tf excl = tf_add(incl, tf_neg(s));
+    const tf total = tf_shfl(incl, 31);
+    const tf t = tf_mulf(total, u);
+    const unsigned over = __ballot_sync(0xffffffffu, tf_gt(incl, t) && hi > lo);
+    const unsigned nonzero = __ballot_sync(0xffffffffu, s.h > 0.0f);
     const int L = over ? (__ffs(over) - 1) : (nonzero ? 31 - __clz(nonzero) : 0);
     const int Llo = L * per;
     const int Lhi = min(nblk, Llo + per);
-    const double Lexcl = __shfl_sync(0xffffffffu, excl, L);
+    const tf Lexcl = tf_shfl(excl, L);
     int bsel = -1;
-    double bbase = Lexcl;
+    tf bbase = Lexcl;
     int last_sel = -1;            // last block with weight seen (clamp when rounding leaves t past the end)
-    double last_base = Lexcl;
+    tf last_base = Lexcl;
     for (int c0 = Llo; c0 < Lhi && bsel < 0; c0 += 32) {
         const int i = c0 + lane;
-        const double w = (i < Lhi) ? block_weight(S, i) : 0.0;
-        const double wi = warp_incl_scan_d(w, lane);
-        const double run = bbase + (wi - w);
-        const unsigned cross = __ballot_sync(0xffffffffu, i < Lhi && w > 0.0 && run + w > t);
-        const unsigned pos = __ballot_sync(0xffffffffu, i < Lhi && w > 0.0);
+        const tf w = (i < Lhi) ? block_weight(S, i) : tf_of(0.0f);
+        const tf wi = warp_incl_scan_tf(w, lane);
+        const tf run = tf_add(bbase, tf_add(wi, tf_neg(w)));
+        const unsigned cross = __ballot_sync(0xffffffffu, i < Lhi && w.h > 0.0f && tf_gt(tf_add(run, w), t));
+        const unsigned pos = __ballot_sync(0xffffffffu, i < Lhi && w.h > 0.0f);
         if (cross) {
             const int q = __ffs(cross) - 1;
             bsel = c0 + q;
-            bbase = __shfl_sync(0xffffffffu, run, q);
+            bbase = tf_shfl(run, q);
         } else {
             if (pos) {
                 const int q = 31 - __clz(pos);
                 last_sel = c0 + q;
-                last_base = __shfl_sync(0xffffffffu, run, q);
+                last_base = tf_shfl(run, q);
             }
-            bbase += __shfl_sync(0xffffffffu, wi, 31);
+            bbase = tf_add(bbase, tf_shfl(wi, 31));
         }
     }
     if (bsel < 0) {
@@ -637,13 +624,13 @@ __device__ double locate_block(const BlockSource &S, int nblk, double u, int lan
 // Warp-wide scan inside block beta of row (b, row): the first element whose
 // running weight exceeds t.  residual == false: exp weights relative to the
 // block max, scaled by the block factor; residual == true: max(0, p - q).
-__device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, double base, double t,
+__device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, tf base, tf t,
                           bool residual, float invS, int lane) {
     const size_t rowz = in_row(P, b, row) * static_cast<size_t>(P.V);
     const int e0 = beta * kBlk + lane * 8;
     float w[8];
     const float nMc2 = neg_mc2(residual ? S.m : __ldcg(S.bmax + beta), S.c2);
-    double fac = residual ? 1.0 : block_factor(S, beta);
+    const float fac = residual ? 1.0f : block_factor(S, beta);
     const float *qrow =
         residual ? P.q + in_draft(P, b, row) * static_cast<size_t>(P.V) : nullptr;
 #pragma unroll
@@ -657,20 +644,20 @@ __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row,
         w[i] = wi;
     }
     const float s = lane_sum8(w);
-    double ls = static_cast<double>(s) * fac;
-    double incl = warp_incl_scan_d(ls, lane);
-    double lbase = base + (incl - ls);
-    unsigned hit = __ballot_sync(0xffffffffu, lbase + ls > t && s > 0.0f);
+    const tf ls = tf_prod(s, fac);
+    const tf incl = warp_incl_scan_tf(ls, lane);
+    const tf lbase = tf_add(base, tf_add(incl, tf_neg(ls)));
+    unsigned hit = __ballot_sync(0xffffffffu, tf_gt(tf_add(lbase, ls), t) && s > 0.0f);
     unsigned pos = __ballot_sync(0xffffffffu, s > 0.0f);
     int L = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : 0);
     int j = -1;
     if (lane == L) {
-        double acc = lbase;
+        tf acc = lbase;
         int last_pos = 0;
         for (int i = 0; i < 8; ++i) {
             if (w[i] > 0.0f) last_pos = i;
-            acc += static_cast<double>(w[i]) * fac;
-            if (hit && w[i] > 0.0f && acc > t) {
+            acc = tf_add(acc, tf_prod(w[i], fac));
+            if (hit && w[i] > 0.0f && tf_gt(acc, t)) {
                 j = i;
                 break;
             }
@@ -686,24 +673,21 @@ __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row,
 
 // Sample one token from row `row` of request b (warp-wide): residual weights
 // if `residual` (falling back to p when the residual has no mass), else p.
-__device__ int sample_row(const Params &P, int b, int row, bool residual, double u, int lane) {
+__device__ int sample_row(const Params &P, int b, int row, bool residual, float u, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + row;
     const float m = __ldcg(&P.rowstat[ri].m);
-    const double Srow = __ldcg(&P.rowstat[ri].S);
+    const float Sh = __ldcg(&P.rowstat[ri].Sh);
     const float c2 = kLog2e / __ldg(P.temperature + b);
     int beta;
-    double base;
+    tf base;
     if (residual) {
         BlockSource S{P.bsumB + static_cast<size_t>(b) * P.nblk, nullptr, m, c2};
-        double Z = locate_block(S, P.nblk, u, lane, beta, base);
-        if (Z > 0.0) {
-            float invS = static_cast<float>(1.0 / Srow);
-            return scan_block(P, S, b, row, beta, base, u * Z, true, invS, lane);
-        }
+        const tf Z = locate_block(S, P.nblk, u, lane, beta, base);
+        if (Z.h > 0.0f) return scan_block(P, S, b, row, beta, base, tf_mulf(Z, u), true, 1.0f / Sh, lane);
     }
     BlockSource S{P.bsumA + ri * P.nblk, P.bmaxA + ri * P.nblk, m, c2};
-    double tot = locate_block(S, P.nblk, u, lane, beta, base);
-    return scan_block(P, S, b, row, beta, base, u * tot, false, 0.0f, lane);
+    const tf tot = locate_block(S, P.nblk, u, lane, beta, base);
+    return scan_block(P, S, b, row, beta, base, tf_mulf(tot, u), false, 0.0f, lane);
 }
 
 // --------------------------------------------------- request finalisation --
@@ -765,7 +749,7 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
     bonus = __shfl_sync(0xffffffffu, bonus, 0);
     if (SMP && bonus) {
         const int a = Rb - 1;
-        double u = static_cast<double>(__ldg(P.u_sample + in_row(P, b, a)));
+        const float u = __ldg(P.u_sample + in_row(P, b, a));
         int t = sample_row(P, b, a, false, u, lane);
         if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = t;
     }
@@ -796,7 +780,7 @@ __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) 
 // accept test of node n+1 (xtok < 0: no child, or its token is out of range).
 template <bool SMP>
 __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
-                            double Srow, int xtok, float zx, float qx, float ux, int lane) {
+                            tf Srow, int xtok, float zx, float qx, float ux, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
     const int Rb = rows_of(P, b);
     uint32_t rejected = 0;   // sampled row with a child whose draft was rejected
@@ -807,11 +791,12 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
             rsv = kResolved | static_cast<uint32_t>(g);
             if (!isfinite(gmax)) set_status(P, SPEC_STATUS_NONFINITE);
         } else {
-            if (!isfinite(m) || !isfinite(Srow)) set_status(P, SPEC_STATUS_NONFINITE);
+            if (!isfinite(m) || !isfinite(Srow.h)) set_status(P, SPEC_STATUS_NONFINITE);
             RowStat st;
             st.m = m;
+            st.Sh = Srow.h;
+            st.Sl = Srow.l;
             st.pad = 0.0f;
-            st.S = Srow;
             P.rowstat[ri] = st;
             uint32_t acc = 0;
             if (n < Rb - 1) {
@@ -820,8 +805,9 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
                 } else if (qx == 0.0f) {
                     acc = 1;
                 } else {
-                    const double ph = static_cast<double>(ex2(__fmul_rn(__fsub_rn(zx, m), c2))) / Srow;
-                    acc = static_cast<double>(ux) < ph / static_cast<double>(qx);
+                    // u < p(x) / q(x) with p(x) = e(x) / S, multiplied through by q(x) S > 0
+                    const float ex = ex2(__fmul_rn(__fsub_rn(zx, m), c2));
+                    acc = ux * (qx * Srow.h) < ex;
                 }
                 rejected = acc == 0;
             }
@@ -1136,7 +1122,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             ++b_loaded;
             const size_t ri = static_cast<size_t>(b) * P.R + a;
             const float m = __ldcg(&P.rowstat[ri].m);
-            const double Srow = __ldcg(&P.rowstat[ri].S);
+            const float Sh = __ldcg(&P.rowstat[ri].Sh);
             const float c2 = kLog2e / __ldg(P.temperature + b);
             const size_t rowe = in_row(P, b, a) * static_cast<size_t>(P.V);
             const size_t qrowe = in_draft(P, b, a) * static_cast<size_t>(P.V);
@@ -1158,7 +1144,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     I.cnt = min(P.esb, P.V - e);
                     I.c2 = c2;
                     I.m = m;
-                    I.invS = static_cast<float>(1.0 / Srow);
+                    I.invS = 1.0f / Sh;
                     I.gz = P.logits + (rowe + e) * ES;
                     I.gq = reinterpret_cast<const uint8_t *>(P.q + qrowe + e);
                     const uint8_t *sz, *sq;
@@ -1739,7 +1725,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
         } else if (kind == kA) {
             const bool greedy = !SMP || (c2 == 0.0f);
             float um = 0.0f;
-            double uS = 0.0;
+            tf uS = tf_of(0.0f);
             if (greedy) {
                 warp_cand(v, grp);
                 if (P.esize == 2) {
@@ -1764,10 +1750,9 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
             } else {
                 // combine the consumer warps' (M_w, S_w) into the unit's (m, S)
                 um = warp_max(v);
-                double t = 0.0;
-                if (lane < kConsumerWarps && sw != 0.0f)
-                    t = static_cast<double>(sw) * static_cast<double>(ex2(__fmul_rn(__fsub_rn(v, um), c2)));
-                uS = warp_sum_d(t);
+                tf t = tf_of(0.0f);
+                if (lane < kConsumerWarps && sw != 0.0f) t = tf_prod(sw, ex2(__fmul_rn(__fsub_rn(v, um), c2)));
+                uS = warp_sum_tf(t);
             }
             const size_t ri = static_cast<size_t>(b) * P.R + n;
             if (P.ns == 1) {
@@ -1779,7 +1764,8 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                     Partial pr;
                     pr.v = greedy ? v : um;
                     pr.idx = grp;
-                    pr.s = uS;
+                    pr.sh = uS.h;
+                    pr.sl = uS.l;
                     P.partial[ri * P.ns + j] = pr;
                     // acq_rel: publishes the partial and the consumers' block data
                     old = atom_add_acqrel(P.row_ctr + ri, 1u);
@@ -1791,7 +1777,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                         float gv = -INFINITY;
                         int gg = -1;
                         float rm = 0.0f;
-                        double rS = 0.0;
+                        tf rS = tf_of(0.0f);
                         if (greedy) {
                             for (int q = lane; q < P.ns; q += 32) {
                                 const Partial *pp = P.partial + ri * P.ns + q;
@@ -1802,14 +1788,14 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                             float lm = -INFINITY;
                             for (int q = lane; q < P.ns; q += 32) lm = fmaxf(lm, __ldcg(&P.partial[ri * P.ns + q].v));
                             rm = warp_max(lm);
-                            double t = 0.0;
+                            tf t = tf_of(0.0f);
                             for (int q = lane; q < P.ns; q += 32) {
                                 const Partial *pp = P.partial + ri * P.ns + q;
-                                const double ps = __ldcg(&pp->s);
-                                if (ps != 0.0)
-                                    t += ps * static_cast<double>(ex2(__fmul_rn(__fsub_rn(__ldcg(&pp->v), rm), c2)));
+                                const tf ps{__ldcg(&pp->sh), __ldcg(&pp->sl)};
+                                if (ps.h != 0.0f)
+                                    t = tf_add(t, tf_mulf(ps, ex2(__fmul_rn(__fsub_rn(__ldcg(&pp->v), rm), c2))));
                             }
-                            rS = warp_sum_d(t);
+                            rS = warp_sum_tf(t);
                         }
                         resolve_row<SMP>(P, b, n, greedy, c2, gg, gv, rm, rS, xtok, zx, qx, ux, lane);
                     }
@@ -1825,7 +1811,7 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == static_cast<uint32_t>(P.ncb - 1)) {
                 __syncwarp();
-                double u = static_cast<double>(__ldg(P.u_sample + in_row(P, b, n)));
+                const float u = __ldg(P.u_sample + in_row(P, b, n));
                 int t = sample_row(P, b, n, true, u, lane);
                 if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + n] = t;
             }

@@ -259,10 +259,19 @@ __device__ bool wait_rows(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
-__device__ __forceinline__ float zval(const unsigned char *zs, bool bf16, int i) {
-    return bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t *>(zs)[i]) : reinterpret_cast<const float *>(zs)[i];
+// Logits 4g .. 4g+3 of this CTA's slice as fp32 (one 8- or 16-byte shared load).
+template <int ES>
+__device__ __forceinline__ float4 zgroup(const unsigned char *zs, int g) {
+    if constexpr (ES == 2) {
+        const uint2 v = reinterpret_cast<const uint2 *>(zs)[g];
+        return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    } else {
+        return reinterpret_cast<const float4 *>(zs)[g];
+    }
 }
 
+template <int ES>
 __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(128) unsigned char dyn[];
     __shared__ Shared sh;
@@ -272,17 +281,26 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
     const int b = static_cast<int>(blockIdx.x) / C;
     const int S = P.slice, V = P.V, N = P.N, D1 = P.max_depth + 1;
     const int tid = threadIdx.x;
-    const bool bf16 = P.bf16 != 0;
-    const int es = bf16 ? 2 : 4;
+    constexpr bool bf16 = ES == 2;
+    constexpr int es = ES;
     float *ev = reinterpret_cast<float *>(dyn);               // e of this CTA's columns
     float *qv = ev + S;                                       // q of this CTA's columns
     unsigned char *zs = dyn + 8 * static_cast<size_t>(S);     // logits of this CTA's columns, as stored
     const int lo = rank * S;
     const int n = max(0, min(S, V - lo));
-    // Thread t owns the contiguous chunk [t*E, t*E + E) of the CTA's columns;
-    // E is odd so that consecutive threads fall in different banks.
-    const int E = ((n + kThreads - 1) / kThreads) | 1;
-    const int c0 = min(n, tid * E), c1 = min(n, c0 + E);
+    // Columns n .. npad-1 are padding (logit -inf, q 0), so every pass runs
+    // over whole groups of four columns without masks.  The per-node passes
+    // give group g to thread g mod 512 (consecutive threads, consecutive
+    // groups: conflict-free, coalesced); the final draw gives thread t the
+    // contiguous groups [t*Eg, t*Eg + Eg), Eg odd so that the threads' 16-byte
+    // accesses fall in different banks, and its prefix runs in column order.
+    const int npad = (n + 7) & ~7;
+    const int ng = npad / 4;
+    const int Eg = ((ng + kThreads - 1) / kThreads) | 1;
+    const int g0 = min(ng, tid * Eg), g1 = min(ng, g0 + Eg);
+    const int c0 = 4 * g0, c1 = 4 * g1;
+    const float4 *ev4 = reinterpret_cast<const float4 *>(ev);
+    const float4 *qv4 = reinterpret_cast<const float4 *>(qv);
     const bool lead = rank == 0 && tid == 0;
     const size_t rows = static_cast<size_t>(N) + 1;
     // bulk parts of this CTA's slices (16-byte multiples); the rest by plain loads
@@ -334,6 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
         }
         if (m > 0)
             for (int i = static_cast<int>(qmain / 4) + tid; i < n; i += kThreads) qv[i] = __ldg(P.q + roff + lo + i);
+        for (int i = n + tid; i < npad; i += kThreads) {
+            if constexpr (bf16)
+                reinterpret_cast<uint16_t *>(zs)[i] = 0xff80u;  // bf16 -inf
+            else
+                reinterpret_cast<float *>(zs)[i] = -INFINITY;
+            qv[i] = 0.0f;
+        }
         for (int k = tid; k < m; k += kThreads) {
             const int x = sh.tok[P.child_list[kb + k] - 1];
             sh.qx[k] = (x >= 0 && x < V) ? __ldg(P.q + roff + x) : 0.0f;
@@ -348,47 +373,34 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
         // exchange gives M = max m_r, the scales f_r = 2^((m_r - M) c2) and
         // S = sum_r f_r * sum_r, so p = e * f_r / S on rank r
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-        {
-            int i = c0;
-            for (; i + 3 < c1; i += 4) {
-                const float z0 = zval(zs, bf16, i), z1 = zval(zs, bf16, i + 1);
-                const float z2 = zval(zs, bf16, i + 2), z3 = zval(zs, bf16, i + 3);
-                mx0 = fmaxf(mx0, z0);
-                mx1 = fmaxf(mx1, z1);
-                mx2 = fmaxf(mx2, z2);
-                mx3 = fmaxf(mx3, z3);
-                bad |= nonfinite(z0) | nonfinite(z1) | nonfinite(z2) | nonfinite(z3);
-            }
-            for (; i < c1; ++i) {
-                const float z = zval(zs, bf16, i);
-                mx0 = fmaxf(mx0, z);
-                bad |= nonfinite(z);
-            }
+        bool nan = false;
+        for (int g = tid; g < ng; g += kThreads) {
+            const float4 z = zgroup<ES>(zs, g);
+            mx0 = fmaxf(mx0, z.x);
+            mx1 = fmaxf(mx1, z.y);
+            mx2 = fmaxf(mx2, z.z);
+            mx3 = fmaxf(mx3, z.w);
+            nan |= (z.x != z.x) | (z.y != z.y) | (z.z != z.z) | (z.w != z.w);
         }
-        const float mr = block_max(fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)), sh);
+        const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        bad |= nan | (mt == INFINITY);
+        const float mr = block_max(mt, sh);
         const float mrs = mr == -INFINITY ? 0.0f : mr;  // an empty or all -inf slice contributes nothing
         float sh0, sl0;
         {
             float s0 = 0.0f, k0 = 0.0f, s1 = 0.0f, k1 = 0.0f, s2 = 0.0f, k2 = 0.0f, s3 = 0.0f, k3 = 0.0f;
-            int i = c0;
-            for (; i + 3 < c1; i += 4) {
-                const float e0 = ex2((zval(zs, bf16, i) - mrs) * c2);
-                const float e1 = ex2((zval(zs, bf16, i + 1) - mrs) * c2);
-                const float e2 = ex2((zval(zs, bf16, i + 2) - mrs) * c2);
-                const float e3 = ex2((zval(zs, bf16, i + 3) - mrs) * c2);
-                ev[i] = e0;
-                ev[i + 1] = e1;
-                ev[i + 2] = e2;
-                ev[i + 3] = e3;
-                kadd(s0, k0, e0);
-                kadd(s1, k1, e1);
-                kadd(s2, k2, e2);
-                kadd(s3, k3, e3);
-            }
-            for (; i < c1; ++i) {
-                const float e = ex2((zval(zs, bf16, i) - mrs) * c2);
-                ev[i] = e;
-                kadd(s0, k0, e);
+            for (int g = tid; g < ng; g += kThreads) {
+                const float4 z = zgroup<ES>(zs, g);
+                float4 e;
+                e.x = ex2((z.x - mrs) * c2);
+                e.y = ex2((z.y - mrs) * c2);
+                e.z = ex2((z.z - mrs) * c2);
+                e.w = ex2((z.w - mrs) * c2);
+                reinterpret_cast<float4 *>(ev)[g] = e;
+                kadd(s0, k0, e.x);
+                kadd(s1, k1, e.y);
+                kadd(s2, k2, e.z);
+                kadd(s3, k3, e.w);
             }
             sh0 = s0;
             sl0 = -k0;
@@ -464,14 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             float rh, rl;
             {
                 float s0 = 0.0f, k0 = 0.0f, s1 = 0.0f, k1 = 0.0f, s2 = 0.0f, k2 = 0.0f, s3 = 0.0f, k3 = 0.0f;
-                int i = c0;
-                for (; i + 3 < c1; i += 4) {
-                    kadd(s0, k0, fmaxf(0.0f, fmaf(-Tnf, qv[i], ev[i] * pscale)));
-                    kadd(s1, k1, fmaxf(0.0f, fmaf(-Tnf, qv[i + 1], ev[i + 1] * pscale)));
-                    kadd(s2, k2, fmaxf(0.0f, fmaf(-Tnf, qv[i + 2], ev[i + 2] * pscale)));
-                    kadd(s3, k3, fmaxf(0.0f, fmaf(-Tnf, qv[i + 3], ev[i + 3] * pscale)));
+                for (int g = tid; g < ng; g += kThreads) {
+                    const float4 e = ev4[g], q = qv4[g];
+                    kadd(s0, k0, fmaxf(0.0f, fmaf(-Tnf, q.x, e.x * pscale)));
+                    kadd(s1, k1, fmaxf(0.0f, fmaf(-Tnf, q.y, e.y * pscale)));
+                    kadd(s2, k2, fmaxf(0.0f, fmaf(-Tnf, q.z, e.z * pscale)));
+                    kadd(s3, k3, fmaxf(0.0f, fmaf(-Tnf, q.w, e.w * pscale)));
                 }
-                for (; i < c1; ++i) kadd(s0, k0, fmaxf(0.0f, fmaf(-Tnf, qv[i], ev[i] * pscale)));
                 rh = s0;
                 rl = -k0;
                 tf_add(rh, rl, s1, -k1);
@@ -499,10 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             const float Tf = Tmh;
             float s = 0.0f, k = 0.0f;
             int lastpos = -1;
-            for (int i = c0; i < c1; ++i) {
-                const float w = resid ? fmaxf(0.0f, fmaf(-Tf, qv[i], ev[i] * pscale)) : ev[i] * pscale;
-                kadd(s, k, w);
-                if (w > 0.0f) lastpos = lo + i;
+            for (int g = g0; g < g1; ++g) {
+                const float4 e = ev4[g];
+                const float4 q = resid ? qv4[g] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                const float w[4] = {fmaxf(0.0f, fmaf(-Tf, q.x, e.x * pscale)), fmaxf(0.0f, fmaf(-Tf, q.y, e.y * pscale)),
+                                    fmaxf(0.0f, fmaf(-Tf, q.z, e.z * pscale)), fmaxf(0.0f, fmaf(-Tf, q.w, e.w * pscale))};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    kadd(s, k, w[j]);
+                    if (w[j] > 0.0f) lastpos = lo + 4 * g + j;
+                }
             }
             float exh, exl, inh, inl, th, tl;
             block_scan2(s, -k, exh, exl, inh, inl, th, tl, sh);
@@ -542,14 +559,24 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                 if (holds) {
                     float s2 = 0.0f, k2 = 0.0f;
                     int cand = -1;
-                    for (int i = c0; i < c1; ++i) {
-                        const float w = resid ? fmaxf(0.0f, fmaf(-Tf, qv[i], ev[i] * pscale)) : ev[i] * pscale;
-                        kadd(s2, k2, w);
-                        if (w > 0.0f) {
-                            cand = lo + i;  // the last positive column so far: the answer if t is never passed
-                            float ph = exh, pl = exl;
-                            tf_add(ph, pl, s2, -k2);
-                            if (((ph - trh) + (pl - trl)) > 0.0f) break;
+                    bool done = false;
+                    for (int g = g0; g < g1 && !done; ++g) {
+                        const float4 e = ev4[g];
+                        const float4 q = resid ? qv4[g] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        const float w[4] = {fmaxf(0.0f, fmaf(-Tf, q.x, e.x * pscale)),
+                                            fmaxf(0.0f, fmaf(-Tf, q.y, e.y * pscale)),
+                                            fmaxf(0.0f, fmaf(-Tf, q.z, e.z * pscale)),
+                                            fmaxf(0.0f, fmaf(-Tf, q.w, e.w * pscale))};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (done) continue;
+                            kadd(s2, k2, w[j]);
+                            if (w[j] > 0.0f) {
+                                cand = lo + 4 * g + j;  // the last positive column so far: the answer if t is never passed
+                                float ph = exh, pl = exl;
+                                tf_add(ph, pl, s2, -k2);
+                                if (((ph - trh) + (pl - trl)) > 0.0f) done = true;
+                            }
                         }
                     }
                     sh.pick = cand;
@@ -610,9 +637,12 @@ spec_status_t ts_setup() {
     if (st != SPEC_OK) return st;
     if (dev < 0 || dev >= 64) return fail(SPEC_ERR_UNSUPPORTED, "device index out of range%s");
     if (!g_ts_dev[dev].ok) {
-        const void *k = reinterpret_cast<const void *>(ts::tree_sampled_kernel);
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ts::kSmemBudget);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        const void *ks[2] = {reinterpret_cast<const void *>(ts::tree_sampled_kernel<2>),
+                             reinterpret_cast<const void *>(ts::tree_sampled_kernel<4>)};
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+            e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, ts::kSmemBudget);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "sampled tree kernel setup: %s", cudaGetErrorString(e));
         g_ts_dev[dev].ok = 1;
     }
@@ -704,7 +734,8 @@ extern "C" spec_status_t spec_verify_tree_sampled(const void *target_logits, spe
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ts::tree_sampled_kernel, P);
+    cudaError_t e = P.bf16 ? cudaLaunchKernelEx(&cfg, ts::tree_sampled_kernel<2>, P)
+                           : cudaLaunchKernelEx(&cfg, ts::tree_sampled_kernel<4>, P);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "sampled tree launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
