@@ -87,8 +87,9 @@ struct Shared {
     int32_t tok[kMaxNodes];                // node tokens of this request (node n at n-1)
     float ua[kMaxNodes];                   // u_accept of this request (node n at n-1)
     float qx[kMaxNodes];                   // q_c(x) of the current node's children, in child order
-    float ex[kMaxNodes];                   // e(x) of the same, on its owner's scale
-    uint8_t exo[kMaxNodes];                // owner rank of each child's column
+    float fr[kMaxCluster];                 // per-rank scale 2^((m_r - M) c2) of the current row (thread 0)
+    float exb[2][kMaxNodes];               // e(x) of the same on the owner's own scale, pushed by the
+                                           // owner; double-buffered by the parity of the node's depth
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -386,9 +387,27 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
         bad |= nan | (mt == INFINITY);
         const float mr = block_max(mt, sh);
         const float mrs = mr == -INFINITY ? 0.0f : mr;  // an empty or all -inf slice contributes nothing
+        // the owner of each child's column pushes e(x) = 2^((z_x - m_r) c2) into
+        // every CTA before the exchange below, whose barrier makes it visible
+        for (int k = tid; k < m; k += kThreads) {
+            const int x = sh.tok[P.child_list[kb + k] - 1];
+            if (x >= lo && x < lo + n) {
+                const int xl = x - lo;
+                float z;
+                if constexpr (bf16)
+                    z = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(zs)[xl]) << 16);
+                else
+                    z = reinterpret_cast<const float *>(zs)[xl];
+                const float v = ex2((z - mrs) * c2);
+                for (int r = 0; r < C; ++r) *cl.map_shared_rank(&sh.exb[d & 1][k], r) = v;
+            }
+        }
+        // A thread's four running sums each take about ten terms (plain fp32,
+        // relative error near 1e-7); they and everything beyond the thread
+        // combine as two-float.
         float sh0, sl0;
         {
-            float s0 = 0.0f, k0 = 0.0f, s1 = 0.0f, k1 = 0.0f, s2 = 0.0f, k2 = 0.0f, s3 = 0.0f, k3 = 0.0f;
+            float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
             for (int g = tid; g < ng; g += kThreads) {
                 const float4 z = zgroup<ES>(zs, g);
                 float4 e;
@@ -397,16 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                 e.z = ex2((z.z - mrs) * c2);
                 e.w = ex2((z.w - mrs) * c2);
                 reinterpret_cast<float4 *>(ev)[g] = e;
-                kadd(s0, k0, e.x);
-                kadd(s1, k1, e.y);
-                kadd(s2, k2, e.z);
-                kadd(s3, k3, e.w);
+                s0 += e.x;
+                s1 += e.y;
+                s2 += e.z;
+                s3 += e.w;
             }
             sh0 = s0;
-            sl0 = -k0;
-            tf_add(sh0, sl0, s1, -k1);
-            tf_add(sh0, sl0, s2, -k2);
-            tf_add(sh0, sl0, s3, -k3);
+            sl0 = 0.0f;
+            tf_add(sh0, sl0, s1, 0.0f);
+            tf_add(sh0, sl0, s2, 0.0f);
+            tf_add(sh0, sl0, s3, 0.0f);
         }
         block_sum2(sh0, sl0, sh);
         const float4 *row = cluster_exchange(cl, sh, parity, rank, make_float4(mr, sh0, sl0, 0.0f), C);
@@ -416,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
         for (int r = 0; r < C; ++r) {
             const float f = row[r].x == -INFINITY ? 0.0f : ex2((row[r].x - M) * c2);
             if (r == rank) fmine = f;
+            if (tid == 0) sh.fr[r] = f;  // read only by thread 0, in the tests (the slots get reused)
             float ph, pl;
             tf_mul(row[r].y, row[r].z, f, ph, pl);
             tf_add(Sh, Sl, ph, pl);
@@ -426,19 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             Sl = 0.0f;
         }
         const float pscale = fmine / Sh;  // p = e * pscale on this rank
-        // (3) e(x) of the children, scaled to p(x) * S (every CTA is past step 2)
-        for (int k = tid; k < m; k += kThreads) {
-            const int x = sh.tok[P.child_list[kb + k] - 1];
-            float v = 0.0f;
-            if (x >= 0 && x < V) {
-                const int owner = x / S;
-                const float fo = row[owner].x == -INFINITY ? 0.0f : ex2((row[owner].x - M) * c2);
-                v = *cl.map_shared_rank(ev + (x - owner * S), owner) * fo;
-            }
-            sh.ex[k] = v;
-        }
-        __syncthreads();
-
         // (4) children in index order; p' is max(0, p - Tm q) / ST.  Child x is
         // accepted iff q(x) == 0 or u * ST * q(x) < p(x) - Tm * q(x), both
         // sides multiplied through by S > 0 (no division)
@@ -456,9 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                     if (qx == 0.0f) {
                         acc = 1;
                     } else {
+                        // e(x) * f_owner = p(x) * S
+                        const float fo = sh.fr[x / S];
                         const float qS = qx * Sh;
                         const float lhs = sh.ua[nd - 1] * (STh * qS);
-                        const float rhs = fmaf(-Tmh, qS, sh.ex[k]);
+                        const float rhs = fmaf(-Tmh, qS, sh.exb[d & 1][k] * fo);
                         acc = lhs < rhs;
                     }
                 }
@@ -475,19 +484,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             const float Tnf = Tnh;
             float rh, rl;
             {
-                float s0 = 0.0f, k0 = 0.0f, s1 = 0.0f, k1 = 0.0f, s2 = 0.0f, k2 = 0.0f, s3 = 0.0f, k3 = 0.0f;
+                float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
                 for (int g = tid; g < ng; g += kThreads) {
                     const float4 e = ev4[g], q = qv4[g];
-                    kadd(s0, k0, fmaxf(0.0f, fmaf(-Tnf, q.x, e.x * pscale)));
-                    kadd(s1, k1, fmaxf(0.0f, fmaf(-Tnf, q.y, e.y * pscale)));
-                    kadd(s2, k2, fmaxf(0.0f, fmaf(-Tnf, q.z, e.z * pscale)));
-                    kadd(s3, k3, fmaxf(0.0f, fmaf(-Tnf, q.w, e.w * pscale)));
+                    s0 += fmaxf(0.0f, fmaf(-Tnf, q.x, e.x * pscale));
+                    s1 += fmaxf(0.0f, fmaf(-Tnf, q.y, e.y * pscale));
+                    s2 += fmaxf(0.0f, fmaf(-Tnf, q.z, e.z * pscale));
+                    s3 += fmaxf(0.0f, fmaf(-Tnf, q.w, e.w * pscale));
                 }
                 rh = s0;
-                rl = -k0;
-                tf_add(rh, rl, s1, -k1);
-                tf_add(rh, rl, s2, -k2);
-                tf_add(rh, rl, s3, -k3);
+                rl = 0.0f;
+                tf_add(rh, rl, s1, 0.0f);
+                tf_add(rh, rl, s2, 0.0f);
+                tf_add(rh, rl, s3, 0.0f);
             }
             block_sum2(rh, rl, sh);
             const float4 *rrow = cluster_exchange(cl, sh, parity, rank, make_float4(rh, rl, 0.0f, 0.0f), C);
