@@ -76,6 +76,7 @@ struct Params {
 
 struct Shared {
     uint64_t bar;                          // the current node's row copies
+    uint64_t xbar[2];                      // cluster exchanges, by exchange parity
     float4 slot[2][kMaxCluster];           // pushed by every rank, double-buffered by exchange parity
     float ws[kWarps], wc[kWarps];          // warp partials (two-float)
     float wxs[kWarps], wxc[kWarps];        // warp exclusive prefixes (two-float, final draw)
@@ -234,19 +235,70 @@ __device__ __forceinline__ void block_scan2(float s, float c, float &exh, float 
     tl = sh.tot[1];
 }
 
-// Every CTA pushes its float4 into slot[parity][its rank] of every CTA of the
-// cluster (threads 0..C-1, one remote store each), then one cluster barrier;
-// afterwards every thread reads the C local slots.  A slot is rewritten only
-// after every CTA has passed the barrier that follows its last read (all of
-// this CTA's threads arrive at the next barrier only after reading), so one
-// barrier per exchange suffices.  Returns the slot row to read.
-__device__ __forceinline__ const float4 *cluster_exchange(cg::cluster_group &cl, Shared &sh, int &parity, int rank,
-                                                          float4 v, int C) {
-    if (static_cast<int>(threadIdx.x) < C) *cl.map_shared_rank(&sh.slot[parity][rank], static_cast<int>(threadIdx.x)) = v;
-    cl.sync();
-    const float4 *row = sh.slot[parity];
-    parity ^= 1;
-    return row;
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t local, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// Remote shared-memory stores that complete bytes on the destination CTA's
+// mbarrier (the destination waits on its own barrier; no cluster barrier).
+__device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_f1(uint32_t dst, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+                 "r"(__float_as_uint(v)), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Exchange number xk: every CTA sends its float4 into slot[xk & 1][its rank]
+// of every CTA (threads 0..C-1, one st.async each) and waits on its own
+// barrier xbar[xk & 1] (phase (xk >> 1) & 1) for C such stores plus `extra`
+// bytes of other pushes tied to this exchange; then every thread reads the C
+// local slots.  A slot or barrier phase is reused two exchanges later: a CTA
+// sends exchange xk + 2 only after receiving every CTA's exchange xk + 1, and
+// every CTA passes a block barrier between reading exchange xk and sending
+// xk + 1, so nothing lands before it has been read.  The wait is bounded;
+// after one time-out the CTA stops waiting (late) and its results are
+// undefined (the caller reports SPEC_STATUS_WAIT_TIMEOUT).
+__device__ __forceinline__ const float4 *cluster_exchange(Shared &sh, int &xk, int rank, float4 v, int C, uint32_t extra,
+                                                          bool &late) {
+    const int p = xk & 1;
+    if (threadIdx.x == 0) mbar_expect_tx(&sh.xbar[p], 16u * static_cast<uint32_t>(C) + extra);
+    if (static_cast<int>(threadIdx.x) < C) {
+        const int r = static_cast<int>(threadIdx.x);
+        st_async_f4(mapa_u32(smem_u32(&sh.slot[p][rank]), r), v, mapa_u32(smem_u32(&sh.xbar[p]), r));
+    }
+    if (!late) {
+        const uint32_t ph = static_cast<uint32_t>(xk >> 1) & 1u;
+        if (!mbar_try_wait_cluster(&sh.xbar[p], ph)) {
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait_cluster(&sh.xbar[p], ph)) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    late = true;
+                    break;
+                }
+            }
+        }
+    }
+    ++xk;
+    return sh.slot[p];
 }
 
 __device__ __forceinline__ bool nonfinite(float f) { return (f != f) || f == INFINITY; }
@@ -307,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
     // bulk parts of this CTA's slices (16-byte multiples); the rest by plain loads
     const uint32_t zmain = P.zbulk ? static_cast<uint32_t>((n * es) & ~15) : 0u;
     const uint32_t qmain = P.qbulk ? static_cast<uint32_t>((n * 4) & ~15) : 0u;
-    int parity = 0;
+    int xk = 0;          // cluster exchanges so far
     uint32_t phase = 0;
     bool bad = false, late = false;
 
@@ -317,6 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
     }
     if (tid == 0) {
         mbar_init(&sh.bar, 1);
+        mbar_init(&sh.xbar[0], 1);
+        mbar_init(&sh.xbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
     float T = __ldg(P.temperature + b);
@@ -326,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
     }
     const float c2 = kLog2e / T;
     if (lead) P.out_path[static_cast<size_t>(b) * D1] = 0;
-    __syncthreads();
+    cl.sync();  // every CTA's barriers exist before anyone pushes into them
 
     int cur = 0, d = 0;
     for (;;) {
@@ -388,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
         const float mr = block_max(mt, sh);
         const float mrs = mr == -INFINITY ? 0.0f : mr;  // an empty or all -inf slice contributes nothing
         // the owner of each child's column pushes e(x) = 2^((z_x - m_r) c2) into
-        // every CTA before the exchange below, whose barrier makes it visible
+        // every CTA, completing on the barrier of the exchange below
         for (int k = tid; k < m; k += kThreads) {
             const int x = sh.tok[P.child_list[kb + k] - 1];
             if (x >= lo && x < lo + n) {
@@ -399,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                 else
                     z = reinterpret_cast<const float *>(zs)[xl];
                 const float v = ex2((z - mrs) * c2);
-                for (int r = 0; r < C; ++r) *cl.map_shared_rank(&sh.exb[d & 1][k], r) = v;
+                const uint32_t dl = smem_u32(&sh.exb[d & 1][k]), bl = smem_u32(&sh.xbar[xk & 1]);
+                for (int r = 0; r < C; ++r) st_async_f1(mapa_u32(dl, r), v, mapa_u32(bl, r));
             }
         }
         // A thread's four running sums each take about ten terms (plain fp32,
@@ -428,7 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             tf_add(sh0, sl0, s3, 0.0f);
         }
         block_sum2(sh0, sl0, sh);
-        const float4 *row = cluster_exchange(cl, sh, parity, rank, make_float4(mr, sh0, sl0, 0.0f), C);
+        uint32_t nin = 0;  // children with a column: each CTA receives one 4-byte push for each
+        for (int k = 0; k < m; ++k) {
+            const int x = sh.tok[P.child_list[kb + k] - 1];
+            nin += (x >= 0 && x < V) ? 1u : 0u;
+        }
+        const float4 *row = cluster_exchange(sh, xk, rank, make_float4(mr, sh0, sl0, 0.0f), C, 4u * nin, late);
         float M = -INFINITY;
         for (int r = 0; r < C; ++r) M = fmaxf(M, row[r].x);
         float Sh = 0.0f, Sl = 0.0f, fmine = 0.0f;
@@ -499,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                 tf_add(rh, rl, s3, 0.0f);
             }
             block_sum2(rh, rl, sh);
-            const float4 *rrow = cluster_exchange(cl, sh, parity, rank, make_float4(rh, rl, 0.0f, 0.0f), C);
+            const float4 *rrow = cluster_exchange(sh, xk, rank, make_float4(rh, rl, 0.0f, 0.0f), C, 0u, late);
             float Snh = 0.0f, Snl = 0.0f;
             for (int r = 0; r < C; ++r) tf_add(Snh, Snl, rrow[r].x, rrow[r].y);
             if (Snh > 0.0f) {  // a residual of no mass leaves p' as it is
@@ -534,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             block_scan2(s, -k, exh, exl, inh, inl, th, tl, sh);
             const int clast = block_imax(lastpos, sh);
             const float4 *trow =
-                cluster_exchange(cl, sh, parity, rank, make_float4(th, tl, __int_as_float(clast), 0.0f), C);
+                cluster_exchange(sh, xk, rank, make_float4(th, tl, __int_as_float(clast), 0.0f), C, 0u, late);
             // t = u * total, then the first CTA whose running end exceeds t
             float toth = 0.0f, totl = 0.0f;
             for (int r = 0; r < C; ++r) tf_add(toth, totl, trow[r].x, trow[r].y);
@@ -619,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
         __syncthreads();  // this node's reads of zs, qv and the child arrays end before the next copies
     }
     if (late) {
-        // a row copy outlived its wait: give it one more bounded wait so no
-        // copy lands in this CTA's shared memory after exit
+        // a row copy or an exchange outlived its wait: one more bounded wait
+        // for the last row copy, so no copy lands here after exit
         wait_rows(&sh.bar, phase ^ 1u);
         if (tid == 0 && P.status) atomicOr(P.status, SPEC_STATUS_WAIT_TIMEOUT);
     }
