@@ -42,6 +42,7 @@ METRIC = "verified draft positions/sec and achieved HBM GB/s vs GB300 peak (1 GP
 UNIT = "verified draft positions/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+OTHER_NAMES = ["sampled_chain", "sweep", "greedy_tree", "ragged", "ngram", "sampled_tree", "next_step"]
 KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_chain_gb300", "csrc", f)
                for f in ("spec_verify.cu", "ptx.cuh", "twofloat.cuh")]
 
@@ -57,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--only", choices=OTHER_NAMES, default=None,
+                    help="run just this secondary workload (kernel-only timing) and print its JSON")
     ap.add_argument("--sweep-b", type=int, default=64, help="batch of the secondary sweep workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the baseline leg")
     ap.add_argument("--quick", action="store_true",
@@ -474,6 +477,11 @@ def main():
     torch.cuda.set_device(dev)
     dist = init_dist(world, True)
     sv.load_library()
+    if args.only:
+        res = others(sv, W, dev, dist, measured_peak()[0], args)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "also": res}))
+        return 0
 
     x = workload_default()
     case = ChainCase(sv, x, dev, with_fixup=True)
@@ -554,22 +562,29 @@ def main():
 
 
 def others(sv, W, dev, dist, peak, args):
-    """Secondary workloads (kernel-only device time): sampled chain, greedy
-    tree, the k = 8, V = 152064 sampled sweep, the ragged greedy chain,
-    n-gram lookup drafting, the sampled tree, next-step preparation and tree
-    KV compaction."""
-    import torch
+    """Secondary workloads (kernel-only device time): sampled chain, the k = 8,
+    V = 152064 sampled sweep, greedy tree, the ragged greedy chain, n-gram
+    lookup drafting, the sampled tree, next-step preparation and tree KV
+    compaction (or only the one --only names)."""
+    want = lambda name: args.only is None or args.only == name
     out = []
-    # sampled chain, B=32 k=4 V=128256 T=0.7, lambda = 0.3
-    x = W.chain_sampled(seed=3, B=32, k=4, V=128256, temperature=0.7, lam=0.3)
-    out.append(_other_chain(sv, x, dev, dist, peak, "sampled chain B=32 k=4 V=128256 T=0.7 lambda=0.3 (Zipf)"))
-    x = W.chain_sampled(seed=5, B=args.sweep_b, k=8, V=152064, temperature=1.0, lam=0.3)
-    out.append(_other_chain(sv, x, dev, dist, peak, "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % args.sweep_b))
-    out.append(_other_tree(sv, W, dev, dist, peak))
-    out.append(_other_ragged(sv, W, dev, dist, peak))
-    out.append(_other_ngram(sv, W, dev, dist, peak))
-    out.append(_other_tree_sampled(sv, W, dev, dist, peak))
-    out.extend(_other_next_step(sv, W, dev, dist, peak))
+    if want("sampled_chain"):
+        x = W.chain_sampled(seed=3, B=32, k=4, V=128256, temperature=0.7, lam=0.3)
+        out.append(_other_chain(sv, x, dev, dist, peak, "sampled chain B=32 k=4 V=128256 T=0.7 lambda=0.3 (Zipf)"))
+    if want("sweep"):
+        x = W.chain_sampled(seed=5, B=args.sweep_b, k=8, V=152064, temperature=1.0, lam=0.3)
+        out.append(_other_chain(sv, x, dev, dist, peak,
+                                "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % args.sweep_b))
+    if want("greedy_tree"):
+        out.append(_other_tree(sv, W, dev, dist, peak))
+    if want("ragged"):
+        out.append(_other_ragged(sv, W, dev, dist, peak))
+    if want("ngram"):
+        out.append(_other_ngram(sv, W, dev, dist, peak))
+    if want("sampled_tree"):
+        out.append(_other_tree_sampled(sv, W, dev, dist, peak))
+    if want("next_step"):
+        out.extend(_other_next_step(sv, W, dev, dist, peak))
     return out
 
 
