@@ -558,14 +558,20 @@ struct BlockSource {
     float m, c2;
 };
 
+// 2^((M_beta - m) c2) for a block maximum M_beta (exp weights), 1 for residuals.
+__device__ __forceinline__ float block_factor_of(const BlockSource &S, float bm) {
+    return S.bmax ? ex2(__fmul_rn(__fsub_rn(bm, S.m), S.c2)) : 1.0f;
+}
+
 __device__ __forceinline__ float block_factor(const BlockSource &S, int beta) {
-    if (!S.bmax) return 1.0f;
-    return ex2(__fmul_rn(__fsub_rn(__ldcg(S.bmax + beta), S.m), S.c2));
+    return block_factor_of(S, S.bmax ? __ldcg(S.bmax + beta) : 0.0f);
 }
 
 __device__ __forceinline__ tf block_weight(const BlockSource &S, int beta) {
     return tf_prod(__ldcg(S.bsum + beta), block_factor(S, beta));
 }
+
+constexpr int kLocBatch = 16;   // block sums a lane loads at once (one round trip at V = 128256)
 
 // Warp-wide: total weight and the block holding t = u * total.  Returns the
 // total; beta/base receive the block and the weight before it (all lanes).
@@ -576,8 +582,21 @@ __device__ tf locate_block(const BlockSource &S, int nblk, float u, int lane, in
     const int per = (nblk + 31) / 32;
     const int lo = lane * per;
     const int hi = min(nblk, lo + per);
+    // the lane's block sums and maxima are loaded kLocBatch at a time
+    // (independent loads in flight together), then added in block order
     tf s = tf_of(0.0f);
-    for (int i = lo; i < hi; ++i) s = tf_add(s, block_weight(S, i));
+    for (int i0 = lo; i0 < hi; i0 += kLocBatch) {
+        float bs[kLocBatch], bm[kLocBatch];
+#pragma unroll
+        for (int j = 0; j < kLocBatch; ++j) {
+            const int i = i0 + j;
+            bs[j] = i < hi ? __ldcg(S.bsum + i) : 0.0f;
+            bm[j] = (S.bmax && i < hi) ? __ldcg(S.bmax + i) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kLocBatch; ++j)
+            if (i0 + j < hi) s = tf_add(s, tf_prod(bs[j], block_factor_of(S, bm[j])));
+    }
     const tf incl = warp_incl_scan_tf(s, lane);
     const tf excl = tf_add(incl, tf_neg(s));
     const tf total = tf_shfl(incl, 31);

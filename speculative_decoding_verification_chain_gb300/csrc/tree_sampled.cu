@@ -40,6 +40,7 @@
 #include "common.h"
 #include "ptx.cuh"
 #include "spec_verify.h"
+#include "twofloat.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -112,28 +113,18 @@ __device__ __forceinline__ void kadd(float &s, float &c, float v) {
     s = t;
 }
 
-// s + e == a + b exactly (Knuth's TwoSum).
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-    s = a + b;
-    const float bb = s - a;
-    e = (a - (s - bb)) + (b - bb);
-}
-
-// (hi, lo) += (bh, bl) as two-float numbers (about 44 significant bits).
+// Two-float helpers on split (hi, lo) registers, over the shared two-float
+// arithmetic.
 __device__ __forceinline__ void tf_add(float &hi, float &lo, float bh, float bl) {
-    float s, e;
-    two_sum(hi, bh, s, e);
-    e += lo + bl;
-    hi = s + e;
-    lo = e - (hi - s);
+    const tf r = sv::tf_add(tf{hi, lo}, tf{bh, bl});
+    hi = r.h;
+    lo = r.l;
 }
 
-// (hi, lo) = (ah, al) * f, two-float times float.
 __device__ __forceinline__ void tf_mul(float ah, float al, float f, float &hi, float &lo) {
-    const float p = ah * f;
-    const float e = fmaf(ah, f, -p) + al * f;
-    hi = p + e;
-    lo = e - (hi - p);
+    const tf r = tf_mulf(tf{ah, al}, f);
+    hi = r.h;
+    lo = r.l;
 }
 
 // Block sum of the threads' two-float values; warp 0 combines the warps; the
