@@ -131,6 +131,20 @@ spec_status_t spec_verify_chain(const void *target_logits, spec_dtype_t dtype,
                                 void *stream);
 
 /*
+ * spec_verify_chain with the slot_mapping fix-up fused into the same launch:
+ * slot_mapping [B, k+1] int64 device memory, and entry j of request b becomes
+ * padding_slot_id iff j > num_accepted[b] (what spec_fixup_slots in chain mode
+ * writes afterwards), written when request b's outcome is known.  Other
+ * arguments, sizes and errors as spec_verify_chain; slot_mapping must not be
+ * NULL.
+ */
+spec_status_t spec_verify_chain_fused(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                      const int32_t *draft_tokens, const float *temperature, const float *u_accept,
+                                      const float *u_sample, int B, int k, int V, int32_t *out_tokens,
+                                      int32_t *out_num_accepted, int64_t *slot_mapping, int64_t padding_slot_id,
+                                      int32_t *d_status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Ragged chain verification: a different number of drafts per request, packed
  * (the vLLM speculative-decoding walkthrough's per-step metadata:
  * cu_num_draft_tokens offsets into packed draft and target rows).  Greedy and

@@ -72,6 +72,8 @@ def load_library():
         lib.spec_workspace_init.restype = I
         lib.spec_verify_chain.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, P, Z, P]
         lib.spec_verify_chain.restype = I
+        lib.spec_verify_chain_fused.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, ctypes.c_int64, P, P, Z, P]
+        lib.spec_verify_chain_fused.restype = I
         lib.spec_verify_chain_ragged.argtypes = [P, I, P, P, P, I, P, P, P, I, I, I, P, P, P, P, Z, P]
         lib.spec_verify_chain_ragged.restype = I
         lib.spec_fixup_slots_ragged.argtypes = [P, I, P, I, P, ctypes.c_int64, P]
@@ -189,8 +191,12 @@ def reset_counters(ws):
 # ---------------------------------------------------------------- entries --
 def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u_sample=None,
                  draft_probs=None, *, out_tokens=None, out_num_accepted=None, status=None,
-                 workspace=None, stream=None) -> Tuple[object, object]:
+                 workspace=None, stream=None, slot_mapping=None,
+                 padding_slot_id: int = PADDING_SLOT_ID) -> Tuple[object, object]:
     """Chain verify-and-accept on the GPU.
+
+    With ``slot_mapping`` ([B, k+1] int64 CUDA) the slot fix-up runs in the
+    same launch: entries j > num_accepted[b] become ``padding_slot_id``.
 
     A caller-supplied ``workspace`` (uint8 CUDA tensor of at least
     workspace_bytes(B, k+1, V) bytes) must be zero-filled before its first use
@@ -225,13 +231,21 @@ def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
     _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, (B, k + 1), dev)
     sh = _stream_handle(dev, stream)
     nbytes = workspace_bytes(B, k + 1, V, code)
     ws = workspace if workspace is not None else _workspace(dev, sh, nbytes, ("chain", B, k + 1, V, code))
-    rc = lib.spec_verify_chain(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperature),
-                               _ptr(u_accept), _ptr(u_sample), B, k, V, _ptr(out_tokens),
-                               _ptr(out_num_accepted), _ptr(status), _ptr(ws), ws.numel(), sh)
-    _check("spec_verify_chain", rc)
+    if slot_mapping is not None:
+        rc = lib.spec_verify_chain_fused(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperature),
+                                         _ptr(u_accept), _ptr(u_sample), B, k, V, _ptr(out_tokens),
+                                         _ptr(out_num_accepted), _ptr(slot_mapping), int(padding_slot_id),
+                                         _ptr(status), _ptr(ws), ws.numel(), sh)
+        _check("spec_verify_chain_fused", rc)
+    else:
+        rc = lib.spec_verify_chain(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(temperature),
+                                   _ptr(u_accept), _ptr(u_sample), B, k, V, _ptr(out_tokens),
+                                   _ptr(out_num_accepted), _ptr(status), _ptr(ws), ws.numel(), sh)
+        _check("spec_verify_chain", rc)
     return out_tokens, out_num_accepted
 
 

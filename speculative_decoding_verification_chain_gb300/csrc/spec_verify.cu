@@ -107,6 +107,8 @@ struct Params {
     int32_t *out_count;          // chain: num_accepted, tree: length
     int32_t *out_path;           // tree only
     int32_t *status;             // may be null
+    int64_t *slots;              // chains: slot_mapping fixed up in the finalisation, or null
+    int64_t pad;                 // ... PADDING_SLOT_ID
     // workspace
     unsigned long long *stats;   // [8], never cleared by the kernel
     uint32_t *ctrl;              // [32]: 0 claim counter, 1 exit counter
@@ -764,8 +766,17 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
             bonus = 1;
         }
         P.out_count[b] = P.tree ? d + 1 : d;
+        acc[0] = static_cast<uint8_t>(d < 255 ? d : 255);   // accepted count for the slot fix-up below
     }
     bonus = __shfl_sync(0xffffffffu, bonus, 0);
+    if (P.slots && !P.tree) {
+        // the slot_mapping fix-up fused here: request b's slots 0..a keep their
+        // values (row 0 is the last accepted token), the rest become padding
+        __syncwarp();
+        const int a = acc[0];
+        int64_t *sl = P.slots + in_row(P, b, 0);
+        for (int j = a + 1 + lane; j < Rb; j += 32) sl[j] = P.pad;
+    }
     if (SMP && bonus) {
         const int a = Rb - 1;
         const float u = __ldg(P.u_sample + in_row(P, b, a));
@@ -2274,11 +2285,12 @@ extern "C" spec_status_t spec_workspace_init(void *workspace, size_t bytes, void
     return SPEC_OK;
 }
 
-extern "C" spec_status_t spec_verify_chain(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
-                                           const int32_t *draft_tokens, const float *temperature,
-                                           const float *u_accept, const float *u_sample, int B, int k, int V,
-                                           int32_t *out_tokens, int32_t *out_num_accepted, int32_t *d_status,
-                                           void *workspace, size_t workspace_bytes, void *stream) {
+namespace sv {
+spec_status_t verify_chain_common(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                  const int32_t *draft_tokens, const float *temperature, const float *u_accept,
+                                  const float *u_sample, int B, int k, int V, int32_t *out_tokens,
+                                  int32_t *out_num_accepted, int64_t *slot_mapping, int64_t padding_slot_id,
+                                  int32_t *d_status, void *workspace, size_t workspace_bytes, void *stream) {
     g_err[0] = 0;
     if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype%s");
     if (B < 1 || k < 1 || k > kMaxRows - 1 || V < 1 || V >= (1 << 30))
@@ -2303,12 +2315,38 @@ extern "C" spec_status_t spec_verify_chain(const void *target_logits, spec_dtype
     P.out_count = out_num_accepted;
     P.out_path = nullptr;
     P.status = d_status;
+    P.slots = slot_mapping;
+    P.pad = padding_slot_id;
     P.B = B;
     P.R = k + 1;
     P.V = V;
     P.D = k;
     P.tree = 0;
     return launch_verify(P, dtype, workspace, workspace_bytes, stream);
+}
+}  // namespace sv
+
+extern "C" spec_status_t spec_verify_chain(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                           const int32_t *draft_tokens, const float *temperature,
+                                           const float *u_accept, const float *u_sample, int B, int k, int V,
+                                           int32_t *out_tokens, int32_t *out_num_accepted, int32_t *d_status,
+                                           void *workspace, size_t workspace_bytes, void *stream) {
+    return sv::verify_chain_common(target_logits, dtype, draft_probs, draft_tokens, temperature, u_accept, u_sample,
+                                   B, k, V, out_tokens, out_num_accepted, nullptr, 0, d_status, workspace,
+                                   workspace_bytes, stream);
+}
+
+extern "C" spec_status_t spec_verify_chain_fused(const void *target_logits, spec_dtype_t dtype,
+                                                 const float *draft_probs, const int32_t *draft_tokens,
+                                                 const float *temperature, const float *u_accept,
+                                                 const float *u_sample, int B, int k, int V, int32_t *out_tokens,
+                                                 int32_t *out_num_accepted, int64_t *slot_mapping,
+                                                 int64_t padding_slot_id, int32_t *d_status, void *workspace,
+                                                 size_t workspace_bytes, void *stream) {
+    if (!slot_mapping) return sv::fail(SPEC_ERR_INVALID_ARG, "slot_mapping is NULL%s");
+    return sv::verify_chain_common(target_logits, dtype, draft_probs, draft_tokens, temperature, u_accept, u_sample,
+                                   B, k, V, out_tokens, out_num_accepted, slot_mapping, padding_slot_id, d_status,
+                                   workspace, workspace_bytes, stream);
 }
 
 extern "C" spec_status_t spec_verify_chain_ragged(const void *target_logits, spec_dtype_t dtype,

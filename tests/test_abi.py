@@ -107,6 +107,16 @@ def test_tree_sampled_host_checks(lib):
         assert lib.spec_last_error() != b""
 
 
+def test_fused_chain_host_checks(lib):
+    # slot_mapping is required; the rest is checked as for spec_verify_chain
+    rc = lib.spec_verify_chain_fused(0x1000, 0, None, 0x2000, None, None, None, 2, 3, 100, 0x3000, 0x4000,
+                                     None, -1, None, 0x5000, 1 << 20, None)
+    assert rc == 1 and lib.spec_last_error() != b""
+    rc = lib.spec_verify_chain_fused(0x1000, 0, None, 0x2000, None, None, None, 0, 3, 100, 0x3000, 0x4000,
+                                     0x6000, -1, None, 0x5000, 1 << 20, None)
+    assert rc == 1
+
+
 def test_next_step_host_checks(lib):
     def call(ot=0x1000, stride=4, na=0x2000, pos=0x3000, bt=0x4000, mb=4, bs=16, B=2, P=3, rpr=4, cu=None,
              hid=None, rb=0, nt=0x5000, npos=0x6000, ns=0x7000):

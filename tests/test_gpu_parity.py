@@ -255,6 +255,38 @@ def test_sweep_full_size_with_slot_fixup(sv, O, dev, B):
     assert (slots.cpu().numpy() == exp).all()
 
 
+# ------------------------------------------------- fused slot fix-up --
+FUSED = [("greedy", dict(B=64, k=5, V=128256)), ("greedy", dict(B=7, k=31, V=1000)),
+         ("greedy", dict(B=3, k=255, V=300)), ("sampled", dict(B=32, k=4, V=128256)),
+         ("sampled", dict(B=9, k=8, V=5003)), ("mixed", dict(B=24, k=6, V=20011))]
+
+
+@pytest.mark.parametrize("kind,cfg", FUSED, ids=["%s-%d-%d-%d" % (k_, c["B"], c["k"], c["V"]) for k_, c in FUSED])
+def test_fused_fixup_matches_the_separate_fixup(sv, O, dev, kind, cfg):
+    """spec_verify_chain_fused: the same tokens and counts as spec_verify_chain,
+    and the slot map the oracle's fix-up writes for those counts."""
+    import torch
+    if kind == "greedy":
+        x = W.chain_greedy(seed=60 + cfg["k"], **cfg)
+    elif kind == "sampled":
+        x = W.chain_sampled(seed=61 + cfg["k"], temperature=0.8, lam=0.4, **cfg)
+    else:
+        x = W.chain_mixed(seed=62, **cfg)
+    sampled = x.draft_probs is not None
+    args = [cuda(x.logits, dev), cuda(x.draft_tokens, dev)]
+    if sampled:
+        args += [cuda(x.temperature, dev), cuda(x.u_accept, dev), cuda(x.u_sample, dev), cuda(x.draft_probs, dev)]
+    slots = cuda(x.slot_mapping, dev)
+    ot, na = sv.verify_chain(*args, slot_mapping=slots, padding_slot_id=-7)
+    ot2, na2 = sv.verify_chain(*args)
+    torch.cuda.synchronize(dev)
+    got_a = na.cpu().numpy()
+    assert (ot.cpu().numpy() == ot2.cpu().numpy()).all() and (got_a == na2.cpu().numpy()).all()
+    ref = oracle_chain(O, x)
+    compare_chain(ot.cpu().numpy(), got_a, ref)
+    assert (slots.cpu().numpy() == O.fixup_slots(x.slot_mapping, num_accepted=got_a, pad=-7)).all()
+
+
 # -------------------------------------------------------------------- tree --
 TREES = [(4, 2, 2, 1, 1), (3, 3, 1), (1, 1, 1, 1), (5,), (2, 2, 2, 2, 2, 2)]
 
