@@ -336,50 +336,71 @@ def time_steps(case, steps, dev, dist=None, verify_only=False):
 
 def e2e_leg(sv, x, dev, steps, dist=None):
     """Host buffers in pinned memory; per step: H2D of the step's inputs, the
-    C-ABI verify and fix-up, D2H of the step's results; events on the stream."""
+    C-ABI verify (slot fix-up fused), D2H of the step's results; events on the
+    streams.  Two device input sets alternate: the copy stream loads step i+1's
+    inputs while the compute stream verifies step i (the host link, not the
+    kernel, bounds the step), and each step's results are read back before its
+    input set is refilled."""
     import torch
     sampled = x.draft_probs is not None
     host = dict(z=x.logits, tok=x.draft_tokens, slots=x.slot_mapping)
     if sampled:
         host.update(T=x.temperature, ua=x.u_accept, us=x.u_sample, q=x.draft_probs)
-    pinned, devbuf = {}, {}
+    pinned = {}
     for k_, a in host.items():
         a = np.ascontiguousarray(a)
-        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
-        pinned[k_] = t
-        devbuf[k_] = torch.empty_like(t, device=dev)
-    if x.dtype == 0:
-        zdev = lambda: devbuf["z"].view(torch.bfloat16)
-    else:
-        zdev = lambda: devbuf["z"]
-    out_d = torch.empty((x.B, x.k + 1), dtype=torch.int32, device=dev)
-    na_d = torch.empty((x.B,), dtype=torch.int32, device=dev)
+        pinned[k_] = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+    sets = [{k_: torch.empty_like(t, device=dev) for k_, t in pinned.items()} for _ in range(2)]
+    outs = [dict(out=torch.empty((x.B, x.k + 1), dtype=torch.int32, device=dev),
+                 na=torch.empty((x.B,), dtype=torch.int32, device=dev)) for _ in range(2)]
     out_h = torch.empty((x.B, x.k + 1), dtype=torch.int32).pin_memory()
     na_h = torch.empty((x.B,), dtype=torch.int32).pin_memory()
     slots_h = torch.empty_like(pinned["slots"]).pin_memory()
     h2d = sum(int(t.numel() * t.element_size()) for t in pinned.values())
     d2h = int(out_h.numel() * 4 + na_h.numel() * 4 + slots_h.numel() * 8)
+    compute = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+    for e in freed:
+        e.record(compute)
 
-    def step():
-        for k_ in pinned:
-            devbuf[k_].copy_(pinned[k_], non_blocking=True)
-        sv.verify_chain(zdev(), devbuf["tok"], devbuf.get("T"), devbuf.get("ua"), devbuf.get("us"),
-                        devbuf.get("q"), out_tokens=out_d, out_num_accepted=na_d, slot_mapping=devbuf["slots"])
-        out_h.copy_(out_d, non_blocking=True)
-        na_h.copy_(na_d, non_blocking=True)
-        slots_h.copy_(devbuf["slots"], non_blocking=True)
+    def load(i):
+        s_ = i & 1
+        copy.wait_event(freed[s_])          # the set's previous step has read it and its results are out
+        with torch.cuda.stream(copy):
+            for k_, t in pinned.items():
+                sets[s_][k_].copy_(t, non_blocking=True)
+        loaded[s_].record(copy)
 
-    for _ in range(3):
-        step()
+    def verify(i):
+        s_ = i & 1
+        d, o = sets[s_], outs[s_]
+        compute.wait_event(loaded[s_])
+        z = d["z"].view(torch.bfloat16) if x.dtype == 0 else d["z"]
+        sv.verify_chain(z, d["tok"], d.get("T"), d.get("ua"), d.get("us"), d.get("q"), out_tokens=o["out"],
+                        out_num_accepted=o["na"], slot_mapping=d["slots"])
+        out_h.copy_(o["out"], non_blocking=True)
+        na_h.copy_(o["na"], non_blocking=True)
+        slots_h.copy_(d["slots"], non_blocking=True)
+        freed[s_].record(compute)
+
+    def run(n):
+        load(0)
+        for i in range(n):
+            if i + 1 < n:
+                load(i + 1)
+            verify(i)
+
+    run(3)
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
-    st = torch.cuda.current_stream(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(steps):
-        step()
-    e1.record(st)
+    e0.record(compute)
+    copy.wait_event(e0)
+    run(steps)
+    e1.record(compute)
     torch.cuda.synchronize(dev)
     barrier(dist, dev)
     ms = reduce_max(dist, e0.elapsed_time(e1), dev)

@@ -179,6 +179,22 @@ spec_status_t spec_verify_chain_ragged(const void *target_logits, spec_dtype_t d
                                        void *stream);
 
 /*
+ * spec_verify_chain_ragged with the ragged slot_mapping fix-up fused into the
+ * same launch: slot_mapping holds total_drafts + B int64 entries packed as for
+ * spec_fixup_slots_ragged, and slot j of request b (entry cu[b] + b + j)
+ * becomes padding_slot_id iff j > num_accepted[b].  slot_mapping must not be
+ * NULL; everything else as spec_verify_chain_ragged.
+ */
+spec_status_t spec_verify_chain_ragged_fused(const void *target_logits, spec_dtype_t dtype,
+                                             const float *draft_probs, const int32_t *draft_tokens,
+                                             const int32_t *cu_num_draft_tokens, int total_drafts,
+                                             const float *temperature, const float *u_accept, const float *u_sample,
+                                             int B, int max_k, int V, int32_t *out_tokens,
+                                             int32_t *out_num_accepted, int64_t *slot_mapping,
+                                             int64_t padding_slot_id, int32_t *d_status, void *workspace,
+                                             size_t workspace_bytes, void *stream);
+
+/*
  * Greedy token-tree verification (EAGLE-style tree, one verification forward).
  *
  *  target_logits [B, N+1, V] device, bf16 or fp32, 16-byte aligned.  Row n is

@@ -74,6 +74,9 @@ def load_library():
         lib.spec_verify_chain.restype = I
         lib.spec_verify_chain_fused.argtypes = [P, I, P, P, P, P, P, I, I, I, P, P, P, ctypes.c_int64, P, P, Z, P]
         lib.spec_verify_chain_fused.restype = I
+        lib.spec_verify_chain_ragged_fused.argtypes = [P, I, P, P, P, I, P, P, P, I, I, I, P, P, P, ctypes.c_int64,
+                                                       P, P, Z, P]
+        lib.spec_verify_chain_ragged_fused.restype = I
         lib.spec_verify_chain_ragged.argtypes = [P, I, P, P, P, I, P, P, P, I, I, I, P, P, P, P, Z, P]
         lib.spec_verify_chain_ragged.restype = I
         lib.spec_fixup_slots_ragged.argtypes = [P, I, P, I, P, ctypes.c_int64, P]
@@ -251,8 +254,12 @@ def verify_chain(target_logits, draft_tokens, temperature=None, u_accept=None, u
 
 def verify_chain_ragged(target_logits, draft_tokens, cu_num_draft_tokens, max_k: int, temperature=None,
                         u_accept=None, u_sample=None, draft_probs=None, *, out_tokens=None,
-                        out_num_accepted=None, status=None, workspace=None, stream=None) -> Tuple[object, object]:
+                        out_num_accepted=None, status=None, workspace=None, stream=None, slot_mapping=None,
+                        padding_slot_id: int = PADDING_SLOT_ID) -> Tuple[object, object]:
     """Chain verify-and-accept with a different number of drafts per request.
+
+    With ``slot_mapping`` ([cu[B] + B] int64 CUDA, packed like the logits rows)
+    the ragged slot fix-up runs in the same launch.
 
     cu_num_draft_tokens [B+1] int32 CUDA (cu[0] = 0, non-decreasing): request b
     has k_b = cu[b+1] - cu[b] <= max_k drafts.  target_logits [cu[B] + B, V]
@@ -287,14 +294,22 @@ def verify_chain_ragged(target_logits, draft_tokens, cu_num_draft_tokens, max_k:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     _need(out_tokens, "out_tokens", torch.int32, (B, max_k + 1), dev)
     _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, (total + B,), dev)
     sh = _stream_handle(dev, stream)
     nbytes = workspace_bytes(B, max_k + 1, V, code)
     ws = workspace if workspace is not None else _workspace(dev, sh, nbytes, ("chain", B, max_k + 1, V, code))
-    rc = lib.spec_verify_chain_ragged(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(cu), total,
-                                      _ptr(temperature), _ptr(u_accept), _ptr(u_sample), B, max_k, V,
-                                      _ptr(out_tokens), _ptr(out_num_accepted), _ptr(status), _ptr(ws),
-                                      ws.numel(), sh)
-    _check("spec_verify_chain_ragged", rc)
+    if slot_mapping is not None:
+        rc = lib.spec_verify_chain_ragged_fused(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(cu),
+                                                total, _ptr(temperature), _ptr(u_accept), _ptr(u_sample), B, max_k,
+                                                V, _ptr(out_tokens), _ptr(out_num_accepted), _ptr(slot_mapping),
+                                                int(padding_slot_id), _ptr(status), _ptr(ws), ws.numel(), sh)
+        _check("spec_verify_chain_ragged_fused", rc)
+    else:
+        rc = lib.spec_verify_chain_ragged(_ptr(z), code, _ptr(draft_probs), _ptr(draft_tokens), _ptr(cu), total,
+                                          _ptr(temperature), _ptr(u_accept), _ptr(u_sample), B, max_k, V,
+                                          _ptr(out_tokens), _ptr(out_num_accepted), _ptr(status), _ptr(ws),
+                                          ws.numel(), sh)
+        _check("spec_verify_chain_ragged", rc)
     return out_tokens, out_num_accepted
 
 

@@ -2349,13 +2349,13 @@ extern "C" spec_status_t spec_verify_chain_fused(const void *target_logits, spec
                                    workspace, workspace_bytes, stream);
 }
 
-extern "C" spec_status_t spec_verify_chain_ragged(const void *target_logits, spec_dtype_t dtype,
-                                                  const float *draft_probs, const int32_t *draft_tokens,
-                                                  const int32_t *cu_num_draft_tokens, int total_drafts,
-                                                  const float *temperature, const float *u_accept,
-                                                  const float *u_sample, int B, int max_k, int V,
-                                                  int32_t *out_tokens, int32_t *out_num_accepted, int32_t *d_status,
-                                                  void *workspace, size_t workspace_bytes, void *stream) {
+namespace sv {
+spec_status_t verify_chain_ragged_common(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                         const int32_t *draft_tokens, const int32_t *cu_num_draft_tokens,
+                                         int total_drafts, const float *temperature, const float *u_accept,
+                                         const float *u_sample, int B, int max_k, int V, int32_t *out_tokens,
+                                         int32_t *out_num_accepted, int64_t *slot_mapping, int64_t padding_slot_id,
+                                         int32_t *d_status, void *workspace, size_t workspace_bytes, void *stream) {
     g_err[0] = 0;
     if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype%s");
     if (B < 1 || max_k < 0 || max_k > kMaxRows - 1 || V < 1 || V >= (1 << 30) || total_drafts < 0 ||
@@ -2384,6 +2384,8 @@ extern "C" spec_status_t spec_verify_chain_ragged(const void *target_logits, spe
     P.out_count = out_num_accepted;
     P.out_path = nullptr;
     P.status = d_status;
+    P.slots = slot_mapping;
+    P.pad = padding_slot_id;
     P.B = B;
     P.R = max_k + 1;
     P.V = V;
@@ -2392,6 +2394,32 @@ extern "C" spec_status_t spec_verify_chain_ragged(const void *target_logits, spe
     P.cu = cu_num_draft_tokens;
     P.total_drafts = total_drafts;
     return launch_verify(P, dtype, workspace, workspace_bytes, stream);
+}
+}  // namespace sv
+
+extern "C" spec_status_t spec_verify_chain_ragged(const void *target_logits, spec_dtype_t dtype,
+                                                  const float *draft_probs, const int32_t *draft_tokens,
+                                                  const int32_t *cu_num_draft_tokens, int total_drafts,
+                                                  const float *temperature, const float *u_accept,
+                                                  const float *u_sample, int B, int max_k, int V,
+                                                  int32_t *out_tokens, int32_t *out_num_accepted, int32_t *d_status,
+                                                  void *workspace, size_t workspace_bytes, void *stream) {
+    return sv::verify_chain_ragged_common(target_logits, dtype, draft_probs, draft_tokens, cu_num_draft_tokens,
+                                          total_drafts, temperature, u_accept, u_sample, B, max_k, V, out_tokens,
+                                          out_num_accepted, nullptr, 0, d_status, workspace, workspace_bytes, stream);
+}
+
+extern "C" spec_status_t spec_verify_chain_ragged_fused(
+    const void *target_logits, spec_dtype_t dtype, const float *draft_probs, const int32_t *draft_tokens,
+    const int32_t *cu_num_draft_tokens, int total_drafts, const float *temperature, const float *u_accept,
+    const float *u_sample, int B, int max_k, int V, int32_t *out_tokens, int32_t *out_num_accepted,
+    int64_t *slot_mapping, int64_t padding_slot_id, int32_t *d_status, void *workspace, size_t workspace_bytes,
+    void *stream) {
+    if (!slot_mapping) return sv::fail(SPEC_ERR_INVALID_ARG, "slot_mapping is NULL%s");
+    return sv::verify_chain_ragged_common(target_logits, dtype, draft_probs, draft_tokens, cu_num_draft_tokens,
+                                          total_drafts, temperature, u_accept, u_sample, B, max_k, V, out_tokens,
+                                          out_num_accepted, slot_mapping, padding_slot_id, d_status, workspace,
+                                          workspace_bytes, stream);
 }
 
 extern "C" spec_status_t spec_verify_tree(const void *target_logits, spec_dtype_t dtype, const int32_t *node_tokens,

@@ -127,6 +127,33 @@ def test_ragged_slot_fixup(sv, O, dev):
     assert (slots.cpu().numpy() == exp).all()
 
 
+@pytest.mark.parametrize("mode", ["greedy", "mixed"])
+def test_ragged_fused_slot_fixup(sv, O, dev, mode):
+    """spec_verify_chain_ragged_fused: the verify's results and, in the same
+    launch, the slot map the oracle's fix-up writes for those counts."""
+    import torch
+    x = W.chain_ragged(seed=908, B=24, max_k=6, V=4001, mode=mode, min_k=0)
+    sampled = x.draft_probs is not None
+    slots = cuda(x.slot_mapping, dev)
+    ot, na = sv.verify_chain_ragged(
+        cuda(x.logits, dev), cuda(x.draft_tokens, dev), cuda(x.cu, dev), x.max_k,
+        cuda(x.temperature, dev) if sampled else None, cuda(x.u_accept, dev) if sampled else None,
+        cuda(x.u_sample, dev) if sampled else None, cuda(x.draft_probs, dev) if sampled else None,
+        slot_mapping=slots, padding_slot_id=-3)
+    torch.cuda.synchronize(dev)
+    got_t, got_a = ot.cpu().numpy(), na.cpu().numpy()
+    ref_t, ref_a = run_ragged(sv, x, dev)
+    assert (got_t == ref_t).all() and (got_a == ref_a).all()
+    check_against_oracle(O, x, got_t, got_a)
+    exp = x.slot_mapping.copy()
+    for b in range(x.B):
+        lo = int(x.cu[b]) + b
+        kb = int(x.cu[b + 1] - x.cu[b])
+        exp[lo:lo + kb + 1] = O.fixup_slots(x.slot_mapping[lo:lo + kb + 1][None, :], num_accepted=got_a[b:b + 1],
+                                            pad=-3)[0]
+    assert (slots.cpu().numpy() == exp).all()
+
+
 def test_ragged_offsets_out_of_order_are_flagged_not_faulted(sv, dev):
     """Offsets that break the rules are clamped inside the packed inputs and
     reported in the status word; the call completes."""
