@@ -61,7 +61,8 @@ def parse_args():
     ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--only", choices=OTHER_NAMES, default=None,
                     help="run just this secondary workload (kernel-only timing) and print its JSON")
-    ap.add_argument("--sweep-b", type=int, default=64, help="batch of the secondary sweep workload")
+    ap.add_argument("--sweep-b", type=int, default=None,
+                    help="one batch of the sweep workload (default: B = 1, 8, 64 and 256)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the baseline leg")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: time the verify kernel over exactly --steps launches, no clock sampling")
@@ -591,12 +592,16 @@ def others(sv, W, dev, dist, peak, args):
     want = lambda name: args.only is None or args.only == name
     out = []
     if want("sampled_chain"):
-        x = W.chain_sampled(seed=3, B=32, k=4, V=128256, temperature=0.7, lam=0.3)
-        out.append(_other_chain(sv, x, dev, dist, peak, "sampled chain B=32 k=4 V=128256 T=0.7 lambda=0.3 (Zipf)"))
+        # the draft's closeness to the target at three levels (lambda = 0.3 first)
+        for lam in (0.3, 0.1, 0.6):
+            x = W.chain_sampled(seed=3, B=32, k=4, V=128256, temperature=0.7, lam=lam)
+            out.append(_other_chain(sv, x, dev, dist, peak,
+                                    "sampled chain B=32 k=4 V=128256 T=0.7 lambda=%g (Zipf)" % lam))
     if want("sweep"):
-        x = W.chain_sampled(seed=5, B=args.sweep_b, k=8, V=152064, temperature=1.0, lam=0.3)
-        out.append(_other_chain(sv, x, dev, dist, peak,
-                                "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % args.sweep_b))
+        for Bs in ([args.sweep_b] if args.sweep_b else [64, 1, 8, 256]):
+            x = W.chain_sampled(seed=5, B=Bs, k=8, V=152064, temperature=1.0, lam=0.3)
+            out.append(_other_chain(sv, x, dev, dist, peak,
+                                    "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % Bs))
     if want("greedy_tree"):
         out.append(_other_tree(sv, W, dev, dist, peak))
     if want("ragged"):
