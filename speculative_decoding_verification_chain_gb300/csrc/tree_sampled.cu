@@ -53,7 +53,7 @@ constexpr int kMaxNodes = SPEC_MAX_ROWS;            // N + 1
 constexpr int kMaxCluster = 16;
 constexpr int kSmemBudget = 220 * 1024;             // dynamic: e, q (fp32) and the logits slice as stored
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s
 
 // Columns per CTA for a logits element of es bytes (8 + es bytes a column).
 __host__ __device__ constexpr int slice_cap(int es) { return (kSmemBudget / (8 + es)) & ~7; }
