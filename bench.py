@@ -443,8 +443,7 @@ def workload_default():
 
 
 WORKLOAD_NAME = ("greedy chain: B=64 requests, k=5 drafts, V=128256, bf16 logits N(0,3^2), "
-                 "draft = row argmax w.p. 0.8 else uniform; step = verify + slot_mapping fix-up "
-                 "(one launch, spec_verify_chain_fused)")
+                 "draft = row argmax w.p. 0.8 else uniform; step = verify + slot_mapping fix-up")
 
 
 def reference_main(args, world, rank):
