@@ -5,6 +5,9 @@
 
 namespace sv {
 
+// Clears the message spec_last_error() returns (at the start of a call).
+void clear_error();
+
 // Records the message (fmt with one %s for detail) for spec_last_error() and
 // returns s.
 spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "");

@@ -186,6 +186,7 @@ extern "C" spec_status_t spec_prepare_next_step(const int32_t *out_tokens, int o
                                                 int32_t *last_row, void *hidden_out, int32_t *d_status,
                                                 void *stream) {
     using namespace sv;
+    clear_error();
     if (B < 0 || out_stride < 1 || max_blocks < 0 || block_size < 1 || P_next < 0)
         return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, out_stride >= 1, max_blocks >= 0, block_size >= 1, P_next >= 0%s");
     if (!cu_num_draft_tokens && rows_per_req < 1)
@@ -233,6 +234,7 @@ extern "C" spec_status_t spec_compact_tree_kv(void *kv, int64_t num_slots, int64
                                               int path_stride, const int32_t *out_len, int B, int32_t *d_status,
                                               void *stream) {
     using namespace sv;
+    clear_error();
     if (B < 0 || num_slots < 0 || row_bytes < 16 || row_bytes % 16 != 0 || slot_stride < 1 || path_stride < 1 ||
         path_stride > ns::kMaxPath)
         return fail(SPEC_ERR_INVALID_ARG,

@@ -722,6 +722,7 @@ extern "C" spec_status_t spec_verify_tree_sampled(const void *target_logits, spe
                                                   int max_depth, int32_t *out_path, int32_t *out_tokens,
                                                   int32_t *out_len, int32_t *d_status, void *stream) {
     using namespace sv;
+    clear_error();
     if (B < 1 || N < 0 || N > SPEC_MAX_ROWS - 1 || V < 1 || max_depth < 0 || max_depth > SPEC_MAX_ROWS - 1)
         return fail(SPEC_ERR_INVALID_ARG, "need B >= 1, 0 <= N <= 255, V >= 1, 0 <= max_depth <= 255%s");
     if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype%s");
