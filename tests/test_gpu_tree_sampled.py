@@ -173,3 +173,29 @@ def test_host_checks(sv, dev):
                                x.parent, cuda(x.temperature, dev), cuda(x.u_accept, dev), cuda(x.u_sample, dev),
                                max_depth=0)
     assert torch.cuda.is_available()
+
+
+def test_one_child_per_level_equals_the_sampled_chain_kernel(sv, O, dev):
+    """Two separate GPU paths on the same inputs: the sampled tree with one child
+    per level and the chain verify agree (tokens, counts), except where the
+    oracle flags the deciding test or draw."""
+    import torch
+    x = W.chain_sampled(seed=950, B=40, k=4, V=20011, temperature=0.8, lam=0.3, dtype=W.FP32)
+    k = x.k
+    parent = W.parents_in_order((1,) * k)
+    q = np.zeros((x.B, k + 1, x.V), np.float32)
+    q[:, :k] = x.draft_probs
+    p, t, n = sv.verify_tree_sampled(cuda(x.logits, dev), cuda(q, dev), cuda(x.draft_tokens, dev), parent,
+                                     cuda(x.temperature, dev), cuda(x.u_accept, dev), cuda(x.u_sample, dev))
+    ot, na = sv.verify_chain(cuda(x.logits, dev), cuda(x.draft_tokens, dev), cuda(x.temperature, dev),
+                             cuda(x.u_accept, dev), cuda(x.u_sample, dev), cuda(x.draft_probs, dev))
+    torch.cuda.synchronize(dev)
+    ref = O.verify_chain(x.logits, x.dtype, x.draft_tokens, x.temperature, x.u_sample, x.draft_probs, x.u_accept)
+    tl, tt, ca, ct = n.cpu().numpy(), t.cpu().numpy(), na.cpu().numpy(), ot.cpu().numpy()
+    same = 0
+    for b in range(x.B):
+        if tl[b] - 1 == ca[b] and (tt[b] == ct[b]).all():
+            same += 1
+        else:
+            assert ref["flag_accept"][b].any() or ref["flag_sample"][b], b
+    assert same >= x.B - 2
