@@ -90,7 +90,7 @@ struct RowStat {
     float pad;
 };
 
-struct Partial {  // result of one split of a row
+struct __align__(16) Partial {  // result of one split of a row (read as one float4)
     float v;      // greedy: max value; sampled: max logit m
     int32_t idx;  // greedy: row index of the first occurrence of v
     float sh, sl; // sampled: sum of 2^((z - m) c2) over the split, two-float
@@ -863,8 +863,11 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
         for (int base = 0; base < Rb - 1 && f < 0; base += 32) {
             const int i = base + lane;
             uint32_t rs = 0;
+            // after a rejection at row n only the rows before it matter: the
+            // later ones are not read (a rejection at row 0 decides at once)
             if (i < Rb - 1) rs = (i == n) ? (kResolved | (rej_n ? 0u : 1u))
-                                         : ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
+                                 : (rej_n && i > n) ? 0u
+                                 : ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
             const unsigned notacc = __ballot_sync(0xffffffffu, i < Rb - 1 && !((rs & kResolved) && (rs & 1u)));
             if (notacc) {
                 const int l = __ffs(notacc) - 1;
@@ -1814,6 +1817,19 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                                 cand_merge(gv, gg, __ldcg(&pp->v), __ldcg(&pp->idx));
                             }
                             warp_cand(gv, gg);
+                        } else if (P.ns <= 32) {
+                            // one split per lane, read once (one round trip)
+                            float pv = -INFINITY;
+                            tf ps = tf_of(0.0f);
+                            if (lane < P.ns) {
+                                const float4 w = __ldcg(reinterpret_cast<const float4 *>(P.partial + ri * P.ns + lane));
+                                pv = w.x;
+                                ps = tf{w.z, w.w};
+                            }
+                            rm = warp_max(pv);
+                            tf t = tf_of(0.0f);
+                            if (ps.h != 0.0f) t = tf_mulf(ps, ex2(__fmul_rn(__fsub_rn(pv, rm), c2)));
+                            rS = warp_sum_tf(t);
                         } else {
                             float lm = -INFINITY;
                             for (int q = lane; q < P.ns; q += 32) lm = fmaxf(lm, __ldcg(&P.partial[ri * P.ns + q].v));
