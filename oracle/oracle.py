@@ -230,9 +230,9 @@ def ngram_propose(tokens: np.ndarray, lengths: np.ndarray, n_min: int, n_max: in
 
 
 def fixup_slots(slot_mapping: np.ndarray, num_accepted: Optional[np.ndarray] = None,
-                path: Optional[np.ndarray] = None, pad: int = -1) -> np.ndarray:
+                path: Optional[np.ndarray] = None, pad: int = -1, lib=None) -> np.ndarray:
     """Returns a fixed-up copy of slot_mapping [B, P]."""
-    lib = _load()
+    lib = _load(lib)
     s = np.array(slot_mapping, dtype=np.int64, copy=True, order="C")
     B, P = s.shape
     na = _c(num_accepted, np.int32)

@@ -152,11 +152,57 @@ def _compaction_bad(O, lib):
     return ns.compaction_mismatches(O, paths, parent, lib=lib)
 
 
+def _greedy_bad(O, lib):
+    """Greedy chains against brute force (numpy first-occurrence argmax): drafts
+    that never, always and sometimes match."""
+    bad = 0
+    for seed, p_match in ((11, 0.0), (12, 1.0), (13, 0.7)):
+        x = W.chain_greedy(seed=seed, B=16, k=5, V=3001, p_match=p_match)
+        am = np.argmax(W.logits_as_f32(x.logits, x.dtype), axis=-1)
+        r = O.verify_chain(x.logits, x.dtype, x.draft_tokens, x.temperature, x.u_sample, lib=lib)
+        for b in range(x.B):
+            a = 0
+            while a < x.k and x.draft_tokens[b, a] == am[b, a]:
+                a += 1
+            want = [int(t) for t in x.draft_tokens[b, :a]] + [int(am[b, a])] + [-1] * (x.k - a)
+            bad += int(r["num_accepted"][b] != a) + int(r["out_tokens"][b].tolist() != want)
+    return bad
+
+
+def _fixup_bad(O, lib):
+    """Slot fix-up by its meaning: a chain keeps slots 0..a, a tree keeps the
+    root and its path's nodes; everything else becomes the pad value."""
+    g = np.random.default_rng(70)
+    B, P = 9, 7
+    s = W.slot_map(g, B, P)
+    a = np.array([0, 1, 2, 3, 4, 5, 6, 0, 6], np.int32)
+    keep = np.arange(P)[None, :] <= a[:, None]
+    out = O.fixup_slots(s, num_accepted=a, pad=-1, lib=lib)
+    bad = int((out != np.where(keep, s, -1)).any(axis=1).sum())
+    path = np.full((B, 3), -1, np.int32)
+    path[:, 0] = 0
+    path[1, 1:] = [3, 5]
+    path[2, 1] = 6
+    keep = np.zeros((B, P), bool)
+    keep[:, 0] = True
+    keep[1, [3, 5]] = True
+    keep[2, 6] = True
+    out = O.fixup_slots(s, path=path, pad=-7, lib=lib)
+    return bad + int((out != np.where(keep, s, -7)).any(axis=1).sum())
+
+
 _SNAPSHOT_LOOP = """        for (int i = 1; i < L; ++i) {
             const int node = path[(size_t)b * path_stride + i];"""
 
 
 CASES = [
+    ("greedy_emits_draft", "                out[i] = g;\n                a = i;",
+     "                out[i] = x;\n                a = i;", lambda O, lib: _greedy_bad(O, lib) > 0),
+    ("greedy_accept_reversed", "if (x != g) {", "if (x == g) {", lambda O, lib: _greedy_bad(O, lib) > 0),
+    ("fixup_off_by_one", "keep = j <= num_accepted[b];", "keep = j < num_accepted[b];",
+     lambda O, lib: _fixup_bad(O, lib) > 0),
+    ("fixup_tree_path_stride", "keep = path[(size_t)b * path_stride + i] == j;", "keep = path[(size_t)b + i] == j;",
+     lambda O, lib: _fixup_bad(O, lib) > 0),
     ("residual_sign", "double d = p[j] - (double)qi[j];", "double d = (double)qi[j] - p[j];",
      lambda O, lib: _lossless(O, lib) < 1e-6),
     ("residual_noclip", "r[j] = d > 0.0 ? d : 0.0;", "r[j] = d > 0.0 ? d : -d;",
@@ -230,6 +276,8 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _tree_q_equal_p(O, lib) == 0
     assert _next_step_bad(O, lib) == 0
     assert _compaction_bad(O, lib) == 0
+    assert _greedy_bad(O, lib) == 0
+    assert _fixup_bad(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
