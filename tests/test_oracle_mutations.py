@@ -203,6 +203,13 @@ CASES = [
      lambda O, lib: _fixup_bad(O, lib) > 0),
     ("fixup_tree_path_stride", "keep = path[(size_t)b * path_stride + i] == j;", "keep = path[(size_t)b + i] == j;",
      lambda O, lib: _fixup_bad(O, lib) > 0),
+    ("q_zero_rejects", "if (qh == 0.0) {\n                    accept = 1;", "if (qh == 0.0) {\n                    accept = 0;",
+     lambda O, lib: pins.sampled_edge_violations(O, lib) > 0),
+    ("sampled_out_of_range_accepts", "accept = 0; /* out-of-range draft: p(x) = 0 */", "accept = 1;",
+     lambda O, lib: pins.sampled_edge_violations(O, lib) > 0),
+    ("accept_row_shift", "row_softmax(J->logits, J->dtype, zbase + (size_t)i * row, V, T, p);",
+     "row_softmax(J->logits, J->dtype, zbase + (size_t)(i + 1) * row, V, T, p);",
+     lambda O, lib: _residual_mismatches(O, lib) > 10),
     ("residual_sign", "double d = p[j] - (double)qi[j];", "double d = (double)qi[j] - p[j];",
      lambda O, lib: _lossless(O, lib) < 1e-6),
     ("residual_noclip", "r[j] = d > 0.0 ? d : 0.0;", "r[j] = d > 0.0 ? d : -d;",
@@ -278,6 +285,7 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _compaction_bad(O, lib) == 0
     assert _greedy_bad(O, lib) == 0
     assert _fixup_bad(O, lib) == 0
+    assert pins.sampled_edge_violations(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])

@@ -178,6 +178,37 @@ def test_bonus_sampler_is_inverse_cdf(oracle_mod):
         assert (r["out_tokens"][b, :k] == tok[b]).all()
 
 
+def sampled_edge_violations(O, lib=None):
+    """Sampled drafts at the edges of the accept rule.  A draft with q(x) = 0
+    and p(x) > 0 has p/q = inf > u: accepted, even at the largest uniform.  A
+    draft outside [0, V) has p(x) = 0, so p/q = 0 and it is rejected for any u
+    (here u = 0); the token at that position is the residual draw, numpy
+    cumsum + searchsorted on max(0, p - q).  Returns the number of requests
+    that break either rule."""
+    g = np.random.default_rng(27)
+    B, k, V, T = 40, 2, 64, 1.0
+    z = (g.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    q = _softmax64(z[:, :k] + g.standard_normal((B, k, V)), 1.0).astype(np.float32)
+    tok = g.integers(0, V, size=(B, k)).astype(np.int32)
+    ua = W.method_uniforms(g, (B, k))
+    us = W.method_uniforms(g, (B, k + 1))
+    h = B // 2
+    q[np.arange(h), 0, tok[:h, 0]] = 0.0            # first half: q(x) = 0 at position 0
+    ua[:h, 0] = np.float32(1.0 - 2.0 ** -24)
+    tok[h:, 0] = np.array([V, -1, V + 7, 1 << 30] * (B // 8), np.int32)[:B - h]
+    ua[h:, 0] = 0.0                                 # second half: out of range at position 0
+    r = O.verify_chain(z, W.FP32, tok, np.full(B, T, np.float32), us, q, ua, lib=lib)
+    bad = int((r["num_accepted"][:h] < 1).sum())
+    for b in range(h, B):
+        j, _, _ = _residual_token_numpy(z[b, 0], T, q[b, 0], float(us[b, 0]))
+        bad += int(r["num_accepted"][b] != 0 or (not r["flag_sample"][b] and r["out_tokens"][b, 0] != j))
+    return bad
+
+
+def test_sampled_q_zero_accepts_and_out_of_range_rejects(oracle_mod):
+    assert sampled_edge_violations(oracle_mod) == 0
+
+
 def test_zero_drafts_emit_the_row0_token(oracle_mod):
     """A request with no drafts (k = 0, ragged batches) accepts nothing and emits
     the bonus token of row 0: numpy argmax when greedy, else the inverse CDF of
