@@ -222,6 +222,21 @@ def test_zero_draft_probability_accepts(sv, O, dev):
     assert (got_a >= 1).all()
 
 
+def test_sampled_out_of_range_drafts_are_rejections(sv, O, dev):
+    """p(x) = 0 outside the vocabulary: rejected even at u = 0, the token at
+    that position is the residual draw, and the status word says so."""
+    import torch
+    x = W.chain_sampled(seed=79, B=8, k=3, V=4000, temperature=1.0, lam=0.3)
+    x.u_accept[:, 0] = 0.0
+    x.draft_tokens[:, 0] = np.array([-1, 4000, 1 << 29, -(1 << 29)] * 2, np.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    got_t, got_a = run_chain(sv, x, dev, status=st)
+    ref = oracle_chain(O, x)
+    compare_chain(got_t, got_a, ref)
+    assert (got_a == 0).all() and (ref["num_accepted"] == 0).all()
+    assert int(st.item()) & sv.STATUS_TOKEN_RANGE
+
+
 def test_mixed_greedy_and_sampled_batch(sv, O, dev):
     x = W.chain_mixed(seed=88, B=24, k=4, V=12000)
     got_t, got_a = run_chain(sv, x, dev)
