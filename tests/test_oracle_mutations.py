@@ -101,7 +101,8 @@ def _tree_mismatches(O, lib):
     bad = 0
     for b in range(t.B):
         path, out = pins._tree_bruteforce(zf[b], t.node_tokens[b], t.parent)
-        bad += int(list(r["tokens"][b, :len(path)]) != out or r["length"][b] != len(path))
+        bad += int(list(r["tokens"][b, :len(path)]) != out or r["length"][b] != len(path)
+                   or r["path"][b, :len(path)].tolist() != list(path))
     return bad
 
 
@@ -203,6 +204,8 @@ CASES = [
      lambda O, lib: _fixup_bad(O, lib) > 0),
     ("fixup_tree_path_stride", "keep = path[(size_t)b * path_stride + i] == j;", "keep = path[(size_t)b + i] == j;",
      lambda O, lib: _fixup_bad(O, lib) > 0),
+    ("tree_tie_last", "if (acc[n] && depth[n] > depth[best])", "if (acc[n] && depth[n] >= depth[best])",
+     lambda O, lib: _tree_mismatches(O, lib) > 0),
     ("q_zero_rejects", "if (qh == 0.0) {\n                    accept = 1;", "if (qh == 0.0) {\n                    accept = 0;",
      lambda O, lib: pins.sampled_edge_violations(O, lib) > 0),
     ("sampled_out_of_range_accepts", "accept = 0; /* out-of-range draft: p(x) = 0 */", "accept = 1;",
