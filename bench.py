@@ -114,11 +114,17 @@ def measured_peak():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the sources the verify kernel is compiled from."""
+    """Hash of the code the verify kernel is compiled from: comments removed
+    and whitespace collapsed, so a change to the code (not to its comments)
+    orphans the profiled counters."""
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode("utf-8"))
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

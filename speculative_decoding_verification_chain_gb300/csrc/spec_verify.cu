@@ -4,30 +4,34 @@
 // per request) and greedy token trees.  A chain is handled as a tree whose
 // node n has parent n-1, so both share one scheduler.
 //
-// Work.  An "A unit" is one split of one logits row of one request (a whole
-// row, or a few adjacent 16 KiB sub-chunks of it when the batch is too small
-// to fill the GPU with whole rows); a "B unit" is a 16384-element chunk of the
-// rejected row of a sampled request (residual pass).  Units are numbered
+// Work.  A row of logits is cut into stages of at most 64 KiB (32768 bf16 or
+// 16384 fp32 elements), balanced in size and a whole number of 256-element
+// blocks.  An "A unit" is one split of one row: the whole row, or a run of its
+// stages when the batch has too few rows to fill the GPU.  A "B unit" is a
+// 12288-element chunk (four stages of 3072 elements, logits plus q) of the
+// rejected row of a sampled request: the residual pass.  Units are numbered
 // (node, request, split)-major, so a parent row is claimed long before its
 // children; B units come after every A unit.
 //
-// Roles inside a block:
+// Roles inside a block (480 threads):
 //   * warp 0, producer: claims units with one global atomic (one claim ahead),
-//     drops a row whose node is already known to be rejected (some ancestor
+//     drops a row whose node is already known to be rejected (an ancestor
 //     edge resolved and failed) without reading it, and streams the rest into
-//     a ring of shared-memory stages with cp.async.bulk copies that complete
-//     on per-stage mbarriers;
-//   * warps 2..9, consumers: reduce each 16 KiB stage -- running argmax
-//     (greedy) or, per 256-element block, the block max M and
+//     a ring of three shared-memory stages, one cp.async.bulk copy each,
+//     completing on per-stage mbarriers;
+//   * warps 3..14, consumers: reduce each stage in 24 KiB passes -- running
+//     argmax (greedy) or, per 256-element block, the block max M and
 //     sum 2^((z - M) log2(e)/T) (sampled), or the residual block sums of
-//     max(0, p - q) (B units) -- and hand each finished unit to the epilogue;
-//   * warp 1, epilogue: combines a unit's partials; the last split of a row
-//     resolves it (its argmax, or its softmax statistics and the accept test
-//     min(1, p/q) of its one child); the last row of a request walks the
-//     tree, picks the deepest accepted node and writes the outputs; a sampled
-//     request rejected at row a then releases its B units, whose last one
-//     locates u * (residual mass) in the block sums and scans one
-//     256-element block for the token.  The residual is never written out.
+//     max(0, p - q) (B units) -- and hand each finished unit to an epilogue;
+//   * warps 1..2, epilogues: combine a unit's partials; the last split of a
+//     row resolves it (its argmax, or its softmax statistics and the accept
+//     test min(1, p/q) of its one child); the last row of a request walks the
+//     tree, picks the deepest accepted node, writes the outputs and (chains,
+//     when asked) pads the rejected slots of slot_mapping.  A sampled request
+//     rejected at row a publishes that decision as soon as row a resolves; its
+//     B units then run, and the last one locates u * (residual mass) in the
+//     block sums and scans one 256-element block for the token.  The residual
+//     is never written out.
 //
 // Every wait is bounded by a wall-clock limit and reports
 // SPEC_STATUS_WAIT_TIMEOUT instead of hanging.  The last block to exit clears
@@ -35,7 +39,8 @@
 //
 // Arithmetic: logits are widened to fp32 exactly; exponentials use the SFU
 // ex2 approximation on (z - M) * log2(e)/T with M a block max; row statistics
-// and the inverse-CDF prefix across blocks are combined in fp64.
+// and the inverse-CDF prefixes across blocks are two-float fp32 sums (about
+// 48 significant bits) rather than fp64, whose issue rate on this part is low.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
