@@ -40,7 +40,7 @@
 // Arithmetic: logits are widened to fp32 exactly; exponentials use the SFU
 // ex2 approximation on (z - M) * log2(e)/T with M a block max; row statistics
 // and the inverse-CDF prefixes across blocks are two-float fp32 sums (about
-// 48 significant bits) rather than fp64, whose issue rate on this part is low.
+// 44 significant bits) rather than fp64, whose issue rate on this part is low.
 
 #include <cuda_runtime.h>
 #include <stdint.h>

@@ -21,14 +21,18 @@
 // columns [r * slice, (r + 1) * slice) of the current node's row in shared
 // memory: the logits as stored (one bulk-async copy), e = 2^((z - M) log2e/T)
 // in fp32, and q (a second bulk copy, issued with the first whenever the node
-// has children).  Row max, sums, residual masses and prefix sums are combined
-// across the cluster through distributed shared memory after one cluster
-// barrier each; thread 0 of every CTA combines the ranks' values in rank
-// order, so every CTA holds the same numbers and takes the same decisions.
-// All arithmetic is fp32: per-thread sums are compensated (Kahan) and every
-// combination beyond a thread is two-float (about 44 significant bits); FP64
-// issue is scarce on this part and its latency sits on the walk's critical
-// path.
+// has children).  Values are combined across the cluster by exchanges: each
+// CTA pushes one float4 (its max with its sum, a residual mass, a chunk
+// total) into a slot of every CTA with st.async, completing on that CTA's
+// own mbarrier, and each CTA reads the C slots in rank order, so every CTA
+// holds the same numbers and takes the same decisions.  The row max and sum
+// share one exchange: a CTA's sum is taken against its own max m_r and
+// rescaled by 2^((m_r - M) log2e/T) afterwards.  The CTA owning a child's
+// column pushes that child's e(x) with the same exchange.
+// All arithmetic is fp32: a thread's few running sums are plain fp32 and
+// every combination beyond a thread is two-float (about 44 significant
+// bits); FP64 issue is scarce on this part and its latency sits on the
+// walk's critical path.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
