@@ -117,7 +117,9 @@ def _ngram_mismatches(O, lib):
     for b in range(B):
         s = t[b, :ln[b]]
         n, e = ng._numpy_search(s, 1, 5)
-        bad += int((r["match_len"][b], r["match_end"][b]) != (n, e))
+        draft = [int(v) for v in s[e + 1:e + 5]] if e >= 0 else []
+        bad += int((r["match_len"][b], r["match_end"][b]) != (n, e) or r["count"][b] != len(draft)
+                   or r["draft"][b].tolist() != draft + [-1] * (4 - len(draft)))
     return bad
 
 
@@ -144,6 +146,25 @@ def _next_step_bad(O, lib):
     r = O.prepare_next_step(g["out_tokens"], g["a"], g["pos"], g["bt"], 4, 3, rows_per_req=4, lib=lib)
     return int((r["next_position"] != g["next_position"]).sum() + (r["next_slots"] != g["slots"]).any(axis=1).sum()
                + (r["last_row"] != g["last_row"]).sum() + (r["next_token"] != g["next_token"]).sum())
+
+
+def _hidden_bad(O, lib):
+    """The gathered hidden row is the last accepted position's row, found by
+    numpy indexing (padded and ragged row layouts)."""
+    import test_oracle_next_step as ns
+    out_tokens, a, pos, bt, hid = ns.random_case(52, B=64)
+    k1 = out_tokens.shape[1]
+    r = O.prepare_next_step(out_tokens, a, pos, bt, 16, 2, rows_per_req=k1, hidden=hid, lib=lib)
+    bad = int((r["hidden_out"] != hid[np.arange(len(a)) * k1 + a]).any(axis=1).sum())
+    g = np.random.default_rng(62)
+    ks = g.integers(0, 8, size=40)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    ot = g.integers(0, 1000, size=(40, 9)).astype(np.int32)
+    aa = np.array([g.integers(0, kk + 1) for kk in ks], np.int32)
+    hh = g.standard_normal((int(cu[-1]) + 40, 8)).astype(np.float32)
+    r = O.prepare_next_step(ot, aa, np.zeros(40, np.int32), np.zeros((40, 1), np.int32), 64, 0, cu=cu,
+                            hidden=hh, lib=lib)
+    return bad + int((r["hidden_out"] != hh[cu[:-1] + np.arange(40) + aa]).any(axis=1).sum())
 
 
 def _compaction_bad(O, lib):
@@ -206,6 +227,13 @@ CASES = [
      lambda O, lib: _fixup_bad(O, lib) > 0),
     ("tree_tie_last", "if (acc[n] && depth[n] > depth[best])", "if (acc[n] && depth[n] >= depth[best])",
      lambda O, lib: _tree_mismatches(O, lib) > 0),
+    ("ngram_draft_offset", "v = s[best_e + 1 + j];", "v = s[best_e + j];",
+     lambda O, lib: _ngram_mismatches(O, lib) > 0),
+    ("next_slot_offset", "slot = (int64_t)e * block_size + pos % block_size;", "slot = (int64_t)e * block_size;",
+     lambda O, lib: _next_step_bad(O, lib) > 0),
+    ("next_negative_block", "if (e >= 0)\n", "if (1)\n", lambda O, lib: _next_step_bad(O, lib) > 0),
+    ("next_hidden_row", "hidden_in + (size_t)r * (size_t)row_bytes", "hidden_in + (size_t)r0 * (size_t)row_bytes",
+     lambda O, lib: _hidden_bad(O, lib) > 0),
     ("q_zero_rejects", "if (qh == 0.0) {\n                    accept = 1;", "if (qh == 0.0) {\n                    accept = 0;",
      lambda O, lib: pins.sampled_edge_violations(O, lib) > 0),
     ("sampled_out_of_range_accepts", "accept = 0; /* out-of-range draft: p(x) = 0 */", "accept = 1;",
@@ -289,6 +317,7 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _greedy_bad(O, lib) == 0
     assert _fixup_bad(O, lib) == 0
     assert pins.sampled_edge_violations(O, lib) == 0
+    assert _hidden_bad(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
