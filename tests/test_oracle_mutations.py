@@ -234,6 +234,7 @@ CASES = [
     ("next_negative_block", "if (e >= 0)\n", "if (1)\n", lambda O, lib: _next_step_bad(O, lib) > 0),
     ("next_hidden_row", "hidden_in + (size_t)r * (size_t)row_bytes", "hidden_in + (size_t)r0 * (size_t)row_bytes",
      lambda O, lib: _hidden_bad(O, lib) > 0),
+    ("cdf_ties_inclusive", "        if (c > t) {", "        if (c >= t) {", lambda O, lib: pins.u_zero_violations(O, lib) > 0),
     ("q_zero_rejects", "if (qh == 0.0) {\n                    accept = 1;", "if (qh == 0.0) {\n                    accept = 0;",
      lambda O, lib: pins.sampled_edge_violations(O, lib) > 0),
     ("sampled_out_of_range_accepts", "accept = 0; /* out-of-range draft: p(x) = 0 */", "accept = 1;",
@@ -318,6 +319,7 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert _fixup_bad(O, lib) == 0
     assert pins.sampled_edge_violations(O, lib) == 0
     assert _hidden_bad(O, lib) == 0
+    assert pins.u_zero_violations(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])

@@ -209,6 +209,44 @@ def test_sampled_q_zero_accepts_and_out_of_range_rejects(oracle_mod):
     assert sampled_edge_violations(oracle_mod) == 0
 
 
+def u_zero_violations(O, lib=None):
+    """u = 0 gives t = 0, and the inverse CDF takes the smallest j whose prefix
+    exceeds t: the first token with mass, never a zero-mass token before it.
+    Bonus draws (first half): row 1's first five logits are -inf, so p = 0
+    there.  Residual draws (second half): q puts 0.2 on each of tokens 0..4,
+    above p, so max(0, p - q) is 0 there; the draft (token 0) is rejected at
+    the largest uniform.  Both must give token 5, as numpy searchsorted does."""
+    g = np.random.default_rng(28)
+    B, k, V, T = 16, 1, 40, 1.0
+    h = B // 2
+    z = g.standard_normal((B, k + 1, V)).astype(np.float32)
+    z[:h, 1, :5] = -np.inf
+    q = np.zeros((B, k, V), np.float32)
+    q[:, 0, 10] = 1.0                              # first half: the draft (10) is accepted at u = 0
+    q[h:, 0, :] = 0.0
+    q[h:, 0, :5] = 0.2
+    tok = np.full((B, k), 10, np.int32)
+    tok[h:, 0] = 0
+    ua = np.zeros((B, k), np.float32)
+    ua[h:, 0] = np.float32(1.0 - 2.0 ** -24)
+    us = np.zeros((B, k + 1), np.float32)
+    r = O.verify_chain(z, W.FP32, tok, np.full(B, T, np.float32), us, q, ua, lib=lib)
+    bad = int((r["num_accepted"][:h] != 1).sum() + (r["num_accepted"][h:] != 0).sum())
+    for b in range(B):
+        a = 1 if b < h else 0
+        if b < h:
+            c = np.cumsum(_softmax64(z[b, 1], T))
+            j = int(np.searchsorted(c, 0.0, side="right"))
+        else:
+            j, _, _ = _residual_token_numpy(z[b, 0], T, q[b, 0], 0.0)
+        bad += int(j != 5 or r["out_tokens"][b, a] != 5)
+    return bad
+
+
+def test_draws_at_u_zero_skip_zero_mass_tokens(oracle_mod):
+    assert u_zero_violations(oracle_mod) == 0
+
+
 def test_zero_drafts_emit_the_row0_token(oracle_mod):
     """A request with no drafts (k = 0, ragged batches) accepts nothing and emits
     the bonus token of row 0: numpy argmax when greedy, else the inverse CDF of
