@@ -140,6 +140,11 @@ def _tree_q_equal_p(O, lib):
     return ts.q_equal_p_mismatches(O, lib)
 
 
+def _tree_zero_q(O, lib):
+    import test_oracle_tree_sampled as ts
+    return ts.zero_q_violations(O, lib)
+
+
 def _next_step_bad(O, lib):
     import test_oracle_next_step as ns
     g = ns.golden_case()
@@ -235,6 +240,10 @@ CASES = [
     ("next_hidden_row", "hidden_in + (size_t)r * (size_t)row_bytes", "hidden_in + (size_t)r0 * (size_t)row_bytes",
      lambda O, lib: _hidden_bad(O, lib) > 0),
     ("cdf_ties_inclusive", "        if (c > t) {", "        if (c >= t) {", lambda O, lib: pins.u_zero_violations(O, lib) > 0),
+    ("tree_sampled_q_zero_rejects", "if (qh == 0.0) {\n                        accept = 1;",
+     "if (qh == 0.0) {\n                        accept = 0;", lambda O, lib: _tree_zero_q(O, lib) > 0),
+    ("tree_sampled_out_of_range_accepts", "int accept = 0;", "int accept = 1;",
+     lambda O, lib: _tree_zero_q(O, lib) > 0),
     ("q_zero_rejects", "if (qh == 0.0) {\n                    accept = 1;", "if (qh == 0.0) {\n                    accept = 0;",
      lambda O, lib: pins.sampled_edge_violations(O, lib) > 0),
     ("sampled_out_of_range_accepts", "accept = 0; /* out-of-range draft: p(x) = 0 */", "accept = 1;",
@@ -320,6 +329,7 @@ def test_real_oracle_passes_the_mutation_checks(oracle_mod):
     assert pins.sampled_edge_violations(O, lib) == 0
     assert _hidden_bad(O, lib) == 0
     assert pins.u_zero_violations(O, lib) == 0
+    assert _tree_zero_q(O, lib) == 0
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
