@@ -247,6 +247,24 @@ def test_draws_at_u_zero_skip_zero_mass_tokens(oracle_mod):
     assert u_zero_violations(oracle_mod) == 0
 
 
+@pytest.mark.parametrize("lam", [0.1, 0.6])
+def test_bench_chain_bytes_match_the_oracle(oracle_mod, lam):
+    """The benchmark's algorithmic bytes come from num_accepted and the
+    temperatures alone; on a mixed greedy / sampled batch they equal the
+    oracle's own count, request by request."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    x = W.chain_mixed(seed=91, B=24, k=4, V=3001, lam=lam)
+    r = oracle_mod.verify_chain(x.logits, x.dtype, x.draft_tokens, x.temperature, x.u_sample,
+                                x.draft_probs, x.u_accept)
+    assert 0 < (x.temperature > 0).sum() < x.B
+    for b in range(x.B):
+        alg, _, _ = bench.chain_bytes(r["num_accepted"][b:b + 1], x.temperature[b:b + 1], x.k, x.V, 2)
+        assert alg == r["b_alg"][b], b
+
+
 def test_zero_drafts_emit_the_row0_token(oracle_mod):
     """A request with no drafts (k = 0, ragged batches) accepts nothing and emits
     the bonus token of row 0: numpy argmax when greedy, else the inverse CDF of
