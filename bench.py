@@ -224,6 +224,27 @@ def chain_bytes(num_accepted, temperature, k, V, s_z):
     return float(alg), float(par), float(dense)
 
 
+def tree_greedy_bytes(parent, node_tokens, g_rows, path, length, V, s_z):
+    """Algorithmic bytes of greedy tree verification: per request the root row,
+    the row of every accepted node that has children, and the chosen node's row
+    (its bonus or correction token).  A node is accepted iff its parent is and
+    its token equals the argmax of its parent's row; the GPU's path fixes the
+    argmaxes along the path only, so the accepted nodes off it come from the
+    row argmaxes g_rows [B, N+1] (first index on ties)."""
+    N = len(parent) - 1
+    has_child = np.zeros(N + 1, bool)
+    has_child[np.asarray(parent)[1:]] = True
+    rows = 0
+    for b in range(len(length)):
+        acc = np.zeros(N + 1, bool)
+        acc[0] = True
+        for n in range(1, N + 1):
+            acc[n] = acc[parent[n]] and node_tokens[b, n - 1] == g_rows[b, parent[n]]
+        best = path[b, length[b] - 1]
+        rows += sum(1 for n in range(N + 1) if n == 0 or n == best or (acc[n] and has_child[n]))
+    return float(rows * V * s_z)
+
+
 # ------------------------------------------------------------ GPU timing --
 def to_dev(a, dev):
     import torch
@@ -688,30 +709,9 @@ def _other_tree(sv, W, dev, dist, peak, target_s=0.5):
     ms = time_steps(case, n, dev, dist)
     c1 = sv.workspace_counters(ws)
     us = ms * 1e3 / n
-    # algorithmic rows: root, accepted nodes with children, the chosen node
-    path = outs[0][0].cpu().numpy()
-    ln = outs[0][2].cpu().numpy()
-    zf = None
-    rows = 0
-    par = t.parent
-    has_child = np.zeros(t.N + 1, bool)
-    has_child[par[1:]] = True
-    g_rows = None
-    for b in range(t.B):
-        # accepted set: recompute from the GPU path and tokens is not enough; count
-        # the rows the method must read from the chosen path and accepted siblings
-        acc = np.zeros(t.N + 1, bool)
-        acc[0] = True
-        # a node is accepted iff its parent is accepted and its token equals the
-        # parent's argmax; the GPU's own path fixes the argmax along the path only,
-        # so accepted off-path nodes are counted by re-deriving argmaxes on host
-        if g_rows is None:
-            g_rows = np.argmax(W.logits_as_f32(t.logits, t.dtype), axis=-1)
-        for n_ in range(1, t.N + 1):
-            acc[n_] = acc[par[n_]] and t.node_tokens[b, n_ - 1] == g_rows[b, par[n_]]
-        best = path[b, ln[b] - 1]
-        rows += sum(1 for n_ in range(t.N + 1) if n_ == 0 or n_ == best or (acc[n_] and has_child[n_]))
-    b_alg = float(rows * t.V * 2)
+    g_rows = np.argmax(W.logits_as_f32(t.logits, t.dtype), axis=-1)
+    b_alg = tree_greedy_bytes(t.parent, t.node_tokens, g_rows, outs[0][0].cpu().numpy(),
+                              outs[0][2].cpu().numpy(), t.V, 2)
     b_dense = float(t.logits.nbytes)
     ach = b_alg / (us * 1e-6) / 1e9
     return {"workload": "greedy tree B=16 N=60 levels (4,8,16,16,16) V=128256 bf16",

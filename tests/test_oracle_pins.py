@@ -265,6 +265,23 @@ def test_bench_chain_bytes_match_the_oracle(oracle_mod, lam):
         assert alg == r["b_alg"][b], b
 
 
+def test_bench_greedy_tree_bytes_match_the_oracle(oracle_mod):
+    """The benchmark's greedy-tree algorithmic bytes (root, accepted nodes with
+    children, the chosen node) equal the oracle's own count."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    t = W.tree_greedy(seed=57, B=24, V=501, children_per_level=(4, 2, 2, 1, 1), p_match=0.7)
+    r = oracle_mod.verify_tree(t.logits, t.dtype, t.node_tokens, t.parent)
+    g = np.argmax(W.logits_as_f32(t.logits, t.dtype), axis=-1)
+    assert (r["length"] > 2).any()
+    for b in range(t.B):
+        got = bench.tree_greedy_bytes(t.parent, t.node_tokens[b:b + 1], g[b:b + 1], r["path"][b:b + 1],
+                                      r["length"][b:b + 1], t.V, 2)
+        assert got == r["b_alg"][b], b
+
+
 def test_zero_drafts_emit_the_row0_token(oracle_mod):
     """A request with no drafts (k = 0, ragged batches) accepts nothing and emits
     the bonus token of row 0: numpy argmax when greedy, else the inverse CDF of
