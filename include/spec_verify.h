@@ -419,6 +419,32 @@ size_t spec_noalloc_scratch_bytes(void);
 /* Text of the last error recorded on the calling thread ("" if none). */
 const char *spec_last_error(void);
 
+/*
+ * Tuning and test settings, process-wide; normal use needs neither.  A call
+ * reads them when it sets up its launch, so a call captured in a CUDA graph
+ * keeps the values in force at capture time.
+ *
+ * spec_set_wait_limit_ns: the limit, in nanoseconds, of every wait a kernel of
+ * this library makes on other blocks, warps or cluster peers (default
+ * 500000000, i.e. 0.5 s; 0 = give up at once unless the awaited event has
+ * already happened).  A wait that runs out sets
+ * SPEC_STATUS_WAIT_TIMEOUT and the kernel finishes early: the outputs of the
+ * requests involved are undefined, bulk copies already in flight are still
+ * waited for (with the default limit) before a block exits, and the workspace
+ * counters are left zero as after any call.  Returns the previous limit.
+ * Tests set the limit to 0 to drive the time-out path; there is no reason to
+ * change it otherwise.
+ *
+ * spec_set_tuning: splits = units each logits row of the chain / greedy-tree
+ * verify kernel is cut into (0 = automatic: whole rows when the batch has
+ * about two rows per SM, finer otherwise); ahead = stages the kernel's copy
+ * ring keeps in flight (0 = automatic, i.e. all 3; else 2 or 3).  Results do
+ * not depend on either.  Other values return SPEC_ERR_INVALID_ARG and change
+ * nothing.
+ */
+unsigned long long spec_set_wait_limit_ns(unsigned long long ns);
+spec_status_t spec_set_tuning(int splits, int ahead);
+
 #ifdef __cplusplus
 }
 #endif

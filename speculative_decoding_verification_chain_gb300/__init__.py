@@ -99,6 +99,10 @@ def load_library():
         lib.spec_noalloc_scratch_bytes.restype = Z
         lib.spec_last_error.argtypes = []
         lib.spec_last_error.restype = ctypes.c_char_p
+        lib.spec_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.spec_set_wait_limit_ns.restype = ctypes.c_ulonglong
+        lib.spec_set_tuning.argtypes = [I, I]
+        lib.spec_set_tuning.restype = I
         _lib = lib
         return lib
 
@@ -189,6 +193,18 @@ def workspace_counters(ws) -> dict:
 
 def reset_counters(ws):
     ws[:64].zero_()
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """spec_set_wait_limit_ns: limit of the kernels' inter-block waits (test
+    setting; default 0.5 s).  Returns the previous limit."""
+    return int(load_library().spec_set_wait_limit_ns(int(ns)))
+
+
+def set_tuning(splits: int = 0, ahead: int = 0):
+    """spec_set_tuning: row splits and copy-ring depth of the verify kernel
+    (0 = automatic)."""
+    _check("spec_set_tuning", load_library().spec_set_tuning(int(splits), int(ahead)))
 
 
 # ---------------------------------------------------------------- entries --

@@ -16,4 +16,9 @@ spec_status_t fail(spec_status_t s, const char *fmt, const char *detail = "");
 // its SM count.
 spec_status_t require_sm103(int *sms);
 
+// Limit in nanoseconds of the kernels' waits on other blocks and warps
+// (spec_set_wait_limit_ns); copies still in flight at a kernel's exit are
+// always waited for with the default limit.
+unsigned long long wait_limit_ns();
+
 }  // namespace sv

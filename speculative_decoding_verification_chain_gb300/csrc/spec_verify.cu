@@ -48,6 +48,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.h"
@@ -78,7 +79,8 @@ constexpr uint32_t kIdxMask = 0x3fffffffu;
 constexpr uint32_t kDecided = 0x80000000u;
 constexpr uint32_t kNeedsResidual = 0x40000000u;
 constexpr uint32_t kSkipInc = 0x10000u;                 // split counter: skipped splits count here
-constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s
+constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s: default wait limit; always the limit
+                                                            // on copies still in flight at exit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kEarlyMax = 4;                            // children per node given an early-rejection check
 constexpr uint32_t kFirstF = 1u << 6;                   // stage flag: first stage of its unit
@@ -147,6 +149,7 @@ struct Params {
     const int32_t *cu;           // ragged chains: request b has cu[b+1] - cu[b] drafts (null: R - 1 each)
     int total_drafts;            // ragged chains: cu[B] (packed draft rows; logit rows add one per request)
     int ahead;                   // stages the producer may have in flight
+    unsigned long long wait_ns;  // limit of every inter-block or inter-warp wait
     int16_t parent[kMaxRows];
     uint8_t depth[kMaxRows];
     uint8_t kid_off[kMaxRows + 1];   // tree: children of n are kid_list[kid_off[n] .. kid_off[n+1])
@@ -243,13 +246,23 @@ __device__ __forceinline__ void set_status(const Params &P, int bits) {
 }
 
 // Bounded wait on an mbarrier phase; gives up (and raises the block's abort
-// flag) after kWaitLimitNs or as soon as another role has aborted.
+// flag) after P.wait_ns (at the first failed try when it is 0) or as soon as
+// another role has aborted.
 __device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parity) {
+    if (P.wait_ns == 0) {
+        // limit 0: one non-blocking test (try_wait may suspend the thread first)
+        if (mbar_test_wait(bar, parity)) return true;
+        if (!*reinterpret_cast<volatile int *>(&S.abort_flag)) {
+            *reinterpret_cast<volatile int *>(&S.abort_flag) = 1;
+            set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
+        }
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
-    unsigned long long t0 = globaltimer();
+    const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
         if (*reinterpret_cast<volatile int *>(&S.abort_flag)) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > P.wait_ns) {
             *reinterpret_cast<volatile int *>(&S.abort_flag) = 1;
             set_status(P, SPEC_STATUS_WAIT_TIMEOUT);
             return false;
@@ -1144,7 +1157,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                 if (!(stv & kDecided)) {
                     unsigned long long t0 = globaltimer();
                     while (!(stv & kDecided)) {
-                        if (globaltimer() - t0 > kWaitLimitNs) break;
+                        if (P.wait_ns == 0 || globaltimer() - t0 > P.wait_ns) break;
                         __nanosleep(200);
                         stv = ld_acquire(P.req_state + b);
                     }
@@ -2094,33 +2107,39 @@ spec_status_t require_sm103(int *sms) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Process-wide tuning and test settings (spec_set_tuning, spec_set_wait_limit_ns),
+// read once per call when the launch is set up.
+std::atomic<int> g_tune_splits{0};
+std::atomic<int> g_tune_ahead{0};
+std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 // Splits per row: whole rows when the batch gives every SM about two rows,
 // otherwise finer splits (down to one 16 KiB stage) so small batches still
-// spread over the GPU.  SPEC_VERIFY_SPLITS overrides the choice (tuning).
+// spread over the GPU.  A split count set by spec_set_tuning overrides it.
 int choose_splits(int rows_total, int nsub, int sms) {
     int ns = (2 * sms + rows_total - 1) / rows_total;
-    if (const char *env = getenv("SPEC_VERIFY_SPLITS")) {
-        int v = atoi(env);
-        if (v > 0) ns = v;
-    }
+    const int forced = g_tune_splits.load(std::memory_order_relaxed);
+    if (forced > 0) ns = forced;
     if (ns < 1) ns = 1;
     if (ns > nsub) ns = nsub;
     return ns;
 }
 
-// Stages the producer keeps in flight: the whole ring.  SPEC_VERIFY_AHEAD
-// (2..ring size) overrides it (tuning: fewer stages in flight let a row that
-// turns out not to be needed stop sooner).
+// Stages the producer keeps in flight: the whole ring, unless spec_set_tuning
+// asked for fewer (2..ring size: fewer stages in flight let a row that turns
+// out not to be needed stop sooner).
 int choose_ahead() {
-    int a = kStages;
-    if (const char *env = getenv("SPEC_VERIFY_AHEAD")) {
-        int v = atoi(env);
-        if (v >= 2 && v <= kStages) a = v;
-    }
-    return a;
+    const int forced = g_tune_ahead.load(std::memory_order_relaxed);
+    return (forced >= 2 && forced <= kStages) ? forced : kStages;
 }
 
-spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size_t ws_bytes, void *stream) {
+// clear_counters: zero the layout's counter region on `stream` just before the
+// launch, after every host check has passed (the no-alloc entry point's static
+// scratch keeps whatever the previous call left).
+spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size_t ws_bytes, void *stream,
+                            bool clear_counters = false) {
     Layout L;
     if (!make_layout(P.B, P.R, P.V, dtype, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
     if (!workspace || ws_bytes < L.total)
@@ -2158,6 +2177,7 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     int ns = choose_splits(rows_total > (1 << 30) ? (1 << 30) : static_cast<int>(rows_total), L.nsub, D->sms);
     P.sps = (L.nsub + ns - 1) / ns;
     P.ahead = choose_ahead();
+    P.wait_ns = wait_limit_ns();
     P.ns = (L.nsub + P.sps - 1) / P.sps;
     // units span the padded (node, request, split) space; ragged requests' missing
     // nodes are dropped by the producer without work
@@ -2174,6 +2194,10 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     if (grid > P.units_total) grid = P.units_total;
     if (grid < 1) grid = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (clear_counters) {
+        const cudaError_t ec = cudaMemsetAsync(ws + L.reset, 0, L.reset_bytes, st);
+        if (ec != cudaSuccess) return fail(SPEC_ERR_CUDA, "clearing the workspace counters: %s", cudaGetErrorString(ec));
+    }
     // Calls without temperatures are greedy only: a leaner instantiation without
     // the sampling and residual code.
     const dim3 g3(static_cast<unsigned>(grid));
@@ -2508,6 +2532,19 @@ extern "C" spec_status_t spec_tree_from_choices(const int32_t *flat, const int32
 
 extern "C" const char *spec_last_error(void) { return g_err; }
 
+extern "C" unsigned long long spec_set_wait_limit_ns(unsigned long long ns) {
+    return g_wait_ns.exchange(ns, std::memory_order_relaxed);
+}
+
+extern "C" spec_status_t spec_set_tuning(int splits, int ahead) {
+    g_err[0] = 0;
+    if (splits < 0 || ahead < 0 || (ahead != 0 && (ahead < 2 || ahead > kStages)))
+        return fail(SPEC_ERR_INVALID_ARG, "need splits >= 0 and ahead 0 or in [2, 3]%s");
+    g_tune_splits.store(splits, std::memory_order_relaxed);
+    g_tune_ahead.store(ahead, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
 extern "C" size_t spec_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 extern "C" spec_status_t spec_verify_chain_noalloc(const void *target_logits, spec_dtype_t dtype,
@@ -2536,13 +2573,13 @@ extern "C" spec_status_t spec_verify_chain_noalloc(const void *target_logits, sp
                  L.total, kNoAllocScratchBytes);
         return fail(SPEC_ERR_INVALID_ARG, "%s (use spec_verify_chain with a workspace)", buf);
     }
-    uint8_t *scratch = nullptr;
-    spec_status_t s = noalloc_scratch_ptr(scratch);
+    // The device must be supported before the scratch is looked up (a device
+    // that is not 10.3 reports SPEC_ERR_UNSUPPORTED, not a symbol-lookup error).
+    spec_status_t s = require_sm103(nullptr);
     if (s != SPEC_OK) return s;
-    // The scratch keeps whatever the previous call left; only this layout's
-    // counter region has to start at zero.
-    cudaError_t e = cudaMemsetAsync(scratch + L.reset, 0, L.reset_bytes, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "clearing the no-alloc scratch: %s", cudaGetErrorString(e));
+    uint8_t *scratch = nullptr;
+    s = noalloc_scratch_ptr(scratch);
+    if (s != SPEC_OK) return s;
     Params P;
     memset(&P, 0, sizeof P);
     P.logits = static_cast<const uint8_t *>(target_logits);
@@ -2560,5 +2597,7 @@ extern "C" spec_status_t spec_verify_chain_noalloc(const void *target_logits, sp
     P.V = V;
     P.D = k;
     P.tree = 0;
-    return launch_verify(P, dtype, scratch, kNoAllocScratchBytes, stream);
+    // The scratch keeps whatever the previous call left; launch_verify clears
+    // this layout's counter region once every check has passed.
+    return launch_verify(P, dtype, scratch, kNoAllocScratchBytes, stream, true);
 }

@@ -57,7 +57,7 @@ constexpr int kMaxNodes = SPEC_MAX_ROWS;            // N + 1
 constexpr int kMaxCluster = 16;
 constexpr int kSmemBudget = 220 * 1024;             // dynamic: e, q (fp32) and the logits slice as stored
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s
+constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s: the limit on copies in flight at exit
 
 // Columns per CTA for a logits element of es bytes (8 + es bytes a column).
 __host__ __device__ constexpr int slice_cap(int es) { return (kSmemBudget / (8 + es)) & ~7; }
@@ -75,6 +75,7 @@ struct Params {
     int32_t *status;           // one word or null
     int bf16, B, N, V, max_depth, slice, cluster;
     int zbulk, qbulk;          // rows start on 16-byte boundaries: bulk copies allowed
+    unsigned long long wait_ns;  // limit of the row-copy and cluster-exchange waits
     uint16_t child_off[kMaxNodes + 1];  // children of c: child_list[child_off[c] .. child_off[c+1])
     uint8_t child_list[kMaxNodes];
 };
@@ -230,6 +231,18 @@ __device__ __forceinline__ void block_scan2(float s, float c, float &exh, float 
     tl = sh.tot[1];
 }
 
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint32_t mapa_u32(uint32_t local, int rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
@@ -269,41 +282,47 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
 // local slots.  A slot or barrier phase is reused two exchanges later: a CTA
 // sends exchange xk + 2 only after receiving every CTA's exchange xk + 1, and
 // every CTA passes a block barrier between reading exchange xk and sending
-// xk + 1, so nothing lands before it has been read.  The wait is bounded;
-// after one time-out the CTA stops waiting (late) and its results are
-// undefined (the caller reports SPEC_STATUS_WAIT_TIMEOUT).
+// xk + 1, so nothing lands before it has been read.  The wait is bounded by
+// `limit`; `late` comes back the same in every thread of the CTA (a block
+// barrier ORs it), so the caller can leave the walk at once: after a time-out
+// the slots may still change under the readers and nothing read from them
+// may steer the walk.
 __device__ __forceinline__ const float4 *cluster_exchange(Shared &sh, int &xk, int rank, float4 v, int C, uint32_t extra,
-                                                          bool &late) {
+                                                          unsigned long long limit, bool &late) {
     const int p = xk & 1;
     if (threadIdx.x == 0) mbar_expect_tx(&sh.xbar[p], 16u * static_cast<uint32_t>(C) + extra);
     if (static_cast<int>(threadIdx.x) < C) {
         const int r = static_cast<int>(threadIdx.x);
         st_async_f4(mapa_u32(smem_u32(&sh.slot[p][rank]), r), v, mapa_u32(smem_u32(&sh.xbar[p]), r));
     }
-    if (!late) {
-        const uint32_t ph = static_cast<uint32_t>(xk >> 1) & 1u;
-        if (!mbar_try_wait_cluster(&sh.xbar[p], ph)) {
-            const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait_cluster(&sh.xbar[p], ph)) {
-                if (globaltimer() - t0 > kWaitLimitNs) {
-                    late = true;
-                    break;
-                }
+    bool mine = false;
+    const uint32_t ph = static_cast<uint32_t>(xk >> 1) & 1u;
+    if (limit == 0) {
+        mine = !mbar_test_wait_cluster(&sh.xbar[p], ph);   // one non-blocking test
+    } else if (!mbar_try_wait_cluster(&sh.xbar[p], ph)) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait_cluster(&sh.xbar[p], ph)) {
+            if (globaltimer() - t0 > limit) {
+                mine = true;
+                break;
             }
         }
     }
+    late = __syncthreads_or(mine) != 0;
     ++xk;
     return sh.slot[p];
 }
 
 __device__ __forceinline__ bool nonfinite(float f) { return (f != f) || f == INFINITY; }
 
-// Bounded wait on the row-copy barrier; false after kWaitLimitNs.
-__device__ bool wait_rows(uint64_t *bar, uint32_t parity) {
+// Bounded wait on the row-copy barrier; false after `limit` nanoseconds (at
+// the first failed try when it is 0).
+__device__ bool wait_rows(uint64_t *bar, uint32_t parity, unsigned long long limit) {
+    if (limit == 0) return mbar_test_wait(bar, parity);   // one non-blocking test
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait_sleep(bar, parity, 100000u))
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit) return false;
     return true;
 }
 
@@ -414,11 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             const int x = sh.tok[P.child_list[kb + k] - 1];
             sh.qx[k] = (x >= 0 && x < V) ? __ldg(P.q + roff + x) : 0.0f;
         }
+        bool copy_late = false;
         if (zmain + qbytes > 0) {
-            if (!wait_rows(&sh.bar, phase)) late = true;
+            copy_late = !wait_rows(&sh.bar, phase, P.wait_ns);
             phase ^= 1u;
         }
-        __syncthreads();
+        // a copy that outlived its wait ends the walk (the same in every thread)
+        late = __syncthreads_or(copy_late) != 0;
+        if (late) break;
 
         // (2) this CTA's max m_r, e = 2^((z - m_r) c2) and its sum; one cluster
         // exchange gives M = max m_r, the scales f_r = 2^((m_r - M) c2) and
@@ -484,7 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             const int x = sh.tok[P.child_list[kb + k] - 1];
             nin += (x >= 0 && x < V) ? 1u : 0u;
         }
-        const float4 *row = cluster_exchange(sh, xk, rank, make_float4(mr, sh0, sl0, 0.0f), C, 4u * nin, late);
+        const float4 *row =
+            cluster_exchange(sh, xk, rank, make_float4(mr, sh0, sl0, 0.0f), C, 4u * nin, P.wait_ns, late);
+        if (late) break;
         float M = -INFINITY;
         for (int r = 0; r < C; ++r) M = fmaxf(M, row[r].x);
         float Sh = 0.0f, Sl = 0.0f, fmine = 0.0f;
@@ -555,7 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                 tf_add(rh, rl, s3, 0.0f);
             }
             block_sum2(rh, rl, sh);
-            const float4 *rrow = cluster_exchange(sh, xk, rank, make_float4(rh, rl, 0.0f, 0.0f), C, 0u, late);
+            const float4 *rrow =
+                cluster_exchange(sh, xk, rank, make_float4(rh, rl, 0.0f, 0.0f), C, 0u, P.wait_ns, late);
+            if (late) break;
             float Snh = 0.0f, Snl = 0.0f;
             for (int r = 0; r < C; ++r) tf_add(Snh, Snl, rrow[r].x, rrow[r].y);
             if (Snh > 0.0f) {  // a residual of no mass leaves p' as it is
@@ -565,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
                 STl = Snl;
             }
         }
+        if (late) break;
         if (next < 0) {
             // one draw from p' (p, or max(0, p - Tm q) after a rejection): the
             // smallest column whose prefix exceeds t = u * total.  Prefixes run
@@ -589,8 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
             float exh, exl, inh, inl, th, tl;
             block_scan2(s, -k, exh, exl, inh, inl, th, tl, sh);
             const int clast = block_imax(lastpos, sh);
-            const float4 *trow =
-                cluster_exchange(sh, xk, rank, make_float4(th, tl, __int_as_float(clast), 0.0f), C, 0u, late);
+            const float4 *trow = cluster_exchange(sh, xk, rank, make_float4(th, tl, __int_as_float(clast), 0.0f), C,
+                                                  0u, P.wait_ns, late);
+            if (late) break;
             // t = u * total, then the first CTA whose running end exceeds t
             float toth = 0.0f, totl = 0.0f;
             for (int r = 0; r < C; ++r) tf_add(toth, totl, trow[r].x, trow[r].y);
@@ -677,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_sampled_kernel(const __grid_
     if (late) {
         // a row copy or an exchange outlived its wait: one more bounded wait
         // for the last row copy, so no copy lands here after exit
-        wait_rows(&sh.bar, phase ^ 1u);
+        wait_rows(&sh.bar, phase ^ 1u, kWaitLimitNs);
         if (tid == 0 && P.status) atomicOr(P.status, SPEC_STATUS_WAIT_TIMEOUT);
     }
     if (bad && P.status) atomicOr(P.status, SPEC_STATUS_NONFINITE);
@@ -787,6 +815,7 @@ extern "C" spec_status_t spec_verify_tree_sampled(const void *target_logits, spe
     P.cluster = C;
     P.zbulk = (static_cast<long long>(V) * es) % 16 == 0;
     P.qbulk = V % 4 == 0;
+    P.wait_ns = wait_limit_ns();
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(C));

@@ -509,6 +509,30 @@ def tree_sampled(seed: int = 6, B: int = 16, V: int = 128256,
         u_accept=method_uniforms(g[2], (B, N)), u_sample=method_uniforms(g[2], (B, N + 1)))
 
 
+def redraw(x, seed: int):
+    """The same logits and draft distributions with fresh draws: draft tokens
+    drawn again from q (children of c i.i.d. from q_c for trees) and new method
+    uniforms.  Each result is an independent trial of the accept / resample
+    process on fixed distributions (the rates of rare events, such as positions
+    near a flag window, are measured over many such trials without making the
+    expensive rows again)."""
+    from dataclasses import replace
+    g = _streams(seed)
+    if isinstance(x, TreeInputs):
+        par = np.asarray(x.parent)
+        toks = np.empty_like(x.node_tokens)
+        for b in range(x.B):
+            if x.N > 0:
+                toks[b] = _draw_from_rows(g[1], x.draft_probs[b][par[1:]])
+        return replace(x, node_tokens=toks, u_accept=method_uniforms(g[2], (x.B, x.N)),
+                       u_sample=method_uniforms(g[2], (x.B, x.N + 1)))
+    toks = np.empty_like(x.draft_tokens)
+    for b in range(x.B):
+        toks[b] = _draw_from_rows(g[1], x.draft_probs[b])
+    return replace(x, draft_tokens=toks, u_accept=method_uniforms(g[2], (x.B, x.k)),
+                   u_sample=method_uniforms(g[2], (x.B, x.k + 1)))
+
+
 # ----------------------------------------------------------------------------
 # the five named workloads
 # ----------------------------------------------------------------------------

@@ -18,3 +18,20 @@ def oracle_mod():
     from oracle import oracle as O
     O.build()
     return O
+
+
+# Lines that tests record for the end-of-run summary (flag budget fractions).
+_REPORT = []
+
+
+@pytest.fixture(scope="session")
+def report():
+    """report(line): print `line` in the terminal summary, even under -q."""
+    return _REPORT.append
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    if _REPORT:
+        terminalreporter.section("measured rates")
+        for line in _REPORT:
+            terminalreporter.write_line(line)

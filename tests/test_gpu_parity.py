@@ -386,16 +386,24 @@ def test_workspace_is_left_clean_between_calls(sv, O, dev):
 
 
 # ------------------------------------------- skipped rows, producer run-ahead --
-@pytest.mark.parametrize("ahead", [2, 3])
-def test_results_do_not_depend_on_producer_run_ahead(sv, O, dev, ahead, monkeypatch):
-    """How many stages the producer keeps in flight changes the timing of
-    claims and so which rows are skipped; the answers must not change."""
-    monkeypatch.setenv("SPEC_VERIFY_AHEAD", str(ahead))
+@pytest.fixture
+def tuning(sv):
+    """spec_set_tuning for one test, put back to automatic afterwards."""
+    yield sv.set_tuning
+    sv.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("ahead,splits", [(2, 0), (3, 0), (3, 3), (2, 1)])
+def test_results_do_not_depend_on_producer_run_ahead(sv, O, dev, ahead, splits, tuning):
+    """How many stages the producer keeps in flight, and how finely rows are
+    split, change the timing of claims and so which rows are skipped; the
+    answers must not change."""
+    tuning(splits, ahead)
     x = W.chain_greedy(seed=61 + ahead, B=16, k=5, V=128256, p_match=0.5)
     got_t, got_a = run_chain(sv, x, dev)
     ref = oracle_chain(O, x)
     assert (got_a == ref["num_accepted"]).all() and (got_t == ref["out_tokens"]).all()
-    t = W.tree_greedy(seed=62 + ahead, B=4, V=50000)
+    t = W.tree_greedy(seed=62 + ahead + splits, B=4, V=50000)
     path, toks, ln = sv.verify_tree(cuda(t.logits, dev), cuda(t.node_tokens, dev), t.parent)
     r = O.verify_tree(t.logits, t.dtype, t.node_tokens, t.parent)
     assert (ln.cpu().numpy() == r["length"]).all()
@@ -405,12 +413,12 @@ def test_results_do_not_depend_on_producer_run_ahead(sv, O, dev, ahead, monkeypa
     compare_chain(got_t, got_a, oracle_chain(O, xs))
 
 
-def test_rejected_first_drafts_skip_later_rows(sv, O, dev, monkeypatch):
+def test_rejected_first_drafts_skip_later_rows(sv, O, dev, tuning):
     """Every first draft wrong: rows 1..k are never needed.  Many are skipped
     at claim (the first stage of row 0 already shows the rejection), and the
     counters stay consistent."""
     import torch
-    monkeypatch.setenv("SPEC_VERIFY_AHEAD", "3")
+    tuning(0, 3)
     x = W.chain_greedy(seed=64, B=32, k=5, V=128256, p_match=0.0)
     z, tok = cuda(x.logits, dev), cuda(x.draft_tokens, dev)
     ws = torch.zeros(sv.workspace_bytes(x.B, x.k + 1, x.V), dtype=torch.uint8, device=dev)

@@ -102,3 +102,25 @@ def test_noalloc_rejects_sizes_beyond_the_scratch(sv, dev):
                                        None, None)
     assert rc == 1
     assert b"scratch" in lib.spec_last_error()
+
+
+def test_noalloc_calls_take_no_device_memory(sv, dev):
+    """The point of the entry point: a call allocates nothing.  With inputs and
+    outputs made beforehand, the device's free memory is the same before and
+    after several calls (the first call on the device, which sets up the
+    kernels and looks up the scratch address, is made before the reading)."""
+    import torch
+    x = W.chain_sampled(seed=521, B=8, k=4, V=30011, temperature=0.8, lam=0.3)
+    args = [cuda(a, dev) for a in (x.logits, x.draft_tokens, x.temperature, x.u_accept, x.u_sample, x.draft_probs)]
+    out = torch.empty((x.B, x.k + 1), dtype=torch.int32, device=dev)
+    na = torch.empty((x.B,), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    sv.verify_chain_noalloc(*args, out_tokens=out, out_num_accepted=na, status=st)
+    torch.cuda.synchronize(dev)
+    free0, _ = torch.cuda.mem_get_info(dev)
+    for _ in range(4):
+        sv.verify_chain_noalloc(*args, out_tokens=out, out_num_accepted=na, status=st)
+    torch.cuda.synchronize(dev)
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0, (free0, free1)
+    assert int(st.item()) == 0
