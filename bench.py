@@ -436,6 +436,42 @@ def e2e_leg(sv, x, dev, steps, dist=None):
 
 
 # ------------------------------------------------------------ CPU leg ---
+# Sampled workloads whose GPU results the CPU leg checks against the oracle:
+# (kind, the workload's result line, inputs, GPU outputs).
+_PARITY_JOBS = []
+
+
+def cpu_parity_leg():
+    """Part of the CPU-baseline leg: the oracle on each sampled secondary
+    workload's batch, compared with the GPU's results of that batch.  Adds to
+    each result line the fraction of positions (B x (k+1) rows, B x (N+1)
+    tree nodes) the oracle flags and the fraction where the GPU differs."""
+    from oracle import oracle as O
+    threads = os.cpu_count() or 1
+    for kind, res, x, got in _PARITY_JOBS:
+        if kind == "chain":
+            ref = O.verify_chain(x.logits, x.dtype, x.draft_tokens, x.temperature, x.u_sample, x.draft_probs,
+                                 x.u_accept, nthreads=threads)
+            ot, na = got
+            a, ra = na.astype(np.int64), ref["num_accepted"].astype(np.int64)
+            tok_differ = np.array([a[b] == ra[b] and ot[b, a[b]] != ref["out_tokens"][b, a[b]]
+                                   for b in range(x.B)])
+            differ = int((a != ra).sum() + tok_differ.sum())
+            positions = x.B * (x.k + 1)
+        else:
+            ref = O.verify_tree_sampled(x.logits, x.dtype, x.node_tokens, x.parent, x.temperature, x.u_accept,
+                                        x.u_sample, x.draft_probs)
+            path, toks, ln = got
+            differ = int(sum(1 for b in range(x.B) if not (ln[b] == ref["length"][b]
+                                                            and (path[b] == ref["path"][b]).all()
+                                                            and (toks[b] == ref["tokens"][b]).all())))
+            positions = x.B * (x.N + 1)
+        flagged = int(ref["flag_accept"].sum() + ref["flag_sample"].sum())
+        res["parity_vs_oracle"] = {"positions": positions, "flagged_frac": flagged / positions,
+                                   "differ_frac": differ / positions}
+    _PARITY_JOBS.clear()
+
+
 def oracle_leg(x, seconds, rows_hint=None):
     """Times the CPU oracle on whole-request samples of the workload on all host
     cores; returns (positions/s, threads, sample description, oracle result of
@@ -603,6 +639,7 @@ def main():
         line["cpu_baseline"] = {"value": pos, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
                                 "parity_vs_gpu": {"requests": int(x.B),
                                                   "mismatched_requests": int((got_t != ref["out_tokens"]).any(1).sum())}}
+        cpu_parity_leg()
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:
@@ -662,6 +699,10 @@ def _other_chain(sv, x, dev, dist, peak, name, target_s=0.5):
            "bytes_per_launch": {"algorithmic": b_alg, "position_parallel": b_par, "dense": b_dense,
                                 "streamed_by_kernel": (c1["bytes_loaded"] - c0["bytes_loaded"]) / n},
            "mean_accepted": float(na.mean())}
+    if x.draft_probs is not None:
+        a = na.astype(np.int64)
+        res["alpha_achieved"] = float(a.sum() / max(1, (a + (a < x.k)).sum()))
+        _PARITY_JOBS.append(("chain", res, x, (case.copies[0]["out"].cpu().numpy(), na)))
     del case
     torch.cuda.empty_cache()
     return res
@@ -896,11 +937,13 @@ def _other_tree_sampled(sv, W, dev, dist, peak, target_s=0.5):
     path, length = outs[0][0].cpu().numpy(), outs[0][2].cpu().numpy()
     b_alg = tree_sampled_bytes(x.parent, path, length, x.V, 2)
     ach = b_alg / (us * 1e-6) / 1e9
-    return {"workload": "sampled tree B=16 N=60 levels (4,8,16,16,16) V=128256 bf16 T=0.7 lambda=0.3 (Zipf)",
-            "positions_per_s": float(x.B * x.N) / (us * 1e-6), "tokens_per_s": float(length.sum()) / (us * 1e-6),
-            "kernel_us": us, "achieved_gbs_alg": ach, "frac_alg": ach / peak,
-            "bytes_per_launch": {"algorithmic": b_alg, "dense_inputs": float(per_copy)},
-            "mean_tokens_per_request": float(length.mean())}
+    res = {"workload": "sampled tree B=16 N=60 levels (4,8,16,16,16) V=128256 bf16 T=0.7 lambda=0.3 (Zipf)",
+           "positions_per_s": float(x.B * x.N) / (us * 1e-6), "tokens_per_s": float(length.sum()) / (us * 1e-6),
+           "kernel_us": us, "achieved_gbs_alg": ach, "frac_alg": ach / peak,
+           "bytes_per_launch": {"algorithmic": b_alg, "dense_inputs": float(per_copy)},
+           "mean_tokens_per_request": float(length.mean())}
+    _PARITY_JOBS.append(("tree", res, x, (path, outs[0][1].cpu().numpy(), length)))
+    return res
 
 
 def _other_next_step(sv, W, dev, dist, peak, target_s=0.3):

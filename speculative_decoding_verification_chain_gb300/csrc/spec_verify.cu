@@ -78,13 +78,11 @@ constexpr uint32_t kResolved = 0x80000000u;
 constexpr uint32_t kIdxMask = 0x3fffffffu;
 constexpr uint32_t kDecided = 0x80000000u;
 constexpr uint32_t kNeedsResidual = 0x40000000u;
-constexpr uint32_t kSkipInc = 0x10000u;                 // split counter: skipped splits count here
 constexpr unsigned long long kWaitLimitNs = 500000000ull;   // 0.5 s: default wait limit; always the limit
                                                             // on copies still in flight at exit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kEarlyMax = 4;                            // children per node given an early-rejection check
 constexpr uint32_t kFirstF = 1u << 6;                   // stage flag: first stage of its unit
-constexpr uint32_t kSkipF = 1u << 7;                    // stage flag: empty, the unit's row is not needed
 constexpr int kThrOff = kSubBytes + 64;                 // A stage: 16-byte chunks holding the children's logits
 static_assert(kThrOff + 16 * kEarlyMax <= kStageBytes, "threshold chunks do not fit in the stage");
 static_assert(kResSlots % kEpilogueWarps == 0, "result slots must split evenly over the epilogue warps");
@@ -125,6 +123,7 @@ struct Params {
     uint32_t *req_state;         // [B] decision
     uint32_t *res_ctr;           // [B] residual units done
     uint32_t *early;             // [B*R] node known rejected before its parent row resolved
+    unsigned long long *req_mask;   // [B] rows resolved (mask decisions, R <= 64)
     uint32_t *reset_base;
     uint32_t reset_words;
     RowStat *rowstat;            // [B*R]
@@ -149,6 +148,9 @@ struct Params {
     const int32_t *cu;           // ragged chains: request b has cu[b+1] - cu[b] drafts (null: R - 1 each)
     int total_drafts;            // ragged chains: cu[B] (packed draft rows; logit rows add one per request)
     int ahead;                   // stages the producer may have in flight
+    int mask_mode;               // R <= 64: requests decide from their resolved-row mask and rows of
+                                 // nodes known rejected are dropped without accounting; else every row
+                                 // is streamed and a request finalises when all its rows have settled
     unsigned long long wait_ns;  // limit of every inter-block or inter-warp wait
     int16_t parent[kMaxRows];
     uint8_t depth[kMaxRows];
@@ -179,7 +181,6 @@ struct __align__(16) StageInfo {
 
 struct ResSlot {
     int kind, b, n, j;
-    int skip;                   // the unit was skipped (empty stage): account only
     float c2;
     int xtok;
     float zx, qx, ux;
@@ -234,6 +235,12 @@ __device__ __forceinline__ uint32_t atom_add_acqrel(uint32_t *p, uint32_t v) {
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+__device__ __forceinline__ unsigned long long atom_or_acqrel_u64(unsigned long long *p, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
 // 2^x by the SFU approximation (results below 2^-126 flush to zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -247,8 +254,8 @@ __device__ __forceinline__ void set_status(const Params &P, int bits) {
 
 // Bounded wait on an mbarrier phase; gives up (and raises the block's abort
 // flag) after P.wait_ns (at the first failed try when it is 0) or as soon as
-// another role has aborted.
-__device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parity) {
+// another role has aborted.  The phase-already-complete case stays inline.
+__device__ __noinline__ bool wait_bar_slow(const Params &P, Smem &S, uint64_t *bar, uint32_t parity) {
     if (P.wait_ns == 0) {
         // limit 0: one non-blocking test (try_wait may suspend the thread first)
         if (mbar_test_wait(bar, parity)) return true;
@@ -258,7 +265,6 @@ __device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parit
         }
         return false;
     }
-    if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
         if (*reinterpret_cast<volatile int *>(&S.abort_flag)) return false;
@@ -269,6 +275,11 @@ __device__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parit
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool wait_bar(const Params &P, Smem &S, uint64_t *bar, uint32_t parity) {
+    if (P.wait_ns != 0 && mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(P, S, bar, parity);
 }
 
 // ------------------------------------------------------------ weights --
@@ -506,16 +517,25 @@ __device__ __forceinline__ float warp_sum_scatter(const float (&v)[N], int lane)
     return c;
 }
 
+// Mode-dependent device code: MODE 0 = chains in the padded layout, 1 = ragged
+// chains (per-request draft counts from cu_num_draft_tokens), 2 = greedy trees.
+// Each mode's kernel compiles only the paths it runs (smaller code, fewer
+// run-time branches on the hot paths).
+template <int MODE>
+struct Dev {
+static constexpr bool kTree = MODE == 2;
+static constexpr bool kRagged = MODE == 1;
+
 // ------------------------------------------------------------ topology --
-__device__ __forceinline__ int parent_of(const Params &P, int n) { return P.tree ? P.parent[n] : n - 1; }
-__device__ __forceinline__ int depth_of(const Params &P, int n) { return P.tree ? P.depth[n] : n; }
+static __device__ __forceinline__ int parent_of(const Params &P, int n) { return kTree ? P.parent[n] : n - 1; }
+static __device__ __forceinline__ int depth_of(const Params &P, int n) { return kTree ? P.depth[n] : n; }
 
 // Request b's first draft slot in the packed per-draft inputs (tokens, accept
 // uniforms, q rows) and its number of drafts.  Padded batches: b * (R - 1) and
 // R - 1.  Ragged chains read the offsets; offsets outside [0, total] or a count
 // above R - 1 are clamped (and flagged) so no read leaves the inputs.
-__device__ __forceinline__ void draft_span(const Params &P, int b, int &first, int &count) {
-    if (!P.cu) {
+static __device__ __forceinline__ void draft_span(const Params &P, int b, int &first, int &count) {
+    if (!kRagged) {
         first = b * (P.R - 1);
         count = P.R - 1;
         return;
@@ -531,8 +551,8 @@ __device__ __forceinline__ void draft_span(const Params &P, int b, int &first, i
 }
 
 // Rows (nodes) of request b: drafts + 1.
-__device__ __forceinline__ int rows_of(const Params &P, int b) {
-    if (!P.cu) return P.R;
+static __device__ __forceinline__ int rows_of(const Params &P, int b) {
+    if (!kRagged) return P.R;
     int first, count;
     draft_span(P, b, first, count);
     return count + 1;
@@ -540,32 +560,32 @@ __device__ __forceinline__ int rows_of(const Params &P, int b) {
 
 // Input row of node n of request b in the logits (packed: each request's rows
 // follow its drafts' offsets, one extra row per request).
-__device__ __forceinline__ size_t in_row(const Params &P, int b, int n) {
-    if (!P.cu) return static_cast<size_t>(b) * P.R + n;
+static __device__ __forceinline__ size_t in_row(const Params &P, int b, int n) {
+    if (!kRagged) return static_cast<size_t>(b) * P.R + n;
     int first, count;
     draft_span(P, b, first, count);
     return static_cast<size_t>(first) + b + n;
 }
 
 // Per-draft input index of draft slot i (node i + 1) of request b.
-__device__ __forceinline__ size_t in_draft(const Params &P, int b, int i) {
-    if (!P.cu) return static_cast<size_t>(b) * (P.R - 1) + i;
+static __device__ __forceinline__ size_t in_draft(const Params &P, int b, int i) {
+    if (!kRagged) return static_cast<size_t>(b) * (P.R - 1) + i;
     int first, count;
     draft_span(P, b, first, count);
     return static_cast<size_t>(first) + i;
 }
 
-__device__ __forceinline__ int node_token(const Params &P, int b, int n) {
+static __device__ __forceinline__ int node_token(const Params &P, int b, int n) {
     return __ldg(P.tokens + in_draft(P, b, n - 1));
 }
 
 // Edge parent -> child accepted, given the parent's resolved row state.
-__device__ __forceinline__ bool edge_ok(uint32_t rs, bool greedy, int child_token) {
+static __device__ __forceinline__ bool edge_ok(uint32_t rs, bool greedy, int child_token) {
     if (!(rs & kResolved)) return false;
     return greedy ? (static_cast<int>(rs & kIdxMask) == child_token) : ((rs & 1u) != 0u);
 }
 
-__device__ __forceinline__ bool is_greedy(const Params &P, int b) {
+static __device__ __forceinline__ bool is_greedy(const Params &P, int b) {
     return !P.temperature || !(__ldg(P.temperature + b) > 0.0f);
 }
 
@@ -579,26 +599,26 @@ struct BlockSource {
 };
 
 // 2^((M_beta - m) c2) for a block maximum M_beta (exp weights), 1 for residuals.
-__device__ __forceinline__ float block_factor_of(const BlockSource &S, float bm) {
+static __device__ __forceinline__ float block_factor_of(const BlockSource &S, float bm) {
     return S.bmax ? ex2(__fmul_rn(__fsub_rn(bm, S.m), S.c2)) : 1.0f;
 }
 
-__device__ __forceinline__ float block_factor(const BlockSource &S, int beta) {
+static __device__ __forceinline__ float block_factor(const BlockSource &S, int beta) {
     return block_factor_of(S, S.bmax ? __ldcg(S.bmax + beta) : 0.0f);
 }
 
-__device__ __forceinline__ tf block_weight(const BlockSource &S, int beta) {
+static __device__ __forceinline__ tf block_weight(const BlockSource &S, int beta) {
     return tf_prod(__ldcg(S.bsum + beta), block_factor(S, beta));
 }
 
-constexpr int kLocBatch = 16;   // block sums a lane loads at once (one round trip at V = 128256)
+static constexpr int kLocBatch = 16;   // block sums a lane loads at once (one round trip at V = 128256)
 
 // Warp-wide: total weight and the block holding t = u * total.  Returns the
 // total; beta/base receive the block and the weight before it (all lanes).
 // Lane l owns blocks [l*per, (l+1)*per); the lane whose range holds t is then
 // scanned by the whole warp, one block per lane.  Sums and prefixes are
 // two-float.
-__device__ tf locate_block(const BlockSource &S, int nblk, float u, int lane, int &beta, tf &base) {
+static __device__ tf locate_block(const BlockSource &S, int nblk, float u, int lane, int &beta, tf &base) {
     const int per = (nblk + 31) / 32;
     const int lo = lane * per;
     const int hi = min(nblk, lo + per);
@@ -663,7 +683,7 @@ __device__ tf locate_block(const BlockSource &S, int nblk, float u, int lane, in
 // Warp-wide scan inside block beta of row (b, row): the first element whose
 // running weight exceeds t.  residual == false: exp weights relative to the
 // block max, scaled by the block factor; residual == true: max(0, p - q).
-__device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, tf base, tf t,
+static __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row, int beta, tf base, tf t,
                           bool residual, float invS, int lane) {
     const size_t rowz = in_row(P, b, row) * static_cast<size_t>(P.V);
     const int e0 = beta * kBlk + lane * 8;
@@ -712,7 +732,7 @@ __device__ int scan_block(const Params &P, const BlockSource &S, int b, int row,
 
 // Sample one token from row `row` of request b (warp-wide): residual weights
 // if `residual` (falling back to p when the residual has no mass), else p.
-__device__ int sample_row(const Params &P, int b, int row, bool residual, float u, int lane) {
+static __device__ int sample_row(const Params &P, int b, int row, bool residual, float u, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + row;
     const float m = __ldcg(&P.rowstat[ri].m);
     const float Sh = __ldcg(&P.rowstat[ri].Sh);
@@ -730,22 +750,36 @@ __device__ int sample_row(const Params &P, int b, int row, bool residual, float 
 }
 
 // --------------------------------------------------- request finalisation --
-// Warp-wide.  Every row of request b is settled: walk the tree, write the
-// outputs, publish the decision (and draw the bonus token of a sampled
-// request that accepted every draft).
-template <bool SMP>
-__device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int lane) {
+// Warp-wide: row states and node tokens of request b into the warp's scratch
+// (after the caller's acquire of every row it will use).  Returns whether a
+// draft token is outside [0, V).
+static __device__ bool load_request(const Params &P, Smem &S, int slot, int b, int Rb, int lane) {
     uint32_t *rs = S.fin_rs[slot];
     int *tok = S.fin_tok[slot];
-    uint8_t *acc = S.fin_acc[slot];
-    const int Rb = rows_of(P, b);
     int range_bad = 0;
     for (int i = lane; i < Rb; i += 32) {
         rs[i] = ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
         tok[i] = i > 0 ? node_token(P, b, i) : -1;
         if (i > 0 && (tok[i] < 0 || tok[i] >= P.V)) range_bad = 1;
     }
-    if (__any_sync(0xffffffffu, range_bad) && lane == 0) set_status(P, SPEC_STATUS_TOKEN_RANGE);
+    __syncwarp();
+    return __any_sync(0xffffffffu, range_bad) != 0;
+}
+
+// Warp-wide.  Request b is decided (every row its outcome depends on is
+// resolved): walk the tree, write the outputs, publish the decision (and draw
+// the bonus token of a sampled request that accepted every draft).  With
+// `loaded`, the warp's scratch already holds the request's states and tokens
+// and range_bad says whether a token was out of range.
+template <bool SMP>
+static __device__ int finalize_request(const Params &P, Smem &S, int slot, int b, int lane, bool loaded,
+                                             bool range_bad) {
+    uint32_t *rs = S.fin_rs[slot];
+    int *tok = S.fin_tok[slot];
+    uint8_t *acc = S.fin_acc[slot];
+    const int Rb = rows_of(P, b);
+    if (!loaded) range_bad = load_request(P, S, slot, b, Rb, lane);
+    if (range_bad && lane == 0) set_status(P, SPEC_STATUS_TOKEN_RANGE);
     __syncwarp();
     const bool greedy = !SMP || is_greedy(P, b);
     int bonus = 0;
@@ -783,23 +817,17 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
         } else {
             bonus = 1;
         }
-        P.out_count[b] = P.tree ? d + 1 : d;
+        P.out_count[b] = kTree ? d + 1 : d;
         acc[0] = static_cast<uint8_t>(d < 255 ? d : 255);   // accepted count for the slot fix-up below
     }
     bonus = __shfl_sync(0xffffffffu, bonus, 0);
-    if (P.slots && !P.tree) {
+    if (P.slots && !kTree) {
         // the slot_mapping fix-up fused here: request b's slots 0..a keep their
         // values (row 0 is the last accepted token), the rest become padding
         __syncwarp();
         const int a = acc[0];
         int64_t *sl = P.slots + in_row(P, b, 0);
         for (int j = a + 1 + lane; j < Rb; j += 32) sl[j] = P.pad;
-    }
-    if (SMP && bonus) {
-        const int a = Rb - 1;
-        const float u = __ldg(P.u_sample + in_row(P, b, a));
-        int t = sample_row(P, b, a, false, u, lane);
-        if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + a] = t;
     }
     if (lane == 0) {
         // Residual units read the decision and then this request's row data:
@@ -808,18 +836,105 @@ __device__ void finalize_request(const Params &P, Smem &S, int slot, int b, int 
         else st_relaxed(P.req_state + b, decision);
     }
     __syncwarp();
+    // a sampled request that accepted every draft draws its bonus token from the
+    // last row; the caller draws it (one draw site per kernel)
+    return (SMP && bonus) ? Rb - 1 : -1;
 }
 
-// One more row of request b is settled (resolved or known dead).
-template <bool SMP>
-__device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) {
+// Counting decisions (R > 64): one more row of request b has settled; true
+// when it was the request's last (every row resolved: the request is decided).
+static __device__ __forceinline__ bool settle_row(const Params &P, int b, int lane) {
     uint32_t old = 0;
     if (lane == 0) old = atom_add_acqrel(P.req_ctr + b, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == static_cast<uint32_t>(rows_of(P, b) - 1)) {
-        __syncwarp();   // the whole warp reads after lane 0's acquire
-        finalize_request<SMP>(P, S, slot, b, lane);
+    return old == static_cast<uint32_t>(rows_of(P, b) - 1);
+}
+
+// Chains: with the rows of mask m resolved (rows 0..r-1, r its trailing ones),
+// is request b decided?  Yes once one of rows 0..r-1 rejects its draft
+// (notacc: rows whose draft is not accepted), or every row is resolved.
+static __device__ __forceinline__ bool chain_decided(unsigned long long m, int Rb, unsigned long long notacc) {
+    const int r = (~m == 0ull) ? 64 : __ffsll(static_cast<long long>(~m)) - 1;
+    const int f = notacc ? __ffsll(static_cast<long long>(notacc)) - 1 : 64;
+    return f < r || r >= Rb;
+}
+
+// Greedy trees: with the rows of mask m resolved, is the request decided?
+// Yes once every accepted node (the root; a child whose parent is accepted and
+// resolved with an argmax equal to the child's token) is resolved.  Warp-wide:
+// lane l holds nodes l and l + 32; the accepted set grows one level per step.
+static __device__ __forceinline__ bool tree_decided(const Params &P, const uint32_t *rs, const int *tok, int Rb,
+                                                    unsigned long long m, int lane) {
+    bool e[2];
+    int par[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        par[h] = (c >= 1 && c < Rb) ? P.parent[c] : 0;
+        e[h] = c >= 1 && c < Rb && ((m >> par[h]) & 1ull) && edge_ok(rs[par[h]], true, tok[c]);
     }
+    unsigned long long a = 1ull;
+    for (int step = 0; step < 64; ++step) {
+        const unsigned long long na =
+            1ull | static_cast<unsigned long long>(__ballot_sync(0xffffffffu, e[0] && ((a >> par[0]) & 1ull))) |
+            (static_cast<unsigned long long>(__ballot_sync(0xffffffffu, e[1] && ((a >> par[1]) & 1ull))) << 32);
+        if (na == a) break;
+        a = na;
+    }
+    return (a & ~m) == 0ull;
+}
+
+// Mask decisions (R <= 64): row n of request b is resolved (its state written by
+// this warp's lane 0).  One atomic adds it to the request's mask; true for the
+// warp whose row turns the request from undecided to decided (it finalises the
+// request; the request's states and tokens are then in its scratch, and
+// range_bad says whether a token was out of range).  Rows of nodes known
+// rejected are never streamed and never recorded: nothing waits for them.
+static __device__ bool record_row(const Params &P, Smem &S, int slot, int b, int n, bool greedy, int lane,
+                           bool &range_bad) {
+    unsigned long long old = 0;
+    if (lane == 0) old = atom_or_acqrel_u64(P.req_mask + b, 1ull << n);
+    old = (static_cast<unsigned long long>(__shfl_sync(0xffffffffu, static_cast<uint32_t>(old >> 32), 0)) << 32) |
+          __shfl_sync(0xffffffffu, static_cast<uint32_t>(old), 0);
+    const unsigned long long now = old | (1ull << n);
+    // Only a row that can change the outcome needs the request's states: for a
+    // chain the row that extends the resolved prefix, for a tree a row whose
+    // parent is resolved (or the root).
+    if (kTree) {
+        if (n > 0 && !((old >> P.parent[n]) & 1ull)) return false;
+    } else {
+        const int r_old = (~old == 0ull) ? 64 : __ffsll(static_cast<long long>(~old)) - 1;
+        if (n != r_old) return false;
+    }
+    __syncwarp();   // the whole warp reads after lane 0's acquire
+    const int Rb = rows_of(P, b);
+    range_bad = load_request(P, S, slot, b, Rb, lane);
+    const uint32_t *rs = S.fin_rs[slot];
+    const int *tok = S.fin_tok[slot];
+    bool turn;
+    if (kTree) {
+        turn = tree_decided(P, rs, tok, Rb, now, lane) && !tree_decided(P, rs, tok, Rb, old, lane);
+    } else {
+        unsigned long long notacc = 0;
+        for (int base = 0; base < Rb - 1; base += 32) {
+            const int i = base + lane;
+            const bool na = i < Rb - 1 && !edge_ok(rs[i], greedy, tok[i + 1]);
+            notacc |= static_cast<unsigned long long>(__ballot_sync(0xffffffffu, na)) << base;
+        }
+        turn = chain_decided(now, Rb, notacc) && !chain_decided(old, Rb, notacc);
+    }
+    return turn;
+}
+
+// A row is done: record it (mask decisions) or settle it (counting), and
+// finalise the request if this row decided it.  Returns the row of a bonus draw
+// the caller must make, or -1.
+template <bool SMP>
+static __device__ __forceinline__ int finish_row(const Params &P, Smem &S, int slot, int b, int n, bool greedy, int lane) {
+    bool range_bad = false;
+    const bool loaded = P.mask_mode != 0;
+    const bool fin = loaded ? record_row(P, S, slot, b, n, greedy, lane, range_bad) : settle_row(P, b, lane);
+    return fin ? finalize_request<SMP>(P, S, slot, b, lane, loaded, range_bad) : -1;
 }
 
 // Warp-wide: resolve row n of request b once all its splits are in.
@@ -827,11 +942,10 @@ __device__ void settle_row(const Params &P, Smem &S, int slot, int b, int lane) 
 // (m, Srow) are the row statistics and (xtok, zx, qx, ux) the operands of the
 // accept test of node n+1 (xtok < 0: no child, or its token is out of range).
 template <bool SMP>
-__device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
+static __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2, int gidx, float gmax, float m,
                             tf Srow, int xtok, float zx, float qx, float ux, int lane) {
     const size_t ri = static_cast<size_t>(b) * P.R + n;
     const int Rb = rows_of(P, b);
-    uint32_t rejected = 0;   // sampled row with a child whose draft was rejected
     if (lane == 0) {
         uint32_t rsv;
         if (!SMP || greedy) {
@@ -857,80 +971,131 @@ __device__ void resolve_row(const Params &P, int b, int n, bool greedy, float c2
                     const float ex = ex2(__fmul_rn(__fsub_rn(zx, m), c2));
                     acc = ux * (qx * Srow.h) < ex;
                 }
-                rejected = acc == 0;
             }
             rsv = kResolved | acc;
         }
-        // Relaxed: skip checks and the early decisions use only the value; readers
-        // of the row's data (block sums and maxima, statistics) synchronise through
-        // the settle atomic that follows (acq_rel, same thread, cumulative over the
+        // Relaxed: skip checks use only the value; readers of the row's data (block
+        // sums and maxima, statistics) synchronise through the atomic that follows
+        // (the mask OR or the settle add: acq_rel, same thread, cumulative over the
         // consumers' writes this warp observed at the stage barrier) or through a
         // decision this thread publishes with release.
         st_relaxed(P.rowstate + ri, rsv);
     }
     __syncwarp();
-    // Sampled chain: publish the decision as soon as it is known, so the residual
-    // pass need not wait for the later rows (the finaliser writes the same value
-    // and covers every case left here): a rejection at this row with every
-    // earlier draft accepted (this thread wrote the row statistics the residual
-    // pass reads), or every draft accepted (no residual pass: its units can leave).
-    if (SMP && !greedy && !P.tree && P.units_total > P.units_a) {
-        const uint32_t rej_n = __shfl_sync(0xffffffffu, rejected, 0);
-        int f = -1;   // first draft not known accepted
-        bool rej = false;
-        for (int base = 0; base < Rb - 1 && f < 0; base += 32) {
-            const int i = base + lane;
-            uint32_t rs = 0;
-            // after a rejection at row n only the rows before it matter: the
-            // later ones are not read (a rejection at row 0 decides at once)
-            if (i < Rb - 1) rs = (i == n) ? (kResolved | (rej_n ? 0u : 1u))
-                                 : (rej_n && i > n) ? 0u
-                                 : ld_acquire(P.rowstate + static_cast<size_t>(b) * P.R + i);
-            const unsigned notacc = __ballot_sync(0xffffffffu, i < Rb - 1 && !((rs & kResolved) && (rs & 1u)));
-            if (notacc) {
-                const int l = __ffs(notacc) - 1;
-                f = base + l;
-                rej = __shfl_sync(0xffffffffu, (rs & kResolved) != 0u, l);
+}
+
+// --------------------------------------------------------------- roles --
+// Producer (warp 0).  What the producer needs of an A unit before streaming it,
+// loaded one stage ahead so the loads are in flight while the previous unit's
+// last stage streams: lane i (and i + 32) holds edge i of the unit's path
+// counted from the node upwards (the early-rejection flag of the edge's child,
+// the state of its parent row, the child's token); lane c < kEarlyMax the token
+// of child c (greedy rows: the consumers' early-rejection check); every lane the
+// request's temperature; lane 0, for a sampled row, node n+1's token and accept
+// uniform.
+struct Ahead {
+    int u;                       // unit, or -1 when none is known
+    int b, n, j;                 // request, node, split (A units)
+    int check;                   // the node's path is checked before it is streamed
+    int echild[2];
+    uint32_t ef[2], rs[2];
+    int etok[2];
+    int ktok;
+    float temp;
+    int xtok;
+    float ux;
+};
+
+static __device__ void ahead_load(const Params &P, Ahead &A, int u, bool check, int lane) {
+    A.u = u;
+    A.check = 0;
+    A.ktok = -1;
+    A.temp = 0.0f;
+    A.xtok = -1;
+    A.ux = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        A.ef[h] = 0u;
+        A.rs[h] = 0u;
+        A.etok[h] = -1;
+        A.echild[h] = 0;
+    }
+    if (u < 0 || u >= P.units_a) return;
+    const int per_node = P.B * P.ns;
+    const int n = u / per_node;
+    const int rem = u - n * per_node;
+    const int b = rem / P.ns;
+    A.n = n;
+    A.b = b;
+    A.j = rem - b * P.ns;
+    int first, count;   // request b's drafts: tokens[first + i] is node i + 1's token
+    draft_span(P, b, first, count);
+    const int Rb = count + 1;
+    if (n >= Rb) return;   // ragged: this request has fewer rows
+    if (P.temperature) A.temp = __ldg(P.temperature + b);
+    // children's tokens (greedy early-rejection check)
+    int nk, k0 = 0;
+    if (kTree) {
+        k0 = P.kid_off[n];
+        nk = P.kid_off[n + 1] - k0;
+    } else {
+        nk = n < Rb - 1 ? 1 : 0;
+    }
+    if (lane < min(nk, kEarlyMax))
+        A.ktok = __ldg(P.tokens + first + (kTree ? static_cast<int>(P.kid_list[k0 + lane]) : n + 1) - 1);
+    if (P.u_accept && lane == 0 && n < Rb - 1) {
+        A.xtok = __ldg(P.tokens + first + n);
+        A.ux = __ldg(P.u_accept + first + n);
+    }
+    if (!check || n == 0) return;
+    A.check = 1;
+    const int d = depth_of(P, n);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        if (i < d) {
+            int child = n;
+            if (kTree) {
+#pragma unroll 1
+                for (int q = 0; q < i; ++q) child = P.parent[child];
+            } else {
+                child = n - i;
             }
-        }
-        if (lane == 0) {
-            if (f < 0) st_release(P.req_state + b, kDecided);   // every draft accepted: bonus, no residual
-            else if (rej && f == n) st_release(P.req_state + b, kDecided | kNeedsResidual | static_cast<uint32_t>(f));
+            A.echild[h] = child;
+            A.etok[h] = __ldg(P.tokens + first + child - 1);
         }
     }
 }
 
-// --------------------------------------------------------------- roles --
-// Producer (warp 0): is node n of request b already known to be rejected?
-// (An edge on its path rejected by a resolved parent row, or flagged early.)
-__device__ bool node_dead(const Params &P, int b, int n, bool greedy, int lane) {
-    if (n == 0) return false;
-    const int d = depth_of(P, n);
-    bool dead = false;
-    for (int base = 0; base < d && !dead; base += 32) {
-        int i = base + lane;
-        bool bad = false;
-        if (i < d) {
-            int child = n;
-            if (P.tree) {
-                for (int s = 0; s < i; ++s) child = P.parent[child];
-            } else {
-                child = n - i;
-            }
-            int par = parent_of(P, child);
-            const size_t rb = static_cast<size_t>(b) * P.R;
-            const uint32_t ef = ld_relaxed(P.early + rb + child);
-            const uint32_t rs = ld_relaxed(P.rowstate + rb + par);
-            bad = ef != 0u || ((rs & kResolved) && !edge_ok(rs, greedy, node_token(P, b, child)));
+// The changing facts of the unit's path (early-rejection flags, parent row
+// states): loaded when the unit is about to start, so they are as fresh as
+// possible; they arrive while the producer waits for the unit's first slot.
+static __device__ __forceinline__ void check_issue(const Params &P, Ahead &A, int lane) {
+    if (!A.check) return;
+    const size_t rb = static_cast<size_t>(A.b) * P.R;
+    const int d = depth_of(P, A.n);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (lane + 32 * h < d) {
+            A.ef[h] = ld_relaxed(P.early + rb + A.echild[h]);
+            A.rs[h] = ld_relaxed(P.rowstate + rb + parent_of(P, A.echild[h]));
         }
-        dead = __any_sync(0xffffffffu, bad);
     }
-    return dead;
+}
+
+// Is the A unit's node known to be rejected?  (An edge on its path flagged
+// early, or rejected by its resolved parent row.)  Warp-wide.
+static __device__ __forceinline__ bool ahead_dead(const Ahead &A, bool greedy) {
+    bool bad = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        bad |= A.ef[h] != 0u || ((A.rs[h] & kResolved) && !edge_ok(A.rs[h], greedy, A.etok[h]));
+    return A.check && __any_sync(0xffffffffu, bad);
 }
 
 // Copy geometry: 16-byte aligned bulk range covering [g, g + cnt*es), clipped
 // to the tensor's last full 16 bytes; elements past the clip come from global.
-__device__ __forceinline__ void copy_geom(const uint8_t *g, int cnt, int es, unsigned long long end, int &sh,
+static __device__ __forceinline__ void copy_geom(const uint8_t *g, int cnt, int es, unsigned long long end, int &sh,
                                           int &tail, const uint8_t *&src, uint32_t &nbytes) {
     unsigned long long a0 = reinterpret_cast<unsigned long long>(g);
     unsigned long long a1 = a0 + static_cast<unsigned long long>(cnt) * es;
@@ -952,13 +1117,13 @@ __device__ __forceinline__ void copy_geom(const uint8_t *g, int cnt, int es, uns
 }
 
 template <int ES, bool SMP>
-__device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
+static __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
     int it = 0;   // stages issued
-    int u_next = static_cast<int>(blockIdx.x);   // first unit without a claim
     const int claim_base = static_cast<int>(gridDim.x);
     bool aborted = false;
     unsigned long long loaded_bytes = 0;
     int a_loaded = 0, a_skipped = 0, b_loaded = 0, b_skipped = 0;
+    const bool dropping = P.mask_mode != 0;   // rows of nodes known rejected are not streamed
 
     // Reserve the next stage: at most P.ahead stages are issued and not yet
     // released (stage it - ahead released; consumers release in order, so its
@@ -972,99 +1137,115 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
         return true;
     };
 
-    bool first = true;   // the block's first unit: no row can be resolved or flagged yet, no check
+    // Claims run ahead of the work: the claim for the unit after `cur` is issued
+    // one stage before that unit's lookahead loads, which go out with cur's last
+    // stage (so with one-stage units, the claim goes out with the previous
+    // unit's stage).  A block holds at most two claimed units it has not started.
+    int pc = 0;               // lane 0: result of the claim in flight
+    bool pc_live = false;     // a claim is in flight
+    auto claim_issue = [&]() {
+        if (lane == 0) pc = claim_base + static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
+        pc_live = true;
+    };
+    Ahead cur, nxt;
+    bool nxt_known = false;
+    bool checks = false;      // the block's first unit is not checked: nothing can be known yet
+    // The next unit: take its claim (issuing it if none is in flight) and load its
+    // lookahead facts; with one-stage units, claim the unit after it at once.
+    auto advance_next = [&](bool one_stage) {
+        if (nxt_known) return;
+        if (!pc_live) claim_issue();
+        const int v = __shfl_sync(0xffffffffu, pc, 0);
+        pc_live = false;
+        ahead_load(P, nxt, v, dropping && checks, lane);
+        checks = true;
+        nxt_known = true;
+        if (one_stage && v < P.units_total) claim_issue();
+    };
+    // The first unit is static (block b takes unit b) and is never dropped: before
+    // anything else, its first stages start moving into L2, so HBM is busy while
+    // the producer sets up (its bulk copies then find the bytes on chip).
+    if (lane == 0 && !kRagged && static_cast<int>(blockIdx.x) < P.units_a) {
+        const int u0 = static_cast<int>(blockIdx.x);
+        const int n0 = u0 / (P.B * P.ns);
+        const int r0 = u0 - n0 * (P.B * P.ns);
+        const int b0 = r0 / P.ns;
+        const int s0 = (r0 - b0 * P.ns) * P.sps;
+        const int ns0 = min(min(P.nsub, s0 + P.sps) - s0, P.ahead);
+        const int e0 = s0 * P.esub;
+        const int e1 = min(P.V, e0 + ns0 * P.esub);
+        const unsigned long long a0 =
+            reinterpret_cast<unsigned long long>(P.logits) + (in_row(P, b0, n0) * P.V + e0) * ES;
+        const unsigned long long lo = a0 & ~15ull;
+        const unsigned long long hi = min((a0 + static_cast<unsigned long long>(e1 - e0) * ES + 15ull) & ~15ull,
+                                          P.logits_end & ~15ull);
+        if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void *>(lo), static_cast<uint32_t>(hi - lo));
+    }
+    // the next unit is claimed at once
+    pc = static_cast<int>(blockIdx.x);
+    pc_live = true;
+    advance_next(true);
+    cur = nxt;
+    nxt_known = false;
+
     while (!aborted) {
-        int u = __shfl_sync(0xffffffffu, u_next, 0);
+        const int u = cur.u;
         if (u < 0 || u >= P.units_total) break;
-        // The following unit is claimed late (two stages before this one ends) so a
-        // block never holds a claimed unit long while others run out of work.
-        bool claimed = false;
-        auto claim_next = [&]() {
-            if (lane == 0) u_next = claim_base + static_cast<int>(atomicAdd(P.ctrl + 0, 1u));
-            claimed = true;
-        };
         if (u < P.units_a) {
             // ---------------- A unit: split j of row n of request b
-            const int per_node = P.B * P.ns;
-            const int n = u / per_node;
-            const int rem = u - n * per_node;
-            const int b = rem / P.ns;
-            const int j = rem - b * P.ns;
-            if (P.cu && n >= rows_of(P, b)) {   // ragged: this request has fewer rows
-                claim_next();
-                continue;
-            }
-            const bool greedy = !SMP || is_greedy(P, b);
-            const float c2 = greedy ? 0.0f : kLog2e / __ldg(P.temperature + b);
+            const int n = cur.n, b = cur.b, j = cur.j;
             const int s0 = j * P.sps;
             const int s1 = min(P.nsub, s0 + P.sps);
-            // Greedy rows: draft tokens of (up to kEarlyMax) children, for the
-            // consumers' early-rejection check (loaded alongside the dead check).
-            int nk = 0, ktok = -1;
-            if (greedy) {
-                int k0 = 0;
-                if (P.tree) {
-                    k0 = P.kid_off[n];
-                    nk = P.kid_off[n + 1] - k0;
-                } else {
-                    nk = n < rows_of(P, b) - 1 ? 1 : 0;
-                }
-                nk = min(nk, kEarlyMax);
-                if (lane < nk) ktok = node_token(P, b, P.tree ? static_cast<int>(P.kid_list[k0 + lane]) : n + 1);
-            }
-            const bool check = !first;
-            first = false;
-            if (check && node_dead(P, b, n, greedy, lane)) {
-                // not needed: an empty stage carries the unit to the epilogue for its accounting
-                ++a_skipped;
-                int st;
-                if (!acquire_stage(st)) {
+            const bool one_stage = P.sps == 1;
+            bool skip = kRagged && n >= rows_of(P, b);   // ragged: this request has fewer rows
+            const bool greedy = !SMP || !(cur.temp > 0.0f);
+            const float c2 = greedy ? 0.0f : kLog2e / cur.temp;
+            int st0 = -1;   // the first stage's slot, reserved while the check's loads fly
+            if (!skip && dropping) {
+                check_issue(P, cur, lane);
+                if (!acquire_stage(st0)) {
                     aborted = true;
                     break;
                 }
-                if (lane == 0) {
-                    StageInfo &I = S.info[st];
-                    I.b = b;
-                    I.n = n;
-                    I.j = j;
-                    I.e0 = 0;
-                    I.cnt = 0;
-                    I.c2 = c2;
-                    I.xtok = -1;
-                    I.sh = 0;
-                    I.tail = 0;
-                    I.gz = P.logits;
-                    I.flags = kA | (1 << 4) | kSkipF;
-                    mbar_arrive(&S.full[st]);
+                if (ahead_dead(cur, greedy)) {
+                    skip = true;
+                    ++a_skipped;
                 }
-                ++it;
-                claim_next();
+            }
+            if (skip) {
+                advance_next(one_stage);
+                cur = nxt;
+                nxt_known = false;
                 continue;
             }
             ++a_loaded;
             const size_t rowe = in_row(P, b, n) * static_cast<size_t>(P.V);
-            // accept-test operands of node n+1 (sampled rows): loaded now, used by the
-            // epilogue after the whole row has streamed
-            int xtok = -1;
-            float zx = 0.0f, qx = 0.0f, ux = 0.0f;
-            if (SMP && lane == 0 && !greedy && n < rows_of(P, b) - 1) {
-                const int x = node_token(P, b, n + 1);
-                ux = __ldg(P.u_accept + in_draft(P, b, n));
-                if (x >= 0 && x < P.V) {
-                    xtok = x;
-                    zx = logit_global(P, rowe + x);
-                    qx = __ldg(P.q + in_draft(P, b, n) * P.V + x);
-                }
+            // accept-test operands of node n+1 (sampled rows): loaded now, written
+            // into the unit's last stage (the loads overlap the stage waits)
+            float zx = 0.0f, qx = 0.0f;
+            const int xtok = (!greedy && cur.xtok >= 0 && cur.xtok < P.V) ? cur.xtok : -1;
+            if (SMP && lane == 0 && !greedy && xtok >= 0) {
+                zx = logit_global(P, rowe + static_cast<size_t>(xtok));
+                qx = __ldg(P.q + in_draft(P, b, n) * P.V + static_cast<size_t>(xtok));
+            }
+            int nk = 0;
+            if (greedy) {
+                if (kTree) nk = P.kid_off[n + 1] - P.kid_off[n];
+                else nk = n < rows_of(P, b) - 1 ? 1 : 0;
+                nk = min(nk, kEarlyMax);
             }
             for (int s = s0; s < s1; ++s) {
-                int st;
-                if (!acquire_stage(st)) {
-                    aborted = true;
-                    break;
+                int st = st0;
+                if (s != s0 || st0 < 0) {
+                    if (!acquire_stage(st)) {
+                        aborted = true;
+                        break;
+                    }
                 }
+                const bool last = (s == s1 - 1);
+                if (s == max(s0, s1 - 2) && !one_stage && !last && !pc_live && !nxt_known) claim_issue();
                 if (lane == 0) {
                     StageInfo &I = S.info[st];
-                    const int last = (s == s1 - 1);
                     I.b = b;
                     I.n = n;
                     I.j = j;
@@ -1075,14 +1256,14 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     if (last) {
                         I.zx = zx;
                         I.qx = qx;
-                        I.ux = ux;
+                        I.ux = cur.ux;
                     }
                     I.gz = P.logits + (rowe + I.e0) * ES;
                     const uint8_t *src;
                     uint32_t nb;
                     copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, src, nb);
                     const int fast = (I.sh == 0 && I.tail == I.cnt && (I.cnt & 7) == 0);
-                    I.flags = kA | (last << 4) | (fast << 5) | (s == s0 ? kFirstF : 0u);
+                    I.flags = kA | (static_cast<int>(last) << 4) | (fast << 5) | (s == s0 ? kFirstF : 0u);
                     loaded_bytes += nb;
                     fence_proxy_async();
                     uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
@@ -1101,11 +1282,10 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     }
                 }
                 if (s == s0) {
-                    // the children's logits travel with the first stage (their tokens
-                    // may still be in flight when the row's copy has gone out)
+                    // the children's logits travel with the first stage
                     int kt[kEarlyMax];
 #pragma unroll
-                    for (int c = 0; c < kEarlyMax; ++c) kt[c] = __shfl_sync(0xffffffffu, ktok, c);
+                    for (int c = 0; c < kEarlyMax; ++c) kt[c] = __shfl_sync(0xffffffffu, cur.ktok, c);
                     if (lane == 0) {
                         StageInfo &I = S.info[st];
                         uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
@@ -1142,12 +1322,11 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
                     }
                 }
                 ++it;
-                if (s == max(s0, s1 - 2)) claim_next();
+                if (last) advance_next(one_stage);   // the next unit's lookahead rides on this stage
             }
-            if (!claimed) claim_next();
+            if (aborted) break;
         } else if (SMP) {
             // ---------------- B unit: chunk c of the rejected row of request b
-            claim_next();
             const int v = u - P.units_a;
             const int b = v / P.ncb;
             const int c = v - b * P.ncb;
@@ -1168,56 +1347,65 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
             const int a = static_cast<int>(stv & kIdxMask);
             if (!(stv & kDecided) || !(stv & kNeedsResidual) || a >= rows_of(P, b) - 1) {
                 ++b_skipped;
-                continue;
-            }
-            ++b_loaded;
-            const size_t ri = static_cast<size_t>(b) * P.R + a;
-            const float m = __ldcg(&P.rowstat[ri].m);
-            const float Sh = __ldcg(&P.rowstat[ri].Sh);
-            const float c2 = kLog2e / __ldg(P.temperature + b);
-            const size_t rowe = in_row(P, b, a) * static_cast<size_t>(P.V);
-            const size_t qrowe = in_draft(P, b, a) * static_cast<size_t>(P.V);
-            const int e_begin = c * P.ecb;
-            const int e_end = min(P.V, e_begin + P.ecb);
-            for (int e = e_begin; e < e_end; e += P.esb) {
-                int st;
-                if (!acquire_stage(st)) {
-                    aborted = true;
-                    break;
-                }
-                if (lane == 0) {
-                    StageInfo &I = S.info[st];
-                    const int last = (e + P.esb >= e_end);
-                    I.b = b;
-                    I.n = a;
-                    I.j = c;
-                    I.e0 = e;
-                    I.cnt = min(P.esb, P.V - e);
-                    I.c2 = c2;
-                    I.m = m;
-                    I.invS = 1.0f / Sh;
-                    I.gz = P.logits + (rowe + e) * ES;
-                    I.gq = reinterpret_cast<const uint8_t *>(P.q + qrowe + e);
-                    const uint8_t *sz, *sq;
-                    uint32_t nz, nq;
-                    copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, sz, nz);
-                    copy_geom(I.gq, I.cnt, 4, P.q_end, I.shq, I.tailq, sq, nq);
-                    const int fast = (I.sh == 0 && I.tail == I.cnt && I.shq == 0 && I.tailq == I.cnt && (I.cnt & 7) == 0);
-                    I.flags = kB | (last << 4) | (fast << 5);
-                    loaded_bytes += nz + nq;
-                    fence_proxy_async();
-                    uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
-                    if (nz + nq) {
-                        mbar_expect_tx(&S.full[st], nz + nq);
-                        if (nz) bulk_g2s(dst, sz, nz, &S.full[st]);
-                        if (nq) bulk_g2s(dst + P.qoff, sq, nq, &S.full[st]);
-                    } else {
-                        mbar_arrive(&S.full[st]);
+                advance_next(false);
+            } else {
+                ++b_loaded;
+                const size_t ri = static_cast<size_t>(b) * P.R + a;
+                const float m = __ldcg(&P.rowstat[ri].m);
+                const float Sh = __ldcg(&P.rowstat[ri].Sh);
+                const float c2 = kLog2e / __ldg(P.temperature + b);
+                const size_t rowe = in_row(P, b, a) * static_cast<size_t>(P.V);
+                const size_t qrowe = in_draft(P, b, a) * static_cast<size_t>(P.V);
+                const int e_begin = c * P.ecb;
+                const int e_end = min(P.V, e_begin + P.ecb);
+                for (int e = e_begin; e < e_end; e += P.esb) {
+                    int st;
+                    if (!acquire_stage(st)) {
+                        aborted = true;
+                        break;
                     }
+                    const int last = (e + P.esb >= e_end);
+                    if (!last && e + 2 * P.esb >= e_end && !pc_live && !nxt_known) claim_issue();
+                    if (lane == 0) {
+                        StageInfo &I = S.info[st];
+                        I.b = b;
+                        I.n = a;
+                        I.j = c;
+                        I.e0 = e;
+                        I.cnt = min(P.esb, P.V - e);
+                        I.c2 = c2;
+                        I.m = m;
+                        I.invS = 1.0f / Sh;
+                        I.gz = P.logits + (rowe + e) * ES;
+                        I.gq = reinterpret_cast<const uint8_t *>(P.q + qrowe + e);
+                        const uint8_t *sz, *sq;
+                        uint32_t nz, nq;
+                        copy_geom(I.gz, I.cnt, ES, P.logits_end, I.sh, I.tail, sz, nz);
+                        copy_geom(I.gq, I.cnt, 4, P.q_end, I.shq, I.tailq, sq, nq);
+                        const int fast =
+                            (I.sh == 0 && I.tail == I.cnt && I.shq == 0 && I.tailq == I.cnt && (I.cnt & 7) == 0);
+                        I.flags = kB | (last << 4) | (fast << 5);
+                        loaded_bytes += nz + nq;
+                        fence_proxy_async();
+                        uint8_t *dst = ring + static_cast<size_t>(st) * kStageBytes;
+                        if (nz + nq) {
+                            mbar_expect_tx(&S.full[st], nz + nq);
+                            if (nz) bulk_g2s(dst, sz, nz, &S.full[st]);
+                            if (nq) bulk_g2s(dst + P.qoff, sq, nq, &S.full[st]);
+                        } else {
+                            mbar_arrive(&S.full[st]);
+                        }
+                    }
+                    ++it;
+                    if (last) advance_next(false);
                 }
-                ++it;
+                if (aborted) break;
             }
+        } else {
+            advance_next(false);
         }
+        cur = nxt;
+        nxt_known = false;
     }
     // End marker (not after an abort: the consumers are leaving already).
     if (!aborted) {
@@ -1242,7 +1430,7 @@ __device__ void producer(const Params &P, Smem &S, uint8_t *ring, int lane) {
 
 // Fold a finished sum s (relative to reference max M) into a warp's running
 // (Mw, Sw + Sc) statistics, with Neumaier compensation.
-__device__ __forceinline__ void fold_stats(float M, float s, float c2, float &Mw, float &Sw, float &Sc) {
+static __device__ __forceinline__ void fold_stats(float M, float s, float c2, float &Mw, float &Sw, float &Sc) {
     if (M == -INFINITY) return;   // an all -inf stretch adds nothing
     float add;
     if (M > Mw) {
@@ -1261,7 +1449,7 @@ __device__ __forceinline__ void fold_stats(float M, float s, float c2, float &Mw
 }
 
 // Does either bf16 half of a exceed the matching half of b?  (NaN: no.)
-__device__ __forceinline__ bool bf16x2_any_gt(uint32_t a, uint32_t b) {
+static __device__ __forceinline__ bool bf16x2_any_gt(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("{\n\t.reg .pred p, q;\n\t"
         "setp.gt.bf16x2 p|q, %1, %2;\n\t"
@@ -1275,7 +1463,7 @@ __device__ __forceinline__ bool bf16x2_any_gt(uint32_t a, uint32_t b) {
 // Packed running maximum of the two bf16 halves with the row index of the
 // group that first set each half's record (branch-free): the half of `a`
 // that beats the record moves it to group start ge.  NaN freezes both.
-__device__ __forceinline__ void bf16x2_record(uint32_t a, uint32_t &pk, int ge, int &glo, int &ghi) {
+static __device__ __forceinline__ void bf16x2_record(uint32_t a, uint32_t &pk, int ge, int &glo, int &ghi) {
     asm("{\n\t.reg .pred plo, phi;\n\t"
         "setp.gt.bf16x2 plo|phi, %3, %2;\n\t"
         "selp.s32 %0, %4, %0, plo;\n\t"
@@ -1286,14 +1474,14 @@ __device__ __forceinline__ void bf16x2_record(uint32_t a, uint32_t &pk, int ge, 
 }
 
 // A bf16 value (given as its exact float) in both halves of a word.
-__device__ __forceinline__ uint32_t bf16_pair(float m) {
+static __device__ __forceinline__ uint32_t bf16_pair(float m) {
     const uint32_t h = __float_as_uint(m) >> 16;
     return h | (h << 16);
 }
 
 // Eight logits of a 16-byte (bf16) or 32-byte (fp32) register pair as floats.
 template <int ES>
-__device__ __forceinline__ void unpack8(const uint4 a, const uint4 c, float x[8]) {
+static __device__ __forceinline__ void unpack8(const uint4 a, const uint4 c, float x[8]) {
     if (ES == 2) {
         x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x);
         x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
@@ -1310,7 +1498,7 @@ __device__ __forceinline__ void unpack8(const uint4 a, const uint4 c, float x[8]
 // Greedy step over one 8-element group already in registers (row index of its
 // first element: e_first).
 template <int ES>
-__device__ __forceinline__ void greedy_regs(const uint4 a, const uint4 c, int e_first, float &best, int &bidx,
+static __device__ __forceinline__ void greedy_regs(const uint4 a, const uint4 c, int e_first, float &best, int &bidx,
                                             float &mx) {
     const float m = (ES == 2) ? vmax8_bf16(a) : vmax8_f32(a, c);
     mx = fmax_nan(mx, m);
@@ -1329,7 +1517,7 @@ __device__ __forceinline__ void greedy_regs(const uint4 a, const uint4 c, int e_
 // Greedy step over one 8-element group: NaN-propagating max into mx, and if
 // the group's max beats `best`, the group's first element equal to it.
 template <int ES>
-__device__ __forceinline__ void group_step(const View &v, int g, int e_row0, bool fast, float &best, int &bidx,
+static __device__ __forceinline__ void group_step(const View &v, int g, int e_row0, bool fast, float &best, int &bidx,
                                            float &mx, uint32_t &bad) {
     if (fast) {
         if (ES == 2) {
@@ -1378,7 +1566,7 @@ __device__ __forceinline__ void group_step(const View &v, int g, int e_row0, boo
 
 // Loads the 8 elements of lane `lane` in block blk of a stage.
 template <int ES>
-__device__ __forceinline__ int load_block8(const View &v, int blk, int lane, bool fast, float x[8], uint32_t &bad) {
+static __device__ __forceinline__ int load_block8(const View &v, int blk, int lane, bool fast, float x[8], uint32_t &bad) {
     const int e = blk * kBlk + lane * 8;
     if (fast) {
         if (ES == 2) {
@@ -1401,7 +1589,7 @@ __device__ __forceinline__ int load_block8(const View &v, int blk, int lane, boo
 }
 
 template <int ES, bool SMP>
-__device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, int lane, uint32_t &bad) {
+static __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, int lane, uint32_t &bad) {
     int it = 0;      // stages consumed
     int uc = 0;      // units handed to the epilogue
     float best = -INFINITY;   // greedy: running max of this lane
@@ -1475,7 +1663,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 if (lane < nk) {
                     const int ko = I.kofs[lane];
                     const int bb = I.b, nn = I.n;
-                    const int kid = P.tree ? static_cast<int>(P.kid_list[P.kid_off[nn] + lane]) : nn + 1;
+                    const int kid = kTree ? static_cast<int>(P.kid_list[P.kid_off[nn] + lane]) : nn + 1;
                     eidx = bb * P.R + kid;
                     if (ko >= 0) {
                         const uint8_t *pz = stage + kThrOff + 16 * lane + ko;
@@ -1714,7 +1902,6 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
                 }
                 if (cw == 0) {
                     R.kind = kind;
-                    R.skip = (hot.x & kSkipF) != 0u;
                     R.b = b;
                     R.n = n;
                     R.j = j;
@@ -1743,7 +1930,7 @@ __device__ void consumer(const Params &P, Smem &S, const uint8_t *ring, int cw, 
 }
 
 template <bool SMP>
-__device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
+static __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
     int uc = e;   // this warp takes units e, e + kEpilogueWarps, ...
     while (true) {
         const int slot = uc % kResSlots;
@@ -1755,7 +1942,6 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
         const float c2 = R.c2;
         const int xtok = R.xtok;
         const float zx = R.zx, qx = R.qx, ux = R.ux;
-        const bool skip = R.skip != 0;
         float v = lane < kConsumerWarps ? R.v[lane] : -INFINITY;
         int grp = lane < kConsumerWarps ? R.idx[lane] : -1;
         const float sw = lane < kConsumerWarps ? R.s[lane] : 0.0f;
@@ -1763,17 +1949,9 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.res_empty[slot]);
         uc += kEpilogueWarps;
-        if (kind == kA && skip) {
-            // skipped row: counts as a skipped split, the row stays unresolved
-            if (P.ns == 1) {
-                settle_row<SMP>(P, S, e, b, lane);
-            } else {
-                uint32_t old = 0;
-                if (lane == 0) old = atom_add_acqrel(P.row_ctr + static_cast<size_t>(b) * P.R + n, kSkipInc);
-                old = __shfl_sync(0xffffffffu, old, 0) + kSkipInc;
-                if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) settle_row<SMP>(P, S, e, b, lane);
-            }
-        } else if (kind == kA) {
+        int draw_row = -1;        // an inverse-CDF draw this warp makes for request b: the bonus token
+        bool draw_res = false;    // (p of the last row) or the residual token (max(0, p - q) of row n)
+        if (kind == kA) {
             const bool greedy = !SMP || (c2 == 0.0f);
             float um = 0.0f;
             tf uS = tf_of(0.0f);
@@ -1806,10 +1984,8 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                 uS = warp_sum_tf(t);
             }
             const size_t ri = static_cast<size_t>(b) * P.R + n;
-            if (P.ns == 1) {
-                resolve_row<SMP>(P, b, n, greedy, c2, grp, v, um, uS, xtok, zx, qx, ux, lane);
-                settle_row<SMP>(P, S, e, b, lane);
-            } else {
+            bool resolve_now = true;
+            if (P.ns > 1) {
                 uint32_t old = 0;
                 if (lane == 0) {
                     Partial pr;
@@ -1822,49 +1998,35 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
                     old = atom_add_acqrel(P.row_ctr + ri, 1u);
                 }
                 old = __shfl_sync(0xffffffffu, old, 0) + 1u;
-                if ((old & 0xffffu) + (old >> 16) == static_cast<uint32_t>(P.ns)) {
-                    if ((old >> 16) == 0u) {
-                        // every split loaded: combine the splits and resolve the row
-                        float gv = -INFINITY;
-                        int gg = -1;
-                        float rm = 0.0f;
-                        tf rS = tf_of(0.0f);
-                        if (greedy) {
-                            for (int q = lane; q < P.ns; q += 32) {
-                                const Partial *pp = P.partial + ri * P.ns + q;
-                                cand_merge(gv, gg, __ldcg(&pp->v), __ldcg(&pp->idx));
-                            }
-                            warp_cand(gv, gg);
-                        } else if (P.ns <= 32) {
-                            // one split per lane, read once (one round trip)
-                            float pv = -INFINITY;
-                            tf ps = tf_of(0.0f);
-                            if (lane < P.ns) {
-                                const float4 w = __ldcg(reinterpret_cast<const float4 *>(P.partial + ri * P.ns + lane));
-                                pv = w.x;
-                                ps = tf{w.z, w.w};
-                            }
-                            rm = warp_max(pv);
-                            tf t = tf_of(0.0f);
-                            if (ps.h != 0.0f) t = tf_mulf(ps, ex2(__fmul_rn(__fsub_rn(pv, rm), c2)));
-                            rS = warp_sum_tf(t);
-                        } else {
-                            float lm = -INFINITY;
-                            for (int q = lane; q < P.ns; q += 32) lm = fmaxf(lm, __ldcg(&P.partial[ri * P.ns + q].v));
-                            rm = warp_max(lm);
-                            tf t = tf_of(0.0f);
-                            for (int q = lane; q < P.ns; q += 32) {
-                                const Partial *pp = P.partial + ri * P.ns + q;
-                                const tf ps{__ldcg(&pp->sh), __ldcg(&pp->sl)};
-                                if (ps.h != 0.0f)
-                                    t = tf_add(t, tf_mulf(ps, ex2(__fmul_rn(__fsub_rn(__ldcg(&pp->v), rm), c2))));
-                            }
-                            rS = warp_sum_tf(t);
+                // The last split in resolves the row.  (Splits of a row found dead
+                // are never streamed, so such a row never completes: nothing needs it.)
+                resolve_now = old == static_cast<uint32_t>(P.ns);
+                if (resolve_now) {
+                    __syncwarp();   // the whole warp reads the partials after lane 0's acquire
+                    if (greedy) {
+                        v = -INFINITY;
+                        grp = -1;
+                        for (int q = lane; q < P.ns; q += 32) {
+                            const Partial *pp = P.partial + ri * P.ns + q;
+                            cand_merge(v, grp, __ldcg(&pp->v), __ldcg(&pp->idx));
                         }
-                        resolve_row<SMP>(P, b, n, greedy, c2, gg, gv, rm, rS, xtok, zx, qx, ux, lane);
+                        warp_cand(v, grp);
+                    } else {
+                        float lm = -INFINITY;
+                        for (int q = lane; q < P.ns; q += 32) lm = fmaxf(lm, __ldcg(&P.partial[ri * P.ns + q].v));
+                        um = warp_max(lm);
+                        tf t = tf_of(0.0f);
+                        for (int q = lane; q < P.ns; q += 32) {
+                            const float4 w = __ldcg(reinterpret_cast<const float4 *>(P.partial + ri * P.ns + q));
+                            if (w.z != 0.0f) t = tf_add(t, tf_mulf(tf{w.z, w.w}, ex2(__fmul_rn(__fsub_rn(w.x, um), c2))));
+                        }
+                        uS = warp_sum_tf(t);
                     }
-                    settle_row<SMP>(P, S, e, b, lane);
                 }
+            }
+            if (resolve_now) {
+                resolve_row<SMP>(P, b, n, greedy, c2, grp, v, um, uS, xtok, zx, qx, ux, lane);
+                draw_row = finish_row<SMP>(P, S, e, b, n, greedy, lane);
             }
         } else if (SMP) {
             // B unit: the last chunk of a request's residual draws the token
@@ -1875,16 +2037,22 @@ __device__ void epilogue(const Params &P, Smem &S, int e, int lane) {
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == static_cast<uint32_t>(P.ncb - 1)) {
                 __syncwarp();
-                const float u = __ldg(P.u_sample + in_row(P, b, n));
-                int t = sample_row(P, b, n, true, u, lane);
-                if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + n] = t;
+                draw_row = n;
+                draw_res = true;
             }
+        }
+        if (SMP && draw_row >= 0) {
+            const float u = __ldg(P.u_sample + in_row(P, b, draw_row));
+            const int t = sample_row(P, b, draw_row, draw_res, u, lane);
+            if (lane == 0) P.out_tokens[static_cast<size_t>(b) * (P.D + 1) + draw_row] = t;
         }
     }
 }
 
+};  // struct Dev
+
 // --------------------------------------------------------------- kernel --
-template <int ES, bool SMP>
+template <int ES, bool SMP, int MODE>
 __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
@@ -1910,9 +2078,9 @@ __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P)
     }
     __syncthreads();
 
-    if (warp == 0) producer<ES, SMP>(P, S, ring, lane);
-    else if (warp <= kEpilogueWarps) epilogue<SMP>(P, S, warp - 1, lane);
-    else consumer<ES, SMP>(P, S, ring, warp - 1 - kEpilogueWarps, lane, bad);
+    if (warp == 0) Dev<MODE>::template producer<ES, SMP>(P, S, ring, lane);
+    else if (warp <= kEpilogueWarps) Dev<MODE>::template epilogue<SMP>(P, S, warp - 1, lane);
+    else Dev<MODE>::template consumer<ES, SMP>(P, S, ring, warp - 1 - kEpilogueWarps, lane, bad);
 
     bad = __any_sync(0xffffffffu, bad != 0);
     if (lane == 0 && bad) set_status(P, SPEC_STATUS_NONFINITE);
@@ -1984,7 +2152,7 @@ spec_status_t fail(spec_status_t s, const char *fmt, const char *detail) {
 }
 
 struct Layout {
-    size_t stats, reset, reset_bytes, ctrl, row_ctr, rowstate, req_ctr, req_state, res_ctr, early;
+    size_t stats, reset, reset_bytes, ctrl, req_mask, row_ctr, rowstate, req_ctr, req_state, res_ctr, early;
     size_t rowstat, partial, bmaxA, bsumA, bsumB, total;
     int esub, nsub, esb, ecb, qoff, ncb, nblk;
 };
@@ -2012,6 +2180,8 @@ bool make_layout(int B, int R, int V, spec_dtype_t dtype, Layout &L) {
     L.reset = off;
     L.ctrl = off;
     off += 32 * 4;
+    L.req_mask = off;
+    off += static_cast<size_t>(B) * 8;
     L.row_ctr = off;
     off += BR * 4;
     L.rowstate = off;
@@ -2071,11 +2241,15 @@ spec_status_t device_info(DeviceInfo *&out) {
             return fail(SPEC_ERR_UNSUPPORTED, "needs compute capability 10.3 (sm_103a), device is %s", buf);
         }
         cudaDeviceGetAttribute(&D.sms, cudaDevAttrMultiProcessorCount, dev);
-        const void *kernels[4] = {reinterpret_cast<const void *>(verify_kernel<2, false>),
-                                  reinterpret_cast<const void *>(verify_kernel<4, false>),
-                                  reinterpret_cast<const void *>(verify_kernel<2, true>),
-                                  reinterpret_cast<const void *>(verify_kernel<4, true>)};
-        for (int q = 0; q < 4 && e == cudaSuccess; ++q) {
+        // every instantiation: (element size 2 / 4) x (greedy-only / sampled) per mode
+        // (padded chains, ragged chains), and greedy-only trees; even q are bf16
+        const void *kernels[10] = {
+            reinterpret_cast<const void *>(verify_kernel<2, false, 0>), reinterpret_cast<const void *>(verify_kernel<4, false, 0>),
+            reinterpret_cast<const void *>(verify_kernel<2, true, 0>), reinterpret_cast<const void *>(verify_kernel<4, true, 0>),
+            reinterpret_cast<const void *>(verify_kernel<2, false, 1>), reinterpret_cast<const void *>(verify_kernel<4, false, 1>),
+            reinterpret_cast<const void *>(verify_kernel<2, true, 1>), reinterpret_cast<const void *>(verify_kernel<4, true, 1>),
+            reinterpret_cast<const void *>(verify_kernel<2, false, 2>), reinterpret_cast<const void *>(verify_kernel<4, false, 2>)};
+        for (int q = 0; q < 10 && e == cudaSuccess; ++q) {
             e = cudaFuncSetAttribute(kernels[q], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes));
             int nb = 0;
@@ -2086,7 +2260,7 @@ spec_status_t device_info(DeviceInfo *&out) {
         if (D.blocks_per_sm[0] < 1 || D.blocks_per_sm[1] < 1) {
             cudaFuncAttributes fa;
             memset(&fa, 0, sizeof fa);
-            cudaFuncGetAttributes(&fa, verify_kernel<2, true>);
+            cudaFuncGetAttributes(&fa, verify_kernel<2, true, 0>);
             char buf[200];
             snprintf(buf, sizeof buf, " (%d registers, max %d threads, %zu B static + %zu B dynamic shared, %d threads)",
                      fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes, kSmemBytes, kThreads);
@@ -2157,6 +2331,8 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     P.req_state = reinterpret_cast<uint32_t *>(ws + L.req_state);
     P.res_ctr = reinterpret_cast<uint32_t *>(ws + L.res_ctr);
     P.early = reinterpret_cast<uint32_t *>(ws + L.early);
+    P.req_mask = reinterpret_cast<unsigned long long *>(ws + L.req_mask);
+    P.mask_mode = P.R <= 64;
     P.reset_base = reinterpret_cast<uint32_t *>(ws + L.reset);
     P.reset_words = static_cast<uint32_t>(L.reset_bytes / 4);
     P.rowstat = reinterpret_cast<RowStat *>(ws + L.rowstat);
@@ -2201,12 +2377,24 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
     // Calls without temperatures are greedy only: a leaner instantiation without
     // the sampling and residual code.
     const dim3 g3(static_cast<unsigned>(grid));
-    if (P.q || P.temperature) {
-        if (dtype == SPEC_BF16) verify_kernel<2, true><<<g3, kThreads, kSmemBytes, st>>>(P);
-        else verify_kernel<4, true><<<g3, kThreads, kSmemBytes, st>>>(P);
+    const bool bf = dtype == SPEC_BF16;
+    if (P.tree) {
+        if (bf) verify_kernel<2, false, 2><<<g3, kThreads, kSmemBytes, st>>>(P);
+        else verify_kernel<4, false, 2><<<g3, kThreads, kSmemBytes, st>>>(P);
+    } else if (P.cu) {
+        if (P.q || P.temperature) {
+            if (bf) verify_kernel<2, true, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
+            else verify_kernel<4, true, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
+        } else {
+            if (bf) verify_kernel<2, false, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
+            else verify_kernel<4, false, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
+        }
+    } else if (P.q || P.temperature) {
+        if (bf) verify_kernel<2, true, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
+        else verify_kernel<4, true, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
     } else {
-        if (dtype == SPEC_BF16) verify_kernel<2, false><<<g3, kThreads, kSmemBytes, st>>>(P);
-        else verify_kernel<4, false><<<g3, kThreads, kSmemBytes, st>>>(P);
+        if (bf) verify_kernel<2, false, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
+        else verify_kernel<4, false, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
