@@ -435,15 +435,20 @@ const char *spec_last_error(void);
  * Tests set the limit to 0 to drive the time-out path; there is no reason to
  * change it otherwise.
  *
- * spec_set_tuning: splits = units each logits row of the chain / greedy-tree
- * verify kernel is cut into (0 = automatic: whole rows when the batch has
- * about two rows per SM, finer otherwise); ahead = stages the kernel's copy
- * ring keeps in flight (0 = automatic, i.e. all 3; else 2 or 3).  Results do
- * not depend on either.  Other values return SPEC_ERR_INVALID_ARG and change
- * nothing.
+ * spec_set_tuning: splits = units each logits row of the persistent chain /
+ * greedy-tree kernel is cut into (0 = automatic: whole rows when the batch has
+ * about two rows per SM, finer otherwise); ahead = stages that kernel's copy
+ * ring keeps in flight (0 = automatic, i.e. all 3; else 2 or 3); path = 0
+ * (automatic: padded chains whose per-request thread-block clusters all fit on
+ * the GPU at once are verified one cluster per request, the rest by the
+ * persistent kernel) or 1 (the persistent kernel for every batch).  Greedy
+ * results do not depend on any of them; sampled tokens can differ between the
+ * two kernels only where the arithmetic of the accept test or the draw falls
+ * within rounding of a decision boundary.  Other values return
+ * SPEC_ERR_INVALID_ARG and change nothing.
  */
 unsigned long long spec_set_wait_limit_ns(unsigned long long ns);
-spec_status_t spec_set_tuning(int splits, int ahead);
+spec_status_t spec_set_tuning(int splits, int ahead, int path);
 
 #ifdef __cplusplus
 }

@@ -101,7 +101,7 @@ def load_library():
         lib.spec_last_error.restype = ctypes.c_char_p
         lib.spec_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.spec_set_wait_limit_ns.restype = ctypes.c_ulonglong
-        lib.spec_set_tuning.argtypes = [I, I]
+        lib.spec_set_tuning.argtypes = [I, I, I]
         lib.spec_set_tuning.restype = I
         _lib = lib
         return lib
@@ -201,10 +201,11 @@ def set_wait_limit_ns(ns: int) -> int:
     return int(load_library().spec_set_wait_limit_ns(int(ns)))
 
 
-def set_tuning(splits: int = 0, ahead: int = 0):
-    """spec_set_tuning: row splits and copy-ring depth of the verify kernel
-    (0 = automatic)."""
-    _check("spec_set_tuning", load_library().spec_set_tuning(int(splits), int(ahead)))
+def set_tuning(splits: int = 0, ahead: int = 0, path: int = 0):
+    """spec_set_tuning: row splits and copy-ring depth of the persistent verify
+    kernel (0 = automatic), and path (0 = padded chains that fit go to the
+    cluster-per-request kernel, 1 = the persistent kernel for every batch)."""
+    _check("spec_set_tuning", load_library().spec_set_tuning(int(splits), int(ahead), int(path)))
 
 
 # ---------------------------------------------------------------- entries --

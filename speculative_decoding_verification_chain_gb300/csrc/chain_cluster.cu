@@ -1,0 +1,935 @@
+// chain_cluster.cu -- chain verification with one thread-block cluster per
+// request, for batches whose clusters all fit on the GPU at once.
+//
+// What it computes is the chain step of the persistent verify kernel
+// (EAGLE-3 review, "Speculative Decoding": drafts checked front to back, the
+// first rejection ends the step and is resampled, a bonus token when every
+// draft passes; the review's small-draft section: greedy accepts iff the draft
+// is the target argmax, else emits the argmax; sampling accepts x with
+// probability min(1, p(x)/q(x)) and resamples from norm(max(0, p - q))).
+//
+// Layout.  Request b owns a cluster of C CTAs; CTA r holds columns
+// [r * S, r * S + S) of a row in shared memory.
+//   (1) Phase 1 streams every row's slice through a ring of bulk-async copies
+//       (one row slice a stage), walking the rows last to first so that the
+//       ring ends holding rows 0, 1, ...: the rows a rejection most often
+//       lands on.  Each thread folds the groups tid, tid + 512, ... of the row
+//       into running statistics and each warp leaves one partial per row;
+//       nothing waits on a block reduction while the rows stream.
+//         * greedy (T == 0): the slice's maximum and the first column holding it;
+//           the row's argmax is the largest value, lowest column.
+//         * sampled: the slice's max m_r and sum_r = sum 2^((z - m_r) log2e/T)
+//           (two-float), and e(x) on its own scale in the CTA holding the draft
+//           token's column.  M = max m_r, S = sum_r 2^((m_r - M) log2e/T) sum_r,
+//           and the accept test u q(x) S < e(x) 2^((m_owner - M) log2e/T)
+//           needs no division.
+//   (2) The warps' partials become the CTA's statistics of every row, and one
+//       exchange sends them to every CTA of the cluster (st.async into a slot
+//       of each CTA, completing on the receiver's mbarrier); every CTA then
+//       holds the same numbers, and warp i takes draft i's decision.
+//   (3) The first rejection a (or k) ends the chain.  A greedy request emits
+//       the argmax of row a; a sampled one draws by inverse CDF over the
+//       residual max(0, p - q) of row a (p of row k for the bonus token; p when
+//       the residual has no mass): per-thread sums over contiguous column
+//       chunks, a block scan, one exchange of the CTA totals, then one warp
+//       rescans the chunk holding t = u * total, a lane per group.  Row a's
+//       logits are read in place when the ring still holds them, and q of row
+//       a is copied into the free stages around them.
+// Every row's logits are read once, whether or not the chain reaches it: the
+// cost of a row read in vain is small next to a walk that waits on a cluster
+// round trip per row.
+//
+// Every wait is bounded (the caller's limit); a wait that runs out ends the
+// walk for the whole CTA (a block barrier ORs the outcome) and sets
+// SPEC_STATUS_WAIT_TIMEOUT; copies in flight are waited for before exit and
+// no CTA leaves before the cluster barrier, so no remote store lands in a
+// finished CTA.
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <climits>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "common.h"
+#include "ptx.cuh"
+#include "spec_verify.h"
+#include "twofloat.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+namespace cc {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCluster = 16;
+constexpr int kSmemBudget = 212 * 1024;   // dynamic: the ring, or the drawn row's slices
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned long long kWaitLimitNs = 500000000ull;   // the limit on copies in flight at exit
+
+struct Params {
+    const void *logits;          // [B, k+1, V] bf16 bits or fp32
+    const float *q;              // [B, k, V] or null (every request greedy)
+    const int32_t *tokens;       // [B, k]
+    const float *temperature;    // [B] or null
+    const float *u_accept;       // [B, k] or null
+    const float *u_sample;       // [B, k+1] or null
+    int32_t *out_tokens;         // [B, k+1]
+    int32_t *out_count;          // [B]
+    int64_t *slots;              // [B, k+1] or null: slot_mapping fix-up
+    int64_t pad;
+    int32_t *status;             // one word or null
+    unsigned long long *stats;   // workspace diagnostic counters or null
+    unsigned long long logits_end, q_end;
+    unsigned long long wait_ns;
+    int B, k, V, C, S;           // requests, drafts, vocabulary, CTAs per request, columns per CTA
+    int zbulk, qbulk;            // rows start on 16-byte boundaries: bulk copies allowed
+    int stages;                  // phase-1 ring stages
+    unsigned long long stage_bytes;
+    unsigned long long smem;     // dynamic shared memory of the launch
+};
+
+constexpr int kMaxRowsCC = 16;   // rows per request (k + 1) this kernel takes
+constexpr int kMaxStages = 3;    // phase-1 ring
+
+struct Shared {
+    uint64_t bar;                      // the drawn row's copies (phase 2)
+    uint64_t sbar[kMaxStages];         // phase-1 ring stages
+    uint64_t rbar;                     // the one exchange of every row's statistics
+    uint64_t xbar[2];                  // draw exchanges, by parity
+    float4 slot[2][kMaxCluster];       // pushed by every rank
+    float4 rows[kMaxCluster][kMaxRowsCC];   // every rank's statistics of every row
+    float4 mine[kMaxRowsCC];           // this CTA's statistics of every row
+    float pa[kMaxRowsCC][kWarps];      // per-warp partials of every row: sampled (max, sum hi, sum lo),
+    float pb[kMaxRowsCC][kWarps];      // greedy (value, column)
+    float pc[kMaxRowsCC][kWarps];
+    float zx[kMaxRowsCC];              // the draft token's logit, in the CTA holding its column
+    float rowM[kMaxRowsCC];            // sampled: row max M
+    tf rowS[kMaxRowsCC];               // ... and sum S (two-float)
+    int arg[kMaxRowsCC];               // greedy: row argmax
+    int acc[kMaxRowsCC];               // draft i passes its test
+    float qx[kMaxRowsCC];              // q_i(x_{i+1}) of each draft
+    float ws[kWarps], wc[kWarps], wxs[kWarps], wxc[kWarps];
+    int wi[kWarps];
+    float tot[2];
+    int holder;                        // the thread whose chunk holds the draw point
+    tf hex;                            // its exclusive prefix
+    int32_t tok[kMaxRowsCC];           // the request's draft tokens
+    float ua[kMaxRowsCC];              // its accept uniforms
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Eight logits of group g (8 columns) of the slice, as fp32.
+template <int ES>
+__device__ __forceinline__ void group8(const unsigned char *zs, int g, float x[8]) {
+    if constexpr (ES == 2) {
+        const uint4 w = reinterpret_cast<const uint4 *>(zs)[g];
+        x[0] = bf_lo(w.x); x[1] = bf_hi(w.x); x[2] = bf_lo(w.y); x[3] = bf_hi(w.y);
+        x[4] = bf_lo(w.z); x[5] = bf_hi(w.z); x[6] = bf_lo(w.w); x[7] = bf_hi(w.w);
+    } else {
+        const float4 a = reinterpret_cast<const float4 *>(zs)[2 * g], c = reinterpret_cast<const float4 *>(zs)[2 * g + 1];
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+    }
+}
+
+// Bounded wait on a cluster-scope barrier phase; `late` comes back the same in
+// every thread of the CTA.
+__device__ __forceinline__ bool cluster_phase_late(uint64_t *bar, uint32_t ph, unsigned long long limit) {
+    bool mine = false;
+    if (limit == 0) {
+        mine = !mbar_test_wait_cluster(bar, ph);
+    } else if (!mbar_try_wait_cluster(bar, ph)) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait_cluster(bar, ph)) {
+            if (globaltimer() - t0 > limit) {
+                mine = true;
+                break;
+            }
+        }
+    }
+    return __syncthreads_or(mine) != 0;
+}
+
+// Exchange number xk of the draw (see the file comment).
+__device__ __forceinline__ const float4 *exchange(Shared &sh, int &xk, int rank, float4 v, int C,
+                                                  unsigned long long limit, bool &late) {
+    const int p = xk & 1;
+    if (threadIdx.x == 0) mbar_expect_tx(&sh.xbar[p], 16u * static_cast<uint32_t>(C));
+    if (static_cast<int>(threadIdx.x) < C) {
+        const int r = static_cast<int>(threadIdx.x);
+        st_async_f4(mapa_u32(smem_u32(&sh.slot[p][rank]), r), v, mapa_u32(smem_u32(&sh.xbar[p]), r));
+    }
+    late = cluster_phase_late(&sh.xbar[p], static_cast<uint32_t>(xk >> 1) & 1u, limit);
+    ++xk;
+    return sh.slot[p];
+}
+
+__device__ bool wait_copies(uint64_t *bar, uint32_t parity, unsigned long long limit) {
+    if (limit == 0) return mbar_test_wait(bar, parity);
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait_sleep(bar, parity, 100000u))
+        if (globaltimer() - t0 > limit) return false;
+    return true;
+}
+
+// Argmax step: (ov, oi) replaces (v, i) when larger, or equal at a lower column.
+__device__ __forceinline__ void argmax_take(float &v, int &i, float ov, int oi) {
+    if (ov > v || (ov == v && static_cast<unsigned>(oi) < static_cast<unsigned>(i))) {
+        v = ov;
+        i = oi;
+    }
+}
+
+// Exclusive and inclusive two-float prefixes, in thread order, of the threads'
+// values, and the block total (every thread).
+__device__ __forceinline__ void block_scan(tf v, tf &ex, tf &in, tf &tot, Shared &sh) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    tf is = warp_incl_scan_tf(v, lane);
+    if (lane == 31) {
+        sh.ws[w] = is.h;
+        sh.wc[w] = is.l;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tf a = tf_of(0.0f);
+        for (int i = 0; i < kWarps; ++i) {
+            sh.wxs[i] = a.h;
+            sh.wxc[i] = a.l;
+            a = tf_add(a, tf{sh.ws[i], sh.wc[i]});
+        }
+        sh.tot[0] = a.h;
+        sh.tot[1] = a.l;
+    }
+    __syncthreads();
+    const tf base{sh.wxs[w], sh.wxc[w]};
+    in = tf_add(base, is);
+    ex = tf_add(in, tf_neg(v));
+    tot = tf{sh.tot[0], sh.tot[1]};
+}
+
+// The drawn row's slices in shared memory: the logits at zs, q split at group
+// gh between qa (groups below gh) and qb.
+template <int ES>
+struct DrawRow {
+    const unsigned char *zs;
+    const float *qa, *qb;
+    int gh;
+    bool resid;
+    float c2, nm, pscale;
+    // The eight weights of group g: p (times a common factor) or max(0, p - q).
+    __device__ __forceinline__ void weights(int g, float w[8]) const {
+        float z[8];
+        group8<ES>(zs, g, z);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = ex2(fmaf(z[j], c2, nm)) * pscale;
+        if (resid) {
+            const float *qs = g < gh ? qa + 8 * g : qb + 8 * (g - gh);
+            const float4 q0 = reinterpret_cast<const float4 *>(qs)[0], q1 = reinterpret_cast<const float4 *>(qs)[1];
+            w[0] = fmaxf(0.0f, w[0] - q0.x); w[1] = fmaxf(0.0f, w[1] - q0.y);
+            w[2] = fmaxf(0.0f, w[2] - q0.z); w[3] = fmaxf(0.0f, w[3] - q0.w);
+            w[4] = fmaxf(0.0f, w[4] - q1.x); w[5] = fmaxf(0.0f, w[5] - q1.y);
+            w[6] = fmaxf(0.0f, w[6] - q1.z); w[7] = fmaxf(0.0f, w[7] - q1.w);
+        }
+    }
+    __device__ __forceinline__ float gsum(const float w[8]) const {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += w[j];
+        return s;
+    }
+};
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid_constant__ Params P) {
+    extern __shared__ __align__(128) unsigned char dyn[];
+    __shared__ Shared sh;
+    cg::cluster_group cl = cg::this_cluster();
+    const int C = P.C;
+    const int rank = static_cast<int>(cl.block_rank());
+    const int b = static_cast<int>(blockIdx.x) / C;
+    const int S = P.S, V = P.V, k = P.k, R = k + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lo = rank * S;
+    const int n = max(0, min(S, V - lo));          // columns of this CTA
+    const int ng = (n + 7) >> 3;                   // 8-column groups (the last one padded)
+    const bool lead = rank == 0 && tid == 0;
+    float T = P.temperature ? __ldg(P.temperature + b) : 0.0f;
+    const bool greedy = !(T > 0.0f) || !P.q;
+    const float c2 = greedy ? 0.0f : kLog2e / T;
+    const uint32_t zmain = P.zbulk ? static_cast<uint32_t>((n * ES) & ~15) : 0u;
+    const uint32_t qmain = P.qbulk ? static_cast<uint32_t>((n * 4) & ~15) : 0u;
+    const int NS = P.stages;
+    const size_t stage_bytes = P.stage_bytes;
+    auto zrow = [&](int i) -> size_t { return (static_cast<size_t>(b) * R + i) * static_cast<size_t>(V); };
+    auto qrow = [&](int i) -> size_t { return (static_cast<size_t>(b) * k + i) * static_cast<size_t>(V); };
+    // The walk takes the rows last to first, so that when it ends the ring
+    // still holds rows 0, 1, ...: the rows a rejection most often lands on,
+    // whose logits the draw then reads in place.
+    auto row_of = [&](int j) { return R - 1 - j; };
+    unsigned long long bytes = 0;
+    // Step j of the walk into ring stage j % NS: one bulk copy of the 16-byte
+    // aligned part of the row slice (the rest by plain loads after the wait).
+    auto issue = [&](int j) {
+        const int st = j % NS;
+        if (zmain) {
+            fence_proxy_async();
+            mbar_expect_tx(&sh.sbar[st], zmain);
+            bulk_g2s(dyn + st * stage_bytes, static_cast<const unsigned char *>(P.logits) + (zrow(row_of(j)) + lo) * ES,
+                     zmain, &sh.sbar[st]);
+            bytes += zmain;
+        }
+    };
+    if (tid == 0) {
+        mbar_init(&sh.bar, 1);
+        for (int i = 0; i < kMaxStages; ++i) mbar_init(&sh.sbar[i], 1);
+        mbar_init(&sh.rbar, 1);
+        mbar_init(&sh.xbar[0], 1);
+        mbar_init(&sh.xbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+        for (int j = 0; j < min(NS, R); ++j) issue(j);
+    }
+    for (int i = tid; i < k; i += kThreads) {
+        const int x = __ldg(P.tokens + static_cast<size_t>(b) * k + i);
+        sh.tok[i] = x;
+        sh.ua[i] = (!greedy && P.u_accept) ? __ldg(P.u_accept + static_cast<size_t>(b) * k + i) : 0.0f;
+        sh.qx[i] = (!greedy && x >= 0 && x < V) ? __ldg(P.q + qrow(i) + x) : 0.0f;
+    }
+    // this CTA's barriers exist; the other CTAs wait for that (below) only
+    // before their first push into them
+    cluster_arrive();
+    __syncthreads();
+
+    int xk = 0;
+    bool late = false, bad = false;
+    int issued = min(NS, R), consumed = 0;   // walk steps copied into the ring / finished with
+    bool drawn_copy = false;                 // the drawn row's copies (phase 2) were issued
+    // (1) phase 1: every thread folds the groups tid, tid + 512, ... of each
+    // row into running statistics; each warp leaves one partial per row
+    for (int j = 0; j < R; ++j) {
+        const int st = j % NS, i = row_of(j);
+        unsigned char *zr = dyn + st * stage_bytes;
+        bool copy_late = false;
+        if (zmain) copy_late = !wait_copies(&sh.sbar[st], static_cast<uint32_t>((j / NS) & 1), P.wait_ns);
+        late = __syncthreads_or(copy_late) != 0;
+        if (late) break;
+        if constexpr (ES == 2) {
+            const uint16_t *src = static_cast<const uint16_t *>(P.logits) + zrow(i) + lo;
+            for (int c = static_cast<int>(zmain / 2) + tid; c < n; c += kThreads)
+                reinterpret_cast<uint16_t *>(zr)[c] = __ldg(src + c);
+            for (int c = n + tid; c < 8 * ng; c += kThreads) reinterpret_cast<uint16_t *>(zr)[c] = 0xff80u;
+        } else {
+            const float *src = static_cast<const float *>(P.logits) + zrow(i) + lo;
+            for (int c = static_cast<int>(zmain / 4) + tid; c < n; c += kThreads)
+                reinterpret_cast<float *>(zr)[c] = __ldg(src + c);
+            for (int c = n + tid; c < 8 * ng; c += kThreads) reinterpret_cast<float *>(zr)[c] = -INFINITY;
+        }
+        if (zmain < static_cast<uint32_t>(n * ES) || n < 8 * ng) __syncthreads();
+        if (tid == kThreads - 1) {
+            const int x = i < k ? sh.tok[i] : -1;
+            float zx = 0.0f;
+            if (x >= lo && x < lo + n) {
+                if constexpr (ES == 2)
+                    zx = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(zr)[x - lo]) << 16);
+                else
+                    zx = reinterpret_cast<const float *>(zr)[x - lo];
+            }
+            sh.zx[i] = zx;
+        }
+        if (greedy) {
+            float v = -INFINITY;
+            int gi = INT_MAX;
+            bool nan = false;
+            for (int g = tid; g < ng; g += kThreads) {
+                float z[8];
+                group8<ES>(zr, g, z);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    nan |= (z[jj] != z[jj]) || z[jj] == INFINITY;
+                    if (z[jj] > v) {
+                        v = z[jj];
+                        gi = lo + 8 * g + jj;
+                    }
+                }
+            }
+            bad |= nan;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
+            if (lane == 0) {
+                sh.pa[i][warp] = v;
+                sh.pb[i][warp] = __int_as_float(gi);
+            }
+        } else {
+            // online max m and sums s0 + s1 relative to it; a NaN or +inf logit
+            // turns the sum into NaN, a -inf one adds 0
+            float m = -INFINITY, nm = 0.0f, s0 = 0.0f, s1 = 0.0f;
+            for (int g = tid; g < ng; g += kThreads) {
+                float z[8];
+                group8<ES>(zr, g, z);
+                const float gm = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
+                if (gm > m) {
+                    const float f = ex2((m - gm) * c2);
+                    s0 *= f;
+                    s1 *= f;
+                    m = gm;
+                    nm = -m * c2;
+                }
+                s0 += ex2(fmaf(z[0], c2, nm));
+                s1 += ex2(fmaf(z[1], c2, nm));
+                s0 += ex2(fmaf(z[2], c2, nm));
+                s1 += ex2(fmaf(z[3], c2, nm));
+                s0 += ex2(fmaf(z[4], c2, nm));
+                s1 += ex2(fmaf(z[5], c2, nm));
+                s0 += ex2(fmaf(z[6], c2, nm));
+                s1 += ex2(fmaf(z[7], c2, nm));
+            }
+            const float s = s0 + s1;
+            bad |= s != s;
+            float wm = m;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+            tf t = tf_of((m == -INFINITY || !(s == s)) ? 0.0f : s * ex2((m - wm) * c2));
+            t = warp_sum_tf(t);
+            if (lane == 0) {
+                sh.pa[i][warp] = wm;
+                sh.pb[i][warp] = t.h;
+                sh.pc[i][warp] = t.l;
+            }
+        }
+        __syncthreads();   // every thread is done with this stage
+        ++consumed;
+        if (j + NS < R) {
+            if (tid == 0) issue(j + NS);
+            ++issued;
+        }
+    }
+
+    // (2) this CTA's statistics of every row (warp i combines row i's partials)
+    if (!late) {
+        for (int i = warp; i < R; i += kWarps) {
+            const int l = lane & (kWarps - 1);   // both half-warps hold the 16 partials
+            if (greedy) {
+                float v = sh.pa[i][l];
+                int gi = __float_as_int(sh.pb[i][l]);
+#pragma unroll
+                for (int o = kWarps / 2; o > 0; o >>= 1)
+                    argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
+                if (lane == 0) sh.mine[i] = make_float4(v, __int_as_float(gi), 0.0f, 0.0f);
+            } else {
+                const float wm = sh.pa[i][l];
+                float bm = wm;
+#pragma unroll
+                for (int o = kWarps / 2; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                tf u = tf_of(0.0f);
+                if (wm != -INFINITY) u = tf_mulf(tf{sh.pb[i][l], sh.pc[i][l]}, ex2((wm - bm) * c2));
+#pragma unroll
+                for (int o = kWarps / 2; o > 0; o >>= 1) u = tf_add(u, tf_shfl_xor(u, o));
+                // e(x) on this CTA's scale, in the CTA holding the draft token's column
+                const int x = i < k ? sh.tok[i] : -1;
+                const float ex = (x >= lo && x < lo + n && bm != -INFINITY) ? ex2((sh.zx[i] - bm) * c2) : 0.0f;
+                if (lane == 0) sh.mine[i] = make_float4(bm, u.h, u.l, ex);
+            }
+        }
+        __syncthreads();
+    }
+    cluster_wait();   // every CTA's barriers are initialised
+
+    // (3) one exchange of every row's statistics; every CTA then takes the same
+    // decisions (warp i decides draft i)
+    int a = -1;
+    int token = 0;
+    if (!late) {
+        if (tid == 0) mbar_expect_tx(&sh.rbar, 16u * static_cast<uint32_t>(C * R));
+        for (int t = tid; t < C * R; t += kThreads) {
+            const int r = t / R, i = t - r * R;
+            st_async_f4(mapa_u32(smem_u32(&sh.rows[rank][i]), r), sh.mine[i], mapa_u32(smem_u32(&sh.rbar), r));
+        }
+        late = cluster_phase_late(&sh.rbar, 0, P.wait_ns);
+    }
+    if (!late) {
+        for (int i = warp; i < R; i += kWarps) {
+            const bool on = lane < C;
+            const float4 rv = on ? sh.rows[lane][i] : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.0f, 0.0f);
+            const int x = i < k ? sh.tok[i] : -1;
+            const bool x_ok = x >= 0 && x < V;
+            bool accept = false, rbad = false;
+            if (greedy) {
+                float v = rv.x;
+                int gi = __float_as_int(rv.y);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
+                rbad = !(v > -INFINITY);
+                const int g = (gi >= 0 && gi < V) ? gi : 0;
+                if (lane == 0) sh.arg[i] = g;
+                accept = i < k && x_ok && x == g;
+            } else {
+                float M = rv.x;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                const float f = (!on || rv.x == -INFINITY) ? 0.0f : ex2((rv.x - M) * c2);
+                tf St = on ? tf_mulf(tf{rv.y, rv.z}, f) : tf_of(0.0f);
+                St = warp_sum_tf(St);
+                const int owner = x_ok ? x / S : 0;
+                const float eown = __shfl_sync(0xffffffffu, rv.w * f, owner & 31);
+                if (!(St.h > 0.0f) || !(St.h < INFINITY)) {
+                    rbad = true;
+                    St = tf_of(1.0f);
+                }
+                if (lane == 0) {
+                    sh.rowM[i] = M;
+                    sh.rowS[i] = St;
+                }
+                // u < p(x) / q(x), with p(x) = e(x) f_owner / S, multiplied through by q(x) S
+                accept = i < k && x_ok && (sh.qx[i] == 0.0f || sh.ua[i] * (sh.qx[i] * St.h) < eown);
+            }
+            if (lane == 0) {
+                sh.acc[i] = accept ? 1 : 0;
+                bad |= rbad;
+            }
+        }
+        // a draft token outside [0, V) anywhere in the request is reported (as a
+        // rejection where the walk reaches it)
+        if (lead && P.status)
+            for (int i = 0; i < k; ++i)
+                if (sh.tok[i] < 0 || sh.tok[i] >= V) {
+                    atomicOr(P.status, SPEC_STATUS_TOKEN_RANGE);
+                    break;
+                }
+        __syncthreads();
+        a = k;
+        for (int i = 0; i < k; ++i)
+            if (!sh.acc[i]) {
+                a = i;
+                break;
+            }
+        token = greedy ? sh.arg[a] : 0;
+    }
+
+    if (!late && !greedy) {
+        // (4) inverse-CDF draw over the residual max(0, p - q) of row a (p when
+        // a == k, or when the residual has no mass); p = e 2^((m_r - M) c2) / S.
+        // Row a's logits are read in place when the ring still holds them, with
+        // q copied into the free stages around them; else both are copied.
+        const bool want_q = a < k;
+        const int ja = R - 1 - a;                       // the walk step that read row a
+        const int sa = ja % NS;
+        const size_t zb = (static_cast<size_t>(S) * ES + 127) / 128 * 128;
+        const int gh_split = (ng + 1) >> 1;
+        size_t zoff = 0, qoff_a = zb, qoff_b = 0;
+        int gh = ng;                                    // groups of q in the first region
+        bool reload = true;
+        if (ja >= R - NS) {                             // row a's slice is still in stage sa
+            const size_t sz = static_cast<size_t>(sa) * stage_bytes;
+            if (!want_q) {
+                zoff = sz;
+                reload = false;
+            } else if (static_cast<size_t>(ng) * 32 <= stage_bytes) {   // q fits one stage
+                zoff = sz;
+                qoff_a = sa == 0 ? stage_bytes : 0;
+                reload = false;
+            } else if (NS == 3 && static_cast<size_t>(gh_split) * 32 <= stage_bytes) {   // q in the other two
+                zoff = sz;
+                qoff_a = sa == 0 ? stage_bytes : 0;
+                qoff_b = sa == 2 ? stage_bytes : 2 * stage_bytes;
+                gh = gh_split;
+                reload = false;
+            }
+        }
+        const unsigned char *zs = dyn + zoff;
+        float *qa = reinterpret_cast<float *>(dyn + qoff_a);
+        float *qb = reinterpret_cast<float *>(dyn + qoff_b);
+        auto qdst = [&](int c) -> float * { return c < 8 * gh ? qa + c : qb + (c - 8 * gh); };
+        // bulk parts: the z slice when copied again; q's aligned bytes, split at group gh
+        const uint32_t zcopy = reload ? zmain : 0u;
+        uint32_t qa_bytes = 0, qb_bytes = 0;
+        if (want_q && qmain) {
+            const uint32_t cut = static_cast<uint32_t>(gh) * 32u;
+            qa_bytes = qmain < cut ? qmain : cut;
+            qb_bytes = qmain - qa_bytes;
+        }
+        const uint32_t tx = zcopy + qa_bytes + qb_bytes;
+        if (tid == 0 && tx > 0) {
+            fence_proxy_async();
+            mbar_expect_tx(&sh.bar, tx);
+            if (zcopy)
+                bulk_g2s(dyn + zoff, static_cast<const unsigned char *>(P.logits) + (zrow(a) + lo) * ES, zcopy, &sh.bar);
+            if (qa_bytes) bulk_g2s(qa, P.q + qrow(a) + lo, qa_bytes, &sh.bar);
+            if (qb_bytes) bulk_g2s(qb, P.q + qrow(a) + lo + 8 * gh, qb_bytes, &sh.bar);
+            bytes += tx;
+        }
+        drawn_copy = tx > 0;
+        if (reload) {
+            if constexpr (ES == 2) {
+                const uint16_t *src = static_cast<const uint16_t *>(P.logits) + zrow(a) + lo;
+                uint16_t *d = reinterpret_cast<uint16_t *>(dyn + zoff);
+                for (int c = static_cast<int>(zcopy / 2) + tid; c < n; c += kThreads) d[c] = __ldg(src + c);
+                for (int c = n + tid; c < 8 * ng; c += kThreads) d[c] = 0xff80u;
+            } else {
+                const float *src = static_cast<const float *>(P.logits) + zrow(a) + lo;
+                float *d = reinterpret_cast<float *>(dyn + zoff);
+                for (int c = static_cast<int>(zcopy / 4) + tid; c < n; c += kThreads) d[c] = __ldg(src + c);
+                for (int c = n + tid; c < 8 * ng; c += kThreads) d[c] = -INFINITY;
+            }
+        }
+        if (want_q) {
+            for (int c = static_cast<int>((qa_bytes + qb_bytes) / 4) + tid; c < n; c += kThreads)
+                *qdst(c) = __ldg(P.q + qrow(a) + lo + c);
+            for (int c = n + tid; c < 8 * ng; c += kThreads) *qdst(c) = 0.0f;
+        }
+        bool copy_late = false;
+        if (tx > 0) copy_late = !wait_copies(&sh.bar, 0, P.wait_ns);
+        late = __syncthreads_or(copy_late) != 0;
+
+        const float u = P.u_sample ? __ldg(P.u_sample + static_cast<size_t>(b) * R + a) : 0.0f;
+        const float mr = sh.mine[a].x, M = sh.rowM[a];
+        const float Sh = sh.rowS[a].h;
+        DrawRow<ES> D;
+        D.zs = zs;
+        D.qa = qa;
+        D.qb = qb;
+        D.gh = gh;
+        D.resid = want_q;
+        D.c2 = c2;
+        D.nm = mr == -INFINITY ? 0.0f : -mr * c2;
+        D.pscale = (mr == -INFINITY ? 0.0f : ex2((mr - M) * c2)) / Sh;
+        // contiguous chunks of groups per thread (odd length: bank spread)
+        const int Eg = ((ng + kThreads - 1) / kThreads) | 1;
+        const int g0 = min(ng, tid * Eg), g1 = min(ng, g0 + Eg);
+        for (int attempt = 0; attempt < 2 && !late; ++attempt) {
+            if (tid == 0) sh.holder = INT_MAX;
+            tf th = tf_of(0.0f);
+            int lastg = -1;
+            if (mr != -INFINITY)
+                for (int g = g0; g < g1; ++g) {
+                    float w[8];
+                    D.weights(g, w);
+                    const float ws = D.gsum(w);
+                    if (ws > 0.0f) lastg = g;
+                    th = tf_add(th, tf_of(ws));
+                }
+            tf ex, in, tot;
+            block_scan(th, ex, in, tot, sh);
+            int clast = lastg;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) clast = max(clast, __shfl_xor_sync(0xffffffffu, clast, o));
+            if (lane == 0) sh.wi[warp] = clast;
+            __syncthreads();
+            clast = sh.wi[0];
+            for (int w = 1; w < kWarps; ++w) clast = max(clast, sh.wi[w]);
+            const float4 *trow = exchange(sh, xk, rank, make_float4(tot.h, tot.l, __int_as_float(clast), 0.0f),
+                                          C, P.wait_ns, late);
+            if (late) break;
+            tf Z = tf_of(0.0f);
+            for (int r = 0; r < C; ++r) Z = tf_add(Z, tf{trow[r].x, trow[r].y});
+            if (D.resid && !(Z.h > 0.0f)) {
+                D.resid = false;   // a residual of no mass: sample from p
+                __syncthreads();
+                continue;
+            }
+            const tf t = tf_mulf(Z, u);
+            // the CTA holding t: the first whose running end exceeds t
+            tf run = tf_of(0.0f), before = tf_of(0.0f);
+            int rstar = -1, rlast = -1;
+            for (int r = 0; r < C; ++r) {
+                if (__float_as_int(trow[r].z) >= 0) rlast = r;
+                const tf end = tf_add(run, tf{trow[r].x, trow[r].y});
+                if (rstar < 0 && tf_gt(end, t)) {
+                    rstar = r;
+                    before = run;
+                }
+                run = end;
+            }
+            if (rstar < 0) rstar = rlast;   // t at or past the total after rounding: the last positive column
+            if (rank == rstar) {
+                tf tr = tf_add(t, tf_neg(before));   // t relative to this CTA's first column
+                if (tr.h < 0.0f) tr = tf_of(0.0f);
+                if (g1 > g0 && !tf_gt(ex, tr) && tf_gt(in, tr)) atomicMin(&sh.holder, tid);
+                __syncthreads();
+                if (tid == sh.holder) sh.hex = ex;
+                __syncthreads();
+                if (warp == 0) {
+                    const int h = sh.holder;
+                    int pick = -1;
+                    if (h != INT_MAX) {
+                        // the holder's chunk, 32 groups at a time: a lane per
+                        // group, a scan of the group sums, then the crossing
+                        // group's columns in order
+                        const int hg0 = h * Eg, hg1 = min(ng, hg0 + Eg);
+                        tf acc0 = sh.hex;
+                        int lastcol = -1;
+                        for (int base = hg0; base < hg1 && pick < 0; base += 32) {
+                            const int g = base + lane;
+                            float w[8];
+                            float gs = 0.0f;
+                            if (g < hg1) {
+                                D.weights(g, w);
+                                gs = D.gsum(w);
+                            } else {
+#pragma unroll
+                                for (int jj = 0; jj < 8; ++jj) w[jj] = 0.0f;
+                            }
+                            const tf own = tf_of(gs);
+                            const tf endl = tf_add(acc0, warp_incl_scan_tf(own, lane));
+                            const unsigned cross = __ballot_sync(0xffffffffu, g < hg1 && tf_gt(endl, tr));
+                            int mine_pick = -1;
+                            if (cross) {
+                                const int L = __ffs(cross) - 1;
+                                if (lane == L) {
+                                    tf acc = tf_add(endl, tf_neg(own));   // the running sum before group g
+                                    bool done = false;
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj)
+                                        if (!done && w[jj] > 0.0f) {
+                                            mine_pick = lo + 8 * g + jj;
+                                            acc = tf_add(acc, tf_of(w[jj]));
+                                            done = tf_gt(acc, tr);
+                                        }
+                                }
+                                pick = __shfl_sync(0xffffffffu, mine_pick, L);
+                            } else {
+                                const unsigned pos = __ballot_sync(0xffffffffu, gs > 0.0f);
+                                if (pos) {
+                                    const int L = 31 - __clz(pos);
+                                    int lc = -1;
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj)
+                                        if (w[jj] > 0.0f) lc = lo + 8 * g + jj;
+                                    lastcol = __shfl_sync(0xffffffffu, lc, L);
+                                }
+                                acc0 = tf_shfl(endl, 31);
+                            }
+                        }
+                        if (pick < 0) pick = lastcol;
+                    }
+                    if (pick < 0 && clast >= 0) {
+                        // no thread holds t after rounding: this CTA's last positive column
+                        float w[8];
+                        D.weights(clast, w);
+                        int lc = -1;
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            if (w[jj] > 0.0f) lc = lo + 8 * clast + jj;
+                        pick = lc;
+                    }
+                    if (pick < 0) pick = V - 1;
+                    if (lane == 0) P.out_tokens[static_cast<size_t>(b) * R + a] = pick;
+                }
+            }
+            break;
+        }
+    }
+    if (!late && a >= 0) {
+        // (5) outputs: drafts 1..a, the emitted token (greedy: written here), -1
+        // padding, the count, and the slot_mapping fix-up
+        if (lead) {
+            int32_t *ot = P.out_tokens + static_cast<size_t>(b) * R;
+            for (int i = 0; i < a; ++i) ot[i] = sh.tok[i];
+            if (greedy) ot[a] = token;
+            for (int i = a + 1; i < R; ++i) ot[i] = -1;
+            P.out_count[b] = a;
+            if (P.slots) {
+                int64_t *sl = P.slots + static_cast<size_t>(b) * R;
+                for (int j = a + 1; j < R; ++j) sl[j] = P.pad;
+            }
+        }
+    }
+    if (late) {
+        // a copy or an exchange outlived its wait: bounded waits for every copy
+        // still in flight, so none lands here after exit
+        for (int j = consumed; j < issued; ++j)
+            if (zmain) wait_copies(&sh.sbar[j % NS], static_cast<uint32_t>((j / NS) & 1), kWaitLimitNs);
+        if (drawn_copy) wait_copies(&sh.bar, 0, kWaitLimitNs);
+        if (tid == 0 && P.status) atomicOr(P.status, SPEC_STATUS_WAIT_TIMEOUT);
+    }
+    if (bad && P.status) atomicOr(P.status, SPEC_STATUS_NONFINITE);
+    if (tid == 0 && P.stats && bytes) atomicAdd(P.stats + 4, bytes);
+    cl.sync();   // keep this CTA's shared memory alive until the last remote store into it
+}
+
+}  // namespace cc
+
+namespace {
+struct CcDevice {
+    int ok = 0;
+    int sms = 0;
+};
+CcDevice g_cc_dev[64];
+
+spec_status_t cc_setup(int &sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    spec_status_t st = require_sm103(&sms);
+    if (st != SPEC_OK) return st;
+    if (dev < 0 || dev >= 64) return fail(SPEC_ERR_UNSUPPORTED, "device index out of range%s");
+    if (!g_cc_dev[dev].ok) {
+        const void *ks[2] = {reinterpret_cast<const void *>(cc::chain_cluster_kernel<2>),
+                             reinterpret_cast<const void *>(cc::chain_cluster_kernel<4>)};
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+            e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cc::kSmemBudget);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "chain cluster kernel setup: %s", cudaGetErrorString(e));
+        g_cc_dev[dev].ok = 1;
+    }
+    return SPEC_OK;
+}
+}  // namespace
+
+// Geometry of the cluster kernel for vocabulary V with C CTAs a request:
+// columns per CTA, the phase-1 ring (stages of one row slice each) and the
+// dynamic shared memory (the ring, or the drawn row's logits and q slices).
+struct CcGeom {
+    int S, stages;
+    size_t stage_bytes, smem;
+};
+
+static bool cc_geom(int V, int C, int es, CcGeom &G) {
+    G.S = static_cast<int>(((static_cast<long long>(V) + C - 1) / C + 7) / 8 * 8);
+    // a stage holds one row slice of logits, or half of a q slice (whole groups)
+    const size_t slice = static_cast<size_t>(G.S) * es;
+    const size_t half_q = static_cast<size_t>((G.S / 8 + 1) / 2) * 32;
+    G.stage_bytes = ((slice > half_q ? slice : half_q) + 127) / 128 * 128;
+    const size_t fit = static_cast<size_t>(cc::kSmemBudget) / G.stage_bytes;
+    G.stages = static_cast<int>(fit < static_cast<size_t>(cc::kMaxStages) ? fit : static_cast<size_t>(cc::kMaxStages));
+    const size_t draw = (slice + 127) / 128 * 128 + static_cast<size_t>(G.S) * 4;   // logits then q, copied
+    G.smem = G.stages * G.stage_bytes > draw ? G.stages * G.stage_bytes : draw;
+    return G.stages >= 2 && G.smem <= static_cast<size_t>(cc::kSmemBudget);
+}
+
+// Cluster size for a batch of B sampled (or mixed) padded chains with k drafts
+// over vocabulary V: the largest C <= 16 whose slices fit in shared memory and
+// whose B clusters can all be resident at once; 0 when none qualifies or the
+// chains are longer than the kernel takes (the persistent kernel takes the
+// batch).
+int chain_cluster_size(int B, int k, int V, int es) {
+    int sms = 0;
+    if (cc_setup(sms) != SPEC_OK || B < 1 || k + 1 > cc::kMaxRowsCC) return 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::mutex mu;   // guards the per-device memo of resident-cluster counts below
+    for (int C = min(cc::kMaxCluster, sms / B); C >= 1; --C) {
+        CcGeom G;
+        if (!cc_geom(V, C, es, G)) return 0;   // a smaller cluster has larger slices
+        int clusters = 0;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            static std::vector<std::pair<long long, int>> memo[64];
+            const long long key = (static_cast<long long>(es) << 40) | (static_cast<long long>(C) << 32) |
+                                  static_cast<long long>(G.smem);
+            bool found = false;
+            for (auto &kv : memo[dev])
+                if (kv.first == key) {
+                    clusters = kv.second;
+                    found = true;
+                }
+            if (!found) {
+                cudaLaunchConfig_t cfg;
+                memset(&cfg, 0, sizeof cfg);
+                cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(C));
+                cfg.blockDim = dim3(cc::kThreads);
+                cfg.dynamicSmemBytes = G.smem;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                const cudaError_t e =
+                    es == 2 ? cudaOccupancyMaxActiveClusters(&clusters, cc::chain_cluster_kernel<2>, &cfg)
+                            : cudaOccupancyMaxActiveClusters(&clusters, cc::chain_cluster_kernel<4>, &cfg);
+                if (e != cudaSuccess) {
+                    cudaGetLastError();
+                    clusters = 0;
+                }
+                memo[dev].push_back({key, clusters});
+            }
+        }
+        if (clusters >= B) return C;
+    }
+    return 0;
+}
+
+spec_status_t launch_chain_cluster(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                   const int32_t *draft_tokens, const float *temperature, const float *u_accept,
+                                   const float *u_sample, int B, int k, int V, int32_t *out_tokens,
+                                   int32_t *out_num_accepted, int64_t *slot_mapping, int64_t padding_slot_id,
+                                   int32_t *d_status, void *workspace, int C, void *stream) {
+    int sms = 0;
+    spec_status_t st = cc_setup(sms);
+    if (st != SPEC_OK) return st;
+    const int es = dtype == SPEC_BF16 ? 2 : 4;
+    if (C < 1 || C > cc::kMaxCluster) return fail(SPEC_ERR_INVALID_ARG, "cluster size out of range%s");
+    cc::Params P;
+    memset(&P, 0, sizeof P);
+    P.logits = target_logits;
+    P.q = draft_probs;
+    P.tokens = draft_tokens;
+    P.temperature = temperature;
+    P.u_accept = u_accept;
+    P.u_sample = u_sample;
+    P.out_tokens = out_tokens;
+    P.out_count = out_num_accepted;
+    P.slots = slot_mapping;
+    P.pad = padding_slot_id;
+    P.status = d_status;
+    P.stats = static_cast<unsigned long long *>(workspace);
+    P.B = B;
+    P.k = k;
+    P.V = V;
+    P.C = C;
+    CcGeom G;
+    if (!cc_geom(V, C, es, G) || k + 1 > cc::kMaxRowsCC) return fail(SPEC_ERR_INVALID_ARG, "cluster geometry%s");
+    P.S = G.S;
+    P.stages = G.stages;
+    P.stage_bytes = G.stage_bytes;
+    P.smem = G.smem;
+    P.zbulk = (static_cast<long long>(V) * es) % 16 == 0;
+    P.qbulk = V % 4 == 0;
+    P.wait_ns = wait_limit_ns();
+    P.logits_end = reinterpret_cast<unsigned long long>(target_logits) +
+                   static_cast<unsigned long long>(B) * (k + 1) * static_cast<unsigned long long>(V) * es;
+    P.q_end = draft_probs ? reinterpret_cast<unsigned long long>(draft_probs) +
+                                static_cast<unsigned long long>(B) * k * static_cast<unsigned long long>(V) * 4
+                          : 0ull;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(C));
+    cfg.blockDim = dim3(cc::kThreads);
+    cfg.dynamicSmemBytes = G.smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = es == 2 ? cudaLaunchKernelEx(&cfg, cc::chain_cluster_kernel<2>, P)
+                            : cudaLaunchKernelEx(&cfg, cc::chain_cluster_kernel<4>, P);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "chain cluster launch: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+}  // namespace sv

@@ -21,4 +21,16 @@ spec_status_t require_sm103(int *sms);
 // always waited for with the default limit.
 unsigned long long wait_limit_ns();
 
+// Sampled (or mixed) chains in the padded layout whose per-request clusters all
+// fit on the GPU at once go to the cluster kernel (chain_cluster.cu): the
+// cluster size, or 0 for the persistent kernel.  spec_set_tuning can rule the
+// cluster kernel out.
+int chain_cluster_size(int B, int k, int V, int es);
+bool chain_cluster_allowed();
+spec_status_t launch_chain_cluster(const void *target_logits, spec_dtype_t dtype, const float *draft_probs,
+                                   const int32_t *draft_tokens, const float *temperature, const float *u_accept,
+                                   const float *u_sample, int B, int k, int V, int32_t *out_tokens,
+                                   int32_t *out_num_accepted, int64_t *slot_mapping, int64_t padding_slot_id,
+                                   int32_t *d_status, void *workspace, int C, void *stream);
+
 }  // namespace sv

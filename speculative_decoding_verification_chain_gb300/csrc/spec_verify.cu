@@ -2285,6 +2285,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // read once per call when the launch is set up.
 std::atomic<int> g_tune_splits{0};
 std::atomic<int> g_tune_ahead{0};
+std::atomic<int> g_tune_path{0};   // 0: padded chains that fit go to the cluster kernel; 1: persistent only
+
+bool chain_cluster_allowed() { return g_tune_path.load(std::memory_order_relaxed) == 0; }
 std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
@@ -2465,6 +2468,21 @@ spec_status_t verify_chain_common(const void *target_logits, spec_dtype_t dtype,
                     "draft_probs, temperature, u_accept and u_sample must be all given or all NULL%s");
     if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
         return fail(SPEC_ERR_INVALID_ARG, "target_logits and draft_probs must be 16-byte aligned%s");
+    Layout L;
+    if (!make_layout(B, k + 1, V, dtype, L)) return fail(SPEC_ERR_INVALID_ARG, "invalid sizes%s");
+    if (!workspace || workspace_bytes < L.total)
+        return fail(SPEC_ERR_INVALID_ARG, "workspace missing or smaller than spec_workspace_bytes()%s");
+    if (!aligned16(workspace)) return fail(SPEC_ERR_INVALID_ARG, "workspace must be 16-byte aligned%s");
+    // a sampled batch whose per-request clusters fit on the GPU at once: one
+    // cluster per request (greedy-only batches stream best on the persistent
+    // kernel, which skips rows whose drafts are already known rejected)
+    if (chain_cluster_allowed() && draft_probs) {
+        const int C = chain_cluster_size(B, k, V, dtype == SPEC_BF16 ? 2 : 4);
+        if (C > 0)
+            return launch_chain_cluster(target_logits, dtype, draft_probs, draft_tokens, temperature, u_accept,
+                                        u_sample, B, k, V, out_tokens, out_num_accepted, slot_mapping,
+                                        padding_slot_id, d_status, workspace, C, stream);
+    }
     Params P;
     memset(&P, 0, sizeof P);
     P.logits = static_cast<const uint8_t *>(target_logits);
@@ -2724,12 +2742,13 @@ extern "C" unsigned long long spec_set_wait_limit_ns(unsigned long long ns) {
     return g_wait_ns.exchange(ns, std::memory_order_relaxed);
 }
 
-extern "C" spec_status_t spec_set_tuning(int splits, int ahead) {
+extern "C" spec_status_t spec_set_tuning(int splits, int ahead, int path) {
     g_err[0] = 0;
-    if (splits < 0 || ahead < 0 || (ahead != 0 && (ahead < 2 || ahead > kStages)))
-        return fail(SPEC_ERR_INVALID_ARG, "need splits >= 0 and ahead 0 or in [2, 3]%s");
+    if (splits < 0 || ahead < 0 || (ahead != 0 && (ahead < 2 || ahead > kStages)) || path < 0 || path > 1)
+        return fail(SPEC_ERR_INVALID_ARG, "need splits >= 0, ahead 0 or in [2, 3], path 0 or 1%s");
     g_tune_splits.store(splits, std::memory_order_relaxed);
     g_tune_ahead.store(ahead, std::memory_order_relaxed);
+    g_tune_path.store(path, std::memory_order_relaxed);
     return SPEC_OK;
 }
 
@@ -2785,6 +2804,14 @@ extern "C" spec_status_t spec_verify_chain_noalloc(const void *target_logits, sp
     P.V = V;
     P.D = k;
     P.tree = 0;
+    // The same dispatch as spec_verify_chain (the cluster kernel needs no scratch).
+    if (chain_cluster_allowed() && draft_probs) {
+        const int C = chain_cluster_size(B, k, V, dtype == SPEC_BF16 ? 2 : 4);
+        if (C > 0)
+            return launch_chain_cluster(target_logits, dtype, draft_probs, draft_tokens, temperature, u_accept,
+                                        u_sample, B, k, V, out_tokens, out_num_accepted, nullptr, 0, d_status,
+                                        nullptr, C, stream);
+    }
     // The scratch keeps whatever the previous call left; launch_verify clears
     // this layout's counter region once every check has passed.
     return launch_verify(P, dtype, scratch, kNoAllocScratchBytes, stream, true);

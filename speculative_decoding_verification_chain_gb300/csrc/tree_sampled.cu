@@ -231,50 +231,6 @@ __device__ __forceinline__ void block_scan2(float s, float c, float &exh, float 
     tl = sh.tot[1];
 }
 
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint32_t mapa_u32(uint32_t local, int rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-
-// Remote shared-memory stores that complete bytes on the destination CTA's
-// mbarrier (the destination waits on its own barrier; no cluster barrier).
-__device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_async_f1(uint32_t dst, float v, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
-                 "r"(__float_as_uint(v)), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Exchange number xk: every CTA sends its float4 into slot[xk & 1][its rank]
 // of every CTA (threads 0..C-1, one st.async each) and waits on its own
 // barrier xbar[xk & 1] (phase (xk >> 1) & 1) for C such stores plus `extra`

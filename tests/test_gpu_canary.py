@@ -41,6 +41,21 @@ def sv():
     return m
 
 
+@pytest.fixture(autouse=True, params=[0, 1], ids=["cluster", "persistent"])
+def chain_path(request, sv):
+    """Chains run on both kernels: the cluster-per-request kernel (padded
+    chains whose clusters fit on the GPU; the default for them) and the
+    persistent kernel.  Tests of trees, ragged batches and the separate fix-up
+    do not depend on it and run once."""
+    path = request.param
+    name = request.node.name
+    if path == 1 and any(w in name for w in ("tree", "fixup_slots", "ragged", "ngram", "next_step", "kv")):
+        pytest.skip("the path applies to padded chains only")
+    sv.set_tuning(0, 0, path)
+    yield path
+    sv.set_tuning(0, 0, 0)
+
+
 class Guarded:
     """Device buffers with GUARD pattern bytes before and after."""
 

@@ -86,12 +86,18 @@ def test_flag_budget_tiny_chain(sv, O, dev, report):
     _check(report, "tiny chain B=1000 k=4 V=1000", _chain_trials(sv, O, dev, x, 12, 7100))
 
 
+@pytest.mark.parametrize("path", [0, 1], ids=["cluster", "persistent"])
 @pytest.mark.parametrize("lam", [0.1, 0.3, 0.6])
-def test_flag_budget_sampled_chain(sv, O, dev, report, lam):
-    """B = 32, k = 4, V = 128256, T = 0.7, Zipf-shaped logits."""
+def test_flag_budget_sampled_chain(sv, O, dev, report, lam, path):
+    """B = 32, k = 4, V = 128256, T = 0.7, Zipf-shaped logits; on the cluster
+    kernel (the default for this batch) and on the persistent kernel."""
     x = W.chain_sampled(seed=3, B=32, k=4, V=128256, temperature=0.7, lam=lam)
-    _check(report, "sampled chain B=32 k=4 V=128256 lambda=%.1f" % lam,
-           _chain_trials(sv, O, dev, x, 60, 7200 + int(lam * 10)))
+    sv.set_tuning(0, 0, path)
+    try:
+        tot = _chain_trials(sv, O, dev, x, 60, 7200 + int(lam * 10))
+    finally:
+        sv.set_tuning(0, 0, 0)
+    _check(report, "sampled chain B=32 k=4 V=128256 lambda=%.1f %s" % (lam, ("cluster", "persistent")[path]), tot)
 
 
 def test_flag_budget_sweep(sv, O, dev, report):

@@ -30,6 +30,21 @@ def sv():
     return m
 
 
+@pytest.fixture(autouse=True, params=[0, 1], ids=["cluster", "persistent"])
+def chain_path(request, sv):
+    """Chains run on both kernels: the cluster-per-request kernel (padded
+    chains whose clusters fit on the GPU; the default for them) and the
+    persistent kernel.  Tests of trees, ragged batches and the separate fix-up
+    do not depend on it and run once."""
+    path = request.param
+    name = request.node.name
+    if path == 1 and any(w in name for w in ("tree", "fixup_slots", "ragged", "ngram", "next_step", "kv")):
+        pytest.skip("the path applies to padded chains only")
+    sv.set_tuning(0, 0, path)
+    yield path
+    sv.set_tuning(0, 0, 0)
+
+
 @pytest.fixture(scope="module")
 def O(oracle_mod):
     return oracle_mod
@@ -390,7 +405,7 @@ def test_workspace_is_left_clean_between_calls(sv, O, dev):
 def tuning(sv):
     """spec_set_tuning for one test, put back to automatic afterwards."""
     yield sv.set_tuning
-    sv.set_tuning(0, 0)
+    sv.set_tuning(0, 0, 0)
 
 
 @pytest.mark.parametrize("ahead,splits", [(2, 0), (3, 0), (3, 3), (2, 1)])
@@ -398,7 +413,7 @@ def test_results_do_not_depend_on_producer_run_ahead(sv, O, dev, ahead, splits, 
     """How many stages the producer keeps in flight, and how finely rows are
     split, change the timing of claims and so which rows are skipped; the
     answers must not change."""
-    tuning(splits, ahead)
+    tuning(splits, ahead, 1)
     x = W.chain_greedy(seed=61 + ahead, B=16, k=5, V=128256, p_match=0.5)
     got_t, got_a = run_chain(sv, x, dev)
     ref = oracle_chain(O, x)
@@ -418,7 +433,7 @@ def test_rejected_first_drafts_skip_later_rows(sv, O, dev, tuning):
     at claim (the first stage of row 0 already shows the rejection), and the
     counters stay consistent."""
     import torch
-    tuning(0, 3)
+    tuning(0, 3, 1)
     x = W.chain_greedy(seed=64, B=32, k=5, V=128256, p_match=0.0)
     z, tok = cuda(x.logits, dev), cuda(x.draft_tokens, dev)
     ws = torch.zeros(sv.workspace_bytes(x.B, x.k + 1, x.V), dtype=torch.uint8, device=dev)
