@@ -67,6 +67,9 @@ namespace cc {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kCtrlWarp = kWarps - 1;          // decisions and copies; the other warps stream the rows
+constexpr int kStreamWarps = kWarps - 1;
+constexpr int kStreamThreads = kStreamWarps * 32;
 constexpr int kMaxCluster = 16;
 constexpr int kSmemBudget = 212 * 1024;   // dynamic: the ring, or the drawn row's slices
 constexpr float kLog2e = 1.4426950408889634f;
@@ -98,13 +101,14 @@ constexpr int kMaxRowsCC = 16;   // rows per request (k + 1) this kernel takes
 constexpr int kMaxStages = 3;    // phase-1 ring
 
 struct Shared {
-    uint64_t bar;                      // the drawn row's copies (phase 2)
-    uint64_t sbar[kMaxStages];         // phase-1 ring stages
-    uint64_t rbar;                     // the one exchange of every row's statistics
+    uint64_t bar;                      // the drawn row's q copies
+    uint64_t full[kMaxStages];         // ring stage holds its row
+    uint64_t empty[kMaxStages];        // every streaming warp is done with the stage's row
+    uint64_t rbar[kMaxRowsCC];         // every rank's statistics of row i arrived
     uint64_t xbar[2];                  // draw exchanges, by parity
     float4 slot[2][kMaxCluster];       // pushed by every rank
     float4 rows[kMaxCluster][kMaxRowsCC];   // every rank's statistics of every row
-    float4 mine[kMaxRowsCC];           // this CTA's statistics of every row
+    float4 mine[kMaxRowsCC];           // this CTA's statistics of every row walked
     float pa[kMaxRowsCC][kWarps];      // per-warp partials of every row: sampled (max, sum hi, sum lo),
     float pb[kMaxRowsCC][kWarps];      // greedy (value, column)
     float pc[kMaxRowsCC][kWarps];
@@ -113,8 +117,12 @@ struct Shared {
     tf rowS[kMaxRowsCC];               // ... and sum S (two-float)
     int arg[kMaxRowsCC];               // greedy: row argmax
     int acc[kMaxRowsCC];               // draft i passes its test
-    float qx[kMaxRowsCC];              // q_i(x_{i+1}) of each draft
     float ws[kWarps], wc[kWarps], wxs[kWarps], wxc[kWarps];
+    int end_row;                       // the walk's last row, once decided (rows past it are skipped)
+    int abort;                         // a wait of the walk ran out
+    int qfail;                         // a wait before the q copies ran out
+    int a;                             // the first rejection (k: every draft accepted)
+    int issued;                        // rows copied into the ring
     int wi[kWarps];
     float tot[2];
     int holder;                        // the thread whose chunk holds the draw point
@@ -127,6 +135,16 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Bounded wait of one thread on a barrier that remote CTAs complete.
+__device__ __forceinline__ bool cluster_bar_wait(uint64_t *bar, uint32_t ph, unsigned long long limit) {
+    if (limit == 0) return mbar_test_wait_cluster(bar, ph);
+    if (mbar_try_wait_cluster(bar, ph)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait_cluster(bar, ph))
+        if (globaltimer() - t0 > limit) return false;
+    return true;
 }
 
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
@@ -145,6 +163,22 @@ __device__ __forceinline__ void group8(const unsigned char *zs, int g, float x[8
     } else {
         const float4 a = reinterpret_cast<const float4 *>(zs)[2 * g], c = reinterpret_cast<const float4 *>(zs)[2 * g + 1];
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+    }
+}
+
+// Eight logits of group g read from global memory (row slice base zg, n
+// columns; -inf past the end): the groups a bulk copy does not cover.
+template <int ES>
+__device__ __forceinline__ void group8_global(const void *zg, int g, int n, float x[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int c = 8 * g + j;
+        if (c >= n)
+            x[j] = -INFINITY;
+        else if constexpr (ES == 2)
+            x[j] = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const uint16_t *>(zg) + c)) << 16);
+        else
+            x[j] = __ldg(static_cast<const float *>(zg) + c);
     }
 }
 
@@ -207,15 +241,18 @@ __device__ __forceinline__ void block_scan(tf v, tf &ex, tf &in, tf &tot, Shared
         sh.wc[w] = is.l;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        tf a = tf_of(0.0f);
-        for (int i = 0; i < kWarps; ++i) {
-            sh.wxs[i] = a.h;
-            sh.wxc[i] = a.l;
-            a = tf_add(a, tf{sh.ws[i], sh.wc[i]});
+    if (w == 0) {   // warp 0 scans the warps' totals
+        const tf t = lane < kWarps ? tf{sh.ws[lane], sh.wc[lane]} : tf_of(0.0f);
+        const tf inc = warp_incl_scan_tf(t, lane);
+        const tf up{__shfl_up_sync(0xffffffffu, inc.h, 1), __shfl_up_sync(0xffffffffu, inc.l, 1)};
+        if (lane < kWarps) {
+            sh.wxs[lane] = lane ? up.h : 0.0f;
+            sh.wxc[lane] = lane ? up.l : 0.0f;
         }
-        sh.tot[0] = a.h;
-        sh.tot[1] = a.l;
+        if (lane == kWarps - 1) {
+            sh.tot[0] = inc.h;
+            sh.tot[1] = inc.l;
+        }
     }
     __syncthreads();
     const tf base{sh.wxs[w], sh.wxc[w]};
@@ -228,7 +265,9 @@ __device__ __forceinline__ void block_scan(tf v, tf &ex, tf &in, tf &tot, Shared
 // gh between qa (groups below gh) and qb.
 template <int ES>
 struct DrawRow {
-    const unsigned char *zs;
+    const unsigned char *zs;   // groups below gbulk; the rest from zg
+    const void *zg;
+    int gbulk, n;
     const float *qa, *qb;
     int gh;
     bool resid;
@@ -236,7 +275,10 @@ struct DrawRow {
     // The eight weights of group g: p (times a common factor) or max(0, p - q).
     __device__ __forceinline__ void weights(int g, float w[8]) const {
         float z[8];
-        group8<ES>(zs, g, z);
+        if (g < gbulk)
+            group8<ES>(zs, g, z);
+        else
+            group8_global<ES>(zg, g, n, z);
 #pragma unroll
         for (int j = 0; j < 8; ++j) w[j] = ex2(fmaf(z[j], c2, nm)) * pscale;
         if (resid) {
@@ -266,210 +308,220 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
     const int b = static_cast<int>(blockIdx.x) / C;
     const int S = P.S, V = P.V, k = P.k, R = k + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool ctrl = warp == kCtrlWarp;
+    const int tctl = kCtrlWarp * 32;               // issues every bulk copy and owns their bookkeeping
     const int lo = rank * S;
     const int n = max(0, min(S, V - lo));          // columns of this CTA
     const int ng = (n + 7) >> 3;                   // 8-column groups (the last one padded)
     const bool lead = rank == 0 && tid == 0;
-    float T = P.temperature ? __ldg(P.temperature + b) : 0.0f;
-    const bool greedy = !(T > 0.0f) || !P.q;
-    const float c2 = greedy ? 0.0f : kLog2e / T;
     const uint32_t zmain = P.zbulk ? static_cast<uint32_t>((n * ES) & ~15) : 0u;
     const uint32_t qmain = P.qbulk ? static_cast<uint32_t>((n * 4) & ~15) : 0u;
     const int NS = P.stages;
     const size_t stage_bytes = P.stage_bytes;
+    const int gbulk = static_cast<int>(zmain / (8 * ES));   // groups wholly copied into a stage
     auto zrow = [&](int i) -> size_t { return (static_cast<size_t>(b) * R + i) * static_cast<size_t>(V); };
     auto qrow = [&](int i) -> size_t { return (static_cast<size_t>(b) * k + i) * static_cast<size_t>(V); };
-    // The walk takes the rows last to first, so that when it ends the ring
-    // still holds rows 0, 1, ...: the rows a rejection most often lands on,
-    // whose logits the draw then reads in place.
-    auto row_of = [&](int j) { return R - 1 - j; };
     unsigned long long bytes = 0;
-    // Step j of the walk into ring stage j % NS: one bulk copy of the 16-byte
-    // aligned part of the row slice (the rest by plain loads after the wait).
+    // Row j into ring stage j % NS (control lane 0): one bulk copy of the
+    // 16-byte aligned part of the slice; the rest by plain loads after the wait.
+    // A row with nothing to copy in bulk completes its stage by a plain arrive.
     auto issue = [&](int j) {
         const int st = j % NS;
         if (zmain) {
             fence_proxy_async();
-            mbar_expect_tx(&sh.sbar[st], zmain);
-            bulk_g2s(dyn + st * stage_bytes, static_cast<const unsigned char *>(P.logits) + (zrow(row_of(j)) + lo) * ES,
-                     zmain, &sh.sbar[st]);
+            mbar_expect_tx(&sh.full[st], zmain);
+            bulk_g2s(dyn + st * stage_bytes, static_cast<const unsigned char *>(P.logits) + (zrow(j) + lo) * ES, zmain,
+                     &sh.full[st]);
             bytes += zmain;
+        } else {
+            mbar_arrive(&sh.full[st]);
         }
     };
-    if (tid == 0) {
-        mbar_init(&sh.bar, 1);
-        for (int i = 0; i < kMaxStages; ++i) mbar_init(&sh.sbar[i], 1);
-        mbar_init(&sh.rbar, 1);
-        mbar_init(&sh.xbar[0], 1);
-        mbar_init(&sh.xbar[1], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        fence_proxy_async();
-        for (int j = 0; j < min(NS, R); ++j) issue(j);
+    const float T = P.temperature ? __ldg(P.temperature + b) : 0.0f;   // first used after the ring starts
+    // The control warp holds draft i's token, accept uniform and q_i(x) in lane
+    // i.  Its lane 0 starts the ring before anything waits on a load: loads
+    // issued after the whole grid's first copies queue behind them.
+    int xr = -1;
+    float uar = 0.0f, qxr = 0.0f;
+    if (ctrl) {
+        if (lane == 0) {
+            mbar_init(&sh.bar, 1);
+            for (int i = 0; i < kMaxStages; ++i) {
+                mbar_init(&sh.full[i], 1);
+                mbar_init(&sh.empty[i], kStreamWarps);
+            }
+            for (int i = 0; i < kMaxRowsCC; ++i) mbar_init(&sh.rbar[i], 1);
+            mbar_init(&sh.xbar[0], 1);
+            mbar_init(&sh.xbar[1], 1);
+            sh.end_row = R;
+            sh.abort = 0;
+            sh.qfail = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            fence_proxy_async();
+            for (int j = 0; j < min(NS, R); ++j) issue(j);
+        }
+        __syncwarp();
+        if (lane < k) {
+            xr = __ldg(P.tokens + static_cast<size_t>(b) * k + lane);
+            uar = P.u_accept ? __ldg(P.u_accept + static_cast<size_t>(b) * k + lane) : 0.0f;
+            sh.tok[lane] = xr;
+            if (P.q && xr >= 0 && xr < V) qxr = __ldg(P.q + qrow(lane) + xr);   // used at the decisions
+        }
     }
-    for (int i = tid; i < k; i += kThreads) {
-        const int x = __ldg(P.tokens + static_cast<size_t>(b) * k + i);
-        sh.tok[i] = x;
-        sh.ua[i] = (!greedy && P.u_accept) ? __ldg(P.u_accept + static_cast<size_t>(b) * k + i) : 0.0f;
-        sh.qx[i] = (!greedy && x >= 0 && x < V) ? __ldg(P.q + qrow(i) + x) : 0.0f;
-    }
-    // this CTA's barriers exist; the other CTAs wait for that (below) only
-    // before their first push into them
+    // this CTA's barriers exist; the other CTAs wait for that only before their
+    // first push into them
     cluster_arrive();
     __syncthreads();
 
-    int xk = 0;
-    bool late = false, bad = false;
-    int issued = min(NS, R), consumed = 0;   // walk steps copied into the ring / finished with
-    bool drawn_copy = false;                 // the drawn row's copies (phase 2) were issued
-    // (1) phase 1: every thread folds the groups tid, tid + 512, ... of each
-    // row into running statistics; each warp leaves one partial per row
-    for (int j = 0; j < R; ++j) {
-        const int st = j % NS, i = row_of(j);
-        unsigned char *zr = dyn + st * stage_bytes;
-        bool copy_late = false;
-        if (zmain) copy_late = !wait_copies(&sh.sbar[st], static_cast<uint32_t>((j / NS) & 1), P.wait_ns);
-        late = __syncthreads_or(copy_late) != 0;
-        if (late) break;
-        if constexpr (ES == 2) {
-            const uint16_t *src = static_cast<const uint16_t *>(P.logits) + zrow(i) + lo;
-            for (int c = static_cast<int>(zmain / 2) + tid; c < n; c += kThreads)
-                reinterpret_cast<uint16_t *>(zr)[c] = __ldg(src + c);
-            for (int c = n + tid; c < 8 * ng; c += kThreads) reinterpret_cast<uint16_t *>(zr)[c] = 0xff80u;
-        } else {
-            const float *src = static_cast<const float *>(P.logits) + zrow(i) + lo;
-            for (int c = static_cast<int>(zmain / 4) + tid; c < n; c += kThreads)
-                reinterpret_cast<float *>(zr)[c] = __ldg(src + c);
-            for (int c = n + tid; c < 8 * ng; c += kThreads) reinterpret_cast<float *>(zr)[c] = -INFINITY;
-        }
-        if (zmain < static_cast<uint32_t>(n * ES) || n < 8 * ng) __syncthreads();
-        if (tid == kThreads - 1) {
-            const int x = i < k ? sh.tok[i] : -1;
-            float zx = 0.0f;
-            if (x >= lo && x < lo + n) {
-                if constexpr (ES == 2)
-                    zx = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(zr)[x - lo]) << 16);
-                else
-                    zx = reinterpret_cast<const float *>(zr)[x - lo];
+    const bool greedy = !(T > 0.0f) || !P.q;
+    const float c2 = greedy ? 0.0f : kLog2e / T;
+    int a = -1;
+    int issued = min(NS, R);   // rows copied into the ring (control warp)
+    bool bad = false;
+    if (!ctrl) {
+        // (1) streaming warps: rows in order, each thread folding the groups
+        // stid, stid + 480, ... of the row; a warp partial per row
+        const int stid = tid;   // the control warp is the last one
+        for (int j = 0; j < R; ++j) {
+            const int st = j % NS;
+            unsigned char *zr = dyn + st * stage_bytes;
+            bool ok = wait_copies(&sh.full[st], static_cast<uint32_t>((j / NS) & 1), P.wait_ns);
+            if (!ok) {
+                atomicOr(&sh.abort, 1);
+                break;
             }
-            sh.zx[i] = zx;
-        }
-        if (greedy) {
-            float v = -INFINITY;
-            int gi = INT_MAX;
-            bool nan = false;
-            for (int g = tid; g < ng; g += kThreads) {
-                float z[8];
-                group8<ES>(zr, g, z);
+            if (j > *reinterpret_cast<volatile int *>(&sh.end_row)) break;   // the chain ended before row j
+            const void *zg = static_cast<const unsigned char *>(P.logits) + (zrow(j) + lo) * ES;
+            if (stid == 0) {
+                const int x = j < k ? sh.tok[j] : -1;
+                float zx = 0.0f;
+                if (x >= lo && x < lo + n) {
+                    const int c = x - lo;
+                    const unsigned char *src = c < 8 * gbulk ? zr : static_cast<const unsigned char *>(zg);
+                    if constexpr (ES == 2)
+                        zx = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(src)[c]) << 16);
+                    else
+                        zx = reinterpret_cast<const float *>(src)[c];
+                }
+                sh.zx[j] = zx;
+            }
+            if (greedy) {
+                float v = -INFINITY;
+                int gi = INT_MAX;
+                bool nan = false;
+                for (int g = stid; g < ng; g += kStreamThreads) {
+                    float z[8];
+                    if (g < gbulk)
+                        group8<ES>(zr, g, z);
+                    else
+                        group8_global<ES>(zg, g, n, z);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    nan |= (z[jj] != z[jj]) || z[jj] == INFINITY;
-                    if (z[jj] > v) {
-                        v = z[jj];
-                        gi = lo + 8 * g + jj;
+                    for (int jj = 0; jj < 8; ++jj) {
+                        nan |= (z[jj] != z[jj]) || z[jj] == INFINITY;
+                        if (z[jj] > v) {
+                            v = z[jj];
+                            gi = lo + 8 * g + jj;
+                        }
                     }
                 }
-            }
-            bad |= nan;
+                bad |= nan;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
-            if (lane == 0) {
-                sh.pa[i][warp] = v;
-                sh.pb[i][warp] = __int_as_float(gi);
-            }
-        } else {
-            // online max m and sums s0 + s1 relative to it; a NaN or +inf logit
-            // turns the sum into NaN, a -inf one adds 0
-            float m = -INFINITY, nm = 0.0f, s0 = 0.0f, s1 = 0.0f;
-            for (int g = tid; g < ng; g += kThreads) {
-                float z[8];
-                group8<ES>(zr, g, z);
-                const float gm = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
-                if (gm > m) {
-                    const float f = ex2((m - gm) * c2);
-                    s0 *= f;
-                    s1 *= f;
-                    m = gm;
-                    nm = -m * c2;
-                }
-                s0 += ex2(fmaf(z[0], c2, nm));
-                s1 += ex2(fmaf(z[1], c2, nm));
-                s0 += ex2(fmaf(z[2], c2, nm));
-                s1 += ex2(fmaf(z[3], c2, nm));
-                s0 += ex2(fmaf(z[4], c2, nm));
-                s1 += ex2(fmaf(z[5], c2, nm));
-                s0 += ex2(fmaf(z[6], c2, nm));
-                s1 += ex2(fmaf(z[7], c2, nm));
-            }
-            const float s = s0 + s1;
-            bad |= s != s;
-            float wm = m;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-            tf t = tf_of((m == -INFINITY || !(s == s)) ? 0.0f : s * ex2((m - wm) * c2));
-            t = warp_sum_tf(t);
-            if (lane == 0) {
-                sh.pa[i][warp] = wm;
-                sh.pb[i][warp] = t.h;
-                sh.pc[i][warp] = t.l;
-            }
-        }
-        __syncthreads();   // every thread is done with this stage
-        ++consumed;
-        if (j + NS < R) {
-            if (tid == 0) issue(j + NS);
-            ++issued;
-        }
-    }
-
-    // (2) this CTA's statistics of every row (warp i combines row i's partials)
-    if (!late) {
-        for (int i = warp; i < R; i += kWarps) {
-            const int l = lane & (kWarps - 1);   // both half-warps hold the 16 partials
-            if (greedy) {
-                float v = sh.pa[i][l];
-                int gi = __float_as_int(sh.pb[i][l]);
-#pragma unroll
-                for (int o = kWarps / 2; o > 0; o >>= 1)
+                for (int o = 16; o > 0; o >>= 1)
                     argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
-                if (lane == 0) sh.mine[i] = make_float4(v, __int_as_float(gi), 0.0f, 0.0f);
+                if (lane == 0) {
+                    sh.pa[j][warp] = v;
+                    sh.pb[j][warp] = __int_as_float(gi);
+                }
             } else {
-                const float wm = sh.pa[i][l];
+                // online max m and sums s0 + s1 relative to it; a NaN or +inf
+                // logit turns the sum into NaN, a -inf one adds 0
+                float m = -INFINITY, nm = 0.0f, s0 = 0.0f, s1 = 0.0f;
+                for (int g = stid; g < ng; g += kStreamThreads) {
+                    float z[8];
+                    if (g < gbulk)
+                        group8<ES>(zr, g, z);
+                    else
+                        group8_global<ES>(zg, g, n, z);
+                    const float gm =
+                        fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
+                    if (gm > m) {
+                        const float f = ex2((m - gm) * c2);
+                        s0 *= f;
+                        s1 *= f;
+                        m = gm;
+                        nm = -m * c2;
+                    }
+                    s0 += ex2(fmaf(z[0], c2, nm));
+                    s1 += ex2(fmaf(z[1], c2, nm));
+                    s0 += ex2(fmaf(z[2], c2, nm));
+                    s1 += ex2(fmaf(z[3], c2, nm));
+                    s0 += ex2(fmaf(z[4], c2, nm));
+                    s1 += ex2(fmaf(z[5], c2, nm));
+                    s0 += ex2(fmaf(z[6], c2, nm));
+                    s1 += ex2(fmaf(z[7], c2, nm));
+                }
+                const float s = s0 + s1;
+                bad |= s != s;
+                float wm = m;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                tf t = tf_of((m == -INFINITY || !(s == s)) ? 0.0f : s * ex2((m - wm) * c2));
+                t = warp_sum_tf(t);
+                if (lane == 0) {
+                    sh.pa[j][warp] = wm;
+                    sh.pb[j][warp] = t.h;
+                    sh.pc[j][warp] = t.l;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[st]);   // this warp is done with the stage (and its partial is written)
+        }
+    } else {
+        // (2) control warp: per row, the CTA's statistics from the warps'
+        // partials, one exchange with the cluster, the decision; the next row
+        // is copied only once this one is accepted
+        cluster_wait();   // every CTA's barriers are initialised
+        for (int j = 0; j < R; ++j) {
+            const int st = j % NS;
+            const bool drained = wait_copies(&sh.empty[st], static_cast<uint32_t>((j / NS) & 1), P.wait_ns);
+            if (!__all_sync(0xffffffffu, drained)) {
+                atomicOr(&sh.abort, 1);
+                break;
+            }
+            const int x = __shfl_sync(0xffffffffu, xr, j & 31);
+            const bool x_ok = j < k && x >= 0 && x < V;
+            const int l = lane < kStreamWarps ? lane : 0;
+            float4 mine;
+            if (greedy) {
+                float v = lane < kStreamWarps ? sh.pa[j][l] : -INFINITY;
+                int gi = lane < kStreamWarps ? __float_as_int(sh.pb[j][l]) : INT_MAX;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
+                mine = make_float4(v, __int_as_float(gi), 0.0f, 0.0f);
+            } else {
+                const float wm = lane < kStreamWarps ? sh.pa[j][l] : -INFINITY;
                 float bm = wm;
 #pragma unroll
-                for (int o = kWarps / 2; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
                 tf u = tf_of(0.0f);
-                if (wm != -INFINITY) u = tf_mulf(tf{sh.pb[i][l], sh.pc[i][l]}, ex2((wm - bm) * c2));
-#pragma unroll
-                for (int o = kWarps / 2; o > 0; o >>= 1) u = tf_add(u, tf_shfl_xor(u, o));
+                if (wm != -INFINITY) u = tf_mulf(tf{sh.pb[j][l], sh.pc[j][l]}, ex2((wm - bm) * c2));
+                u = warp_sum_tf(u);
                 // e(x) on this CTA's scale, in the CTA holding the draft token's column
-                const int x = i < k ? sh.tok[i] : -1;
-                const float ex = (x >= lo && x < lo + n && bm != -INFINITY) ? ex2((sh.zx[i] - bm) * c2) : 0.0f;
-                if (lane == 0) sh.mine[i] = make_float4(bm, u.h, u.l, ex);
+                const float ex = (x_ok && x >= lo && x < lo + n && bm != -INFINITY) ? ex2((sh.zx[j] - bm) * c2) : 0.0f;
+                mine = make_float4(bm, u.h, u.l, ex);
             }
-        }
-        __syncthreads();
-    }
-    cluster_wait();   // every CTA's barriers are initialised
-
-    // (3) one exchange of every row's statistics; every CTA then takes the same
-    // decisions (warp i decides draft i)
-    int a = -1;
-    int token = 0;
-    if (!late) {
-        if (tid == 0) mbar_expect_tx(&sh.rbar, 16u * static_cast<uint32_t>(C * R));
-        for (int t = tid; t < C * R; t += kThreads) {
-            const int r = t / R, i = t - r * R;
-            st_async_f4(mapa_u32(smem_u32(&sh.rows[rank][i]), r), sh.mine[i], mapa_u32(smem_u32(&sh.rbar), r));
-        }
-        late = cluster_phase_late(&sh.rbar, 0, P.wait_ns);
-    }
-    if (!late) {
-        for (int i = warp; i < R; i += kWarps) {
+            if (lane == 0) mbar_expect_tx(&sh.rbar[j], 16u * static_cast<uint32_t>(C));
+            if (lane < C)
+                st_async_f4(mapa_u32(smem_u32(&sh.rows[rank][j]), lane), mine, mapa_u32(smem_u32(&sh.rbar[j]), lane));
+            const bool got = cluster_bar_wait(&sh.rbar[j], 0, P.wait_ns);
+            if (!__all_sync(0xffffffffu, got)) {
+                atomicOr(&sh.abort, 1);
+                break;
+            }
+            // the decision on draft j from every rank's statistics of row j
             const bool on = lane < C;
-            const float4 rv = on ? sh.rows[lane][i] : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.0f, 0.0f);
-            const int x = i < k ? sh.tok[i] : -1;
-            const bool x_ok = x >= 0 && x < V;
+            const float4 rv = on ? sh.rows[lane][j] : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.0f, 0.0f);
             bool accept = false, rbad = false;
             if (greedy) {
                 float v = rv.x;
@@ -479,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
                     argmax_take(v, gi, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, gi, o));
                 rbad = !(v > -INFINITY);
                 const int g = (gi >= 0 && gi < V) ? gi : 0;
-                if (lane == 0) sh.arg[i] = g;
-                accept = i < k && x_ok && x == g;
+                if (lane == 0) sh.arg[j] = g;
+                accept = x_ok && x == g;
             } else {
                 float M = rv.x;
 #pragma unroll
@@ -495,115 +547,121 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
                     St = tf_of(1.0f);
                 }
                 if (lane == 0) {
-                    sh.rowM[i] = M;
-                    sh.rowS[i] = St;
+                    sh.rowM[j] = M;
+                    sh.rowS[j] = St;
+                    sh.mine[j] = mine;
                 }
+                const float qx = __shfl_sync(0xffffffffu, qxr, j & 31), ua = __shfl_sync(0xffffffffu, uar, j & 31);
                 // u < p(x) / q(x), with p(x) = e(x) f_owner / S, multiplied through by q(x) S
-                accept = i < k && x_ok && (sh.qx[i] == 0.0f || sh.ua[i] * (sh.qx[i] * St.h) < eown);
+                accept = x_ok && (qx == 0.0f || ua * (qx * St.h) < eown);
             }
-            if (lane == 0) {
-                sh.acc[i] = accept ? 1 : 0;
-                bad |= rbad;
+            if (lane == 0) bad |= rbad;
+            if (!accept) {
+                a = j;   // the first rejection, or row k: the bonus row
+                break;
+            }
+            if (j + NS < R) {
+                if (lane == 0) issue(j + NS);
+                ++issued;
             }
         }
         // a draft token outside [0, V) anywhere in the request is reported (as a
         // rejection where the walk reaches it)
-        if (lead && P.status)
-            for (int i = 0; i < k; ++i)
-                if (sh.tok[i] < 0 || sh.tok[i] >= V) {
-                    atomicOr(P.status, SPEC_STATUS_TOKEN_RANGE);
-                    break;
-                }
-        __syncthreads();
-        a = k;
-        for (int i = 0; i < k; ++i)
-            if (!sh.acc[i]) {
-                a = i;
-                break;
-            }
-        token = greedy ? sh.arg[a] : 0;
-    }
-
-    if (!late && !greedy) {
-        // (4) inverse-CDF draw over the residual max(0, p - q) of row a (p when
-        // a == k, or when the residual has no mass); p = e 2^((m_r - M) c2) / S.
-        // Row a's logits are read in place when the ring still holds them, with
-        // q copied into the free stages around them; else both are copied.
-        const bool want_q = a < k;
-        const int ja = R - 1 - a;                       // the walk step that read row a
-        const int sa = ja % NS;
-        const size_t zb = (static_cast<size_t>(S) * ES + 127) / 128 * 128;
-        const int gh_split = (ng + 1) >> 1;
-        size_t zoff = 0, qoff_a = zb, qoff_b = 0;
-        int gh = ng;                                    // groups of q in the first region
-        bool reload = true;
-        if (ja >= R - NS) {                             // row a's slice is still in stage sa
-            const size_t sz = static_cast<size_t>(sa) * stage_bytes;
-            if (!want_q) {
-                zoff = sz;
-                reload = false;
-            } else if (static_cast<size_t>(ng) * 32 <= stage_bytes) {   // q fits one stage
-                zoff = sz;
-                qoff_a = sa == 0 ? stage_bytes : 0;
-                reload = false;
-            } else if (NS == 3 && static_cast<size_t>(gh_split) * 32 <= stage_bytes) {   // q in the other two
-                zoff = sz;
-                qoff_a = sa == 0 ? stage_bytes : 0;
-                qoff_b = sa == 2 ? stage_bytes : 2 * stage_bytes;
-                gh = gh_split;
-                reload = false;
+        const bool bad_token = __any_sync(0xffffffffu, lane < k && (xr < 0 || xr >= V));
+        if (rank == 0 && lane == 0 && bad_token && P.status) atomicOr(P.status, SPEC_STATUS_TOKEN_RANGE);
+        if (lane == 0) {
+            sh.a = a;
+            sh.issued = issued;
+            if (a >= 0) {
+                // streaming warps past the end stop at the next row they wake
+                // on; the first row never copied is completed by a plain arrive
+                // (its stage's previous row was consumed, so that phase is done)
+                *reinterpret_cast<volatile int *>(&sh.end_row) = a;
+                if (issued < R) mbar_arrive(&sh.full[issued % NS]);
             }
         }
-        const unsigned char *zs = dyn + zoff;
-        float *qa = reinterpret_cast<float *>(dyn + qoff_a);
-        float *qb = reinterpret_cast<float *>(dyn + qoff_b);
+        __syncwarp();
+    }
+    if (!ctrl) cluster_wait();
+    __syncthreads();
+    bool late = sh.abort != 0;
+    a = late ? -1 : sh.a;
+    late |= a < 0;
+    const int fake_stage = (!late && sh.issued < R) ? sh.issued % NS : -1;   // its last phase was the plain arrive
+    const int token = (!late && greedy) ? sh.arg[a] : 0;
+
+    int xk = 0;
+    bool drawn_copy = false;   // the drawn row's q copies were issued
+    if (!late && !greedy) {
+        // (3) inverse-CDF draw over the residual max(0, p - q) of row a (p when
+        // a == k, or when the residual has no mass); p = e 2^((m_r - M) c2) / S.
+        // Row a's logits are still in stage a % NS; q of row a goes into the
+        // other stages once the rows copied past the rejection have landed.
+        const bool want_q = a < k;
+        const int sa = a % NS;
+        const int o1 = sa == 0 ? 1 : 0, o2 = sa == 2 ? 1 : 2;   // the other two stages, in order
+        const int gh = ES == 2 ? (ng + 1) >> 1 : ng;             // groups of q in the first of them
+        const unsigned char *zs = dyn + static_cast<size_t>(sa) * stage_bytes;
+        float *qa = reinterpret_cast<float *>(dyn + static_cast<size_t>(o1) * stage_bytes);
+        float *qb = reinterpret_cast<float *>(dyn + static_cast<size_t>(o2) * stage_bytes);
         auto qdst = [&](int c) -> float * { return c < 8 * gh ? qa + c : qb + (c - 8 * gh); };
-        // bulk parts: the z slice when copied again; q's aligned bytes, split at group gh
-        const uint32_t zcopy = reload ? zmain : 0u;
         uint32_t qa_bytes = 0, qb_bytes = 0;
         if (want_q && qmain) {
             const uint32_t cut = static_cast<uint32_t>(gh) * 32u;
             qa_bytes = qmain < cut ? qmain : cut;
             qb_bytes = qmain - qa_bytes;
         }
-        const uint32_t tx = zcopy + qa_bytes + qb_bytes;
-        if (tid == 0 && tx > 0) {
-            fence_proxy_async();
-            mbar_expect_tx(&sh.bar, tx);
-            if (zcopy)
-                bulk_g2s(dyn + zoff, static_cast<const unsigned char *>(P.logits) + (zrow(a) + lo) * ES, zcopy, &sh.bar);
-            if (qa_bytes) bulk_g2s(qa, P.q + qrow(a) + lo, qa_bytes, &sh.bar);
-            if (qb_bytes) bulk_g2s(qb, P.q + qrow(a) + lo + 8 * gh, qb_bytes, &sh.bar);
-            bytes += tx;
-        }
-        drawn_copy = tx > 0;
-        if (reload) {
-            if constexpr (ES == 2) {
-                const uint16_t *src = static_cast<const uint16_t *>(P.logits) + zrow(a) + lo;
-                uint16_t *d = reinterpret_cast<uint16_t *>(dyn + zoff);
-                for (int c = static_cast<int>(zcopy / 2) + tid; c < n; c += kThreads) d[c] = __ldg(src + c);
-                for (int c = n + tid; c < 8 * ng; c += kThreads) d[c] = 0xff80u;
-            } else {
-                const float *src = static_cast<const float *>(P.logits) + zrow(a) + lo;
-                float *d = reinterpret_cast<float *>(dyn + zoff);
-                for (int c = static_cast<int>(zcopy / 4) + tid; c < n; c += kThreads) d[c] = __ldg(src + c);
-                for (int c = n + tid; c < 8 * ng; c += kThreads) d[c] = -INFINITY;
-            }
-        }
         if (want_q) {
-            for (int c = static_cast<int>((qa_bytes + qb_bytes) / 4) + tid; c < n; c += kThreads)
-                *qdst(c) = __ldg(P.q + qrow(a) + lo + c);
-            for (int c = n + tid; c < 8 * ng; c += kThreads) *qdst(c) = 0.0f;
+            if (tid == tctl) {
+                // the last row copied into stage s past the rejection (still in flight), or -1
+                auto last_row = [&](int s) {
+                    int r = -1;
+                    for (int j = a + 1; j < issued; ++j)
+                        if (j % NS == s) r = j;
+                    return r;
+                };
+                bool ok = true;
+                const int r1 = last_row(o1);
+                if (r1 >= 0) ok = wait_copies(&sh.full[o1], static_cast<uint32_t>((r1 / NS) & 1), P.wait_ns);
+                if (ok && qa_bytes) {
+                    mbar_expect_tx_only(&sh.bar, qa_bytes);
+                    fence_proxy_async();
+                    bulk_g2s(qa, P.q + qrow(a) + lo, qa_bytes, &sh.bar);
+                    bytes += qa_bytes;
+                }
+                if (gh < ng) {
+                    const int r2 = last_row(o2);
+                    if (ok && r2 >= 0) ok = wait_copies(&sh.full[o2], static_cast<uint32_t>((r2 / NS) & 1), P.wait_ns);
+                    if (ok && qb_bytes) {
+                        mbar_expect_tx_only(&sh.bar, qb_bytes);
+                        fence_proxy_async();
+                        bulk_g2s(qb, P.q + qrow(a) + lo + 8 * gh, qb_bytes, &sh.bar);
+                        bytes += qb_bytes;
+                    }
+                }
+                mbar_arrive(&sh.bar);   // the phase ends when the copies issued above have landed
+                sh.qfail = ok ? 0 : 1;
+            }
+            drawn_copy = true;
+            __syncthreads();
+            if (!sh.qfail) {
+                // plain loads of what the bulk copies leave, and the padding
+                for (int c = static_cast<int>((qa_bytes + qb_bytes) / 4) + tid; c < n; c += kThreads)
+                    *qdst(c) = __ldg(P.q + qrow(a) + lo + c);
+                for (int c = n + tid; c < 8 * ng; c += kThreads) *qdst(c) = 0.0f;
+            }
+            const bool copy_late = sh.qfail || !wait_copies(&sh.bar, 0, P.wait_ns);
+            late = __syncthreads_or(copy_late) != 0;
         }
-        bool copy_late = false;
-        if (tx > 0) copy_late = !wait_copies(&sh.bar, 0, P.wait_ns);
-        late = __syncthreads_or(copy_late) != 0;
 
         const float u = P.u_sample ? __ldg(P.u_sample + static_cast<size_t>(b) * R + a) : 0.0f;
         const float mr = sh.mine[a].x, M = sh.rowM[a];
         const float Sh = sh.rowS[a].h;
         DrawRow<ES> D;
         D.zs = zs;
+        D.zg = static_cast<const unsigned char *>(P.logits) + (zrow(a) + lo) * ES;
+        D.gbulk = gbulk;
+        D.n = n;
         D.qa = qa;
         D.qb = qb;
         D.gh = gh;
@@ -638,8 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
             const float4 *trow = exchange(sh, xk, rank, make_float4(tot.h, tot.l, __int_as_float(clast), 0.0f),
                                           C, P.wait_ns, late);
             if (late) break;
-            tf Z = tf_of(0.0f);
-            for (int r = 0; r < C; ++r) Z = tf_add(Z, tf{trow[r].x, trow[r].y});
+            // every warp scans the CTA totals in rank order (lane r: rank r)
+            const tf own_r = lane < C ? tf{trow[lane].x, trow[lane].y} : tf_of(0.0f);
+            const tf end_r = warp_incl_scan_tf(own_r, lane);
+            const tf Z = tf_shfl(end_r, C - 1);
             if (D.resid && !(Z.h > 0.0f)) {
                 D.resid = false;   // a residual of no mass: sample from p
                 __syncthreads();
@@ -647,18 +707,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
             }
             const tf t = tf_mulf(Z, u);
             // the CTA holding t: the first whose running end exceeds t
-            tf run = tf_of(0.0f), before = tf_of(0.0f);
-            int rstar = -1, rlast = -1;
-            for (int r = 0; r < C; ++r) {
-                if (__float_as_int(trow[r].z) >= 0) rlast = r;
-                const tf end = tf_add(run, tf{trow[r].x, trow[r].y});
-                if (rstar < 0 && tf_gt(end, t)) {
-                    rstar = r;
-                    before = run;
-                }
-                run = end;
-            }
-            if (rstar < 0) rstar = rlast;   // t at or past the total after rounding: the last positive column
+            const unsigned past = __ballot_sync(0xffffffffu, lane < C && tf_gt(end_r, t));
+            const unsigned pos = __ballot_sync(0xffffffffu, lane < C && __float_as_int(trow[lane].z) >= 0);
+            // t at or past the total after rounding: the last CTA with a positive column
+            const int rstar = past ? __ffs(past) - 1 : (pos ? 31 - __clz(pos) : -1);
+            const tf up{__shfl_up_sync(0xffffffffu, end_r.h, 1), __shfl_up_sync(0xffffffffu, end_r.l, 1)};
+            const int rs = rstar > 0 ? rstar : 0;
+            tf before = tf{__shfl_sync(0xffffffffu, up.h, rs), __shfl_sync(0xffffffffu, up.l, rs)};
+            if (rstar <= 0) before = tf_of(0.0f);
             if (rank == rstar) {
                 tf tr = tf_add(t, tf_neg(before));   // t relative to this CTA's first column
                 if (tr.h < 0.0f) tr = tf_of(0.0f);
@@ -738,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
         }
     }
     if (!late && a >= 0) {
-        // (5) outputs: drafts 1..a, the emitted token (greedy: written here), -1
+        // (4) outputs: drafts 1..a, the emitted token (greedy: written here), -1
         // padding, the count, and the slot_mapping fix-up
         if (lead) {
             int32_t *ot = P.out_tokens + static_cast<size_t>(b) * R;
@@ -754,14 +810,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
     }
     if (late) {
         // a copy or an exchange outlived its wait: bounded waits for every copy
-        // still in flight, so none lands here after exit
-        for (int j = consumed; j < issued; ++j)
-            if (zmain) wait_copies(&sh.sbar[j % NS], static_cast<uint32_t>((j / NS) & 1), kWaitLimitNs);
-        if (drawn_copy) wait_copies(&sh.bar, 0, kWaitLimitNs);
-        if (tid == 0 && P.status) atomicOr(P.status, SPEC_STATUS_WAIT_TIMEOUT);
+        // still in flight (the last copy into each stage), so none lands here
+        // after exit
+        if (tid == tctl) {
+            for (int s = 0; s < NS; ++s) {
+                int r = -1;
+                for (int j = 0; j < issued; ++j)
+                    if (j % NS == s) r = j;
+                // a stage whose last phase was the plain arrive had its copy land before it
+                if (r >= 0 && zmain && s != fake_stage)
+                    wait_copies(&sh.full[s], static_cast<uint32_t>((r / NS) & 1), kWaitLimitNs);
+            }
+            if (drawn_copy) wait_copies(&sh.bar, 0, kWaitLimitNs);
+            if (P.status) atomicOr(P.status, SPEC_STATUS_WAIT_TIMEOUT);
+        }
     }
     if (bad && P.status) atomicOr(P.status, SPEC_STATUS_NONFINITE);
-    if (tid == 0 && P.stats && bytes) atomicAdd(P.stats + 4, bytes);
+    if (tid == tctl && P.stats && bytes) atomicAdd(P.stats + 4, bytes);
     cl.sync();   // keep this CTA's shared memory alive until the last remote store into it
 }
 
@@ -796,8 +861,10 @@ spec_status_t cc_setup(int &sms) {
 }  // namespace
 
 // Geometry of the cluster kernel for vocabulary V with C CTAs a request:
-// columns per CTA, the phase-1 ring (stages of one row slice each) and the
-// dynamic shared memory (the ring, or the drawn row's logits and q slices).
+// columns per CTA and the ring (stages of one row slice each).  The draw keeps
+// row a's logits in its stage and puts q of row a in the others: half of the
+// slice in each of two for bf16 logits (so three stages), all of it in one for
+// fp32 logits.
 struct CcGeom {
     int S, stages;
     size_t stage_bytes, smem;
@@ -805,15 +872,13 @@ struct CcGeom {
 
 static bool cc_geom(int V, int C, int es, CcGeom &G) {
     G.S = static_cast<int>(((static_cast<long long>(V) + C - 1) / C + 7) / 8 * 8);
-    // a stage holds one row slice of logits, or half of a q slice (whole groups)
     const size_t slice = static_cast<size_t>(G.S) * es;
-    const size_t half_q = static_cast<size_t>((G.S / 8 + 1) / 2) * 32;
-    G.stage_bytes = ((slice > half_q ? slice : half_q) + 127) / 128 * 128;
+    const size_t q_part = es == 2 ? static_cast<size_t>((G.S / 8 + 1) / 2) * 32 : static_cast<size_t>(G.S) * 4;
+    G.stage_bytes = ((slice > q_part ? slice : q_part) + 127) / 128 * 128;
     const size_t fit = static_cast<size_t>(cc::kSmemBudget) / G.stage_bytes;
     G.stages = static_cast<int>(fit < static_cast<size_t>(cc::kMaxStages) ? fit : static_cast<size_t>(cc::kMaxStages));
-    const size_t draw = (slice + 127) / 128 * 128 + static_cast<size_t>(G.S) * 4;   // logits then q, copied
-    G.smem = G.stages * G.stage_bytes > draw ? G.stages * G.stage_bytes : draw;
-    return G.stages >= 2 && G.smem <= static_cast<size_t>(cc::kSmemBudget);
+    G.smem = G.stages * G.stage_bytes;
+    return G.stages >= (es == 2 ? 3 : 2);
 }
 
 // Cluster size for a batch of B sampled (or mixed) padded chains with k drafts
