@@ -8,7 +8,7 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SRCS = [os.path.join(PKG, "csrc", f)
-        for f in ("spec_verify.cu", "chain_cluster.cu", "tree_sampled.cu", "next_step.cu", "ngram.cu")]
+        for f in ("spec_verify.cu", "chain_cluster.cu", "greedy_cluster.cu", "tree_sampled.cu", "next_step.cu", "ngram.cu")]
 HDRS = [os.path.join(ROOT, "include", "spec_verify.h"), os.path.join(PKG, "csrc", "common.h"),
         os.path.join(PKG, "csrc", "ptx.cuh"), os.path.join(PKG, "csrc", "twofloat.cuh")]
 SRC = SRCS[0]

@@ -2076,6 +2076,11 @@ __global__ void __maxnreg__(128) verify_kernel(const __grid_constant__ Params P)
         S.consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // Every block of this grid is resident from the start, so the next kernel
+    // may begin launching at once; nothing here touches global memory before
+    // the previous kernel in the stream has completed.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
 
     if (warp == 0) Dev<MODE>::template producer<ES, SMP>(P, S, ring, lane);
@@ -2285,9 +2290,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // read once per call when the launch is set up.
 std::atomic<int> g_tune_splits{0};
 std::atomic<int> g_tune_ahead{0};
-std::atomic<int> g_tune_path{0};   // 0: padded chains that fit go to the cluster kernel; 1: persistent only
+std::atomic<int> g_tune_path{0};   // 0: automatic; 1: persistent only; 2: automatic plus greedy chains on clusters
 
-bool chain_cluster_allowed() { return g_tune_path.load(std::memory_order_relaxed) == 0; }
+bool chain_cluster_allowed() { return g_tune_path.load(std::memory_order_relaxed) != 1; }
+int tuning_path() { return g_tune_path.load(std::memory_order_relaxed); }
 std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
@@ -2310,6 +2316,26 @@ int choose_splits(int rows_total, int nsub, int sms) {
 int choose_ahead() {
     const int forced = g_tune_ahead.load(std::memory_order_relaxed);
     return (forced >= 2 && forced <= kStages) ? forced : kStages;
+}
+
+// Launch with programmatic stream serialisation: the kernel's blocks may be
+// scheduled while the kernel before it in the stream drains (each block waits,
+// griddepcontrol.wait, before its first global memory access), so the launch
+// and the blocks' start-up overlap the previous kernel's tail.
+template <typename K>
+static cudaError_t launch_serialised(K kernel, dim3 grid, cudaStream_t st, const Params &P) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
 // clear_counters: zero the layout's counter region on `stream` just before the
@@ -2377,29 +2403,60 @@ spec_status_t launch_verify(Params &P, spec_dtype_t dtype, void *workspace, size
         const cudaError_t ec = cudaMemsetAsync(ws + L.reset, 0, L.reset_bytes, st);
         if (ec != cudaSuccess) return fail(SPEC_ERR_CUDA, "clearing the workspace counters: %s", cudaGetErrorString(ec));
     }
+    if (!P.cu && !P.q && !P.temperature) {
+        // greedy padded chains and greedy trees: the persistent cluster kernel
+        GreedyClusterArgs A;
+        memset(&A, 0, sizeof A);
+        A.logits = P.logits;
+        A.dtype = dtype;
+        A.tokens = P.tokens;
+        A.parent = P.tree ? P.parent : nullptr;
+        A.B = P.B;
+        A.R = P.R;
+        A.V = P.V;
+        A.D = P.D;
+        A.out_tokens = P.out_tokens;
+        A.out_count = P.out_count;
+        A.out_path = P.out_path;
+        A.slots = P.slots;
+        A.pad = P.pad;
+        A.status = P.status;
+        A.stats = P.stats;
+        A.ctr = P.ctrl;
+        A.rmask = P.req_mask;
+        A.dmask = reinterpret_cast<unsigned long long *>(ws + L.row_ctr);   // B words: R >= 2 rows of 4 bytes each
+        A.fin = P.req_ctr;
+        A.rowstate = P.rowstate;
+        A.reset_base = P.reset_base;
+        A.reset_words = static_cast<int>(P.reset_words);
+        bool launched = false;
+        const spec_status_t gs = launch_greedy_cluster(A, stream, launched);
+        if (gs != SPEC_OK || launched) return gs;
+    }
     // Calls without temperatures are greedy only: a leaner instantiation without
     // the sampling and residual code.
     const dim3 g3(static_cast<unsigned>(grid));
     const bool bf = dtype == SPEC_BF16;
+    cudaError_t e = cudaSuccess;
     if (P.tree) {
-        if (bf) verify_kernel<2, false, 2><<<g3, kThreads, kSmemBytes, st>>>(P);
-        else verify_kernel<4, false, 2><<<g3, kThreads, kSmemBytes, st>>>(P);
+        if (bf) e = launch_serialised(verify_kernel<2, false, 2>, g3, st, P);
+        else e = launch_serialised(verify_kernel<4, false, 2>, g3, st, P);
     } else if (P.cu) {
         if (P.q || P.temperature) {
-            if (bf) verify_kernel<2, true, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
-            else verify_kernel<4, true, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
+            if (bf) e = launch_serialised(verify_kernel<2, true, 1>, g3, st, P);
+            else e = launch_serialised(verify_kernel<4, true, 1>, g3, st, P);
         } else {
-            if (bf) verify_kernel<2, false, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
-            else verify_kernel<4, false, 1><<<g3, kThreads, kSmemBytes, st>>>(P);
+            if (bf) e = launch_serialised(verify_kernel<2, false, 1>, g3, st, P);
+            else e = launch_serialised(verify_kernel<4, false, 1>, g3, st, P);
         }
     } else if (P.q || P.temperature) {
-        if (bf) verify_kernel<2, true, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
-        else verify_kernel<4, true, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
+        if (bf) e = launch_serialised(verify_kernel<2, true, 0>, g3, st, P);
+        else e = launch_serialised(verify_kernel<4, true, 0>, g3, st, P);
     } else {
-        if (bf) verify_kernel<2, false, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
-        else verify_kernel<4, false, 0><<<g3, kThreads, kSmemBytes, st>>>(P);
+        if (bf) e = launch_serialised(verify_kernel<2, false, 0>, g3, st, P);
+        else e = launch_serialised(verify_kernel<4, false, 0>, g3, st, P);
     }
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
 }
@@ -2744,8 +2801,8 @@ extern "C" unsigned long long spec_set_wait_limit_ns(unsigned long long ns) {
 
 extern "C" spec_status_t spec_set_tuning(int splits, int ahead, int path) {
     g_err[0] = 0;
-    if (splits < 0 || ahead < 0 || (ahead != 0 && (ahead < 2 || ahead > kStages)) || path < 0 || path > 1)
-        return fail(SPEC_ERR_INVALID_ARG, "need splits >= 0, ahead 0 or in [2, 3], path 0 or 1%s");
+    if (splits < 0 || ahead < 0 || (ahead != 0 && (ahead < 2 || ahead > kStages)) || path < 0 || path > 2)
+        return fail(SPEC_ERR_INVALID_ARG, "need splits >= 0, ahead 0 or in [2, 3], path 0, 1 or 2%s");
     g_tune_splits.store(splits, std::memory_order_relaxed);
     g_tune_ahead.store(ahead, std::memory_order_relaxed);
     g_tune_path.store(path, std::memory_order_relaxed);

@@ -32,16 +32,21 @@ def sv():
     return m
 
 
-@pytest.fixture(autouse=True, params=[0, 1], ids=["cluster", "persistent"])
+@pytest.fixture(autouse=True, params=[0, 1, 2], ids=["auto", "persistent", "cluster"])
 def chain_path(request, sv):
-    """Chains run on both kernels: the cluster-per-request kernel (padded
-    chains whose clusters fit on the GPU; the default for them) and the
-    persistent kernel.  Tests of trees, ragged batches and the separate fix-up
-    do not depend on it and run once."""
+    """The kernel that verifies: path 0 (automatic) sends sampled padded chains
+    whose per-request clusters fit on the GPU to the chain cluster kernel and
+    greedy trees to the greedy cluster kernel; path 1 sends every batch to the
+    persistent kernel; path 2 is path 0 with greedy padded chains on the greedy
+    cluster kernel too.  Tests of ragged batches, the separate fix-up, n-gram
+    lookup and next-step preparation do not depend on it and run once; trees
+    run on paths 0 and 1."""
     path = request.param
     name = request.node.name
-    if path == 1 and any(w in name for w in ("tree", "fixup_slots", "ragged", "ngram", "next_step", "kv")):
-        pytest.skip("the path applies to padded chains only")
+    if path != 0 and any(w in name for w in ("fixup_slots", "ragged", "ngram", "next_step", "kv")):
+        pytest.skip("the path applies to padded chains and trees only")
+    if path == 2 and "tree" in name:
+        pytest.skip("trees take the same kernel on paths 0 and 2")
     sv.set_tuning(0, 0, path)
     yield path
     sv.set_tuning(0, 0, 0)
