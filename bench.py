@@ -44,8 +44,15 @@ UNIT = "verified draft positions/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 OTHER_NAMES = ["sampled_chain", "sweep", "greedy_tree", "ragged", "ngram", "sampled_tree", "next_step"]
-KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_chain_gb300", "csrc", f)
-               for f in ("spec_verify.cu", "ptx.cuh", "twofloat.cuh")]
+_CSRC = os.path.join(ROOT, "speculative_decoding_verification_chain_gb300", "csrc")
+KERNEL_SRCS = [os.path.join(_CSRC, f) for f in ("spec_verify.cu", "ptx.cuh", "twofloat.cuh")]
+# the sources each profiled kernel is compiled from (its profile's hash covers them)
+PROFILED_SRCS = {
+    "verify_kernel": KERNEL_SRCS,
+    "chain_cluster_kernel": [os.path.join(_CSRC, f) for f in ("chain_cluster.cu", "ptx.cuh", "twofloat.cuh")],
+    "greedy_cluster_kernel": [os.path.join(_CSRC, f) for f in ("greedy_cluster.cu", "ptx.cuh")],
+    "tree_sampled_kernel": [os.path.join(_CSRC, f) for f in ("tree_sampled.cu", "ptx.cuh", "twofloat.cuh")],
+}
 
 
 # ------------------------------------------------------------------ setup --
@@ -113,12 +120,12 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the code the verify kernel is compiled from: comments removed
-    and whitespace collapsed, so a change to the code (not to its comments)
-    orphans the profiled counters."""
+def kernel_source_hash(srcs=None) -> str:
+    """Hash of the code a kernel is compiled from (the verify kernel's by
+    default): comments removed and whitespace collapsed, so a change to the code
+    (not to its comments) orphans the profiled counters."""
     h = hashlib.sha256()
-    for path in KERNEL_SRCS:
+    for path in (srcs or KERNEL_SRCS):
         with open(path, encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -128,9 +135,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name: str):
+def profiled_traffic(name: str, kernel: str = "verify_kernel"):
     """dram read+write bytes per launch from a committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+    taken on the current source of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", name)
     try:
         text = open(path).read()
@@ -138,7 +145,7 @@ def profiled_traffic(name: str):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    if not m or not h or h.group(1) != kernel_source_hash(PROFILED_SRCS[kernel]):
         return None
     return float(m.group(1))
 
@@ -660,6 +667,10 @@ def others(sv, W, dev, dist, peak, args):
             x = W.chain_sampled(seed=3, B=32, k=4, V=128256, temperature=0.7, lam=lam)
             out.append(_other_chain(sv, x, dev, dist, peak,
                                     "sampled chain B=32 k=4 V=128256 T=0.7 lambda=%g (Zipf)" % lam))
+            if lam == 0.3:
+                out[-1]["kernel"] = "chain_cluster_kernel<2>"
+                out[-1]["profiled_traffic"] = profiled_traffic(
+                    "chain_cluster_kernel_sampled_chain_B32_k4_V128256.md", "chain_cluster_kernel")
     if want("sweep"):
         for Bs in ([args.sweep_b] if args.sweep_b else [64, 1, 8, 256]):
             x = W.chain_sampled(seed=5, B=Bs, k=8, V=152064, temperature=1.0, lam=0.3)
@@ -667,12 +678,17 @@ def others(sv, W, dev, dist, peak, args):
                                     "sampled sweep B=%d k=8 V=152064 T=1 lambda=0.3 (Zipf)" % Bs))
     if want("greedy_tree"):
         out.append(_other_tree(sv, W, dev, dist, peak))
+        out[-1]["kernel"] = "greedy_cluster_kernel<2>"
+        out[-1]["profiled_traffic"] = profiled_traffic("greedy_cluster_kernel_greedy_tree_B16_N60_V128256.md",
+                                                       "greedy_cluster_kernel")
     if want("ragged"):
         out.append(_other_ragged(sv, W, dev, dist, peak))
     if want("ngram"):
         out.append(_other_ngram(sv, W, dev, dist, peak))
     if want("sampled_tree"):
         out.append(_other_tree_sampled(sv, W, dev, dist, peak))
+        out[-1]["kernel"] = "tree_sampled_kernel<2>"
+        out[-1]["profiled_traffic"] = profiled_traffic("tree_sampled_kernel_B16_N60_V128256.md", "tree_sampled_kernel")
     if want("next_step"):
         out.extend(_other_next_step(sv, W, dev, dist, peak))
     return out
