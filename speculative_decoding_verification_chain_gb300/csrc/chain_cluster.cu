@@ -808,6 +808,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
             }
         }
     }
+    if (!late && tid == tctl) {
+        // rows copied past the rejection and not waited for by the draw (a
+        // greedy request, or the stages q did not need) land before exit
+        for (int s = 0; s < NS; ++s) {
+            int r = -1;
+            for (int j = a + 1; j < issued; ++j)
+                if (j % NS == s) r = j;
+            if (r >= 0 && zmain) wait_copies(&sh.full[s], static_cast<uint32_t>((r / NS) & 1), kWaitLimitNs);
+        }
+    }
     if (late) {
         // a copy or an exchange outlived its wait: bounded waits for every copy
         // still in flight (the last copy into each stage), so none lands here
