@@ -440,10 +440,11 @@ const char *spec_last_error(void);
  * about two rows per SM, finer otherwise); ahead = stages that kernel's copy
  * ring keeps in flight (0 = automatic, i.e. all 3; else 2 or 3); path = 0
  * (automatic: sampled padded chains whose per-request thread-block clusters
- * all fit on the GPU at once are verified one cluster per request, greedy
- * trees of at most 64 rows by a persistent grid of clusters, the rest by the
- * persistent kernel), 1 (the persistent kernel for every batch) or 2 (as 0,
- * with greedy padded chains of at most 64 rows on the grid of clusters too).  Greedy
+ * all fit on the GPU at once are verified one cluster per request; greedy
+ * trees of at most 64 rows, and greedy padded chains of at most 64 rows with
+ * fewer than two rows per SM, by a persistent grid of clusters; the rest by
+ * the persistent kernel), 1 (the persistent kernel for every batch) or 2 (as
+ * 0, with every greedy padded chain of at most 64 rows on the grid).  Greedy
  * results do not depend on any of them; sampled tokens can differ between the
  * two kernels only where the arithmetic of the accept test or the draw falls
  * within rounding of a decision boundary.  Other values return

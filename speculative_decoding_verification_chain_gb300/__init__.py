@@ -204,9 +204,10 @@ def set_wait_limit_ns(ns: int) -> int:
 def set_tuning(splits: int = 0, ahead: int = 0, path: int = 0):
     """spec_set_tuning: row splits and copy-ring depth of the persistent verify
     kernel (0 = automatic), and path (0 = automatic: sampled padded chains that
-    fit go to the cluster-per-request kernel, greedy trees to the grid of
-    clusters; 1 = the persistent kernel for every batch; 2 = as 0, with greedy
-    padded chains on the grid of clusters too)."""
+    fit go to the cluster-per-request kernel, greedy trees and greedy padded
+    chains with fewer than two rows per SM to the grid of clusters; 1 = the
+    persistent kernel for every batch; 2 = as 0, with every greedy padded chain
+    on the grid of clusters)."""
     _check("spec_set_tuning", load_library().spec_set_tuning(int(splits), int(ahead), int(path)))
 
 

@@ -21,7 +21,9 @@
 //
 // Roles (416 threads per CTA):
 //   * warp 0, copier (every CTA): takes the cluster's work items in order and
-//     streams its slice of each row into the ring;
+//     streams its slice of each row into the ring, unless the row's node has
+//     died since the item went out (its dead-mask word, loaded while the stage
+//     frees): then its warps send a marker, and the epilogue drops the row;
 //   * warp 1, dispatcher (first CTA): claims units, drops those whose node is
 //     already known rejected (a per-request mask of dead nodes, loaded while
 //     the item's flow-control wait is in flight) and sends the rest to every
@@ -73,6 +75,7 @@ constexpr int kMaxBatch = 2;   // units claimed at once (after rounds of dead un
 constexpr int kMaxR = 64;      // rows per request (the masks are 64-bit)
 constexpr int kSmemBudget = 200 * 1024;
 constexpr uint32_t kResolved = 0x80000000u;
+constexpr uint32_t kSkipped = 0xfffffffeu;   // the candidate column of a row a CTA found dead
 constexpr unsigned long long kWaitLimitNs = 500000000ull;   // copies in flight at exit
 
 struct Params {
@@ -110,7 +113,7 @@ struct Shared {
     uint64_t res_full[kResQ], res_free[kResQ];
     uint64_t rec_full[kResQ];         // first CTA: the slot's item record is written
     int2 items[kItems];               // (b, n); b < 0 ends the work
-    int4 stage_item[kStages];         // (b, n, item number, 0); b < 0 ends the work
+    int4 stage_item[kStages];         // (b, n, item number, skipped); b < 0 ends the work
     int2 itemrec[kResQ];              // first CTA: (b, n) of the item whose candidates fill the slot
     uint2 res[kResQ][kMaxC * kStreamWarps];   // first CTA: (value bits, column) per streaming warp
     int path[kEpiWarps][kMaxR];       // finalisation scratch per epilogue warp
@@ -133,6 +136,12 @@ __device__ __forceinline__ void st_async_u2(uint32_t dst, uint32_t x, uint32_t y
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -318,6 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) greedy_cluster_kernel(const __gri
                 }
                 const int2 itm = sh.items[s];
                 remote_arrive(&sh.item_empty[s], 0);   // the slot may be refilled
+                // the node may have died since the item went out: its dead-mask
+                // word loads while the stage frees, and a dead row is not copied
+                unsigned long long dm = 0;
+                if (itm.x >= 0 && itm.y > 0)
+                    dm = P.packed ? (ld_relaxed_u64(P.rmask + itm.x) >> 32) : ld_relaxed_u64(P.dmask + itm.x);
                 const int st = it % kStages;
                 if (it >= kStages &&
                     !wait_local(&sh.empty[st], static_cast<uint32_t>(((it / kStages) - 1) & 1), P.wait_ns)) {
@@ -331,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1) greedy_cluster_kernel(const __gri
                     ++it;
                     break;
                 }
-                sh.stage_item[st] = make_int4(itm.x, itm.y, j, 0);
-                if (zmain) {
+                const bool dead = itm.y > 0 && ((dm >> itm.y) & 1ull);
+                sh.stage_item[st] = make_int4(itm.x, itm.y, j, dead ? 1 : 0);
+                if (zmain && !dead) {
                     fence_proxy_async();
                     mbar_expect_tx(&sh.full[st], zmain);
                     bulk_g2s(dyn + static_cast<size_t>(st) * P.stage_bytes,
@@ -481,14 +496,18 @@ __global__ void __launch_bounds__(kThreads, 1) greedy_cluster_kernel(const __gri
                 }
                 float v = -INFINITY;
                 int g = INT_MAX;
+                bool skipped = false;
                 if (b >= 0)
                     for (int q = lane; q < C * kStreamWarps; q += 32) {
                         const uint2 c = sh.res[rs][q];
+                        skipped |= c.y == kSkipped;
                         argmax_take(v, g, __uint_as_float(c.x), static_cast<int>(c.y));
                     }
+                skipped = __any_sync(0xffffffffu, skipped);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.res_free[rs]);
                 if (b < 0) break;
+                if (skipped) continue;   // its node is dead: nothing waits for the row
                 warp_argmax(v, g);
                 if (!(v > -INFINITY) && lane == 0) set_status(P, SPEC_STATUS_NONFINITE);   // a row -inf throughout
                 const int arg = (g >= 0 && g < V) ? g : 0;
@@ -571,6 +590,16 @@ __global__ void __launch_bounds__(kThreads, 1) greedy_cluster_kernel(const __gri
             }
             const int4 si = sh.stage_item[st];
             if (si.x < 0) break;
+            if (si.w) {
+                // a row found dead at its copy: a marker instead of a candidate
+                if (lane == 0) {
+                    const int rs = si.z % kResQ;
+                    st_async_u2(mapa_u32(smem_u32(&sh.res[rs][rank * kStreamWarps + w]), 0), __float_as_uint(-INFINITY),
+                                kSkipped, mapa_u32(smem_u32(&sh.res_full[rs]), 0));
+                    mbar_arrive(&sh.empty[st]);
+                }
+                continue;
+            }
             const uint8_t *zs = dyn + static_cast<size_t>(st) * P.stage_bytes;
             const uint8_t *zg = P.logits + ((static_cast<size_t>(si.x) * R + si.y) * V + lo) * ES;
             float best = -INFINITY;
@@ -746,13 +775,17 @@ int gc_resident(int C, int es, size_t smem) {
 // See common.h.
 spec_status_t launch_greedy_cluster(const GreedyClusterArgs &A, void *stream, bool &launched) {
     launched = false;
-    // greedy trees by default; greedy padded chains only when asked (path 2):
-    // on them the persistent kernel is faster
+    // Greedy trees always; greedy padded chains with fewer than two rows per SM
+    // (where the persistent kernel would split rows), or every one on path 2.
+    // With two rows per SM or more the persistent kernel's whole-row units
+    // stream faster (B = 64, k = 5, V = 128256: 20.5 against 22.4 us; at B = 48
+    // the grid takes 19.9 against 21.7, at B = 8 10.4 against 12.1).
     const int path = tuning_path();
-    if (path == 1 || (!A.parent && path != 2) || A.R < 2 || A.R > gc::kMaxR) return SPEC_OK;
+    if (path == 1 || A.R < 2 || A.R > gc::kMaxR) return SPEC_OK;
     int sms = 0;
     spec_status_t st = gc_setup(sms);
     if (st != SPEC_OK) return st;
+    if (!A.parent && path != 2 && static_cast<long long>(A.B) * A.R >= 2ll * sms) return SPEC_OK;
     const int es = A.dtype == SPEC_BF16 ? 2 : 4;
     int C = 0, S = 0;
     size_t stage_bytes = 0;

@@ -35,10 +35,10 @@ def sv():
 @pytest.fixture(autouse=True, params=[0, 1, 2], ids=["auto", "persistent", "cluster"])
 def chain_path(request, sv):
     """The kernel that verifies: path 0 (automatic) sends sampled padded chains
-    whose per-request clusters fit on the GPU to the chain cluster kernel and
-    greedy trees to the greedy cluster kernel; path 1 sends every batch to the
-    persistent kernel; path 2 is path 0 with greedy padded chains on the greedy
-    cluster kernel too.  Tests of ragged batches, the separate fix-up, n-gram
+    whose per-request clusters fit on the GPU to the chain cluster kernel, and
+    greedy trees and small greedy padded chains to the greedy cluster kernel;
+    path 1 sends every batch to the persistent kernel; path 2 is path 0 with
+    every greedy padded chain on the greedy cluster kernel.  Tests of ragged batches, the separate fix-up, n-gram
     lookup and next-step preparation do not depend on it and run once; trees
     run on paths 0 and 1."""
     path = request.param
