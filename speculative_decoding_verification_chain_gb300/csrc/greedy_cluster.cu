@@ -15,8 +15,8 @@
 // r of the cluster streams columns [r * S, r * S + S) of the unit's row through
 // a ring of three bulk-copy stages, and every streaming warp sends its argmax
 // candidate straight to the cluster's first CTA (st.async into its shared
-// memory), where an epilogue warp combines the row and publishes it.  A row is
-// a quarter (or less) of a row per SM, so a row resolves in about the time one
+// memory), where an epilogue warp combines the row and publishes it.  Each SM
+// streams a quarter (or less) of a row, so a row resolves in about the time one
 // SM streams 64 KiB: decisions arrive while their children are still queued.
 //
 // Roles (416 threads per CTA):
