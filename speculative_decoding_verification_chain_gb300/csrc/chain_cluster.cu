@@ -358,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
             sh.qfail = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             fence_proxy_async();
-            for (int j = 0; j < min(NS, R); ++j) issue(j);
+            // row 0 alone first when the rows are copied in bulk: rows issued
+            // together land together, and row 0 decides most requests
+            for (int j = 0; j < (zmain ? 1 : min(NS, R)); ++j) issue(j);
         }
         __syncwarp();
         if (lane < k) {
@@ -480,8 +482,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
         // (2) control warp: per row, the CTA's statistics from the warps'
         // partials, one exchange with the cluster, the decision; the next row
         // is copied only once this one is accepted
+        // the rest of the ring goes out once row 0 has landed
+        bool started = true;
+        if (zmain && min(NS, R) > 1) {
+            if (lane == 0) started = wait_copies(&sh.full[0], 0u, P.wait_ns);
+            started = __shfl_sync(0xffffffffu, started, 0) != 0;
+            if (started && lane == 0)
+                for (int j = 1; j < min(NS, R); ++j) issue(j);
+            if (!started) {
+                issued = 1;
+                if (lane == 0) atomicOr(&sh.abort, 1);
+            }
+        }
         cluster_wait();   // every CTA's barriers are initialised
-        for (int j = 0; j < R; ++j) {
+        for (int j = 0; j < R && started; ++j) {
             const int st = j % NS;
             const bool drained = wait_copies(&sh.empty[st], static_cast<uint32_t>((j / NS) & 1), P.wait_ns);
             if (!__all_sync(0xffffffffu, drained)) {
