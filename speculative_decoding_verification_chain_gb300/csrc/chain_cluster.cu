@@ -380,6 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
     int a = -1;
     int issued = min(NS, R);   // rows copied into the ring (control warp)
     bool bad = false;
+    // the bonus row (row k) is folded in contiguous chunks of Es groups per
+    // streaming thread, the layout its draw scans: when the walk accepts every
+    // draft, each thread's fold is already its chunk's share of p
+    const int Es = ((ng + kStreamThreads - 1) / kStreamThreads) | 1;   // odd: bank spread
+    float bonus_m = -INFINITY, bonus_s = 0.0f;
+    int bonus_last = -1;   // the chunk's last group with a logit above -inf
     if (!ctrl) {
         // (1) streaming warps: rows in order, each thread folding the groups
         // stid, stid + 480, ... of the row; a warp partial per row
@@ -438,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
                 // online max m and sums s0 + s1 relative to it; a NaN or +inf
                 // logit turns the sum into NaN, a -inf one adds 0
                 float m = -INFINITY, nm = 0.0f, s0 = 0.0f, s1 = 0.0f;
-                for (int g = stid; g < ng; g += kStreamThreads) {
+                // one group into the running max and sums; true if it holds a logit above -inf
+                auto fold = [&](int g) {
                     float z[8];
                     if (g < gbulk)
                         group8<ES>(zr, g, z);
@@ -461,8 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
                     s1 += ex2(fmaf(z[5], c2, nm));
                     s0 += ex2(fmaf(z[6], c2, nm));
                     s1 += ex2(fmaf(z[7], c2, nm));
+                    return gm > -INFINITY;
+                };
+                if (j == R - 1) {
+                    const int g0 = min(ng, stid * Es), g1 = min(ng, g0 + Es);
+                    for (int g = g0; g < g1; ++g)
+                        if (fold(g)) bonus_last = g;
+                } else {
+                    for (int g = stid; g < ng; g += kStreamThreads) fold(g);
                 }
                 const float s = s0 + s1;
+                if (j == R - 1) {
+                    bonus_m = m;
+                    bonus_s = s;
+                }
                 bad |= s != s;
                 float wm = m;
 #pragma unroll
@@ -683,14 +702,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
         D.c2 = c2;
         D.nm = mr == -INFINITY ? 0.0f : -mr * c2;
         D.pscale = (mr == -INFINITY ? 0.0f : ex2((mr - M) * c2)) / Sh;
-        // contiguous chunks of groups per thread (odd length: bank spread)
-        const int Eg = ((ng + kThreads - 1) / kThreads) | 1;
+        // contiguous chunks of groups per thread (odd length: bank spread); the
+        // bonus row keeps the chunks its streaming pass folded
+        const bool bonus = a == R - 1;
+        const int Eg = bonus ? Es : (((ng + kThreads - 1) / kThreads) | 1);
         const int g0 = min(ng, tid * Eg), g1 = min(ng, g0 + Eg);
         for (int attempt = 0; attempt < 2 && !late; ++attempt) {
             if (tid == 0) sh.holder = INT_MAX;
             tf th = tf_of(0.0f);
             int lastg = -1;
-            if (mr != -INFINITY)
+            if (bonus) {
+                // the streaming pass's fold of this chunk, rescaled to the draw's
+                // units: sum over the chunk of 2^((z - m_t) c2), times
+                // 2^((m_t - m_r) c2) pscale
+                if (mr != -INFINITY && bonus_m != -INFINITY)
+                    th = tf_of(bonus_s * (ex2((bonus_m - mr) * c2) * D.pscale));
+                lastg = bonus_last;
+            } else if (mr != -INFINITY)
                 for (int g = g0; g < g1; ++g) {
                     float w[8];
                     D.weights(g, w);
