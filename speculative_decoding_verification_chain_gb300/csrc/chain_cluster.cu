@@ -9,13 +9,18 @@
 // probability min(1, p(x)/q(x)) and resamples from norm(max(0, p - q))).
 //
 // Layout.  Request b owns a cluster of C CTAs; CTA r holds columns
-// [r * S, r * S + S) of a row in shared memory.
-//   (1) Phase 1 streams every row's slice through a ring of bulk-async copies
-//       (one row slice a stage), walking the rows last to first so that the
-//       ring ends holding rows 0, 1, ...: the rows a rejection most often
-//       lands on.  Each thread folds the groups tid, tid + 512, ... of the row
-//       into running statistics and each warp leaves one partial per row;
-//       nothing waits on a block reduction while the rows stream.
+// [r * S, r * S + S) of a row in a ring of shared-memory stages (three).  Of
+// the sixteen warps, fifteen stream rows and the last one controls the walk.
+//   (1) Copies.  The control warp's lane 0 issues one bulk-async copy per row
+//       slice: row 0 alone first (rows issued together land together, and
+//       row 0 decides most requests), rows 1 and 2 once row 0 has landed, and
+//       row j + 3 only once draft j is accepted, so no row more than two past
+//       the first rejection is read.
+//   (2) Streaming warps take the rows in order as they land.  Each thread
+//       folds the 8-column groups stid, stid + 480, ... of the row into
+//       running statistics (the bonus row k: a contiguous chunk of groups
+//       per thread, the layout its draw scans), each warp leaves one partial
+//       per row and frees the stage; nothing waits on a block reduction.
 //         * greedy (T == 0): the slice's maximum and the first column holding it;
 //           the row's argmax is the largest value, lowest column.
 //         * sampled: the slice's max m_r and sum_r = sum 2^((z - m_r) log2e/T)
@@ -23,21 +28,21 @@
 //           token's column.  M = max m_r, S = sum_r 2^((m_r - M) log2e/T) sum_r,
 //           and the accept test u q(x) S < e(x) 2^((m_owner - M) log2e/T)
 //           needs no division.
-//   (2) The warps' partials become the CTA's statistics of every row, and one
-//       exchange sends them to every CTA of the cluster (st.async into a slot
-//       of each CTA, completing on the receiver's mbarrier); every CTA then
-//       holds the same numbers, and warp i takes draft i's decision.
-//   (3) The first rejection a (or k) ends the chain.  A greedy request emits
+//   (3) The control warp, row by row: the warps' partials become the CTA's
+//       statistics of the row, one exchange sends them to every CTA of the
+//       cluster (st.async into a slot of each CTA, completing on the
+//       receiver's mbarrier), and every CTA takes draft j's decision from the
+//       same C values.
+//   (4) The first rejection a (or k) ends the walk.  A greedy request emits
 //       the argmax of row a; a sampled one draws by inverse CDF over the
 //       residual max(0, p - q) of row a (p of row k for the bonus token; p when
-//       the residual has no mass): per-thread sums over contiguous column
-//       chunks, a block scan, one exchange of the CTA totals, then one warp
+//       the residual has no mass): per-thread sums over contiguous chunks of
+//       groups, a block scan, one exchange of the CTA totals, then one warp
 //       rescans the chunk holding t = u * total, a lane per group.  Row a's
-//       logits are read in place when the ring still holds them, and q of row
-//       a is copied into the free stages around them.
-// Every row's logits are read once, whether or not the chain reaches it: the
-// cost of a row read in vain is small next to a walk that waits on a cluster
-// round trip per row.
+//       logits are still in their stage; q of row a is copied into the other
+//       two stages once the rows in flight there have landed.  The bonus row
+//       needs no pass of its own: its streaming fold already holds each
+//       chunk's sum.
 //
 // Every wait is bounded (the caller's limit); a wait that runs out ends the
 // walk for the whole CTA (a block barrier ORs the outcome) and sets

@@ -2,7 +2,11 @@
 //
 // One persistent kernel (one block per SM) verifies chains (greedy or sampled,
 // per request) and greedy token trees.  A chain is handled as a tree whose
-// node n has parent n-1, so both share one scheduler.
+// node n has parent n-1, so both share one scheduler.  The host part of this
+// file holds the entry points and routes each call: sampled padded chains
+// whose per-request clusters all fit on the GPU go to chain_cluster.cu, greedy
+// trees of at most 64 rows and small greedy padded chains to
+// greedy_cluster.cu, the rest to this kernel.
 //
 // Work.  A row of logits is cut into stages of at most 64 KiB (32768 bf16 or
 // 16384 fp32 elements), balanced in size and a whole number of 256-element
@@ -25,9 +29,13 @@
 //     max(0, p - q) (B units) -- and hand each finished unit to an epilogue;
 //   * warps 1..2, epilogues: combine a unit's partials; the last split of a
 //     row resolves it (its argmax, or its softmax statistics and the accept
-//     test min(1, p/q) of its one child); the last row of a request walks the
-//     tree, picks the deepest accepted node, writes the outputs and (chains,
-//     when asked) pads the rejected slots of slot_mapping.  A sampled request
+//     test min(1, p/q) of its one child).  Each resolved row is recorded in
+//     its request's 64-bit mask of resolved rows (requests over 64 rows count
+//     settled rows instead); the row that decides the request -- a chain
+//     whose resolved prefix holds a rejection, or a tree whose accepted
+//     nodes are all resolved -- walks the tree, picks the deepest accepted
+//     node, writes the outputs and (chains, when asked) pads the rejected
+//     slots of slot_mapping.  A sampled request
 //     rejected at row a publishes that decision as soon as row a resolves; its
 //     B units then run, and the last one locates u * (residual mass) in the
 //     block sums and scans one 256-element block for the token.  The residual
