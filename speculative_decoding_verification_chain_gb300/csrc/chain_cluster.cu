@@ -97,13 +97,13 @@ struct Params {
     unsigned long long wait_ns;
     int B, k, V, C, S;           // requests, drafts, vocabulary, CTAs per request, columns per CTA
     int zbulk, qbulk;            // rows start on 16-byte boundaries: bulk copies allowed
-    int stages;                  // phase-1 ring stages
+    int stages;                  // ring stages
     unsigned long long stage_bytes;
     unsigned long long smem;     // dynamic shared memory of the launch
 };
 
 constexpr int kMaxRowsCC = 16;   // rows per request (k + 1) this kernel takes
-constexpr int kMaxStages = 3;    // phase-1 ring
+constexpr int kMaxStages = 3;    // the ring
 
 struct Shared {
     uint64_t bar;                      // the drawn row's q copies
@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
     int bonus_last = -1;   // the chunk's last group with a logit above -inf
     if (!ctrl) {
         // (1) streaming warps: rows in order, each thread folding the groups
-        // stid, stid + 480, ... of the row; a warp partial per row
+        // stid, stid + 480, ... of the row (the bonus row: its contiguous
+        // chunk); a warp partial per row
         const int stid = tid;   // the control warp is the last one
         for (int j = 0; j < R; ++j) {
             const int st = j % NS;
@@ -504,9 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_cluster_kernel(const __grid
         }
     } else {
         // (2) control warp: per row, the CTA's statistics from the warps'
-        // partials, one exchange with the cluster, the decision; the next row
-        // is copied only once this one is accepted
-        // the rest of the ring goes out once row 0 has landed
+        // partials, one exchange with the cluster, the decision; row j + NS is
+        // copied only once row j is accepted.  First the rest of the ring goes
+        // out, once row 0 has landed.
         bool started = true;
         if (zmain && min(NS, R) > 1) {
             if (lane == 0) started = wait_copies(&sh.full[0], 0u, P.wait_ns);
